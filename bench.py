@@ -1,0 +1,382 @@
+"""Throughput of the fused 4-bit GEMV on GB300: weight-stream GB/s and the
+fraction of the HBM roofline.
+
+Workload (one step): a Qwen3-4B-shaped decode layer at N = 1 — the QKV triple
+(Q4_K 4096x2560, Q4_K 1024x2560, Q6_K 1024x2560), Wo (Q4_K 2560x4096) fused
+with the fp16 residual add, the gate/up pair (2 x Q4_K 9728x2560) and down
+(Q6_K 2560x9728): 63,866,880 packed weight bytes.  Steps rotate over 36
+distinct synthetic layers (2.3 GB, far above the 129 MB L2), so every step
+streams its weights from HBM.  Inputs are resident in HBM when timing starts;
+the timed steps are one CUDA graph replay.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
+
+Prints one JSON line.  Under torchrun (N > 1) every rank runs the same
+workload on its own GPU (replicas; weak scaling) and rank 0 reports the sum.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+N_LAYERS = 36
+METRIC = "weight-stream GB/s and % of GB300 HBM roofline for 4-bit GEMV, N=1..32"
+WORKLOAD = "qwen3_4b_decode_layer_n1"
+
+
+def _peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    return 6800.0, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled during the timed region."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.samples = []
+        self._stop = threading.Event()
+        self._t = None
+
+    def _run(self):
+        while not self._stop.is_set():
+            try:
+                out = subprocess.run(
+                    ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
+                     "--format=csv,noheader,nounits"], capture_output=True, text=True, timeout=5)
+                if out.returncode == 0 and out.stdout.strip():
+                    self.samples.append([v.strip() for v in out.stdout.strip().split(",")])
+            except Exception:
+                pass
+            self._stop.wait(0.1)
+
+    def __enter__(self):
+        self._t = threading.Thread(target=self._run, daemon=True)
+        self._t.start()
+        return self
+
+    def __exit__(self, *a):
+        self._stop.set()
+        if self._t:
+            self._t.join(timeout=10)
+
+    def summary(self):
+        if not self.samples:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"]}
+        sm = sorted(float(s[0]) for s in self.samples)
+        reasons = set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for s in self.samples:
+            for name, v in zip(names, s[4:8]):
+                if v.lower().startswith("active"):
+                    reasons.add(name)
+        return {"sm_mhz": sm[len(sm) // 2], "sm_max_mhz": float(self.samples[0][1]),
+                "reasons": sorted(reasons), "samples": len(self.samples)}
+
+
+def _kernel_source_sha():
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "skinny_gemm_q4_gb300", "csrc")
+    for f in sorted(os.listdir(csrc)):
+        if f.endswith((".cu", ".cuh")):
+            with open(os.path.join(csrc, f), "rb") as fh:
+                h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def _traffic_record():
+    """DRAM bytes per launch of the dominant kernel from the committed ncu
+    summary, or None if the kernel sources changed since it was taken."""
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(p):
+        return None
+    with open(p) as f:
+        rec = json.load(f)
+    if rec.get("source_sha") != _kernel_source_sha():
+        return None
+    return rec.get("dram_bytes_per_launch")
+
+
+def layer_weight_bytes():
+    from skinny_gemm_q4_gb300 import synth
+    return sum(M * synth.row_bytes(qt, K) for _, qt, M, K in synth.LAYER)
+
+
+# ---------------------------------------------------------------- reference
+
+def run_reference(args):
+    """The CPU oracle on a bounded sample of the same workload, timed on this
+    host's cores (single-threaded: the oracle as it stands)."""
+    import numpy as np
+
+    import oracle
+    from skinny_gemm_q4_gb300 import synth
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    oracle.build()
+    frac = 16  # every 16th row of every matrix of the layer
+    mats = []
+    for i, (role, qt, M, K) in enumerate(synth.LAYER):
+        w, sc, g = synth.weights(qt, M, K, seed=0, stream=100 + i)
+        rows = np.arange(0, M, frac)
+        x = synth.activations(1, K, seed=0, stream=200 + i)
+        mats.append((qt, w, M, K, rows, x))
+    sample_bytes = sum(len(r) * synth.row_bytes(qt, K) for qt, w, M, K, r, x in mats)
+
+    def step():
+        for qt, w, M, K, rows, x in mats:
+            oracle.qgemv(qt, w, M, K, x, rows=rows)
+
+    for _ in range(args.warmup):
+        step()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        step()
+    dt = (time.perf_counter() - t0) / args.steps
+    gbs = sample_bytes / dt / 1e9
+    line = {
+        "impl": "reference", "metric": METRIC, "value": round(gbs, 4), "unit": "GB/s",
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(dt * 1e3, 3), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": WORKLOAD, "N": 1, "layers": 1,
+                   "sample": f"every {frac}th row of each of the 7 matrices"},
+        "cpu_baseline": {"value": round(gbs, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
+                         "sample": f"1/{frac} of the rows of one decode layer "
+                                   f"({sample_bytes} weight bytes) per step"},
+        "e2e": {"value": round(gbs, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line))
+
+
+# ---------------------------------------------------------------- our path
+
+def run_ours(args):
+    import numpy as np
+    import torch
+
+    from skinny_gemm_q4_gb300 import build as b
+    from skinny_gemm_q4_gb300 import qgemv as qg
+    from skinny_gemm_q4_gb300 import synth
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    b.build()
+    qg.load()
+    dev = torch.device("cuda", local)
+
+    # 36 synthetic layers generated on the device.
+    layers = []
+    for L in range(N_LAYERS):
+        hs = {}
+        for i, (role, qt, M, K) in enumerate(synth.LAYER):
+            w, sc, g = synth.device_weights(qt, M, K, seed=rank, stream=1000 * L + i, device=dev)
+            hs[role] = qg.QGemv(qt, M, K, w, sc, g, max_tokens=32)
+        layers.append(hs)
+    wbytes = layer_weight_bytes()
+    x_qkv = synth.device_activations(1, 2560, 0, 1, dev)
+    x_o = synth.device_activations(1, 4096, 0, 2, dev)
+    res = synth.device_activations(1, 2560, 0, 3, dev)
+    x_ffn = synth.device_activations(1, 2560, 0, 4, dev)
+    x_dn = synth.device_activations(1, 9728, 0, 5, dev)
+    f16 = torch.float16
+    yq = torch.empty((1, 4096), dtype=f16, device=dev)
+    yk = torch.empty((1, 1024), dtype=f16, device=dev)
+    yv = torch.empty((1, 1024), dtype=f16, device=dev)
+    yo = torch.empty((1, 2560), dtype=f16, device=dev)
+    yg = torch.empty((1, 9728), dtype=f16, device=dev)
+    yu = torch.empty((1, 9728), dtype=f16, device=dev)
+    yd = torch.empty((1, 2560), dtype=f16, device=dev)
+
+    def step(L):
+        h = layers[L]
+        s = torch.cuda.current_stream().cuda_stream
+        qg.qgemv_triple_run(h["wq"].h, h["wk"].h, h["wv"].h, x_qkv.data_ptr(), 1,
+                            yq.data_ptr(), yk.data_ptr(), yv.data_ptr(), qg.OUT_F16, s)
+        qg.qgemv_run_add(h["wo"].h, x_o.data_ptr(), 1, res.data_ptr(), yo.data_ptr(), s)
+        qg.qgemv_pair_run(h["gate"].h, h["up"].h, x_ffn.data_ptr(), 1, yg.data_ptr(),
+                          yu.data_ptr(), qg.OUT_F16, s)
+        qg.qgemv_run(h["down"].h, x_dn.data_ptr(), 1, yd.data_ptr(), qg.OUT_F16, s)
+
+    launches_per_step = 8  # 4 staging + 4 product kernels
+
+    for i in range(args.warmup):
+        step(i % N_LAYERS)
+    torch.cuda.synchronize()
+
+    # Capture exactly K steps as one graph (launch-bound otherwise: a step is
+    # ~10 us of GPU time).
+    side = torch.cuda.Stream(device=dev)
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(side):
+        with torch.cuda.graph(graph, stream=side):
+            for i in range(args.steps):
+                step(i % N_LAYERS)
+    graph.replay()  # untimed
+    torch.cuda.synchronize()
+
+    def barrier():
+        if dist is not None:
+            dist.barrier()
+
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(local) as clk:
+        barrier()
+        torch.cuda.synchronize()
+        start.record()
+        graph.replay()
+        end.record()
+        torch.cuda.synchronize()
+        barrier()
+    ms = start.elapsed_time(end)
+    if dist is not None:
+        t = torch.tensor([ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+    ms_step = ms / args.steps
+    value = world * wbytes * args.steps / (ms / 1e3) / 1e9
+
+    # Dominant kernel: the gate/up pair product (44% of the layer's bytes),
+    # timed alone back to back over the 36 layers (graph), CUDA events on the
+    # launching stream.
+    pair_bytes = 2 * 9728 * synth.row_bytes(synth.Q4_K, 2560)
+    reps = N_LAYERS * 4
+    pg = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(side):
+        with torch.cuda.graph(pg, stream=side):
+            for i in range(reps):
+                h = layers[i % N_LAYERS]
+                qg.qgemv_pair_run(h["gate"].h, h["up"].h, x_ffn.data_ptr(), 1, yg.data_ptr(),
+                                  yu.data_ptr(), qg.OUT_F16, torch.cuda.current_stream().cuda_stream)
+    pg.replay()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    pg.replay()
+    e1.record()
+    torch.cuda.synchronize()
+    pair_us = e0.elapsed_time(e1) * 1e3 / reps
+    peak, peak_kind = _peaks()
+    achieved = pair_bytes / (pair_us * 1e-6) / 1e9
+
+    # End to end through the host-buffer entry point: per matrix, x from
+    # pinned host memory, y back to pinned host memory, synchronized.
+    e2e_steps = min(args.steps, N_LAYERS)
+    hx = {K: torch.from_numpy(np.random.default_rng(K).standard_normal((1, K)).astype(np.float16))
+          .pin_memory() for K in (2560, 4096, 9728)}
+    hy = {M: torch.empty((1, M), dtype=f16).pin_memory() for M in (4096, 1024, 2560, 9728)}
+    h2d = sum(K * 2 for _, _, M, K in synth.LAYER)
+    d2h = sum(M * 2 for _, _, M, K in synth.LAYER)
+    s = torch.cuda.current_stream().cuda_stream
+    for L in range(2):
+        for role, qt, M, K in synth.LAYER:
+            qg.qgemv_run_host(layers[L][role].h, hx[K].data_ptr(), 1, hy[M].data_ptr(),
+                              qg.OUT_F16, s)
+    barrier()
+    t0 = time.perf_counter()
+    for i in range(e2e_steps):
+        for role, qt, M, K in synth.LAYER:
+            qg.qgemv_run_host(layers[i % N_LAYERS][role].h, hx[K].data_ptr(), 1,
+                              hy[M].data_ptr(), qg.OUT_F16, s)
+    e2e_s = (time.perf_counter() - t0) / e2e_steps
+    barrier()
+    e2e_val = world * wbytes / e2e_s / 1e9
+
+    if rank != 0:
+        return
+    # CPU baseline: the oracle on one whole layer (N = 1), single thread.
+    cpu = None
+    if not args.no_cpu_baseline and world == 1:
+        import oracle
+        oracle.build()
+        t_cpu = 0.0
+        for i, (role, qt, M, K) in enumerate(synth.LAYER):
+            h = layers[0][role]
+            w = h._w.cpu().numpy()
+            sc = None if h._scales is None else h._scales.cpu().numpy()
+            x = synth.activations(1, K, seed=0, stream=300 + i)
+            t0 = time.perf_counter()
+            oracle.qgemv(qt, w, M, K, x, scales=sc)
+            t_cpu += time.perf_counter() - t0
+        cpu = {"value": round(wbytes / t_cpu / 1e9, 4), "unit": "GB/s", "cores": 1,
+               "kind": "oracle",
+               "sample": "one whole decode layer (7 matrices, 63.9 MB of weights), N=1"}
+
+    clocks = clk.summary()
+    line = {
+        "metric": METRIC,
+        "value": round(value, 2),
+        "unit": "GB/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(ms_step, 5),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "f16 x, fp32 accumulate, 4-bit weights",
+        "data": "synthetic",
+        "config": {"workload": WORKLOAD, "N": 1, "layers_rotated": N_LAYERS,
+                   "weight_bytes_per_step": wbytes,
+                   "cold": "36 distinct layers (2.3 GB) > L2; no flush needed",
+                   "pct_of_nominal_8TBps": round(100 * value / world / 8000.0, 2),
+                   "pct_of_measured_hbm": round(100 * value / world / peak, 2)},
+        "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak,
+                     "unit": "GB/s", "frac": round(achieved / peak, 4),
+                     "traffic": _traffic_record(),
+                     "kernel": "gate/up pair call (staging + skinny_kernel<Q4_K, G=1>)",
+                     "per_launch_us": round(pair_us, 3), "bytes_per_launch": pair_bytes,
+                     "peak_kind": peak_kind},
+        "cpu_baseline": cpu,
+        "e2e": {"value": round(e2e_val, 3), "unit": "GB/s", "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h,
+                "how": "qgemv_run_host per matrix (pinned host x and y, synchronized)"},
+        "gpu_launches": launches_per_step * args.steps,
+        "clocks": clocks,
+    }
+    print(json.dumps(line))
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,163 @@
+/*
+ * qgemv — fused dequantize-and-multiply for 4-bit block-quantized weights on
+ * GB300 (sm_103a).  C ABI; all pointers are plain device (or, where stated,
+ * host) addresses, all sizes are element counts, and every entry point
+ * returns a status instead of aborting.
+ *
+ * The operation (reflex-llm "docs/kernels.md", K-quant GEMV and batched
+ * K-quant GEMM sections; TandemLLM "Kernels", NVFP4 matrix products):
+ *
+ *     y[N x M] = x[N x K] . W^T,   y[n][m] = sum_k w[m][k] * x[n][k]
+ *
+ * where W[M][K] is stored block-quantized (GGML Q4_K, Q5_K, Q6_K super-blocks
+ * of 256 weights, or NVFP4 W4A16: e2m1 codes, one e4m3 scale per 16 weights
+ * and one fp32 per-tensor scale), x is fp16 and the accumulation is fp32.
+ * The weights are decoded in registers and never written back.  y is stored
+ * token-outer, y[n * M + m] (batched K-quant GEMM section).
+ *
+ * Row invariance (TandemLLM "Kernels", Row invariance and Verify twins):
+ * the bits of y[n][:] depend only on x[n] and W, never on N or on the other
+ * rows of x.  Every reduction order is fixed by (type, M, K); there are no
+ * atomics.
+ *
+ * Layouts (little-endian; the pages give the sizes and fields, the bit
+ * positions follow the GGML K-quant layout):
+ *   Q4_K, 144 B / 256 weights: fp16 d, fp16 dmin, scales[12] (eight 6-bit
+ *         scales and eight 6-bit mins), qs[128] (two nibbles per byte).
+ *   Q5_K, 176 B: d, dmin, scales[12], qh[32] (fifth bits), qs[128].
+ *   Q6_K, 210 B: ql[128], qh[64], int8 scales[16], fp16 d.
+ *   NVFP4: codes uint8[M][K/2] (element 2i low nibble of byte i), e4m3
+ *         scales uint8[M][K/16], fp32 global scale.
+ * A row of a K-quant matrix is K/256 consecutive blocks; rows are contiguous.
+ */
+#ifndef QGEMV_H
+#define QGEMV_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Weight formats.  12 (Q4_K) and 14 (Q6_K) are the GGML type ids used as
+ * template arguments on reflex-llm "docs/performance.md", Path C; 13 follows
+ * GGML's order; the NVFP4 id is this library's own. */
+typedef enum {
+    QG_Q4_K = 12,
+    QG_Q5_K = 13,
+    QG_Q6_K = 14,
+    QG_NVFP4_W4A16 = 256
+} qg_type;
+
+typedef enum {
+    QG_OK = 0,
+    QG_EINVAL = -1,          /* bad argument (null pointer, size, mismatch) */
+    QG_EUNSUPPORTED = -2,    /* valid request this library does not serve   */
+    QG_EALIGN = -3,          /* pointer not aligned as required              */
+    QG_ECUDA = -4,           /* a CUDA call failed; see qgemv_last_error()  */
+    QG_ENOMEM = -5,          /* device allocation failed                     */
+    QG_EFAULT_INJECTED = -6  /* failure forced by QGEMV_FAULT_INJECT         */
+} qg_status;
+
+/* Output element type of y. */
+typedef enum { QG_OUT_F16 = 0, QG_OUT_F32 = 1 } qg_out;
+
+/* Option flags. */
+enum {
+    QG_FLAG_FORCE_REFERENCE = 1u << 0, /* always use the simple reference kernel */
+    QG_FLAG_DEBUG_SYNC = 1u << 1,      /* synchronize the stream after each call and
+                                          report asynchronous errors              */
+    QG_FLAG_NO_FALLBACK = 1u << 2      /* return the fast path's launch error instead
+                                          of retrying on the reference kernel      */
+};
+
+typedef struct {
+    uint32_t flags;      /* QG_FLAG_* */
+    int32_t max_tokens;  /* largest N staged at once (<= 0: 128).  Larger N is
+                            processed in chunks of this many rows. */
+} qg_opts;
+
+typedef struct qg_handle qg_handle;
+
+/* Create a handle for one weight matrix.
+ *   t            format
+ *   M, K         rows (outputs) and columns (reduction length); M >= 1,
+ *                K >= 256 and K % 256 == 0 for every format
+ *   w_dev        device pointer to the packed matrix (row-major rows of
+ *                qgemv_row_bytes(t, K) bytes).  Q4_K/Q5_K/NVFP4 need 16-byte
+ *                alignment; Q6_K needs 2-byte alignment (its 210-byte blocks
+ *                are staged through 16-byte aligned supersets).
+ *   scales_dev   NVFP4 only: e4m3 scales [M][K/16], 16-byte aligned; else NULL
+ *   global_scale NVFP4 only: per-tensor fp32 scale; ignored otherwise
+ *   opts         nullable
+ * Ownership: w_dev and scales_dev are borrowed and must outlive the handle and
+ * stay unchanged while calls are in flight.  The handle owns its plan and a
+ * small device staging buffer for x (max_tokens * K * 2.25 bytes per layout).
+ * Errors: QG_EINVAL, QG_EALIGN, QG_EUNSUPPORTED, QG_ENOMEM, QG_ECUDA. */
+qg_status qgemv_create(qg_handle **h, qg_type t, int64_t M, int64_t K,
+                       const void *w_dev, const void *scales_dev, float global_scale,
+                       const qg_opts *opts);
+
+/* y = x . W^T.  x: fp16 [N][K] device, 16-byte aligned; y: [N][M] device of
+ * type ydt (fp16 rounded to nearest-even, or fp32), 4-byte aligned.
+ * N >= 1.  Work is enqueued on stream (a cudaStream_t; NULL = legacy default
+ * stream); the call does not synchronize unless QG_FLAG_DEBUG_SYNC is set.
+ * Calls on one handle must be ordered on one stream (they share the staging
+ * buffer).  Errors: QG_EINVAL, QG_EALIGN, QG_ECUDA. */
+qg_status qgemv_run(qg_handle *h, const void *x, int64_t N, void *y, qg_out ydt,
+                    void *stream);
+
+/* y = residual + x . W^T, added in fp32 before one rounding to fp16
+ * (reflex-llm "docs/kernels.md": Wo fused with the residual add).
+ * residual, y: fp16 [N][M] device; y may equal residual (in place). */
+qg_status qgemv_run_add(qg_handle *h, const void *x, int64_t N, const void *residual,
+                        void *y, void *stream);
+
+/* Two matrices with the same K sharing x (gate/up pair), one launch.
+ * ya is [N][Ma], yb is [N][Mb]. */
+qg_status qgemv_pair_run(qg_handle *a, qg_handle *b, const void *x, int64_t N,
+                         void *ya, void *yb, qg_out ydt, void *stream);
+
+/* Three matrices with the same K sharing x (QKV triple); formats may differ
+ * (e.g. Q4_K, Q4_K, Q6_K).  One staging pass and one product launch. */
+qg_status qgemv_triple_run(qg_handle *a, qg_handle *b, qg_handle *c, const void *x,
+                           int64_t N, void *ya, void *yb, void *yc, qg_out ydt,
+                           void *stream);
+
+/* Host-buffer form of qgemv_run: x_host (fp16 [N][K]) and y_host ([N][M] of
+ * ydt) are host memory (pinned memory gives the fastest copies).  Copies x to
+ * the device, runs, copies y back and synchronizes the stream before
+ * returning.  The device buffers are owned by the handle and grow on demand. */
+qg_status qgemv_run_host(qg_handle *h, const void *x_host, int64_t N, void *y_host,
+                         qg_out ydt, void *stream);
+
+/* Dequantize the whole matrix to fp32 w_out[M][K] (device, 4-byte aligned)
+ * with the same decoders the product uses.  A test path, not a hot path. */
+qg_status qgemv_dequantize(qg_handle *h, float *w_out, void *stream);
+
+/* Free the handle (does not free the borrowed weights).  NULL is a no-op. */
+void qgemv_destroy(qg_handle *h);
+
+/* Message of the last error on the calling thread ("" if none). */
+const char *qgemv_last_error(void);
+
+/* Bytes per row of the packed matrix (codes only for NVFP4); -1 if K is not
+ * supported for the format.  Pure host function. */
+int64_t qgemv_row_bytes(qg_type t, int64_t K);
+
+/* Launch plan of a handle, for tests and profiling: number of K-split ranks
+ * (a cluster of CTAs per row tile, combined in rank order), rows per CTA for
+ * the given N, and how many kernels one qgemv_run launches.  Pure host. */
+qg_status qgemv_plan_info(const qg_handle *h, int64_t N, int32_t *ksplit,
+                          int32_t *rows_per_cta, int32_t *launches);
+
+/* Human-readable description of the options in effect (flags, environment
+ * overrides QGEMV_FORCE_REFERENCE, QGEMV_DEBUG_SYNC, QGEMV_FAULT_INJECT). */
+const char *qgemv_describe(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* QGEMV_H */

@@ -1,0 +1,484 @@
+// C ABI of the qgemv library: handles, launch plan, argument validation,
+// staging + product launches, reference fallback and error reporting.
+#include <cuda_runtime.h>
+
+#include <cmath>
+#include <cstdarg>
+#include <cstdio>
+#include <cstdlib>
+#include <cstring>
+#include <string>
+
+#include "qg_launch.cuh"
+#include "qgemv.h"
+
+using namespace qg;
+
+struct qg_handle {
+    qg_type type;
+    int64_t M, K;
+    int nb;
+    const uint8_t *w;
+    const uint8_t *sc;
+    float gscale;
+    int64_t row_bytes, sc_row_bytes, w_bytes;
+    uint32_t flags;
+    int max_tokens;
+    int ks;        // K-split ranks, fixed by K
+    int layout;    // staged-x layout this format reads
+    uint8_t *xs;   // staging buffer: max_tokens * nb * kXTok bytes
+    int device;
+    void *hx;      // device buffers of the host-pointer entry point
+    size_t hx_cap;
+    void *hy;
+    size_t hy_cap;
+};
+
+namespace {
+
+thread_local std::string g_err;
+
+qg_status fail(qg_status s, const char *fmt, ...)
+{
+    char buf[512];
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(buf, sizeof buf, fmt, ap);
+    va_end(ap);
+    g_err = buf;
+    return s;
+}
+
+qg_status cuda_fail(cudaError_t e, const char *what)
+{
+    return fail(QG_ECUDA, "%s: %s (%s)", what, cudaGetErrorName(e), cudaGetErrorString(e));
+}
+
+bool env_on(const char *name)
+{
+    const char *v = getenv(name);
+    return v && *v && strcmp(v, "0") != 0;
+}
+
+bool fault_at(const char *site)
+{
+    const char *v = getenv("QGEMV_FAULT_INJECT");
+    return v && strcmp(v, site) == 0;
+}
+
+bool aligned(const void *p, size_t a) { return ((uintptr_t)p % a) == 0; }
+
+int block_bytes(qg_type t)
+{
+    switch (t) {
+    case QG_Q4_K: return 144;
+    case QG_Q5_K: return 176;
+    case QG_Q6_K: return 210;
+    default: return 0;
+    }
+}
+
+bool type_known(int t)
+{
+    return t == QG_Q4_K || t == QG_Q5_K || t == QG_Q6_K || t == QG_NVFP4_W4A16;
+}
+
+int layout_of(qg_type t)
+{
+    return t == QG_Q6_K ? XL_Q6 : (t == QG_NVFP4_W4A16 ? XL_FP4 : XL_Q4);
+}
+
+int tset_bit(qg_type t)
+{
+    switch (t) {
+    case QG_Q4_K: return TS_Q4K;
+    case QG_Q5_K: return TS_Q5K;
+    case QG_Q6_K: return TS_Q6K;
+    default: return TS_FP4;
+    }
+}
+
+// K-split: about six super-blocks per rank, at most 8 ranks (one cluster).
+// Depends on K only, so every row's reduction order is fixed by the shape.
+int plan_ks(int nb)
+{
+    int ks = (nb + 5) / 6;
+    if (ks < 1) ks = 1;
+    if (ks > 8) ks = 8;
+    if (ks > nb) ks = nb;
+    return ks;
+}
+
+int groups_for(int64_t n) { return n >= 32 ? 4 : (int)((n + 7) / 8); }
+
+int rows_per_cta(int G) { return G <= 2 ? Cfg<1>::ROWS : Cfg<4>::ROWS; }
+
+Mat mat_of(const qg_handle *h, void *y, const __half *res)
+{
+    Mat m;
+    m.w = h->w;
+    m.sc = h->sc;
+    m.y = y;
+    m.res = res;
+    m.row_bytes = h->row_bytes;
+    m.sc_row_bytes = h->sc_row_bytes;
+    m.w_bytes = h->w_bytes;
+    m.M = (int)h->M;
+    m.type = (int)h->type;
+    m.tile_begin = 0;
+    m.gscale = h->gscale;
+    return m;
+}
+
+cudaError_t launch_tset(int tset, int G, const Params &p, dim3 grid, cudaStream_t s)
+{
+    switch (tset) {
+    case TS_Q4K: return launch_skinny_q4k(G, p, grid, s);
+    case TS_Q5K: return launch_skinny_q5k(G, p, grid, s);
+    case TS_Q6K: return launch_skinny_q6k(G, p, grid, s);
+    case TS_FP4: return launch_skinny_fp4(G, p, grid, s);
+    case TS_Q4K | TS_Q6K: return launch_skinny_q4k_q6k(G, p, grid, s);
+    default: return cudaErrorInvalidValue;
+    }
+}
+
+bool tset_supported(int tset)
+{
+    return tset == TS_Q4K || tset == TS_Q5K || tset == TS_Q6K || tset == TS_FP4 ||
+           tset == (TS_Q4K | TS_Q6K);
+}
+
+// The whole path for 1..3 handles that share x: staging, then one product
+// launch per chunk of at most max_tokens rows (several launches only when the
+// formats have no common kernel).
+qg_status run_product(qg_handle *const *hs, int nh, const __half *x, int64_t N, void *const *ys,
+                      const __half *res, int out_f32, cudaStream_t s)
+{
+    const qg_handle *h0 = hs[0];
+    uint32_t flags = 0;
+    int max_tokens = h0->max_tokens;
+    for (int i = 0; i < nh; ++i) {
+        flags |= hs[i]->flags;
+        if (hs[i]->max_tokens < max_tokens) max_tokens = hs[i]->max_tokens;
+    }
+    const bool force_ref = (flags & QG_FLAG_FORCE_REFERENCE) != 0;
+    g_err.clear();
+
+    int tset = 0;
+    for (int i = 0; i < nh; ++i) tset |= tset_bit(hs[i]->type);
+
+    for (int64_t c0 = 0; c0 < N; c0 += max_tokens) {
+        const int n = (int)((N - c0) < max_tokens ? (N - c0) : max_tokens);
+        const __half *xc = x + c0 * h0->K;
+        if (force_ref) {
+            for (int i = 0; i < nh; ++i) {
+                Mat m = mat_of(hs[i], (uint8_t *)ys[i] + c0 * hs[i]->M * (out_f32 ? 4 : 2),
+                               res ? res + c0 * hs[i]->M : nullptr);
+                cudaError_t e = launch_ref_gemv(m, (int)h0->K, xc, n, out_f32, s);
+                if (e != cudaSuccess) return cuda_fail(e, "reference kernel launch");
+            }
+            continue;
+        }
+        // Stage x once per layout.
+        uint8_t *xl[XL_COUNT] = {nullptr, nullptr, nullptr};
+        for (int i = 0; i < nh; ++i)
+            if (!xl[hs[i]->layout]) xl[hs[i]->layout] = hs[i]->xs;
+        if (fault_at("stage")) return fail(QG_EFAULT_INJECTED, "injected fault: staging launch");
+        const int64_t tok_stride = (int64_t)h0->nb * kXTok;
+        cudaError_t e = launch_stage(xc, n, (int)h0->K, h0->nb, tok_stride, xl[XL_Q4], xl[XL_Q6],
+                                     xl[XL_FP4], s);
+        if (e != cudaSuccess) return cuda_fail(e, "staging kernel launch");
+
+        const int G = groups_for(n);
+        const int rows = rows_per_cta(G);
+        // Groups of handles that one kernel serves.
+        int groups[3][3];
+        int gsize[3] = {0, 0, 0};
+        int ng = 0;
+        if (tset_supported(tset)) {
+            for (int i = 0; i < nh; ++i) groups[0][gsize[0]++] = i;
+            ng = 1;
+        } else {
+            for (int i = 0; i < nh; ++i) {
+                groups[ng][0] = i;
+                gsize[ng++] = 1;
+            }
+        }
+        for (int gidx = 0; gidx < ng; ++gidx) {
+            Params p;
+            memset(&p, 0, sizeof p);
+            int tiles = 0, gts = 0;
+            for (int j = 0; j < gsize[gidx]; ++j) {
+                const qg_handle *h = hs[groups[gidx][j]];
+                const int idx = groups[gidx][j];
+                p.mat[j] = mat_of(h, (uint8_t *)ys[idx] + c0 * h->M * (out_f32 ? 4 : 2),
+                                  res ? res + c0 * h->M : nullptr);
+                p.mat[j].tile_begin = tiles;
+                tiles += (int)((h->M + rows - 1) / rows);
+                gts |= tset_bit(h->type);
+            }
+            p.nmat = gsize[gidx];
+            for (int l = 0; l < XL_COUNT; ++l) p.xs[l] = xl[l];
+            p.xs_tok_stride = tok_stride;
+            p.N = n;
+            p.tok_base = 0;
+            p.nb = h0->nb;
+            p.ks = h0->ks;
+            p.out_f32 = out_f32;
+            const dim3 grid((unsigned)p.ks, (unsigned)tiles, (unsigned)((n + kTokChunk - 1) / kTokChunk));
+            cudaError_t le;
+            if (fault_at("launch")) {
+                le = cudaErrorLaunchOutOfResources;  // simulated, nothing was launched
+            } else {
+                le = launch_tset(gts, G, p, grid, s);
+            }
+            if (le != cudaSuccess) {
+                cudaGetLastError();  // launch-time errors are not sticky
+                if (flags & QG_FLAG_NO_FALLBACK) {
+                    if (fault_at("launch"))
+                        return fail(QG_EFAULT_INJECTED, "injected fault: product launch");
+                    return cuda_fail(le, "product kernel launch");
+                }
+                for (int j = 0; j < p.nmat; ++j) {
+                    cudaError_t re = launch_ref_gemv(p.mat[j], (int)h0->K, xc, n, out_f32, s);
+                    if (re != cudaSuccess) return cuda_fail(re, "reference kernel launch");
+                }
+                fail(QG_OK, "fast path launch failed (%s); used the reference kernel",
+                     cudaGetErrorName(le));
+            }
+        }
+    }
+    if (flags & QG_FLAG_DEBUG_SYNC) {
+        cudaError_t e = cudaStreamSynchronize(s);
+        if (e == cudaSuccess) e = cudaGetLastError();
+        if (e != cudaSuccess) return cuda_fail(e, "debug synchronize");
+    }
+    return QG_OK;
+}
+
+qg_status check_run_args(const qg_handle *h, const void *x, int64_t N, const void *y, qg_out ydt)
+{
+    if (!h) return fail(QG_EINVAL, "null handle");
+    if (!x || !y) return fail(QG_EINVAL, "null x or y");
+    if (N < 1) return fail(QG_EINVAL, "N must be >= 1 (got %lld)", (long long)N);
+    if (N > (int64_t)1 << 24) return fail(QG_EUNSUPPORTED, "N too large");
+    if (ydt != QG_OUT_F16 && ydt != QG_OUT_F32) return fail(QG_EINVAL, "bad output type");
+    if (!aligned(x, 16)) return fail(QG_EALIGN, "x must be 16-byte aligned");
+    if (!aligned(y, ydt == QG_OUT_F32 ? 4 : 2)) return fail(QG_EALIGN, "y misaligned");
+    return QG_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int64_t qgemv_row_bytes(qg_type t, int64_t K)
+{
+    if (!type_known(t) || K < 256 || K % 256 != 0) return -1;
+    if (t == QG_NVFP4_W4A16) return K / 2;
+    return (K / 256) * block_bytes(t);
+}
+
+const char *qgemv_last_error(void) { return g_err.c_str(); }
+
+const char *qgemv_describe(void)
+{
+    static thread_local std::string d;
+    const char *fi = getenv("QGEMV_FAULT_INJECT");
+    d = std::string("qgemv: GB300 (sm_103a) fused 4-bit GEMV; formats Q4_K=12 Q5_K=13 Q6_K=14 "
+                    "NVFP4_W4A16=256; flags FORCE_REFERENCE=1 DEBUG_SYNC=2 NO_FALLBACK=4; ") +
+        "env QGEMV_FORCE_REFERENCE=" + (env_on("QGEMV_FORCE_REFERENCE") ? "1" : "0") +
+        " QGEMV_DEBUG_SYNC=" + (env_on("QGEMV_DEBUG_SYNC") ? "1" : "0") +
+        " QGEMV_FAULT_INJECT=" + (fi ? fi : "") +
+        "; staging " + std::to_string(kXTok) + " B per token per 256 columns; " +
+        "K split over ceil(K/1536) (<= 8) cluster ranks";
+    return d.c_str();
+}
+
+qg_status qgemv_create(qg_handle **out, qg_type t, int64_t M, int64_t K, const void *w_dev,
+                       const void *scales_dev, float global_scale, const qg_opts *opts)
+{
+    if (!out) return fail(QG_EINVAL, "null output handle pointer");
+    *out = nullptr;
+    if (!type_known(t)) return fail(QG_EUNSUPPORTED, "unknown weight type %d", (int)t);
+    if (M < 1) return fail(QG_EINVAL, "M must be >= 1");
+    if (K < 256 || K % 256 != 0) return fail(QG_EUNSUPPORTED, "K must be a positive multiple of 256");
+    if (M > (int64_t)1 << 30 || K > (int64_t)1 << 24) return fail(QG_EUNSUPPORTED, "shape too large");
+    if (!w_dev) return fail(QG_EINVAL, "null weight pointer");
+    if (!aligned(w_dev, 16)) return fail(QG_EALIGN, "weights must be 16-byte aligned");
+    if (t == QG_NVFP4_W4A16) {
+        if (!scales_dev) return fail(QG_EINVAL, "NVFP4 needs the e4m3 scale array");
+        if (!aligned(scales_dev, 16)) return fail(QG_EALIGN, "scales must be 16-byte aligned");
+        if (!std::isfinite(global_scale)) return fail(QG_EINVAL, "global scale must be finite");
+    }
+    const int max_tokens = (opts && opts->max_tokens > 0) ? opts->max_tokens : 128;
+    if (max_tokens > (1 << 20)) return fail(QG_EUNSUPPORTED, "max_tokens too large");
+    uint32_t flags = opts ? opts->flags : 0u;
+    if (env_on("QGEMV_FORCE_REFERENCE")) flags |= QG_FLAG_FORCE_REFERENCE;
+    if (env_on("QGEMV_DEBUG_SYNC")) flags |= QG_FLAG_DEBUG_SYNC;
+    if (fault_at("create")) return fail(QG_EFAULT_INJECTED, "injected fault: create");
+
+    const int nb = (int)(K / 256);
+    const int64_t rows_needed = (M + Cfg<1>::ROWS - 1) / Cfg<1>::ROWS;
+    if (rows_needed > 65535) return fail(QG_EUNSUPPORTED, "too many rows for one grid");
+
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+
+    qg_handle *h = new (std::nothrow) qg_handle();
+    if (!h) return fail(QG_ENOMEM, "host allocation failed");
+    h->type = t;
+    h->M = M;
+    h->K = K;
+    h->nb = nb;
+    h->w = (const uint8_t *)w_dev;
+    h->sc = (const uint8_t *)scales_dev;
+    h->gscale = (t == QG_NVFP4_W4A16) ? global_scale : 1.0f;
+    h->row_bytes = qgemv_row_bytes(t, K);
+    h->sc_row_bytes = (t == QG_NVFP4_W4A16) ? K / 16 : 0;
+    h->w_bytes = h->row_bytes * M;
+    h->flags = flags;
+    h->max_tokens = max_tokens;
+    h->ks = plan_ks(nb);
+    h->layout = layout_of(t);
+    h->device = dev;
+    const size_t xs_bytes = (size_t)max_tokens * nb * kXTok;
+    e = cudaMalloc((void **)&h->xs, xs_bytes);
+    if (e != cudaSuccess) {
+        cudaGetLastError();
+        delete h;
+        return fail(QG_ENOMEM, "staging buffer allocation of %zu bytes failed", xs_bytes);
+    }
+    *out = h;
+    return QG_OK;
+}
+
+void qgemv_destroy(qg_handle *h)
+{
+    if (!h) return;
+    if (h->xs) cudaFree(h->xs);
+    if (h->hx) cudaFree(h->hx);
+    if (h->hy) cudaFree(h->hy);
+    delete h;
+}
+
+qg_status qgemv_run(qg_handle *h, const void *x, int64_t N, void *y, qg_out ydt, void *stream)
+{
+    qg_status st = check_run_args(h, x, N, y, ydt);
+    if (st != QG_OK) return st;
+    void *ys[1] = {y};
+    return run_product(&h, 1, (const __half *)x, N, ys, nullptr, ydt == QG_OUT_F32,
+                       (cudaStream_t)stream);
+}
+
+qg_status qgemv_run_add(qg_handle *h, const void *x, int64_t N, const void *residual, void *y,
+                        void *stream)
+{
+    qg_status st = check_run_args(h, x, N, y, QG_OUT_F16);
+    if (st != QG_OK) return st;
+    if (!residual) return fail(QG_EINVAL, "null residual");
+    if (!aligned(residual, 2)) return fail(QG_EALIGN, "residual misaligned");
+    void *ys[1] = {y};
+    return run_product(&h, 1, (const __half *)x, N, ys, (const __half *)residual, 0,
+                       (cudaStream_t)stream);
+}
+
+qg_status qgemv_pair_run(qg_handle *a, qg_handle *b, const void *x, int64_t N, void *ya,
+                         void *yb, qg_out ydt, void *stream)
+{
+    qg_status st = check_run_args(a, x, N, ya, ydt);
+    if (st != QG_OK) return st;
+    st = check_run_args(b, x, N, yb, ydt);
+    if (st != QG_OK) return st;
+    if (a->K != b->K) return fail(QG_EINVAL, "pair handles must share K");
+    if (ya == yb) return fail(QG_EINVAL, "pair outputs must differ");
+    qg_handle *hs[2] = {a, b};
+    void *ys[2] = {ya, yb};
+    return run_product(hs, 2, (const __half *)x, N, ys, nullptr, ydt == QG_OUT_F32,
+                       (cudaStream_t)stream);
+}
+
+qg_status qgemv_triple_run(qg_handle *a, qg_handle *b, qg_handle *c, const void *x, int64_t N,
+                           void *ya, void *yb, void *yc, qg_out ydt, void *stream)
+{
+    qg_status st = check_run_args(a, x, N, ya, ydt);
+    if (st == QG_OK) st = check_run_args(b, x, N, yb, ydt);
+    if (st == QG_OK) st = check_run_args(c, x, N, yc, ydt);
+    if (st != QG_OK) return st;
+    if (a->K != b->K || a->K != c->K) return fail(QG_EINVAL, "triple handles must share K");
+    if (ya == yb || ya == yc || yb == yc) return fail(QG_EINVAL, "triple outputs must differ");
+    qg_handle *hs[3] = {a, b, c};
+    void *ys[3] = {ya, yb, yc};
+    return run_product(hs, 3, (const __half *)x, N, ys, nullptr, ydt == QG_OUT_F32,
+                       (cudaStream_t)stream);
+}
+
+qg_status qgemv_run_host(qg_handle *h, const void *x_host, int64_t N, void *y_host, qg_out ydt,
+                         void *stream)
+{
+    if (!h) return fail(QG_EINVAL, "null handle");
+    if (!x_host || !y_host) return fail(QG_EINVAL, "null host buffer");
+    if (N < 1) return fail(QG_EINVAL, "N must be >= 1");
+    if (ydt != QG_OUT_F16 && ydt != QG_OUT_F32) return fail(QG_EINVAL, "bad output type");
+    cudaStream_t s = (cudaStream_t)stream;
+    const size_t xb = (size_t)N * h->K * 2;
+    const size_t yb = (size_t)N * h->M * (ydt == QG_OUT_F32 ? 4 : 2);
+    cudaError_t e;
+    if (h->hx_cap < xb) {
+        if (h->hx) cudaFree(h->hx);
+        h->hx = nullptr;
+        h->hx_cap = 0;
+        e = cudaMalloc(&h->hx, xb);
+        if (e != cudaSuccess) return fail(QG_ENOMEM, "device x buffer allocation failed");
+        h->hx_cap = xb;
+    }
+    if (h->hy_cap < yb) {
+        if (h->hy) cudaFree(h->hy);
+        h->hy = nullptr;
+        h->hy_cap = 0;
+        e = cudaMalloc(&h->hy, yb);
+        if (e != cudaSuccess) return fail(QG_ENOMEM, "device y buffer allocation failed");
+        h->hy_cap = yb;
+    }
+    e = cudaMemcpyAsync(h->hx, x_host, xb, cudaMemcpyHostToDevice, s);
+    if (e != cudaSuccess) return cuda_fail(e, "copy of x to the device");
+    qg_status st = qgemv_run(h, h->hx, N, h->hy, ydt, stream);
+    if (st != QG_OK) return st;
+    e = cudaMemcpyAsync(y_host, h->hy, yb, cudaMemcpyDeviceToHost, s);
+    if (e != cudaSuccess) return cuda_fail(e, "copy of y to the host");
+    e = cudaStreamSynchronize(s);
+    if (e != cudaSuccess) return cuda_fail(e, "stream synchronize");
+    return QG_OK;
+}
+
+qg_status qgemv_dequantize(qg_handle *h, float *w_out, void *stream)
+{
+    if (!h) return fail(QG_EINVAL, "null handle");
+    if (!w_out) return fail(QG_EINVAL, "null output");
+    if (!aligned(w_out, 4)) return fail(QG_EALIGN, "output must be 4-byte aligned");
+    Mat m = mat_of(h, nullptr, nullptr);
+    cudaError_t e = launch_dequant(m, (int)h->K, w_out, (cudaStream_t)stream);
+    if (e != cudaSuccess) return cuda_fail(e, "dequantize kernel launch");
+    if (h->flags & QG_FLAG_DEBUG_SYNC) {
+        e = cudaStreamSynchronize((cudaStream_t)stream);
+        if (e != cudaSuccess) return cuda_fail(e, "debug synchronize");
+    }
+    return QG_OK;
+}
+
+qg_status qgemv_plan_info(const qg_handle *h, int64_t N, int32_t *ksplit, int32_t *rows_cta,
+                          int32_t *launches)
+{
+    if (!h) return fail(QG_EINVAL, "null handle");
+    if (N < 1) return fail(QG_EINVAL, "N must be >= 1");
+    const int64_t chunks = (N + h->max_tokens - 1) / h->max_tokens;
+    const int64_t nfirst = N < h->max_tokens ? N : h->max_tokens;
+    if (ksplit) *ksplit = h->ks;
+    if (rows_cta) *rows_cta = rows_per_cta(groups_for(nfirst));
+    if (launches)
+        *launches = (int32_t)((h->flags & QG_FLAG_FORCE_REFERENCE) ? chunks : 2 * chunks);
+    return QG_OK;
+}
+
+}  // extern "C"

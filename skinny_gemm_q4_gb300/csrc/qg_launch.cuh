@@ -1,0 +1,32 @@
+// Host-side launch entry points of the kernels (one translation unit per
+// weight-format set, so the instantiations compile in parallel).
+#pragma once
+#include <cuda_runtime.h>
+#include "qg_kernels.cuh"
+
+namespace qg {
+
+// Launch skinny_kernel<TSET, G> with `ks` CTAs per cluster along x and
+// programmatic dependent launch enabled.  Returns the launch status.
+cudaError_t launch_skinny(int tset, int G, const Params &p, dim3 grid, cudaStream_t stream);
+// Dynamic shared memory of skinny_kernel<TSET, G>.
+int skinny_smem_bytes(int tset, int G);
+
+cudaError_t launch_stage(const __half *x, int N, int K, int nb, int64_t tok_stride, uint8_t *xq4,
+                         uint8_t *xq6, uint8_t *xfp4, cudaStream_t stream);
+cudaError_t launch_dequant(const Mat &m, int K, float *out, cudaStream_t stream);
+cudaError_t launch_ref_gemv(const Mat &m, int K, const __half *x, int N, int out_f32,
+                            cudaStream_t stream);
+
+// Per type-set launchers (defined in qg_inst_*.cu).
+#define QG_DECLARE_TSET(NAME)                                                           \
+    cudaError_t launch_skinny_##NAME(int G, const Params &p, dim3 grid, cudaStream_t s); \
+    int smem_skinny_##NAME(int G);
+QG_DECLARE_TSET(q4k)
+QG_DECLARE_TSET(q5k)
+QG_DECLARE_TSET(q6k)
+QG_DECLARE_TSET(fp4)
+QG_DECLARE_TSET(q4k_q6k)
+#undef QG_DECLARE_TSET
+
+}  // namespace qg

@@ -1,0 +1,233 @@
+"""Thin ctypes binding of the qgemv C ABI (include/qgemv.h).
+
+Argument marshalling only: every step of the product runs in the CUDA library
+``_build/libqgemv.so``.  If the library is missing this module raises; there
+is no CPU or PyTorch fallback.
+
+The module-level functions carry the C names and take raw pointers/ints.
+``QGemv`` is a convenience wrapper that takes torch CUDA tensors, keeps the
+borrowed weight tensors alive and passes ``torch.cuda.current_stream()``.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(PKG, "_build", "libqgemv.so")
+
+Q4_K = 12
+Q5_K = 13
+Q6_K = 14
+NVFP4_W4A16 = 256
+
+OUT_F16 = 0
+OUT_F32 = 1
+
+FLAG_FORCE_REFERENCE = 1
+FLAG_DEBUG_SYNC = 2
+FLAG_NO_FALLBACK = 4
+
+OK = 0
+STATUS_NAMES = {0: "QG_OK", -1: "QG_EINVAL", -2: "QG_EUNSUPPORTED", -3: "QG_EALIGN",
+                -4: "QG_ECUDA", -5: "QG_ENOMEM", -6: "QG_EFAULT_INJECTED"}
+
+#: every symbol include/qgemv.h declares
+EXPORTS = ["qgemv_create", "qgemv_run", "qgemv_run_add", "qgemv_pair_run", "qgemv_triple_run",
+           "qgemv_run_host", "qgemv_dequantize", "qgemv_destroy", "qgemv_last_error",
+           "qgemv_row_bytes", "qgemv_plan_info", "qgemv_describe"]
+
+
+class QgOpts(ctypes.Structure):
+    _fields_ = [("flags", ctypes.c_uint32), ("max_tokens", ctypes.c_int32)]
+
+
+class QgemvError(RuntimeError):
+    def __init__(self, status: int, what: str, message: str):
+        super().__init__(f"{what}: {STATUS_NAMES.get(status, status)}: {message}")
+        self.status = status
+
+
+_lib = None
+
+
+def load(path: str = LIB_PATH) -> ctypes.CDLL:
+    """Load libqgemv.so (built by ``skinny_gemm_q4_gb300.build``)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(path):
+        raise RuntimeError(f"CUDA library {path} is not built; run "
+                           "`python -m skinny_gemm_q4_gb300.build` first")
+    lib = ctypes.CDLL(path)
+    vp, i64, i32, c_int = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int32, ctypes.c_int
+    lib.qgemv_create.argtypes = [ctypes.POINTER(vp), c_int, i64, i64, vp, vp, ctypes.c_float,
+                                 ctypes.POINTER(QgOpts)]
+    lib.qgemv_run.argtypes = [vp, vp, i64, vp, c_int, vp]
+    lib.qgemv_run_add.argtypes = [vp, vp, i64, vp, vp, vp]
+    lib.qgemv_pair_run.argtypes = [vp, vp, vp, i64, vp, vp, c_int, vp]
+    lib.qgemv_triple_run.argtypes = [vp, vp, vp, vp, i64, vp, vp, vp, c_int, vp]
+    lib.qgemv_run_host.argtypes = [vp, vp, i64, vp, c_int, vp]
+    lib.qgemv_dequantize.argtypes = [vp, vp, vp]
+    lib.qgemv_destroy.argtypes = [vp]
+    lib.qgemv_destroy.restype = None
+    lib.qgemv_last_error.argtypes = []
+    lib.qgemv_last_error.restype = ctypes.c_char_p
+    lib.qgemv_row_bytes.argtypes = [c_int, i64]
+    lib.qgemv_row_bytes.restype = i64
+    lib.qgemv_plan_info.argtypes = [vp, i64, ctypes.POINTER(i32), ctypes.POINTER(i32),
+                                    ctypes.POINTER(i32)]
+    lib.qgemv_describe.argtypes = []
+    lib.qgemv_describe.restype = ctypes.c_char_p
+    for name in ("qgemv_create", "qgemv_run", "qgemv_run_add", "qgemv_pair_run",
+                 "qgemv_triple_run", "qgemv_run_host", "qgemv_dequantize", "qgemv_plan_info"):
+        getattr(lib, name).restype = c_int
+    _lib = lib
+    return lib
+
+
+# ----------------------------------------------------------- C-named calls
+
+def qgemv_last_error() -> str:
+    return load().qgemv_last_error().decode()
+
+
+def _check(status: int, what: str):
+    if status != OK:
+        raise QgemvError(status, what, qgemv_last_error())
+
+
+def qgemv_row_bytes(qtype: int, K: int) -> int:
+    return int(load().qgemv_row_bytes(qtype, K))
+
+
+def qgemv_describe() -> str:
+    return load().qgemv_describe().decode()
+
+
+def qgemv_create(qtype: int, M: int, K: int, w_ptr: int, scales_ptr: int = 0,
+                 global_scale: float = 1.0, flags: int = 0, max_tokens: int = 0) -> int:
+    h = ctypes.c_void_p()
+    opts = QgOpts(flags, max_tokens)
+    _check(load().qgemv_create(ctypes.byref(h), qtype, M, K, w_ptr or None, scales_ptr or None,
+                               global_scale, ctypes.byref(opts)), "qgemv_create")
+    return h.value
+
+
+def qgemv_destroy(h: int):
+    if h:
+        load().qgemv_destroy(h)
+
+
+def qgemv_run(h, x_ptr, N, y_ptr, ydt, stream):
+    _check(load().qgemv_run(h, x_ptr, N, y_ptr, ydt, stream), "qgemv_run")
+
+
+def qgemv_run_add(h, x_ptr, N, res_ptr, y_ptr, stream):
+    _check(load().qgemv_run_add(h, x_ptr, N, res_ptr, y_ptr, stream), "qgemv_run_add")
+
+
+def qgemv_pair_run(a, b, x_ptr, N, ya, yb, ydt, stream):
+    _check(load().qgemv_pair_run(a, b, x_ptr, N, ya, yb, ydt, stream), "qgemv_pair_run")
+
+
+def qgemv_triple_run(a, b, c, x_ptr, N, ya, yb, yc, ydt, stream):
+    _check(load().qgemv_triple_run(a, b, c, x_ptr, N, ya, yb, yc, ydt, stream),
+           "qgemv_triple_run")
+
+
+def qgemv_run_host(h, x_host_ptr, N, y_host_ptr, ydt, stream):
+    _check(load().qgemv_run_host(h, x_host_ptr, N, y_host_ptr, ydt, stream), "qgemv_run_host")
+
+
+def qgemv_dequantize(h, w_out_ptr, stream):
+    _check(load().qgemv_dequantize(h, w_out_ptr, stream), "qgemv_dequantize")
+
+
+def qgemv_plan_info(h, N):
+    ks, rows, launches = ctypes.c_int32(), ctypes.c_int32(), ctypes.c_int32()
+    _check(load().qgemv_plan_info(h, N, ctypes.byref(ks), ctypes.byref(rows),
+                                  ctypes.byref(launches)), "qgemv_plan_info")
+    return ks.value, rows.value, launches.value
+
+
+# ----------------------------------------------------- torch convenience
+
+def _stream_ptr(stream=None) -> int:
+    import torch
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return s.cuda_stream
+
+
+class QGemv:
+    """One weight matrix on the device (borrowed torch uint8 tensors)."""
+
+    def __init__(self, qtype: int, M: int, K: int, w, scales=None, global_scale: float = 1.0,
+                 flags: int = 0, max_tokens: int = 0):
+        self.qtype, self.M, self.K = qtype, M, K
+        self._w, self._scales = w, scales      # keep the borrowed buffers alive
+        self.h = qgemv_create(qtype, M, K, w.data_ptr(),
+                              scales.data_ptr() if scales is not None else 0,
+                              global_scale, flags, max_tokens)
+
+    def close(self):
+        if getattr(self, "h", None):
+            qgemv_destroy(self.h)
+            self.h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    def _y(self, N, out_f32, y):
+        import torch
+        if y is None:
+            y = torch.empty((N, self.M), dtype=torch.float32 if out_f32 else torch.float16,
+                            device=self._w.device)
+        return y
+
+    def run(self, x, y=None, out_f32: bool = False, stream=None):
+        N = x.shape[0]
+        y = self._y(N, out_f32, y)
+        qgemv_run(self.h, x.data_ptr(), N, y.data_ptr(), OUT_F32 if out_f32 else OUT_F16,
+                  _stream_ptr(stream))
+        return y
+
+    def run_add(self, x, residual, y=None, stream=None):
+        N = x.shape[0]
+        y = self._y(N, False, y)
+        qgemv_run_add(self.h, x.data_ptr(), N, residual.data_ptr(), y.data_ptr(),
+                      _stream_ptr(stream))
+        return y
+
+    def dequantize(self, stream=None):
+        import torch
+        w = torch.empty((self.M, self.K), dtype=torch.float32, device=self._w.device)
+        qgemv_dequantize(self.h, w.data_ptr(), _stream_ptr(stream))
+        return w
+
+    def run_host(self, x_host, y_host, out_f32: bool = False, stream=None):
+        qgemv_run_host(self.h, x_host.data_ptr(), x_host.shape[0], y_host.data_ptr(),
+                       OUT_F32 if out_f32 else OUT_F16, _stream_ptr(stream))
+        return y_host
+
+    def plan_info(self, N: int):
+        return qgemv_plan_info(self.h, N)
+
+
+def pair_run(a: QGemv, b: QGemv, x, out_f32: bool = False, stream=None):
+    N = x.shape[0]
+    ya, yb = a._y(N, out_f32, None), b._y(N, out_f32, None)
+    qgemv_pair_run(a.h, b.h, x.data_ptr(), N, ya.data_ptr(), yb.data_ptr(),
+                   OUT_F32 if out_f32 else OUT_F16, _stream_ptr(stream))
+    return ya, yb
+
+
+def triple_run(a: QGemv, b: QGemv, c: QGemv, x, out_f32: bool = False, stream=None):
+    N = x.shape[0]
+    ya, yb, yc = a._y(N, out_f32, None), b._y(N, out_f32, None), c._y(N, out_f32, None)
+    qgemv_triple_run(a.h, b.h, c.h, x.data_ptr(), N, ya.data_ptr(), yb.data_ptr(),
+                     yc.data_ptr(), OUT_F32 if out_f32 else OUT_F16, _stream_ptr(stream))
+    return ya, yb, yc

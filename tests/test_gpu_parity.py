@@ -1,0 +1,212 @@
+"""GPU parity: the CUDA path through the C ABI against the CPU oracle, element
+by element, on seeded inputs that span several tiles, K-split ranks and ragged
+row tails; bit-exact checks where the arithmetic is exact."""
+import numpy as np
+import pytest
+
+import oracle
+from gpu_util import canon, check_close, make_matrix, to_dev, torch
+from skinny_gemm_q4_gb300 import qgemv as qg
+from skinny_gemm_q4_gb300 import synth
+
+pytestmark = pytest.mark.gpu
+
+TYPES = [qg.Q4_K, qg.Q5_K, qg.Q6_K, qg.NVFP4_W4A16]
+ORTYPE = {qg.Q4_K: oracle.Q4_K, qg.Q5_K: oracle.Q5_K, qg.Q6_K: oracle.Q6_K,
+          qg.NVFP4_W4A16: oracle.NVFP4}
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    from skinny_gemm_q4_gb300 import build
+    build.build()
+    t = torch()
+    assert t.cuda.is_available(), "GPU tests need a CUDA device"
+
+
+@pytest.mark.parametrize("qtype", TYPES)
+@pytest.mark.parametrize("M,K", [(37, 768), (130, 2560)])
+def test_dequantize_bit_exact(qtype, M, K):
+    h, w, sc, g = make_matrix(qtype, M, K, seed=3)
+    wd = h.dequantize()
+    torch().cuda.synchronize()
+    ref = oracle.dequantize(ORTYPE[qtype], w, M, K, scales=sc, global_scale=g)
+    got = canon(wd.cpu().numpy())
+    assert np.array_equal(got.view(np.uint32), canon(ref).view(np.uint32))
+
+
+@pytest.mark.parametrize("qtype", TYPES)
+def test_fast_path_one_hot_is_the_exact_weight(qtype):
+    """K = 256, x = e_k for all 256 k (two token chunks of 128): the fast
+    product returns w[m][k] bit for bit (a single exact product, one final
+    rounding), so the fast decoders equal the oracle's dequantization."""
+    M, K = 21, 256
+    h, w, sc, g = make_matrix(qtype, M, K, seed=4)
+    x = np.eye(K, dtype=np.float16)
+    y = h.run(to_dev(x), out_f32=True)
+    torch().cuda.synchronize()
+    ref = oracle.dequantize(ORTYPE[qtype], w, M, K, scales=sc, global_scale=g)
+    assert np.array_equal(canon(y.cpu().numpy()).view(np.uint32),
+                          canon(ref.T).view(np.uint32))
+
+
+CASES = [
+    (qg.Q4_K, 300, 2560), (qg.Q4_K, 77, 4096),
+    (qg.Q5_K, 130, 4096), (qg.Q5_K, 64, 1536),
+    (qg.Q6_K, 200, 2560), (qg.Q6_K, 45, 9728),
+    (qg.NVFP4_W4A16, 150, 5120), (qg.NVFP4_W4A16, 33, 768),
+]
+
+
+@pytest.mark.parametrize("qtype,M,K", CASES)
+@pytest.mark.parametrize("N", [1, 3, 8, 13, 32, 40])
+def test_product_matches_oracle(qtype, M, K, N):
+    h, w, sc, g = make_matrix(qtype, M, K, seed=5)
+    x = synth.activations(N, K, seed=5, duplicate_rows=True)
+    yref, mag = oracle.qgemv(ORTYPE[qtype], w, M, K, x, scales=sc, global_scale=g)
+    xd = to_dev(x)
+    y32 = h.run(xd, out_f32=True)
+    y16 = h.run(xd, out_f32=False)
+    torch().cuda.synchronize()
+    check_close(y32.cpu().numpy(), yref, mag, what=f"fp32 {qtype} {M}x{K} N={N}")
+    check_close(y16.float().cpu().numpy(), yref, mag, fp16_out=True,
+                what=f"fp16 {qtype} {M}x{K} N={N}")
+    # fp16 output is the fp32 result rounded once
+    assert np.array_equal(y16.cpu().numpy(), y32.half().cpu().numpy())
+
+
+@pytest.mark.parametrize("qtype,M,K", [(qg.Q4_K, 9728, 2560), (qg.Q5_K, 2560, 9728),
+                                       (qg.Q6_K, 1024, 2560), (qg.NVFP4_W4A16, 7168, 5120)])
+def test_row_invariance_twins(qtype, M, K):
+    """TandemLLM verify-twin rule: an N-row call equals N one-row calls bit
+    for bit, N = 2..32, with rows that share inputs."""
+    h, w, sc, g = make_matrix(qtype, M, K, seed=6)
+    x = synth.activations(32, K, seed=6, duplicate_rows=True)
+    xd = to_dev(x)
+    singles = [h.run(xd[n:n + 1], out_f32=True) for n in range(32)]
+    one = torch().cat(singles).cpu().numpy()
+    for N in range(2, 33):
+        yN = h.run(xd[:N], out_f32=True).cpu().numpy()
+        assert np.array_equal(yN.view(np.uint32), one[:N].view(np.uint32)), f"N={N}"
+    # duplicated inputs give duplicated outputs
+    assert np.array_equal(one[2], one[0])
+    # N >= 33 (next chunking regime) keeps the same bits too
+    y40 = h.run(to_dev(np.concatenate([x, x[:8]])), out_f32=True).cpu().numpy()
+    assert np.array_equal(y40[:32].view(np.uint32), one.view(np.uint32))
+
+
+@pytest.mark.parametrize("qtype", [qg.Q4_K, qg.Q6_K, qg.NVFP4_W4A16])
+def test_sign_and_power_of_two_scaling_exact(qtype):
+    M, K = 96, 2560 if qtype != qg.NVFP4_W4A16 else 5120
+    h, w, sc, g = make_matrix(qtype, M, K, seed=7)
+    x = synth.activations(5, K, seed=7)
+    y = h.run(to_dev(x), out_f32=True).cpu().numpy()
+    yn = h.run(to_dev(-x), out_f32=True).cpu().numpy()
+    y4 = h.run(to_dev((x.astype(np.float32) * 4).astype(np.float16)), out_f32=True).cpu().numpy()
+    assert np.array_equal(yn, -y)
+    assert np.array_equal(y4, 4 * y)
+
+
+def test_q4k_all_q_zero_min_term():
+    """All q = 0 with uniform mins: y = -dmin * m * sum(x) (within tolerance)."""
+    from packers import pack_q4k_block
+    M, K, N = 64, 2560, 4
+    blk = pack_q4k_block(0.01171875, 0.0078125, [17] * 8, [37] * 8, np.zeros(256, dtype=np.int64))
+    w = np.tile(blk, (M, K // 256))
+    t = torch()
+    h = qg.QGemv(qg.Q4_K, M, K, t.from_numpy(w).cuda())
+    x = synth.activations(N, K, seed=8)
+    y = h.run(to_dev(x), out_f32=True).cpu().numpy()
+    expect = -0.0078125 * 37 * x.astype(np.float64).sum(axis=1)
+    mag = 0.0078125 * 37 * np.abs(x.astype(np.float64)).sum(axis=1)
+    check_close(y, np.repeat(expect[:, None], M, 1), np.repeat(mag[:, None], M, 1))
+
+
+@pytest.mark.parametrize("inplace", [False, True])
+def test_run_add_residual(inplace):
+    M, K, N = 2560, 4096, 3
+    h, w, sc, g = make_matrix(qg.Q4_K, M, K, seed=9)
+    x = synth.activations(N, K, seed=9)
+    r = synth.residual(N, M, seed=9)
+    yref, mag = oracle.qgemv(oracle.Q4_K, w, M, K, x, residual=r)
+    rd = to_dev(r)
+    y = rd if inplace else torch().empty_like(rd)
+    h.run_add(to_dev(x), rd, y)
+    check_close(y.float().cpu().numpy(), yref, mag, fp16_out=True, what="run_add")
+
+
+def test_pair_and_mixed_triple_equal_separate_calls():
+    K, N = 2560, 5
+    a, wa, _, _ = make_matrix(qg.Q4_K, 4096, K, seed=10, stream=1)
+    b, wb, _, _ = make_matrix(qg.Q4_K, 1024, K, seed=10, stream=2)
+    c, wc, _, _ = make_matrix(qg.Q6_K, 1024, K, seed=10, stream=3)
+    x = synth.activations(N, K, seed=10)
+    xd = to_dev(x)
+    ya, yb, yc = qg.triple_run(a, b, c, xd, out_f32=True)
+    for hnd, y, w, t in ((a, ya, wa, oracle.Q4_K), (b, yb, wb, oracle.Q4_K), (c, yc, wc, oracle.Q6_K)):
+        sep = hnd.run(xd, out_f32=True)
+        assert torch().equal(y, sep)
+        yref, mag = oracle.qgemv(t, w, hnd.M, K, x)
+        check_close(y.cpu().numpy(), yref, mag, what="triple")
+    p1, w1, _, _ = make_matrix(qg.Q4_K, 9728, K, seed=11, stream=4)
+    p2, w2, _, _ = make_matrix(qg.Q4_K, 9728, K, seed=11, stream=5)
+    y1, y2 = qg.pair_run(p1, p2, xd)
+    assert torch().equal(y1, p1.run(xd)) and torch().equal(y2, p2.run(xd))
+    rows = np.arange(0, 9728, 97)
+    yref, mag = oracle.qgemv(oracle.Q4_K, w2, 9728, K, x, rows=rows)
+    check_close(y2.float().cpu().numpy()[:, rows], yref, mag, fp16_out=True, what="pair")
+
+
+def test_reference_kernel_and_fallback(monkeypatch):
+    M, K, N = 160, 2560, 6
+    t = torch()
+    w, _, _ = synth.weights(qg.Q4_K, M, K, seed=12, stream=1)
+    wd = t.from_numpy(w).cuda()
+    x = synth.activations(N, K, seed=12)
+    yref, mag = oracle.qgemv(oracle.Q4_K, w, M, K, x)
+    ref = qg.QGemv(qg.Q4_K, M, K, wd, flags=qg.FLAG_FORCE_REFERENCE)
+    check_close(ref.run(to_dev(x), out_f32=True).cpu().numpy(), yref, mag, what="reference")
+    monkeypatch.setenv("QGEMV_FAULT_INJECT", "launch")
+    fb = qg.QGemv(qg.Q4_K, M, K, wd)
+    y = fb.run(to_dev(x), out_f32=True)
+    t.cuda.synchronize()
+    assert "reference" in qg.qgemv_last_error()
+    check_close(y.cpu().numpy(), yref, mag, what="fallback")
+    strict = qg.QGemv(qg.Q4_K, M, K, wd, flags=qg.FLAG_NO_FALLBACK)
+    with pytest.raises(qg.QgemvError) as ei:
+        strict.run(to_dev(x))
+    assert ei.value.status == -6
+    monkeypatch.setenv("QGEMV_FAULT_INJECT", "create")
+    with pytest.raises(qg.QgemvError) as ei:
+        qg.QGemv(qg.Q4_K, M, K, wd)
+    assert ei.value.status == -6
+
+
+def test_run_host_matches_device_path():
+    M, K, N = 512, 2560, 4
+    h, w, sc, g = make_matrix(qg.Q4_K, M, K, seed=13)
+    x = synth.activations(N, K, seed=13)
+    t = torch()
+    xh = t.from_numpy(x).pin_memory()
+    yh = t.empty((N, M), dtype=t.float16).pin_memory()
+    h.run_host(xh, yh)
+    yd = h.run(to_dev(x))
+    t.cuda.synchronize()
+    assert t.equal(yh, yd.cpu())
+
+
+def test_argument_errors_are_statuses():
+    M, K = 64, 2560
+    h, w, sc, g = make_matrix(qg.Q4_K, M, K, seed=14)
+    t = torch()
+    x = t.zeros((2, K), dtype=t.float16, device="cuda")
+    y = t.zeros((2, M), dtype=t.float16, device="cuda")
+    lib = qg.load()
+    assert lib.qgemv_run(h.h, x.data_ptr(), 0, y.data_ptr(), 0, None) == -1
+    assert lib.qgemv_run(h.h, x.data_ptr() + 2, 1, y.data_ptr(), 0, None) == -3
+    assert lib.qgemv_run(h.h, None, 1, y.data_ptr(), 0, None) == -1
+    other, _, _, _ = make_matrix(qg.Q4_K, 64, 4096, seed=14)
+    assert lib.qgemv_pair_run(h.h, other.h, x.data_ptr(), 1, y.data_ptr(), x.data_ptr(), 0,
+                              None) == -1
+    ks, rows, launches = h.plan_info(1)
+    assert ks == 2 and rows == 64 and launches == 2
