@@ -85,9 +85,10 @@ typedef struct qg_handle qg_handle;
  *   M, K         rows (outputs) and columns (reduction length); M >= 1,
  *                K >= 256 and K % 256 == 0 for every format
  *   w_dev        device pointer to the packed matrix (row-major rows of
- *                qgemv_row_bytes(t, K) bytes).  Q4_K/Q5_K/NVFP4 need 16-byte
- *                alignment; Q6_K needs 2-byte alignment (its 210-byte blocks
- *                are staged through 16-byte aligned supersets).
+ *                qgemv_row_bytes(t, K) bytes), 16-byte aligned.  (Inside a
+ *                Q6_K matrix the 210-byte blocks are not aligned; they are
+ *                staged through 16-byte aligned supersets and no byte outside
+ *                the matrix is read.)
  *   scales_dev   NVFP4 only: e4m3 scales [M][K/16], 16-byte aligned; else NULL
  *   global_scale NVFP4 only: per-tensor fp32 scale; ignored otherwise
  *   opts         nullable
@@ -145,6 +146,13 @@ const char *qgemv_last_error(void);
 /* Bytes per row of the packed matrix (codes only for NVFP4); -1 if K is not
  * supported for the format.  Pure host function. */
 int64_t qgemv_row_bytes(qg_type t, int64_t K);
+
+/* Read (and with clear != 0, reset) the handle's device error word.  The
+ * kernels never trap: a bounded wait that runs out (a pipeline that stopped
+ * making progress) sets bit 1 (consumer side) or bit 2 (producer side) and
+ * the kernel returns with undefined results.  Synchronous (a device-to-host
+ * copy of 4 bytes).  *flags_out == 0 means no kernel reported a problem. */
+qg_status qgemv_device_status(qg_handle *h, uint32_t *flags_out, int clear);
 
 /* Launch plan of a handle, for tests and profiling: number of K-split ranks
  * (a cluster of CTAs per row tile, combined in rank order), rows per CTA for

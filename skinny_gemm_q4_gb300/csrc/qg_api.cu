@@ -27,6 +27,7 @@ struct qg_handle {
     int ks;        // K-split ranks, fixed by K
     int layout;    // staged-x layout this format reads
     uint8_t *xs;   // staging buffer: max_tokens * nb * kXTok bytes
+    unsigned int *err;  // device error word written by the kernels (timeouts)
     int device;
     void *hx;      // device buffers of the host-pointer entry point
     size_t hx_cap;
@@ -113,6 +114,43 @@ int groups_for(int64_t n) { return n >= 32 ? 4 : (int)((n + 7) / 8); }
 
 int rows_per_cta(int G) { return G <= 2 ? Cfg<1>::ROWS : Cfg<4>::ROWS; }
 
+int rb_of_tset(int tset)
+{
+    int rb = 0;
+    if (tset & TS_Q4K) rb = rb > Fmt<T_Q4K>::RB ? rb : Fmt<T_Q4K>::RB;
+    if (tset & TS_Q5K) rb = rb > Fmt<T_Q5K>::RB ? rb : Fmt<T_Q5K>::RB;
+    if (tset & TS_Q6K) rb = rb > Fmt<T_Q6K>::RB ? rb : Fmt<T_Q6K>::RB;
+    if (tset & TS_FP4) rb = rb > Fmt<T_FP4>::RB ? rb : Fmt<T_FP4>::RB;
+    return rb;
+}
+
+// Rows per CTA of the N <= 8 kernel: 128 (eight consumer warps) while the
+// weight ring stays within ~100 KB, halved while the grid would leave SMs idle.
+// Any choice gives the same bits: it only moves rows between CTAs.
+int gemv_rows(int tset, const int64_t *Ms, int nm, int ks)
+{
+    int R = (kGemvStages * 128 * rb_of_tset(tset) <= 100 * 1024) ? 128 : 64;
+    auto ctas = [&](int r) {
+        int64_t c = 0;
+        for (int i = 0; i < nm; ++i) c += (Ms[i] + r - 1) / r;
+        return c * ks;
+    };
+    while (R > 32 && ctas(R) < 148) R /= 2;
+    return R;
+}
+
+cudaError_t launch_gemv_tset(int tset, int cw, const Params &p, dim3 grid, int smem, cudaStream_t s)
+{
+    switch (tset) {
+    case TS_Q4K: return launch_gemv_q4k(cw, p, grid, smem, s);
+    case TS_Q5K: return launch_gemv_q5k(cw, p, grid, smem, s);
+    case TS_Q6K: return launch_gemv_q6k(cw, p, grid, smem, s);
+    case TS_FP4: return launch_gemv_fp4(cw, p, grid, smem, s);
+    case TS_Q4K | TS_Q6K: return launch_gemv_q4k_q6k(cw, p, grid, smem, s);
+    default: return cudaErrorInvalidValue;
+    }
+}
+
 Mat mat_of(const qg_handle *h, void *y, const __half *res)
 {
     Mat m;
@@ -179,18 +217,6 @@ qg_status run_product(qg_handle *const *hs, int nh, const __half *x, int64_t N, 
             }
             continue;
         }
-        // Stage x once per layout.
-        uint8_t *xl[XL_COUNT] = {nullptr, nullptr, nullptr};
-        for (int i = 0; i < nh; ++i)
-            if (!xl[hs[i]->layout]) xl[hs[i]->layout] = hs[i]->xs;
-        if (fault_at("stage")) return fail(QG_EFAULT_INJECTED, "injected fault: staging launch");
-        const int64_t tok_stride = (int64_t)h0->nb * kXTok;
-        cudaError_t e = launch_stage(xc, n, (int)h0->K, h0->nb, tok_stride, xl[XL_Q4], xl[XL_Q6],
-                                     xl[XL_FP4], s);
-        if (e != cudaSuccess) return cuda_fail(e, "staging kernel launch");
-
-        const int G = groups_for(n);
-        const int rows = rows_per_cta(G);
         // Groups of handles that one kernel serves.
         int groups[3][3];
         int gsize[3] = {0, 0, 0};
@@ -204,6 +230,72 @@ qg_status run_product(qg_handle *const *hs, int nh, const __half *x, int64_t N, 
                 gsize[ng++] = 1;
             }
         }
+        if (n <= 8) {
+            // N <= 8: one kernel per group, x staged inside the kernel.
+            for (int gidx = 0; gidx < ng; ++gidx) {
+                Params p;
+                memset(&p, 0, sizeof p);
+                int gts = 0;
+                int64_t Ms[3];
+                for (int j = 0; j < gsize[gidx]; ++j) {
+                    gts |= tset_bit(hs[groups[gidx][j]]->type);
+                    Ms[j] = hs[groups[gidx][j]]->M;
+                }
+                const int R = gemv_rows(gts, Ms, gsize[gidx], h0->ks);
+                int tiles = 0;
+                for (int j = 0; j < gsize[gidx]; ++j) {
+                    const int idx = groups[gidx][j];
+                    const qg_handle *h = hs[idx];
+                    p.mat[j] = mat_of(h, (uint8_t *)ys[idx] + c0 * h->M * (out_f32 ? 4 : 2),
+                                      res ? res + c0 * h->M : nullptr);
+                    p.mat[j].tile_begin = tiles;
+                    tiles += (int)((h->M + R - 1) / R);
+                }
+                p.nmat = gsize[gidx];
+                p.x = xc;
+                p.N = n;
+                p.K = (int)h0->K;
+                p.nb = h0->nb;
+                p.ks = h0->ks;
+                p.rows_cta = R;
+                const int nsbr = (h0->nb + h0->ks - 1) / h0->ks;
+                p.xtok = gemv_xtok(nsbr);
+                p.out_f32 = out_f32;
+                p.err = h0->err;
+                const int smem = gemv_smem_bytes(rb_of_tset(gts), R, n, nsbr);
+                const dim3 grid((unsigned)p.ks, (unsigned)tiles, 1u);
+                cudaError_t le = fault_at("launch")
+                                     ? cudaErrorLaunchOutOfResources
+                                     : launch_gemv_tset(gts, R / 16, p, grid, smem, s);
+                if (le != cudaSuccess) {
+                    cudaGetLastError();
+                    if (flags & QG_FLAG_NO_FALLBACK) {
+                        if (fault_at("launch"))
+                            return fail(QG_EFAULT_INJECTED, "injected fault: product launch");
+                        return cuda_fail(le, "product kernel launch");
+                    }
+                    for (int j = 0; j < p.nmat; ++j) {
+                        cudaError_t re = launch_ref_gemv(p.mat[j], (int)h0->K, xc, n, out_f32, s);
+                        if (re != cudaSuccess) return cuda_fail(re, "reference kernel launch");
+                    }
+                    fail(QG_OK, "fast path launch failed (%s); used the reference kernel",
+                         cudaGetErrorName(le));
+                }
+            }
+            continue;
+        }
+        // Stage x once per layout.
+        uint8_t *xl[XL_COUNT] = {nullptr, nullptr, nullptr};
+        for (int i = 0; i < nh; ++i)
+            if (!xl[hs[i]->layout]) xl[hs[i]->layout] = hs[i]->xs;
+        if (fault_at("stage")) return fail(QG_EFAULT_INJECTED, "injected fault: staging launch");
+        const int64_t tok_stride = (int64_t)h0->nb * kXTok;
+        cudaError_t e = launch_stage(xc, n, (int)h0->K, h0->nb, tok_stride, xl[XL_Q4], xl[XL_Q6],
+                                     xl[XL_FP4], s);
+        if (e != cudaSuccess) return cuda_fail(e, "staging kernel launch");
+
+        const int G = groups_for(n);
+        const int rows = rows_per_cta(G);
         for (int gidx = 0; gidx < ng; ++gidx) {
             Params p;
             memset(&p, 0, sizeof p);
@@ -224,7 +316,9 @@ qg_status run_product(qg_handle *const *hs, int nh, const __half *x, int64_t N, 
             p.tok_base = 0;
             p.nb = h0->nb;
             p.ks = h0->ks;
+            p.K = (int)h0->K;
             p.out_f32 = out_f32;
+            p.err = h0->err;
             const dim3 grid((unsigned)p.ks, (unsigned)tiles, (unsigned)((n + kTokChunk - 1) / kTokChunk));
             cudaError_t le;
             if (fault_at("launch")) {
@@ -252,6 +346,10 @@ qg_status run_product(qg_handle *const *hs, int nh, const __half *x, int64_t N, 
         cudaError_t e = cudaStreamSynchronize(s);
         if (e == cudaSuccess) e = cudaGetLastError();
         if (e != cudaSuccess) return cuda_fail(e, "debug synchronize");
+        unsigned int w = 0;
+        e = cudaMemcpy(&w, h0->err, sizeof w, cudaMemcpyDeviceToHost);
+        if (e != cudaSuccess) return cuda_fail(e, "error word read");
+        if (w) return fail(QG_ECUDA, "kernel reported a bounded-wait timeout (0x%x)", w);
     }
     return QG_OK;
 }
@@ -350,6 +448,14 @@ qg_status qgemv_create(qg_handle **out, qg_type t, int64_t M, int64_t K, const v
         delete h;
         return fail(QG_ENOMEM, "staging buffer allocation of %zu bytes failed", xs_bytes);
     }
+    e = cudaMalloc((void **)&h->err, sizeof(unsigned int));
+    if (e == cudaSuccess) e = cudaMemset(h->err, 0, sizeof(unsigned int));
+    if (e != cudaSuccess) {
+        cudaGetLastError();
+        cudaFree(h->xs);
+        delete h;
+        return fail(QG_ENOMEM, "error word allocation failed");
+    }
     *out = h;
     return QG_OK;
 }
@@ -358,6 +464,7 @@ void qgemv_destroy(qg_handle *h)
 {
     if (!h) return;
     if (h->xs) cudaFree(h->xs);
+    if (h->err) cudaFree(h->err);
     if (h->hx) cudaFree(h->hx);
     if (h->hy) cudaFree(h->hy);
     delete h;
@@ -467,6 +574,20 @@ qg_status qgemv_dequantize(qg_handle *h, float *w_out, void *stream)
     return QG_OK;
 }
 
+qg_status qgemv_device_status(qg_handle *h, uint32_t *flags_out, int clear)
+{
+    if (!h) return fail(QG_EINVAL, "null handle");
+    unsigned int w = 0;
+    cudaError_t e = cudaMemcpy(&w, h->err, sizeof w, cudaMemcpyDeviceToHost);
+    if (e != cudaSuccess) return cuda_fail(e, "error word read");
+    if (clear && w) {
+        e = cudaMemset(h->err, 0, sizeof(unsigned int));
+        if (e != cudaSuccess) return cuda_fail(e, "error word reset");
+    }
+    if (flags_out) *flags_out = w;
+    return QG_OK;
+}
+
 qg_status qgemv_plan_info(const qg_handle *h, int64_t N, int32_t *ksplit, int32_t *rows_cta,
                           int32_t *launches)
 {
@@ -476,8 +597,19 @@ qg_status qgemv_plan_info(const qg_handle *h, int64_t N, int32_t *ksplit, int32_
     const int64_t nfirst = N < h->max_tokens ? N : h->max_tokens;
     if (ksplit) *ksplit = h->ks;
     if (rows_cta) *rows_cta = rows_per_cta(groups_for(nfirst));
-    if (launches)
-        *launches = (int32_t)((h->flags & QG_FLAG_FORCE_REFERENCE) ? chunks : 2 * chunks);
+    if (launches) {
+        int64_t l = 0;
+        for (int64_t c = 0; c < chunks; ++c) {
+            const int64_t n = (N - c * h->max_tokens) < h->max_tokens ? (N - c * h->max_tokens)
+                                                                      : h->max_tokens;
+            l += ((h->flags & QG_FLAG_FORCE_REFERENCE) || n <= 8) ? 1 : 2;
+        }
+        *launches = (int32_t)l;
+    }
+    if (rows_cta && nfirst <= 8 && !(h->flags & QG_FLAG_FORCE_REFERENCE)) {
+        const int64_t Ms[1] = {h->M};
+        *rows_cta = gemv_rows(tset_bit(h->type), Ms, 1, h->ks);
+    }
     return QG_OK;
 }
 

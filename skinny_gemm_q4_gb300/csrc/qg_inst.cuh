@@ -41,6 +41,45 @@ static cudaError_t launch_one(const Params &p, dim3 grid, cudaStream_t stream)
     return cudaLaunchKernelEx(&cfg, skinny_kernel<TSET, G>, p);
 }
 
+constexpr int kGemvMaxSmem = 200 * 1024;
+
+template <int TSET, int CW>
+static cudaError_t launch_gemv_one(const Params &p, dim3 grid, int smem, cudaStream_t stream)
+{
+    static int configured[64] = {0};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+    if (smem > kGemvMaxSmem) return cudaErrorInvalidValue;
+    if (!configured[dev]) {
+        e = cudaFuncSetAttribute(gemv_kernel<TSET, CW>,
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize, kGemvMaxSmem);
+        if (e != cudaSuccess) return e;
+        configured[dev] = 1;
+    }
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = dim3(32 * (CW + 1));
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[2];
+    int na = 0;
+    attr[na].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[na].val.programmaticStreamSerializationAllowed = 1;
+    ++na;
+    if (p.ks > 1) {
+        attr[na].id = cudaLaunchAttributeClusterDimension;
+        attr[na].val.clusterDim.x = (unsigned)p.ks;
+        attr[na].val.clusterDim.y = 1;
+        attr[na].val.clusterDim.z = 1;
+        ++na;
+    }
+    cfg.attrs = attr;
+    cfg.numAttrs = na;
+    return cudaLaunchKernelEx(&cfg, gemv_kernel<TSET, CW>, p);
+}
+
 }  // namespace qg
 
 #define QG_DEFINE_TSET(NAME, TSET)                                                          \
@@ -63,6 +102,15 @@ static cudaError_t launch_one(const Params &p, dim3 grid, cudaStream_t stream)
         case 3: return SmemMax<TSET, 3>::TOTAL;                                             \
         case 4: return SmemMax<TSET, 4>::TOTAL;                                             \
         default: return 0;                                                                  \
+        }                                                                                   \
+    }                                                                                       \
+    cudaError_t launch_gemv_##NAME(int cw, const Params &p, dim3 grid, int smem, cudaStream_t s) \
+    {                                                                                       \
+        switch (cw) {                                                                       \
+        case 2: return launch_gemv_one<TSET, 2>(p, grid, smem, s);                          \
+        case 4: return launch_gemv_one<TSET, 4>(p, grid, smem, s);                          \
+        case 8: return launch_gemv_one<TSET, 8>(p, grid, smem, s);                          \
+        default: return cudaErrorInvalidValue;                                              \
         }                                                                                   \
     }                                                                                       \
     }

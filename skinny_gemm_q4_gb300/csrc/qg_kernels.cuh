@@ -1,6 +1,5 @@
 // Skinny fused dequantize-and-multiply kernels: y[N x M] = x[N x K] . W^T for
-// Q4_K, Q5_K, Q6_K and NVFP4 weights, fp16 x, fp32 accumulation, N <= 32 per
-// launch chunk.
+// Q4_K, Q5_K, Q6_K and NVFP4 weights, fp16 x, fp32 accumulation.
 //
 // Scheme (one arithmetic path for every N, so a row's bits never depend on N;
 // TandemLLM "Kernels", Row invariance):
@@ -14,20 +13,26 @@
 //       NVFP4 A = e2m1 * e4m3            (hardware cvt, exact in fp16: six bits)
 //     (reflex-llm "docs/kernels.md": dequantize in registers, never write fp16
 //     weights; TandemLLM "Kernels", NVFP4 matrix products: e2m1*e4m3 is exact.)
-//   * Q4_K/Q5_K: per super-block one MMA chain D1 = sum A*x plus one MMA of the
-//     6-bit mins against the per-sub-block sums of x (split hi+lo in fp16),
-//     folded as acc = fma(d*2^14, D1, acc); acc = fma(-dmin*2^24, D2, acc).
+//   * Q4_K/Q5_K: per super-block two MMA chains D1a (low nibbles, sub-block
+//     2t) and D1b (high nibbles, 2t+1) plus one MMA of the 6-bit mins against
+//     the per-sub-block sums of x (split hi+lo in fp16), folded as
+//       acc = fma(d*2^14, D1a, acc); acc = fma(d*2^14, D1b, acc);
+//       acc = fma(-dmin*2^24, D2, acc).
 //     Q6_K: one MMA per 16-weight scale group, acc = fma(d*sc, D, acc).
-//     NVFP4: one MMA chain over all of K, times the global scale at the end.
+//     NVFP4: two MMA chains over all of K (even / odd steps), added at the
+//     end and multiplied by the global scale.
 //   * The K range is split over a cluster of `ks` CTAs fixed by K alone; the
 //     ranks' partial sums are added in rank order through distributed shared
-//     memory.  No atomics anywhere.
-//   * Weight tiles stream through a multi-stage cp.async (16-byte, L1-bypass)
-//     ring in shared memory; the 210-byte Q6_K blocks are copied as their
-//     16-byte-aligned supersets and decoded at their byte offset.
-//   * x arrives pre-arranged by the staging kernel (qg_stage.cu) in the
-//     B-fragment order of each format, so every B load is one conflict-free
-//     16-byte shared load.
+//     memory.  No atomics in the arithmetic.
+//   * x arrives in the B-fragment order of each format (stage_sb below), so
+//     every B load is one conflict-free 16-byte shared load.
+//
+// Two data-movement variants share the arithmetic above bit for bit:
+//   gemv_kernel   (N <= 8): a producer warp streams the weight tiles with 1-D
+//                 bulk copies (TMA) into an mbarrier ring; consumer warps
+//                 decode and multiply; x is staged inside the kernel.
+//   skinny_kernel (N > 8): 16-byte cp.async ring, x staged by a separate
+//                 kernel (qg_stage.cu) once per call.
 #pragma once
 
 #include "qg_ptx.cuh"
@@ -41,8 +46,11 @@ enum { XL_Q4 = 0, XL_Q6 = 1, XL_FP4 = 2, XL_COUNT = 3 };
 constexpr int kWarps = 4;
 constexpr int kThreads = 32 * kWarps;
 constexpr int kXTok = 576;     // staged bytes per (token, super-block): 512 x + 32 sums + pad
-constexpr int kTokChunk = 32;  // tokens per launch chunk
+constexpr int kTokChunk = 32;  // tokens per launch chunk (skinny_kernel)
 constexpr int kMaxMats = 3;
+
+// Error bits written to Params::err by a kernel (never trap).
+enum { ERR_FULL_TIMEOUT = 1, ERR_EMPTY_TIMEOUT = 2 };
 
 struct Mat {
     const uint8_t *w;      // packed weights (codes for NVFP4)
@@ -61,13 +69,18 @@ struct Mat {
 struct Params {
     Mat mat[kMaxMats];
     int nmat;
-    const uint8_t *xs[XL_COUNT];  // staged x per layout
+    const uint8_t *xs[XL_COUNT];  // staged x per layout (skinny_kernel)
     int64_t xs_tok_stride;        // bytes per token in the staged buffers (nb * kXTok)
-    int N;                        // tokens of this call
+    const __half *x;              // raw x [N][K] (gemv_kernel stages it itself)
+    int N;                        // tokens of this launch
     int tok_base;                 // first token of blockIdx.z == 0
+    int K;
     int nb;                       // 256-wide super-blocks along K
     int ks;                       // K-split ranks (cluster size along x)
+    int rows_cta;                 // rows per CTA (gemv_kernel)
+    int xtok;                     // token stride of the in-kernel x region (gemv_kernel)
     int out_f32;
+    unsigned int *err;            // error word (timeouts)
 };
 
 template <int T>
@@ -86,7 +99,9 @@ struct Fmt<T_Q6K> {
 };
 template <>
 struct Fmt<T_FP4> {
-    static constexpr int BB = 128, RB = 144, VPR = 9, XL = XL_FP4, XV = 32;
+    // row in shared memory: 128 code bytes, 16 scale bytes, 48 bytes of pad
+    // (a 192-byte pitch keeps the two rows of an 8-lane phase on disjoint banks)
+    static constexpr int BB = 128, RB = 192, VPR = 9, XL = XL_FP4, XV = 32;
 };
 
 template <int G>
@@ -116,6 +131,17 @@ struct SmemMax {
     static constexpr int TOTAL = ab > cd ? ab : cd;
 };
 
+template <int TSET>
+struct RBMax {
+    static constexpr int a = (TSET & TS_Q4K) ? Fmt<T_Q4K>::RB : 0;
+    static constexpr int b = (TSET & TS_Q5K) ? Fmt<T_Q5K>::RB : 0;
+    static constexpr int c = (TSET & TS_Q6K) ? Fmt<T_Q6K>::RB : 0;
+    static constexpr int d = (TSET & TS_FP4) ? Fmt<T_FP4>::RB : 0;
+    static constexpr int ab = a > b ? a : b;
+    static constexpr int cd = c > d ? c : d;
+    static constexpr int V = ab > cd ? ab : cd;
+};
+
 __device__ __forceinline__ uint32_t word_of(const uint4 &v, int i)
 {
     return i == 0 ? v.x : i == 1 ? v.y : i == 2 ? v.z : v.w;
@@ -127,6 +153,67 @@ __device__ __forceinline__ uint32_t lds32_any(uint32_t addr)
     uint32_t a0 = addr & ~3u;
     uint32_t lo = lds32(a0), hi = lds32(a0 + 4);
     return __funnelshift_r(lo, hi, (addr & 3u) * 8u);
+}
+
+// ---------------------------------------------------------------------------
+// x staging for one (token, super-block): lane l holds x[256 sb + 8l .. +8].
+// Writes the layouts that are non-null (generic addresses: global or shared).
+//   Q4 : 4-group q = 16t + 8e + j -> 16-byte unit ((j/2)*2 + e)*4 + t, half
+//        j&1, stored (x0, x2, x1, x3); bytes 512..543: for t = 0..3 the fp16
+//        (hi[2t], hi[2t+1], lo[2t], lo[2t+1]) of the sub-block sums
+//        S_s = sum of the 32 x of sub-block s (fp32: sequential within the
+//        lane, then a fixed butterfly), hi = fp16(S), lo = fp16(S - hi).
+//   Q6 : 4-group q = 32h + 8s + 4i + t -> unit (h*4 + s)*4 + t, half i,
+//        stored (x0, x2, x1, x3).
+//   FP4: the raw 8 values of lane l -> unit ((l/16)*4 + (l&3))*4 + ((l/4)&3).
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ void stage_sb(uint4 v, int lane, uint8_t *q4, uint8_t *q6, uint8_t *fp4)
+{
+    if (q4) {
+        uint4 o;
+        o.x = __byte_perm(v.x, v.y, 0x5410);
+        o.y = __byte_perm(v.x, v.y, 0x7632);
+        o.z = __byte_perm(v.z, v.w, 0x5410);
+        o.w = __byte_perm(v.z, v.w, 0x7632);
+        const int u = ((lane & 3) * 2 + ((lane >> 2) & 1)) * 4 + (lane >> 3);
+        *reinterpret_cast<uint4 *>(q4 + 16 * u) = o;
+        const uint32_t w4[4] = {v.x, v.y, v.z, v.w};
+        float s = 0.0f;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            s = __fadd_rn(s, __half2float(__ushort_as_half((unsigned short)(w4[i] & 0xffffu))));
+            s = __fadd_rn(s, __half2float(__ushort_as_half((unsigned short)(w4[i] >> 16))));
+        }
+        s = __fadd_rn(s, __shfl_xor_sync(0xffffffffu, s, 1));
+        s = __fadd_rn(s, __shfl_xor_sync(0xffffffffu, s, 2));
+        const __half hi = __float2half_rn(s);
+        const __half lo = __float2half_rn(__fsub_rn(s, __half2float(hi)));
+        const uint32_t hib = __half_as_ushort(hi), lob = __half_as_ushort(lo);
+        const uint32_t hin = __shfl_down_sync(0xffffffffu, hib, 4);
+        const uint32_t lon = __shfl_down_sync(0xffffffffu, lob, 4);
+        if ((lane & 7) == 0) {
+            uint2 o2;
+            o2.x = hib | (hin << 16);
+            o2.y = lob | (lon << 16);
+            *reinterpret_cast<uint2 *>(q4 + 512 + 8 * (lane >> 3)) = o2;
+        }
+    }
+    if (q6) {
+#pragma unroll
+        for (int hq = 0; hq < 2; ++hq) {
+            const int q = 2 * lane + hq;
+            const int h = q >> 5, s = (q >> 3) & 3, i = (q >> 2) & 1, t = q & 3;
+            const uint32_t a = hq ? v.z : v.x, b = hq ? v.w : v.y;
+            uint2 o2;
+            o2.x = __byte_perm(a, b, 0x5410);
+            o2.y = __byte_perm(a, b, 0x7632);
+            *reinterpret_cast<uint2 *>(q6 + 16 * ((h * 4 + s) * 4 + t) + 8 * i) = o2;
+        }
+    }
+    if (fp4) {
+        const int u = ((lane >> 4) * 4 + (lane & 3)) * 4 + ((lane >> 2) & 3);
+        *reinterpret_cast<uint4 *>(fp4 + 16 * u) = v;
+    }
 }
 
 // ---------------------------------------------------------------------------
@@ -169,14 +256,15 @@ __device__ __forceinline__ KRow k_row_consts(const uint4 &h, int t)
 }
 
 // ---------------------------------------------------------------------------
-// Per-stage compute, one function per format.  `acc` is [MT][G][4] in the
-// mma C-fragment layout: c0/c1 row g tokens 2t/2t+1, c2/c3 row g+8.
+// Per-super-block compute, one function per format.  wsl: this warp's first
+// weight row in shared memory (row pitch Fmt<T>::RB); xsl: this super-block's
+// staged x for token 0 (token stride xtok).  acc is [MT][G][4] in the mma
+// C-fragment layout: c0/c1 row g tokens 2t/2t+1, c2/c3 row g+8.
 // ---------------------------------------------------------------------------
-template <int T, int G>
-__device__ __forceinline__ void compute_kquant(uint32_t wsl, uint32_t xsl, int g, int t,
-                                               int ntok, float (&acc)[Cfg<G>::MT][G][4])
+template <int T, int MT, int G>
+__device__ __forceinline__ void compute_kquant(uint32_t wsl, uint32_t xsl, int xtok, int g, int t,
+                                               int ntok, float (&acc)[MT][G][4])
 {
-    constexpr int MT = Cfg<G>::MT;
     constexpr int RB = Fmt<T>::RB;
     constexpr int QS = (T == T_Q4K) ? 16 : 48;  // qs offset in the block
     KRow rc[MT][2];
@@ -197,23 +285,27 @@ __device__ __forceinline__ void compute_kquant(uint32_t wsl, uint32_t xsl, int g
             }
         }
     }
-    float d1[MT][G][4];
+    float d1[2][MT][G][4];
 #pragma unroll
-    for (int mt = 0; mt < MT; ++mt)
+    for (int e = 0; e < 2; ++e)
 #pragma unroll
-        for (int gi = 0; gi < G; ++gi)
+        for (int mt = 0; mt < MT; ++mt)
 #pragma unroll
-            for (int c = 0; c < 4; ++c) d1[mt][gi][c] = 0.0f;
+            for (int gi = 0; gi < G; ++gi)
+#pragma unroll
+                for (int c = 0; c < 4; ++c) d1[e][mt][gi][c] = 0.0f;
 
+    const bool tokok[G] = {};
+    (void)tokok;
 #pragma unroll
-    for (int e = 0; e < 2; ++e) {
+    for (int jp = 0; jp < 4; ++jp) {
 #pragma unroll
-        for (int jp = 0; jp < 4; ++jp) {
+        for (int e = 0; e < 2; ++e) {
             uint4 B[G];
 #pragma unroll
             for (int gi = 0; gi < G; ++gi) {
                 const int tok = 8 * gi + g;
-                B[gi] = (tok < ntok) ? lds128(xsl + tok * kXTok + ((jp * 2 + e) * 4 + t) * 16)
+                B[gi] = (tok < ntok) ? lds128(xsl + tok * xtok + ((jp * 2 + e) * 4 + t) * 16)
                                      : make_uint4(0u, 0u, 0u, 0u);
             }
 #pragma unroll
@@ -249,7 +341,7 @@ __device__ __forceinline__ void compute_kquant(uint32_t wsl, uint32_t xsl, int g
                     const uint32_t a3 = hmul2(p[1][1], s1);
 #pragma unroll
                     for (int gi = 0; gi < G; ++gi)
-                        mma16816(d1[mt][gi], a0, a1, a2, a3, jj ? B[gi].z : B[gi].x,
+                        mma16816(d1[e][mt][gi], a0, a1, a2, a3, jj ? B[gi].z : B[gi].x,
                                  jj ? B[gi].w : B[gi].y);
                 }
             }
@@ -259,7 +351,7 @@ __device__ __forceinline__ void compute_kquant(uint32_t wsl, uint32_t xsl, int g
 #pragma unroll
     for (int gi = 0; gi < G; ++gi) {
         const int tok = 8 * gi + g;
-        const uint2 bm = (tok < ntok) ? lds64(xsl + tok * kXTok + 512 + 8 * t) : make_uint2(0u, 0u);
+        const uint2 bm = (tok < ntok) ? lds64(xsl + tok * xtok + 512 + 8 * t) : make_uint2(0u, 0u);
 #pragma unroll
         for (int mt = 0; mt < MT; ++mt) {
             float d2[4];
@@ -268,19 +360,19 @@ __device__ __forceinline__ void compute_kquant(uint32_t wsl, uint32_t xsl, int g
 #pragma unroll
             for (int c = 0; c < 4; ++c) {
                 const KRow &r = rc[mt][c >> 1];
-                acc[mt][gi][c] = __fmaf_rn(r.dd, d1[mt][gi][c], acc[mt][gi][c]);
+                acc[mt][gi][c] = __fmaf_rn(r.dd, d1[0][mt][gi][c], acc[mt][gi][c]);
+                acc[mt][gi][c] = __fmaf_rn(r.dd, d1[1][mt][gi][c], acc[mt][gi][c]);
                 acc[mt][gi][c] = __fmaf_rn(r.dm, d2[c], acc[mt][gi][c]);
             }
         }
     }
 }
 
-template <int G>
-__device__ __forceinline__ void compute_q6k(uint32_t wsl, uint32_t xsl, int g, int t, int ntok,
-                                            const int (&boff)[Cfg<G>::MT][2],
-                                            float (&acc)[Cfg<G>::MT][G][4])
+template <int MT, int G>
+__device__ __forceinline__ void compute_q6k(uint32_t wsl, uint32_t xsl, int xtok, int g, int t,
+                                            int ntok, const int (&boff)[MT][2],
+                                            float (&acc)[MT][G][4])
 {
-    constexpr int MT = Cfg<G>::MT;
     constexpr int RB = Fmt<T_Q6K>::RB;
     uint32_t sw[MT][2][4];  // int8 scales, 4 per word
     float dq[MT][2];
@@ -319,7 +411,7 @@ __device__ __forceinline__ void compute_q6k(uint32_t wsl, uint32_t xsl, int g, i
                     const int tok = 8 * gi + g;
                     // unit (h, s, t) holds the 4-groups i = 0 and 1
                     B[gi] = (tok < ntok)
-                                ? lds64(xsl + tok * kXTok + ((h * 4 + s) * 4 + t) * 16 + 8 * i)
+                                ? lds64(xsl + tok * xtok + ((h * 4 + s) * 4 + t) * 16 + 8 * i)
                                 : make_uint2(0u, 0u);
                 }
                 const int grp = 8 * h + i + 2 * s;  // scale index
@@ -336,7 +428,8 @@ __device__ __forceinline__ void compute_q6k(uint32_t wsl, uint32_t xsl, int g, i
                         const uint32_t v = nw | (hw & 0x30303030u);
                         a[rr][0] = hsub2(__byte_perm(v, 0x6464u, 0x5240u), 0x64206420u);
                         a[rr][1] = hsub2(__byte_perm(v, 0x6464u, 0x5341u), 0x64206420u);
-                        const int scv = (int)(int8_t)((sw[mt][rr][grp >> 2] >> (8 * (grp & 3))) & 0xffu);
+                        const int scv =
+                            (int)(int8_t)((sw[mt][rr][grp >> 2] >> (8 * (grp & 3))) & 0xffu);
                         dsc[rr] = dq[mt][rr] * (float)scv;
                     }
 #pragma unroll
@@ -353,11 +446,11 @@ __device__ __forceinline__ void compute_q6k(uint32_t wsl, uint32_t xsl, int g, i
     }
 }
 
-template <int G>
-__device__ __forceinline__ void compute_fp4(uint32_t wsl, uint32_t xsl, int g, int t, int ntok,
-                                            float (&acc)[Cfg<G>::MT][G][4])
+// NVFP4: acc is [2][MT][G][4] (two chains: even and odd steps).
+template <int MT, int G>
+__device__ __forceinline__ void compute_fp4(uint32_t wsl, uint32_t xsl, int xtok, int g, int t,
+                                            int ntok, float (&acc)[2][MT][G][4])
 {
-    constexpr int MT = Cfg<G>::MT;
     constexpr int RB = Fmt<T_FP4>::RB;
 #pragma unroll
     for (int hf = 0; hf < 2; ++hf) {
@@ -382,7 +475,7 @@ __device__ __forceinline__ void compute_fp4(uint32_t wsl, uint32_t xsl, int g, i
 #pragma unroll
             for (int gi = 0; gi < G; ++gi) {
                 const int tok = 8 * gi + g;
-                B[gi] = (tok < ntok) ? lds128(xsl + tok * kXTok + ((hf * 4 + sp) * 4 + t) * 16)
+                B[gi] = (tok < ntok) ? lds128(xsl + tok * xtok + ((hf * 4 + sp) * 4 + t) * 16)
                                      : make_uint4(0u, 0u, 0u, 0u);
             }
 #pragma unroll
@@ -400,7 +493,7 @@ __device__ __forceinline__ void compute_fp4(uint32_t wsl, uint32_t xsl, int g, i
                     }
 #pragma unroll
                     for (int gi = 0; gi < G; ++gi)
-                        mma16816(acc[mt][gi], a[0][0], a[1][0], a[0][1], a[1][1],
+                        mma16816(acc[jj][mt][gi], a[0][0], a[1][0], a[0][1], a[1][1],
                                  jj ? B[gi].z : B[gi].x, jj ? B[gi].w : B[gi].y);
                 }
             }
@@ -408,9 +501,129 @@ __device__ __forceinline__ void compute_fp4(uint32_t wsl, uint32_t xsl, int g, i
     }
 }
 
-// ---------------------------------------------------------------------------
-// One CTA: ROWS rows of one matrix, super-blocks [sb0, sb1) of K.
-// ---------------------------------------------------------------------------
+// Per-CTA accumulator set: K-quants fold into one [MT][G][4]; NVFP4 keeps two
+// chains.  `finish` returns the rank partial sum of element (mt, gi, c).
+template <int T, int MT, int G>
+struct Acc {
+    float a[(T == T_FP4) ? 2 : 1][MT][G][4];
+    __device__ __forceinline__ void zero()
+    {
+#pragma unroll
+        for (int e = 0; e < ((T == T_FP4) ? 2 : 1); ++e)
+#pragma unroll
+            for (int mt = 0; mt < MT; ++mt)
+#pragma unroll
+                for (int gi = 0; gi < G; ++gi)
+#pragma unroll
+                    for (int c = 0; c < 4; ++c) a[e][mt][gi][c] = 0.0f;
+    }
+    __device__ __forceinline__ float partial(int mt, int gi, int c) const
+    {
+        if (T == T_FP4) return __fadd_rn(a[0][mt][gi][c], a[1][mt][gi][c]);
+        return a[0][mt][gi][c];
+    }
+};
+
+template <int T, int MT, int G>
+__device__ __forceinline__ void compute_sb(Acc<T, MT, G> &A, uint32_t wsl, uint32_t xsl, int xtok,
+                                           int g, int t, int ntok, const Mat &m, int row_w, int sb)
+{
+    if (T == T_Q4K || T == T_Q5K) {
+        compute_kquant<T, MT, G>(wsl, xsl, xtok, g, t, ntok, A.a[0]);
+    } else if (T == T_Q6K) {
+        int boff[MT][2];
+#pragma unroll
+        for (int mt = 0; mt < MT; ++mt)
+#pragma unroll
+            for (int rr = 0; rr < 2; ++rr) {
+                const int row = min(row_w + mt * 16 + g + 8 * rr, m.M - 1);
+                boff[mt][rr] =
+                    (int)((uintptr_t)(m.w + (int64_t)row * m.row_bytes + (int64_t)sb * 210) & 15);
+            }
+        compute_q6k<MT, G>(wsl, xsl, xtok, g, t, ntok, boff, A.a[0]);
+    } else {
+        compute_fp4<MT, G>(wsl, xsl, xtok, g, t, ntok,
+                           *reinterpret_cast<float(*)[2][MT][G][4]>(&A.a));
+    }
+}
+
+// Rank-ordered K-split reduction through distributed shared memory, then the
+// epilogue (rank 0 only).  `red` is free shared memory of at least
+// nthreads * MT * G * 4 floats; every thread of every CTA in the cluster must
+// call this.  cid/ncons: this thread's index among the consumer threads.
+template <int T, int MT, int G>
+__device__ __forceinline__ void reduce_and_store(const Acc<T, MT, G> &A, float *red, int rank,
+                                                 int ks, int cid, int ncons, bool consumer,
+                                                 const Params &p, const Mat &m, int row_w,
+                                                 int tok0, int g, int t)
+{
+    float v[MT][G][4];
+#pragma unroll
+    for (int mt = 0; mt < MT; ++mt)
+#pragma unroll
+        for (int gi = 0; gi < G; ++gi)
+#pragma unroll
+            for (int c = 0; c < 4; ++c) v[mt][gi][c] = A.partial(mt, gi, c);
+    if (ks > 1) {
+        if (consumer && rank != 0) {
+#pragma unroll
+            for (int mt = 0; mt < MT; ++mt)
+#pragma unroll
+                for (int gi = 0; gi < G; ++gi)
+#pragma unroll
+                    for (int c = 0; c < 4; ++c)
+                        red[((mt * G + gi) * 4 + c) * ncons + cid] = v[mt][gi][c];
+        }
+        cluster_sync();
+        if (consumer && rank == 0) {
+            for (int r = 1; r < ks; ++r) {
+                const uint32_t ra = map_shared_rank(smem_u32(red), (uint32_t)r);
+#pragma unroll
+                for (int mt = 0; mt < MT; ++mt)
+#pragma unroll
+                    for (int gi = 0; gi < G; ++gi)
+#pragma unroll
+                        for (int c = 0; c < 4; ++c)
+                            v[mt][gi][c] += ld_dsmem_f32(
+                                ra + (((mt * G + gi) * 4 + c) * ncons + cid) * 4);
+            }
+        }
+        cluster_sync();
+    }
+    if (!consumer || rank != 0) return;
+#pragma unroll
+    for (int mt = 0; mt < MT; ++mt) {
+#pragma unroll
+        for (int gi = 0; gi < G; ++gi) {
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+                const int row = row_w + mt * 16 + g + 8 * (c >> 1);
+                const int tok = tok0 + 8 * gi + 2 * t + (c & 1);
+                if (row >= m.M || tok >= p.N) continue;
+                float val = v[mt][gi][c];
+                if (T == T_FP4) val = val * m.gscale;
+                const int64_t o = (int64_t)tok * m.M + row;
+                if (m.res) val = __fadd_rn(__half2float(m.res[o]), val);
+                if (p.out_f32)
+                    reinterpret_cast<float *>(m.y)[o] = val;
+                else
+                    reinterpret_cast<__half *>(m.y)[o] = __float2half_rn(val);
+            }
+        }
+    }
+}
+
+__device__ __forceinline__ int select_mat(const Params &p, int tile)
+{
+    int mi = 0;
+    if (p.nmat > 1 && tile >= p.mat[1].tile_begin) mi = 1;
+    if (p.nmat > 2 && tile >= p.mat[2].tile_begin) mi = 2;
+    return mi;
+}
+
+// ===========================================================================
+// skinny_kernel (N > 8): 4 warps, cp.async ring, x staged by qg_stage.cu.
+// ===========================================================================
 template <int T, int G>
 __device__ __forceinline__ void run_tile(const Params &p, const Mat &m, int rtile, uint8_t *smem)
 {
@@ -481,14 +694,8 @@ __device__ __forceinline__ void run_tile(const Params &p, const Mat &m, int rtil
         if (i < nsb) issue_x(i);
     cp_async_commit();
 
-    float acc[MT][G][4];
-#pragma unroll
-    for (int mt = 0; mt < MT; ++mt)
-#pragma unroll
-        for (int gi = 0; gi < G; ++gi)
-#pragma unroll
-            for (int c = 0; c < 4; ++c) acc[mt][gi][c] = 0.0f;
-
+    Acc<T, MT, G> A;
+    A.zero();
 #pragma unroll 1
     for (int i = 0; i < nsb; ++i) {
         if (i == 0)
@@ -502,82 +709,13 @@ __device__ __forceinline__ void run_tile(const Params &p, const Mat &m, int rtil
         }
         cp_async_commit();
         const uint32_t stage = sbase + (i % STAGES) * S::STAGE;
-        const uint32_t wsl = stage + warp * S::WSLOT;
-        const uint32_t xsl = stage + S::WPART;
-        if (T == T_Q4K || T == T_Q5K) {
-            compute_kquant<T, G>(wsl, xsl, g, t, ntok, acc);
-        } else if (T == T_Q6K) {
-            int boff[MT][2];
-#pragma unroll
-            for (int mt = 0; mt < MT; ++mt)
-#pragma unroll
-                for (int rr = 0; rr < 2; ++rr) {
-                    const int row = min(row_w + mt * 16 + g + 8 * rr, m.M - 1);
-                    boff[mt][rr] = (int)((uintptr_t)(m.w + (int64_t)row * m.row_bytes +
-                                                     (int64_t)(sb0 + i) * 210) &
-                                         15);
-                }
-            compute_q6k<G>(wsl, xsl, g, t, ntok, boff, acc);
-        } else {
-            compute_fp4<G>(wsl, xsl, g, t, ntok, acc);
-        }
+        compute_sb<T, MT, G>(A, stage + warp * S::WSLOT, stage + S::WPART, kXTok, g, t, ntok, m,
+                             row_w, sb0 + i);
     }
     cp_async_wait<0>();
     __syncthreads();
-
-    // K-split: ranks 1..ks-1 publish their partial sums; rank 0 adds them in
-    // rank order and writes y.
-    constexpr int NACC = MT * G * 4;
-    if (ks > 1) {
-        float *red = reinterpret_cast<float *>(smem);
-        if (rank != 0) {
-#pragma unroll
-            for (int mt = 0; mt < MT; ++mt)
-#pragma unroll
-                for (int gi = 0; gi < G; ++gi)
-#pragma unroll
-                    for (int c = 0; c < 4; ++c)
-                        red[((mt * G + gi) * 4 + c) * kThreads + threadIdx.x] = acc[mt][gi][c];
-        }
-        cluster_sync();
-        if (rank == 0) {
-            for (int r = 1; r < ks; ++r) {
-                const uint32_t ra = map_shared_rank(smem_u32(red), (uint32_t)r);
-#pragma unroll
-                for (int mt = 0; mt < MT; ++mt)
-#pragma unroll
-                    for (int gi = 0; gi < G; ++gi)
-#pragma unroll
-                        for (int c = 0; c < 4; ++c)
-                            acc[mt][gi][c] += ld_dsmem_f32(
-                                ra + (((mt * G + gi) * 4 + c) * kThreads + threadIdx.x) * 4);
-            }
-        }
-        cluster_sync();
-    }
-    (void)NACC;
-    if (rank != 0) return;
-
-#pragma unroll
-    for (int mt = 0; mt < MT; ++mt) {
-#pragma unroll
-        for (int gi = 0; gi < G; ++gi) {
-#pragma unroll
-            for (int c = 0; c < 4; ++c) {
-                const int row = row_w + mt * 16 + g + 8 * (c >> 1);
-                const int tok = tok0 + 8 * gi + 2 * t + (c & 1);
-                if (row >= m.M || tok >= p.N) continue;
-                float v = acc[mt][gi][c];
-                if (T == T_FP4) v = v * m.gscale;
-                const int64_t o = (int64_t)tok * m.M + row;
-                if (m.res) v = __fadd_rn(__half2float(m.res[o]), v);
-                if (p.out_f32)
-                    reinterpret_cast<float *>(m.y)[o] = v;
-                else
-                    reinterpret_cast<__half *>(m.y)[o] = __float2half_rn(v);
-            }
-        }
-    }
+    reduce_and_store<T, MT, G>(A, reinterpret_cast<float *>(smem), rank, ks, threadIdx.x, kThreads,
+                               true, p, m, row_w, tok0, g, t);
 }
 
 template <int TSET, int G>
@@ -588,44 +726,211 @@ __global__ void __launch_bounds__(kThreads) skinny_kernel(const __grid_constant_
     // grid to finish before touching anything this grid writes.
     pdl_trigger();
     const int tile = blockIdx.y;
-    int mi = 0;
-    if (p.nmat > 1 && tile >= p.mat[1].tile_begin) mi = 1;
-    if (p.nmat > 2 && tile >= p.mat[2].tile_begin) mi = 2;
-    const Mat &m = p.mat[mi];
+    const Mat &m = p.mat[select_mat(p, tile)];
     const int rtile = tile - m.tile_begin;
-    if constexpr ((TSET & TS_Q4K) != 0) {
-        if (m.type == T_Q4K) {
-            run_tile<T_Q4K, G>(p, m, rtile, smem);
-            return;
-        }
-    }
-    if constexpr ((TSET & TS_Q5K) != 0) {
-        if (m.type == T_Q5K) {
-            run_tile<T_Q5K, G>(p, m, rtile, smem);
-            return;
-        }
-    }
-    if constexpr ((TSET & TS_Q6K) != 0) {
-        if (m.type == T_Q6K) {
-            run_tile<T_Q6K, G>(p, m, rtile, smem);
-            return;
-        }
-    }
-    if constexpr ((TSET & TS_FP4) != 0) {
-        if (m.type == T_FP4) {
-            run_tile<T_FP4, G>(p, m, rtile, smem);
-            return;
-        }
-    }
+    if constexpr ((TSET & TS_Q4K) != 0)
+        if (m.type == T_Q4K) return run_tile<T_Q4K, G>(p, m, rtile, smem);
+    if constexpr ((TSET & TS_Q5K) != 0)
+        if (m.type == T_Q5K) return run_tile<T_Q5K, G>(p, m, rtile, smem);
+    if constexpr ((TSET & TS_Q6K) != 0)
+        if (m.type == T_Q6K) return run_tile<T_Q6K, G>(p, m, rtile, smem);
+    if constexpr ((TSET & TS_FP4) != 0)
+        if (m.type == T_FP4) return run_tile<T_FP4, G>(p, m, rtile, smem);
 }
 
-// Host-side launch entry generated per type set (one translation unit each).
-struct LaunchCfg {
-    dim3 grid;
-    int smem_bytes;
-    int cluster_x;
-    bool pdl;
-    void *stream;
-};
+// ===========================================================================
+// gemv_kernel (N <= 8): warp 0 produces, warps 1..CW consume (16 rows each).
+// Shared memory: [full[STAGES], empty[STAGES] mbarriers | STAGES weight slots
+// of rows_cta * RB bytes | x region: N tokens x (this rank's super-blocks) x
+// 576 bytes, token stride p.xtok].
+// ===========================================================================
+constexpr int kGemvStages = 4;
+
+template <int T>
+__device__ __forceinline__ uint32_t slot_row_bytes()
+{
+    return Fmt<T>::RB;
+}
+
+template <int T, int CW>
+__device__ __forceinline__ void gemv_tile(const Params &p, const Mat &m, int rtile, uint8_t *smem)
+{
+    using F = Fmt<T>;
+    constexpr int STAGES = kGemvStages;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int g = lane >> 2, t = lane & 3;
+    const int R = p.rows_cta;                  // CW * 16 (or fewer for small launches)
+    const int rank = blockIdx.x;
+    const int ks = p.ks;
+    const int sb0 = (rank * p.nb) / ks;
+    const int sb1 = ((rank + 1) * p.nb) / ks;
+    const int nsb = sb1 - sb0;
+    const int ntok = p.N;                      // <= 8
+    const int row0 = rtile * R;
+    const uint32_t sbase = smem_u32(smem);
+    const uint32_t bar_full = sbase, bar_empty = sbase + 8 * STAGES;
+    const int slot_bytes = R * F::RB;
+    const uint32_t slots = sbase + 128;
+    const uint32_t xreg = slots + STAGES * slot_bytes;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < STAGES; ++s) {
+            mbar_init(bar_full + 8 * s, 1);
+            mbar_init(bar_empty + 8 * s, CW);
+        }
+        mbar_fence_init();
+    }
+    __syncthreads();
+
+    // Producer: copy the rows of stage i (super-block sb0 + i) into its slot.
+    auto produce = [&](int i) {
+        const int slot = i % STAGES;
+        const int sb = sb0 + i;
+        const uint32_t dst0 = slots + slot * slot_bytes;
+        const uint32_t fb = bar_full + 8 * slot;
+        uint32_t bytes = 0;
+        // bytes of this lane's rows (Q6_K tails are copied by hand first)
+        for (int r = lane; r < R; r += 32) {
+            const int row = row0 + r;
+            if (row >= m.M) continue;
+            if (T == T_Q6K) {
+                const uint8_t *blk = m.w + (int64_t)row * m.row_bytes + (int64_t)sb * 210;
+                const uint8_t *al = (const uint8_t *)((uintptr_t)blk & ~(uintptr_t)15);
+                const uint8_t *end = m.w + m.w_bytes;
+                uint32_t n = 224;
+                if (al + 224 > end) {
+                    n = (uint32_t)((end - al) & ~(int64_t)15);
+                    uint8_t *d = smem + (dst0 - sbase) + r * F::RB;
+                    for (uint32_t b = n; al + b < end; ++b) d[b] = al[b];
+                }
+                bytes += n;
+            } else if (T == T_FP4) {
+                bytes += 128 + 16;
+            } else {
+                bytes += F::BB;
+            }
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) bytes += __shfl_xor_sync(0xffffffffu, bytes, o);
+        __syncwarp();
+        if (lane == 0) mbar_arrive_expect_tx(fb, bytes);
+        __syncwarp();
+        for (int r = lane; r < R; r += 32) {
+            const int row = row0 + r;
+            if (row >= m.M) continue;
+            const uint32_t dst = dst0 + r * F::RB;
+            if (T == T_Q6K) {
+                const uint8_t *blk = m.w + (int64_t)row * m.row_bytes + (int64_t)sb * 210;
+                const uint8_t *al = (const uint8_t *)((uintptr_t)blk & ~(uintptr_t)15);
+                const uint8_t *end = m.w + m.w_bytes;
+                uint32_t n = 224;
+                if (al + 224 > end) n = (uint32_t)((end - al) & ~(int64_t)15);
+                if (n) bulk_g2s(dst, al, n, fb);
+            } else if (T == T_FP4) {
+                bulk_g2s(dst, m.w + (int64_t)row * m.row_bytes + (int64_t)sb * 128, 128, fb);
+                bulk_g2s(dst + 128, m.sc + (int64_t)row * m.sc_row_bytes + (int64_t)sb * 16, 16,
+                         fb);
+            } else {
+                bulk_g2s(dst, m.w + (int64_t)row * m.row_bytes + (int64_t)sb * F::BB, F::BB, fb);
+            }
+        }
+    };
+
+    unsigned int err = 0;
+    if (warp == 0) {
+        for (int i = 0; i < STAGES && i < nsb; ++i) produce(i);
+    }
+
+    // x for this rank's super-blocks, staged by every warp (after the
+    // programmatic dependency: x may be written by the previous kernel).
+    pdl_wait();
+    {
+        const int nwarps = blockDim.x >> 5;
+        for (int it = warp; it < ntok * nsb; it += nwarps) {
+            const int n = it / nsb, i = it - n * nsb;
+            const uint4 v = *reinterpret_cast<const uint4 *>(
+                p.x + (int64_t)n * p.K + 256 * (sb0 + i) + 8 * lane);
+            uint8_t *dst = smem + (xreg - sbase) + n * p.xtok + i * kXTok;
+            stage_sb(v, lane, F::XL == XL_Q4 ? dst : nullptr, F::XL == XL_Q6 ? dst : nullptr,
+                     F::XL == XL_FP4 ? dst : nullptr);
+        }
+    }
+    __syncthreads();
+
+    Acc<T, 1, 1> A;
+    A.zero();
+    const int c = warp - 1;
+    const int row_w = row0 + c * 16;
+    if (warp == 0) {
+        for (int i = STAGES; i < nsb; ++i) {
+            const int slot = i % STAGES;
+            const uint32_t par = ((i / STAGES) - 1) & 1;
+            if (!mbar_wait(bar_empty + 8 * slot, par)) {
+                err |= ERR_EMPTY_TIMEOUT;
+                break;
+            }
+            produce(i);
+        }
+    } else if (c * 16 < R) {
+        for (int i = 0; i < nsb; ++i) {
+            const int slot = i % STAGES;
+            const uint32_t par = (i / STAGES) & 1;
+            if (!mbar_wait(bar_full + 8 * slot, par)) {
+                err |= ERR_FULL_TIMEOUT;
+                break;
+            }
+            compute_sb<T, 1, 1>(A, slots + slot * slot_bytes + c * 16 * F::RB,
+                                xreg + i * kXTok, p.xtok, g, t, ntok, m, row_w, sb0 + i);
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar_empty + 8 * slot);
+        }
+    } else {
+        // idle consumer warp (fewer rows than warps): still releases slots
+        for (int i = 0; i < nsb; ++i) {
+            const int slot = i % STAGES;
+            if (!mbar_wait(bar_full + 8 * slot, (i / STAGES) & 1)) {
+                err |= ERR_FULL_TIMEOUT;
+                break;
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar_empty + 8 * slot);
+        }
+    }
+    if (err && p.err) atomicOr(p.err, err);
+    __syncthreads();
+    const bool consumer = warp > 0 && c * 16 < R;
+    reduce_and_store<T, 1, 1>(A, reinterpret_cast<float *>(smem + 128), rank, ks,
+                              threadIdx.x - 32, blockDim.x - 32, consumer, p, m, row_w, 0, g, t);
+}
+
+template <int TSET, int CW>
+__global__ void __launch_bounds__(32 * (CW + 1)) gemv_kernel(const __grid_constant__ Params p)
+{
+    extern __shared__ __align__(128) uint8_t smem[];
+    pdl_trigger();
+    const int tile = blockIdx.y;
+    const Mat &m = p.mat[select_mat(p, tile)];
+    const int rtile = tile - m.tile_begin;
+    if constexpr ((TSET & TS_Q4K) != 0)
+        if (m.type == T_Q4K) return gemv_tile<T_Q4K, CW>(p, m, rtile, smem);
+    if constexpr ((TSET & TS_Q5K) != 0)
+        if (m.type == T_Q5K) return gemv_tile<T_Q5K, CW>(p, m, rtile, smem);
+    if constexpr ((TSET & TS_Q6K) != 0)
+        if (m.type == T_Q6K) return gemv_tile<T_Q6K, CW>(p, m, rtile, smem);
+    if constexpr ((TSET & TS_FP4) != 0)
+        if (m.type == T_FP4) return gemv_tile<T_FP4, CW>(p, m, rtile, smem);
+}
+
+// Dynamic shared memory of gemv_kernel for R rows per CTA, N tokens and nsbr
+// super-blocks per rank.
+__host__ __device__ inline int gemv_xtok(int nsbr) { return nsbr * kXTok + ((nsbr & 1) ? 0 : 64); }
+__host__ __device__ inline int gemv_smem_bytes(int rb, int R, int N, int nsbr)
+{
+    const int stages = kGemvStages * R * rb;
+    const int x = N * gemv_xtok(nsbr);
+    const int red = 4 * 4 * R * 2;  // reduction buffer overlays stages+x
+    const int body = stages + x > red ? stages + x : red;
+    return 128 + body;
+}
 
 }  // namespace qg

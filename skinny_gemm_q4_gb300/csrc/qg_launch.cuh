@@ -21,7 +21,8 @@ cudaError_t launch_ref_gemv(const Mat &m, int K, const __half *x, int N, int out
 // Per type-set launchers (defined in qg_inst_*.cu).
 #define QG_DECLARE_TSET(NAME)                                                           \
     cudaError_t launch_skinny_##NAME(int G, const Params &p, dim3 grid, cudaStream_t s); \
-    int smem_skinny_##NAME(int G);
+    int smem_skinny_##NAME(int G);                                                      \
+    cudaError_t launch_gemv_##NAME(int cw, const Params &p, dim3 grid, int smem, cudaStream_t s);
 QG_DECLARE_TSET(q4k)
 QG_DECLARE_TSET(q5k)
 QG_DECLARE_TSET(q6k)

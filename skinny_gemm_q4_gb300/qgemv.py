@@ -35,7 +35,7 @@ STATUS_NAMES = {0: "QG_OK", -1: "QG_EINVAL", -2: "QG_EUNSUPPORTED", -3: "QG_EALI
 #: every symbol include/qgemv.h declares
 EXPORTS = ["qgemv_create", "qgemv_run", "qgemv_run_add", "qgemv_pair_run", "qgemv_triple_run",
            "qgemv_run_host", "qgemv_dequantize", "qgemv_destroy", "qgemv_last_error",
-           "qgemv_row_bytes", "qgemv_plan_info", "qgemv_describe"]
+           "qgemv_row_bytes", "qgemv_plan_info", "qgemv_describe", "qgemv_device_status"]
 
 
 class QgOpts(ctypes.Structure):
@@ -77,10 +77,12 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.qgemv_row_bytes.restype = i64
     lib.qgemv_plan_info.argtypes = [vp, i64, ctypes.POINTER(i32), ctypes.POINTER(i32),
                                     ctypes.POINTER(i32)]
+    lib.qgemv_device_status.argtypes = [vp, ctypes.POINTER(ctypes.c_uint32), c_int]
     lib.qgemv_describe.argtypes = []
     lib.qgemv_describe.restype = ctypes.c_char_p
     for name in ("qgemv_create", "qgemv_run", "qgemv_run_add", "qgemv_pair_run",
-                 "qgemv_triple_run", "qgemv_run_host", "qgemv_dequantize", "qgemv_plan_info"):
+                 "qgemv_triple_run", "qgemv_run_host", "qgemv_dequantize", "qgemv_plan_info",
+                 "qgemv_device_status"):
         getattr(lib, name).restype = c_int
     _lib = lib
     return lib
@@ -151,6 +153,13 @@ def qgemv_plan_info(h, N):
     return ks.value, rows.value, launches.value
 
 
+def qgemv_device_status(h, clear: bool = False) -> int:
+    w = ctypes.c_uint32()
+    _check(load().qgemv_device_status(h, ctypes.byref(w), 1 if clear else 0),
+           "qgemv_device_status")
+    return w.value
+
+
 # ----------------------------------------------------- torch convenience
 
 def _stream_ptr(stream=None) -> int:
@@ -215,6 +224,9 @@ class QGemv:
 
     def plan_info(self, N: int):
         return qgemv_plan_info(self.h, N)
+
+    def device_status(self, clear: bool = False) -> int:
+        return qgemv_device_status(self.h, clear)
 
 
 def pair_run(a: QGemv, b: QGemv, x, out_f32: bool = False, stream=None):

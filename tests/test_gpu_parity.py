@@ -93,6 +93,7 @@ def test_row_invariance_twins(qtype, M, K):
     # N >= 33 (next chunking regime) keeps the same bits too
     y40 = h.run(to_dev(np.concatenate([x, x[:8]])), out_f32=True).cpu().numpy()
     assert np.array_equal(y40[:32].view(np.uint32), one.view(np.uint32))
+    assert h.device_status() == 0
 
 
 @pytest.mark.parametrize("qtype", [qg.Q4_K, qg.Q6_K, qg.NVFP4_W4A16])
@@ -209,4 +210,7 @@ def test_argument_errors_are_statuses():
     assert lib.qgemv_pair_run(h.h, other.h, x.data_ptr(), 1, y.data_ptr(), x.data_ptr(), 0,
                               None) == -1
     ks, rows, launches = h.plan_info(1)
-    assert ks == 2 and rows == 64 and launches == 2
+    assert ks == 2 and rows == 32 and launches == 1      # N <= 8: one kernel
+    ks, rows, launches = h.plan_info(16)
+    assert ks == 2 and rows == 64 and launches == 2      # staging + product
+    assert h.device_status() == 0
