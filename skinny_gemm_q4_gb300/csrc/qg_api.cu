@@ -1,5 +1,7 @@
 // C ABI of the qgemv library: handles, launch plan, argument validation,
 // staging + product launches, reference fallback and error reporting.
+#include <cuda.h>
+#include <cudaTypedefs.h>
 #include <cuda_runtime.h>
 
 #include <cmath>
@@ -28,6 +30,7 @@ struct qg_handle {
     int layout;    // staged-x layout this format reads
     uint8_t *xs;   // staging buffer: max_tokens * nb * kXTok bytes
     unsigned int *err;  // device error word written by the kernels (timeouts)
+    CUtensorMap tmw[3], tms[3];  // 2-D maps for 32, 64, 128 rows per CTA
     int device;
     void *hx;      // device buffers of the host-pointer entry point
     size_t hx_cap;
@@ -117,10 +120,10 @@ int rows_per_cta(int G) { return G <= 2 ? Cfg<1>::ROWS : Cfg<4>::ROWS; }
 int rb_of_tset(int tset)
 {
     int rb = 0;
-    if (tset & TS_Q4K) rb = rb > Fmt<T_Q4K>::RB ? rb : Fmt<T_Q4K>::RB;
-    if (tset & TS_Q5K) rb = rb > Fmt<T_Q5K>::RB ? rb : Fmt<T_Q5K>::RB;
-    if (tset & TS_Q6K) rb = rb > Fmt<T_Q6K>::RB ? rb : Fmt<T_Q6K>::RB;
-    if (tset & TS_FP4) rb = rb > Fmt<T_FP4>::RB ? rb : Fmt<T_FP4>::RB;
+    if (tset & TS_Q4K) rb = rb > Fmt<T_Q4K>::RBG ? rb : Fmt<T_Q4K>::RBG;
+    if (tset & TS_Q5K) rb = rb > Fmt<T_Q5K>::RBG ? rb : Fmt<T_Q5K>::RBG;
+    if (tset & TS_Q6K) rb = rb > Fmt<T_Q6K>::RBG ? rb : Fmt<T_Q6K>::RBG;
+    if (tset & TS_FP4) rb = rb > Fmt<T_FP4>::RBG ? rb : Fmt<T_FP4>::RBG;
     return rb;
 }
 
@@ -151,9 +154,16 @@ cudaError_t launch_gemv_tset(int tset, int cw, const Params &p, dim3 grid, int s
     }
 }
 
-Mat mat_of(const qg_handle *h, void *y, const __half *res)
+int map_index(int R) { return R <= 32 ? 0 : (R <= 64 ? 1 : 2); }
+
+Mat mat_of(const qg_handle *h, void *y, const __half *res, int R = 0)
 {
     Mat m;
+    memset(&m, 0, sizeof m);
+    if (R > 0) {
+        m.tmw = h->tmw[map_index(R)];
+        m.tms = h->tms[map_index(R)];
+    }
     m.w = h->w;
     m.sc = h->sc;
     m.y = y;
@@ -184,6 +194,40 @@ bool tset_supported(int tset)
 {
     return tset == TS_Q4K || tset == TS_Q5K || tset == TS_Q6K || tset == TS_FP4 ||
            tset == (TS_Q4K | TS_Q6K);
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn()
+{
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static bool tried = false;
+    if (!tried) {
+        tried = true;
+        void *ptr = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000,
+                                             cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = (PFN_cuTensorMapEncodeTiled_v12000)ptr;
+        else
+            cudaGetLastError();
+    }
+    return fn;
+}
+
+// 2-D map over rows of `row_bytes` bytes viewed as 8-byte elements; box of
+// box_bytes x box_rows.
+bool encode_rows(CUtensorMap *m, const void *base, int64_t row_bytes, int64_t rows, int box_bytes,
+                 int box_rows)
+{
+    PFN_cuTensorMapEncodeTiled_v12000 fn = encode_fn();
+    if (!fn) return false;
+    cuuint64_t dims[2] = {(cuuint64_t)(row_bytes / 8), (cuuint64_t)rows};
+    cuuint64_t strides[1] = {(cuuint64_t)row_bytes};
+    cuuint32_t box[2] = {(cuuint32_t)(box_bytes / 8), (cuuint32_t)box_rows};
+    cuuint32_t estr[2] = {1, 1};
+    return fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT64, 2, const_cast<void *>(base), dims, strides, box,
+              estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 // The whole path for 1..3 handles that share x: staging, then one product
@@ -247,7 +291,7 @@ qg_status run_product(qg_handle *const *hs, int nh, const __half *x, int64_t N, 
                     const int idx = groups[gidx][j];
                     const qg_handle *h = hs[idx];
                     p.mat[j] = mat_of(h, (uint8_t *)ys[idx] + c0 * h->M * (out_f32 ? 4 : 2),
-                                      res ? res + c0 * h->M : nullptr);
+                                      res ? res + c0 * h->M : nullptr, R);
                     p.mat[j].tile_begin = tiles;
                     tiles += (int)((h->M + R - 1) / R);
                 }
@@ -447,6 +491,20 @@ qg_status qgemv_create(qg_handle **out, qg_type t, int64_t M, int64_t K, const v
         cudaGetLastError();
         delete h;
         return fail(QG_ENOMEM, "staging buffer allocation of %zu bytes failed", xs_bytes);
+    }
+    if (t != QG_Q6_K) {
+        const int bb = (t == QG_NVFP4_W4A16) ? 128 : block_bytes(t);
+        for (int i = 0; i < 3; ++i) {
+            const int R = 32 << i;
+            bool ok = encode_rows(&h->tmw[i], w_dev, h->row_bytes, M, bb, R);
+            if (ok && t == QG_NVFP4_W4A16)
+                ok = encode_rows(&h->tms[i], scales_dev, h->sc_row_bytes, M, 16, R);
+            if (!ok) {
+                cudaFree(h->xs);
+                delete h;
+                return fail(QG_ECUDA, "tensor map encoding failed");
+            }
+        }
     }
     e = cudaMalloc((void **)&h->err, sizeof(unsigned int));
     if (e == cudaSuccess) e = cudaMemset(h->err, 0, sizeof(unsigned int));

@@ -28,12 +28,16 @@
 //     every B load is one conflict-free 16-byte shared load.
 //
 // Two data-movement variants share the arithmetic above bit for bit:
-//   gemv_kernel   (N <= 8): a producer warp streams the weight tiles with 1-D
-//                 bulk copies (TMA) into an mbarrier ring; consumer warps
-//                 decode and multiply; x is staged inside the kernel.
+//   gemv_kernel   (N <= 8): a producer warp streams the weight tiles into an
+//                 mbarrier ring with one 2-D tensor copy (TMA) per stage (Q6_K,
+//                 whose 210-byte rows cannot be described by a tensor map: by
+//                 producer-lane cp.async); consumer warps decode and multiply;
+//                 x is staged inside the kernel.
 //   skinny_kernel (N > 8): 16-byte cp.async ring, x staged by a separate
 //                 kernel (qg_stage.cu) once per call.
 #pragma once
+
+#include <cuda.h>
 
 #include "qg_ptx.cuh"
 
@@ -53,6 +57,8 @@ constexpr int kMaxMats = 3;
 enum { ERR_FULL_TIMEOUT = 1, ERR_EMPTY_TIMEOUT = 2 };
 
 struct Mat {
+    CUtensorMap tmw;       // 2-D map of the packed rows (Q4_K, Q5_K, NVFP4 codes)
+    CUtensorMap tms;       // 2-D map of the NVFP4 scale rows
     const uint8_t *w;      // packed weights (codes for NVFP4)
     const uint8_t *sc;     // NVFP4 e4m3 scales [M][K/16]
     void *y;               // output [N][M]
@@ -87,21 +93,21 @@ template <int T>
 struct Fmt;
 template <>
 struct Fmt<T_Q4K> {
-    static constexpr int BB = 144, RB = 144, VPR = 9, XL = XL_Q4, XV = 34;
+    static constexpr int BB = 144, RB = 144, VPR = 9, XL = XL_Q4, XV = 34, RBG = 144;
 };
 template <>
 struct Fmt<T_Q5K> {
-    static constexpr int BB = 176, RB = 176, VPR = 11, XL = XL_Q4, XV = 34;
+    static constexpr int BB = 176, RB = 176, VPR = 11, XL = XL_Q4, XV = 34, RBG = 176;
 };
 template <>
 struct Fmt<T_Q6K> {
-    static constexpr int BB = 210, RB = 224, VPR = 14, XL = XL_Q6, XV = 32;
+    static constexpr int BB = 210, RB = 224, VPR = 14, XL = XL_Q6, XV = 32, RBG = 224;
 };
 template <>
 struct Fmt<T_FP4> {
     // row in shared memory: 128 code bytes, 16 scale bytes, 48 bytes of pad
     // (a 192-byte pitch keeps the two rows of an 8-lane phase on disjoint banks)
-    static constexpr int BB = 128, RB = 192, VPR = 9, XL = XL_FP4, XV = 32;
+    static constexpr int BB = 128, RB = 192, VPR = 9, XL = XL_FP4, XV = 32, RBG = 144;
 };
 
 template <int G>
@@ -447,11 +453,13 @@ __device__ __forceinline__ void compute_q6k(uint32_t wsl, uint32_t xsl, int xtok
 }
 
 // NVFP4: acc is [2][MT][G][4] (two chains: even and odd steps).
+// Code row r of the warp's tiles at cbase + r * cp (128 bytes), its 16 scale
+// bytes at sbase + r * sp.
 template <int MT, int G>
-__device__ __forceinline__ void compute_fp4(uint32_t wsl, uint32_t xsl, int xtok, int g, int t,
-                                            int ntok, float (&acc)[2][MT][G][4])
+__device__ __forceinline__ void compute_fp4(uint32_t cbase, int cp, uint32_t sbase, int sp,
+                                            uint32_t xsl, int xtok, int g, int t, int ntok,
+                                            float (&acc)[2][MT][G][4])
 {
-    constexpr int RB = Fmt<T_FP4>::RB;
 #pragma unroll
     for (int hf = 0; hf < 2; ++hf) {
         uint4 cw[MT][2];
@@ -460,10 +468,10 @@ __device__ __forceinline__ void compute_fp4(uint32_t wsl, uint32_t xsl, int xtok
         for (int mt = 0; mt < MT; ++mt) {
 #pragma unroll
             for (int rr = 0; rr < 2; ++rr) {
-                const uint32_t ra = wsl + (mt * 16 + g + 8 * rr) * RB;
-                cw[mt][rr] = lds128(ra + 64 * hf + 16 * t);
+                const int r = mt * 16 + g + 8 * rr;
+                cw[mt][rr] = lds128(cbase + r * cp + 64 * hf + 16 * t);
                 // scale bytes 8hf + 2t, 8hf + 2t + 1 of the chunk's 16
-                const uint32_t sw = lds32(ra + 128 + 8 * hf + 4 * (t >> 1));
+                const uint32_t sw = lds32(sbase + r * sp + 8 * hf + 4 * (t >> 1));
                 const uint32_t s2 = e4m3x2_to_h2((sw >> (16 * (t & 1))) & 0xffffu);
                 sA[mt][rr] = __byte_perm(s2, 0u, 0x1010u);
                 sB[mt][rr] = __byte_perm(s2, 0u, 0x3232u);
@@ -524,9 +532,13 @@ struct Acc {
     }
 };
 
+// wsl: the warp's first weight row; for NVFP4 the codes use pitch `cp` and
+// the scales start at `fsc` with a 16-byte pitch when fsc != 0 (else they
+// follow each code row at +128 with the same pitch).
 template <int T, int MT, int G>
 __device__ __forceinline__ void compute_sb(Acc<T, MT, G> &A, uint32_t wsl, uint32_t xsl, int xtok,
-                                           int g, int t, int ntok, const Mat &m, int row_w, int sb)
+                                           int g, int t, int ntok, const Mat &m, int row_w, int sb,
+                                           int cp = Fmt<T>::RB, uint32_t fsc = 0)
 {
     if (T == T_Q4K || T == T_Q5K) {
         compute_kquant<T, MT, G>(wsl, xsl, xtok, g, t, ntok, A.a[0]);
@@ -542,7 +554,7 @@ __device__ __forceinline__ void compute_sb(Acc<T, MT, G> &A, uint32_t wsl, uint3
             }
         compute_q6k<MT, G>(wsl, xsl, xtok, g, t, ntok, boff, A.a[0]);
     } else {
-        compute_fp4<MT, G>(wsl, xsl, xtok, g, t, ntok,
+        compute_fp4<MT, G>(wsl, cp, fsc ? fsc : wsl + 128, fsc ? 16 : cp, xsl, xtok, g, t, ntok,
                            *reinterpret_cast<float(*)[2][MT][G][4]>(&A.a));
     }
 }
@@ -746,17 +758,18 @@ __global__ void __launch_bounds__(kThreads) skinny_kernel(const __grid_constant_
 // ===========================================================================
 constexpr int kGemvStages = 4;
 
-template <int T>
-__device__ __forceinline__ uint32_t slot_row_bytes()
-{
-    return Fmt<T>::RB;
-}
-
+// Slot layout of one stage (R rows of one super-block):
+//   Q4_K / Q5_K : R rows x BB bytes (one 2-D tensor copy)
+//   NVFP4       : R x 128 code bytes, then R x 16 scale bytes (two copies)
+//   Q6_K        : R rows x 224 bytes, the 16-byte aligned superset of each
+//                 210-byte block (cp.async by the producer lanes; the block
+//                 starts (address & 15) bytes into its row)
 template <int T, int CW>
 __device__ __forceinline__ void gemv_tile(const Params &p, const Mat &m, int rtile, uint8_t *smem)
 {
     using F = Fmt<T>;
     constexpr int STAGES = kGemvStages;
+    constexpr bool TMA = (T != T_Q6K);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int g = lane >> 2, t = lane & 3;
     const int R = p.rows_cta;                  // CW * 16 (or fewer for small launches)
@@ -769,70 +782,56 @@ __device__ __forceinline__ void gemv_tile(const Params &p, const Mat &m, int rti
     const int row0 = rtile * R;
     const uint32_t sbase = smem_u32(smem);
     const uint32_t bar_full = sbase, bar_empty = sbase + 8 * STAGES;
-    const int slot_bytes = R * F::RB;
+    const int slot_bytes = R * F::RBG;
     const uint32_t slots = sbase + 128;
     const uint32_t xreg = slots + STAGES * slot_bytes;
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < STAGES; ++s) {
-            mbar_init(bar_full + 8 * s, 1);
+            mbar_init(bar_full + 8 * s, TMA ? 1 : 32);
             mbar_init(bar_empty + 8 * s, CW);
         }
         mbar_fence_init();
     }
+    if (TMA && warp == 0 && lane == 0) {
+        prefetch_tmap(&m.tmw);
+        if (T == T_FP4) prefetch_tmap(&m.tms);
+    }
     __syncthreads();
 
-    // Producer: copy the rows of stage i (super-block sb0 + i) into its slot.
+    // Producer: fill the slot of stage i (super-block sb0 + i).
     auto produce = [&](int i) {
         const int slot = i % STAGES;
         const int sb = sb0 + i;
-        const uint32_t dst0 = slots + slot * slot_bytes;
+        const uint32_t dst = slots + slot * slot_bytes;
         const uint32_t fb = bar_full + 8 * slot;
-        uint32_t bytes = 0;
-        // bytes of this lane's rows (Q6_K tails are copied by hand first)
-        for (int r = lane; r < R; r += 32) {
-            const int row = row0 + r;
-            if (row >= m.M) continue;
-            if (T == T_Q6K) {
-                const uint8_t *blk = m.w + (int64_t)row * m.row_bytes + (int64_t)sb * 210;
-                const uint8_t *al = (const uint8_t *)((uintptr_t)blk & ~(uintptr_t)15);
-                const uint8_t *end = m.w + m.w_bytes;
-                uint32_t n = 224;
-                if (al + 224 > end) {
-                    n = (uint32_t)((end - al) & ~(int64_t)15);
-                    uint8_t *d = smem + (dst0 - sbase) + r * F::RB;
-                    for (uint32_t b = n; al + b < end; ++b) d[b] = al[b];
+        if (TMA) {
+            if (lane == 0) {
+                if (T == T_FP4) {
+                    mbar_arrive_expect_tx(fb, (uint32_t)(R * (128 + 16)));
+                    tma_load_2d(dst, &m.tmw, sb * 16, row0, fb);
+                    tma_load_2d(dst + R * 128, &m.tms, sb * 2, row0, fb);
+                } else {
+                    mbar_arrive_expect_tx(fb, (uint32_t)(R * F::BB));
+                    tma_load_2d(dst, &m.tmw, sb * (F::BB / 8), row0, fb);
                 }
-                bytes += n;
-            } else if (T == T_FP4) {
-                bytes += 128 + 16;
-            } else {
-                bytes += F::BB;
             }
-        }
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) bytes += __shfl_xor_sync(0xffffffffu, bytes, o);
-        __syncwarp();
-        if (lane == 0) mbar_arrive_expect_tx(fb, bytes);
-        __syncwarp();
-        for (int r = lane; r < R; r += 32) {
-            const int row = row0 + r;
-            if (row >= m.M) continue;
-            const uint32_t dst = dst0 + r * F::RB;
-            if (T == T_Q6K) {
-                const uint8_t *blk = m.w + (int64_t)row * m.row_bytes + (int64_t)sb * 210;
-                const uint8_t *al = (const uint8_t *)((uintptr_t)blk & ~(uintptr_t)15);
-                const uint8_t *end = m.w + m.w_bytes;
-                uint32_t n = 224;
-                if (al + 224 > end) n = (uint32_t)((end - al) & ~(int64_t)15);
-                if (n) bulk_g2s(dst, al, n, fb);
-            } else if (T == T_FP4) {
-                bulk_g2s(dst, m.w + (int64_t)row * m.row_bytes + (int64_t)sb * 128, 128, fb);
-                bulk_g2s(dst + 128, m.sc + (int64_t)row * m.sc_row_bytes + (int64_t)sb * 16, 16,
-                         fb);
-            } else {
-                bulk_g2s(dst, m.w + (int64_t)row * m.row_bytes + (int64_t)sb * F::BB, F::BB, fb);
+        } else {
+            const uint8_t *end = m.w + m.w_bytes;
+            for (int v = lane; v < R * 14; v += 32) {
+                const int r = v / 14, c = v - r * 14;
+                const int row = row0 + r;
+                const uint8_t *src = m.w;
+                int n = 0;
+                if (row < m.M) {
+                    const uint8_t *blk = m.w + (int64_t)row * m.row_bytes + (int64_t)sb * 210;
+                    src = (const uint8_t *)((uintptr_t)blk & ~(uintptr_t)15) + c * 16;
+                    const int64_t left = end - src;
+                    n = left >= 16 ? 16 : (left > 0 ? (int)left : 0);
+                }
+                cp_async16(dst + r * 224 + c * 16, src, n);
             }
+            cp_async_mbar_arrive(fb);
         }
     };
 
@@ -879,8 +878,13 @@ __device__ __forceinline__ void gemv_tile(const Params &p, const Mat &m, int rti
                 err |= ERR_FULL_TIMEOUT;
                 break;
             }
-            compute_sb<T, 1, 1>(A, slots + slot * slot_bytes + c * 16 * F::RB,
-                                xreg + i * kXTok, p.xtok, g, t, ntok, m, row_w, sb0 + i);
+            const uint32_t sl = slots + slot * slot_bytes;
+            if (T == T_FP4)
+                compute_sb<T, 1, 1>(A, sl + c * 16 * 128, xreg + i * kXTok, p.xtok, g, t, ntok, m,
+                                    row_w, sb0 + i, 128, sl + R * 128 + c * 16 * 16);
+            else
+                compute_sb<T, 1, 1>(A, sl + c * 16 * F::RBG, xreg + i * kXTok, p.xtok, g, t, ntok,
+                                    m, row_w, sb0 + i, F::RBG);
             __syncwarp();
             if (lane == 0) mbar_arrive(bar_empty + 8 * slot);
         }
@@ -924,9 +928,9 @@ __global__ void __launch_bounds__(32 * (CW + 1)) gemv_kernel(const __grid_consta
 // Dynamic shared memory of gemv_kernel for R rows per CTA, N tokens and nsbr
 // super-blocks per rank.
 __host__ __device__ inline int gemv_xtok(int nsbr) { return nsbr * kXTok + ((nsbr & 1) ? 0 : 64); }
-__host__ __device__ inline int gemv_smem_bytes(int rb, int R, int N, int nsbr)
+__host__ __device__ inline int gemv_smem_bytes(int rbg, int R, int N, int nsbr)
 {
-    const int stages = kGemvStages * R * rb;
+    const int stages = kGemvStages * R * rbg;
     const int x = N * gemv_xtok(nsbr);
     const int red = 4 * 4 * R * 2;  // reduction buffer overlays stages+x
     const int body = stages + x > red ? stages + x : red;

@@ -231,3 +231,31 @@ __device__ __forceinline__ void bar_sync_named(int id, int threads)
 }
 
 }  // namespace qg
+
+namespace qg {
+
+// 2-D tiled tensor copy global->shared, completing on an mbarrier.  tmap is
+// the generic address of a CUtensorMap held in kernel-parameter space.
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const void *tmap, int x, int y,
+                                            uint32_t mbar)
+{
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes "
+        "[%0], [%1, {%2, %3}], [%4];\n" ::"r"(dst),
+        "l"(tmap), "r"(x), "r"(y), "r"(mbar)
+        : "memory");
+}
+
+__device__ __forceinline__ void prefetch_tmap(const void *tmap)
+{
+    asm volatile("prefetch.tensormap [%0];\n" ::"l"(tmap) : "memory");
+}
+
+// Arrive on an mbarrier once all prior cp.async of this thread have landed
+// (the arrival is counted in the barrier's initial count).
+__device__ __forceinline__ void cp_async_mbar_arrive(uint32_t mbar)
+{
+    asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];\n" ::"r"(mbar) : "memory");
+}
+
+}  // namespace qg
