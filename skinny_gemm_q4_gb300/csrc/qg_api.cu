@@ -127,7 +127,7 @@ int rb_of_tset(int tset)
     return rb;
 }
 
-// Rows per CTA of the N <= 8 kernel: 128 (eight consumer warps) while the
+// Rows per CTA of the N <= 8 kernel: 128 (four consumer warps) while the
 // weight ring stays within ~100 KB, halved while the grid would leave SMs idle.
 // Any choice gives the same bits: it only moves rows between CTAs.
 int gemv_rows(int tset, const int64_t *Ms, int nm, int ks)
@@ -310,7 +310,7 @@ qg_status run_product(qg_handle *const *hs, int nh, const __half *x, int64_t N, 
                 const dim3 grid((unsigned)p.ks, (unsigned)tiles, 1u);
                 cudaError_t le = fault_at("launch")
                                      ? cudaErrorLaunchOutOfResources
-                                     : launch_gemv_tset(gts, R / 16, p, grid, smem, s);
+                                     : launch_gemv_tset(gts, R / (16 * kGemvMT), p, grid, smem, s);
                 if (le != cudaSuccess) {
                     cudaGetLastError();
                     if (flags & QG_FLAG_NO_FALLBACK) {

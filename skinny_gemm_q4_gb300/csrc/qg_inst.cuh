@@ -107,9 +107,9 @@ static cudaError_t launch_gemv_one(const Params &p, dim3 grid, int smem, cudaStr
     cudaError_t launch_gemv_##NAME(int cw, const Params &p, dim3 grid, int smem, cudaStream_t s) \
     {                                                                                       \
         switch (cw) {                                                                       \
+        case 1: return launch_gemv_one<TSET, 1>(p, grid, smem, s);                          \
         case 2: return launch_gemv_one<TSET, 2>(p, grid, smem, s);                          \
         case 4: return launch_gemv_one<TSET, 4>(p, grid, smem, s);                          \
-        case 8: return launch_gemv_one<TSET, 8>(p, grid, smem, s);                          \
         default: return cudaErrorInvalidValue;                                              \
         }                                                                                   \
     }                                                                                       \

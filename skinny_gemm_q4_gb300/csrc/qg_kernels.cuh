@@ -225,53 +225,82 @@ __device__ __forceinline__ void stage_sb(uint4 v, int lane, uint8_t *q4, uint8_t
 // ---------------------------------------------------------------------------
 // Q4_K / Q5_K per-row constants from the 16-byte block header.
 // Thread t owns sub-blocks 2t (low nibbles of qs chunk t) and 2t+1 (high).
+// A operand = sc * q * 2^-22, exact in fp16 for every sc*q < 2048:
+//   Q4_K low nibble  (w & 0x000f000f)  = q * 2^-24, times 4 * sc
+//   Q4_K high nibble (w & 0x00f000f0)  = q * 2^-20, times sc / 4
+//   Q5_K both (five bits at bits 0..4) = q5 * 2^-24, times 4 * sc
+// Both scales come from a magic-number fp16 (0x6C00 | sc = 4096 + 4 sc;
+// 0x5C00 | sc = 256 + sc / 4) minus the magic.
 // ---------------------------------------------------------------------------
 struct KRow {
     uint32_t slo, shi;  // fp16x2 broadcast scale for the two sub-blocks
     uint32_t amin;      // fp16x2 (m_2t, m_2t+1) * 2^-24 (subnormals)
-    float dd, dm;       // d * 2^14 and -dmin * 2^24
+    float dd, dm;       // d * 2^22 and -dmin * 2^24
 };
 
-template <int T>
-__device__ __forceinline__ KRow k_row_consts(const uint4 &h, int t)
+// Per-thread selectors for the 6-bit scale/min unpacking (constant per lane).
+struct KSel {
+    uint32_t selx, selz;  // byte gathers of (scales[0..3], scales[8..11]) / (scales[4..7], ..)
+    uint32_t ma, mb;      // 0x3f3f, 0 for t < 2; 0x0f0f, 0x3030 for t >= 2
+    uint32_t sh;          // 0 for t < 2; 4 for t >= 2 (mins: high nibble)
+};
+
+__device__ __forceinline__ KSel k_sel(int t)
 {
-    const int sh = (t & 1) * 16;
-    const uint32_t Y = h.y >> sh, Z = h.z >> sh, W = h.w >> sh;
-    uint32_t sc, mn;
+    KSel s;
     if (t < 2) {
-        sc = Y & 0x3f3fu;
-        mn = Z & 0x3f3fu;
+        // bytes 2t, 2t+1 of word y (scales) / z (mins)
+        s.selx = (t == 0) ? 0x3210u : 0x3232u;
+        s.selz = s.selx;
+        s.ma = 0x3f3fu;
+        s.mb = 0u;
+        s.sh = 0u;
     } else {
-        sc = (W & 0x0f0fu) | ((Y >> 2) & 0x3030u);
-        mn = ((W >> 4) & 0x0f0fu) | ((Z >> 2) & 0x3030u);
+        // [w_2u, w_2u+1, y_2u, y_2u+1] (u = t - 2), word y/z first, w second
+        s.selx = (t == 2) ? 0x1054u : 0x3276u;
+        s.selz = s.selx;
+        s.ma = 0x0f0fu;
+        s.mb = 0x3030u;
+        s.sh = 4u;
     }
+    return s;
+}
+
+template <int T>
+__device__ __forceinline__ KRow k_row_consts(const uint4 &h, const KSel &ks)
+{
+    // scales: t < 2: y bytes & 63; t >= 2: (w & 15) | ((y >> 6) << 4)
+    const uint32_t X = __byte_perm(h.y, h.w, ks.selx);
+    const uint32_t sc = (X & ks.ma) | ((X >> 18) & ks.mb);
+    // mins:   t < 2: z bytes & 63; t >= 2: (w >> 4) | ((z >> 6) << 4)
+    const uint32_t Z = __byte_perm(h.z, h.w, ks.selz);
+    const uint32_t mn = ((Z >> ks.sh) & ks.ma) | ((Z >> 18) & ks.mb);
     KRow r;
-    const uint32_t v = __byte_perm(sc, 0x6464u, 0x5140u);  // (1024+sc0, 1024+sc1)
-    const uint32_t s01 = hsub2(v, 0x64006400u);           // (sc0, sc1), exact
-    // Q4_K: low nibbles are q*2^-24 -> scale sc*2^10; high nibbles sit at
-    // bits 4..7 (q*2^-20) -> scale sc*2^6.  Q5_K decodes both at q*2^-24.
-    const uint32_t hm = hmul2(s01, (T == T_Q4K) ? 0x54006400u : 0x64006400u);
-    r.slo = __byte_perm(hm, 0u, 0x1010u);
-    r.shi = __byte_perm(hm, 0u, 0x3232u);
+    if (T == T_Q4K) {
+        r.slo = hsub2(__byte_perm(sc, 0x5C6Cu, 0x4040u), 0x6C006C00u);  // 4 sc0
+        r.shi = hsub2(__byte_perm(sc, 0x5C6Cu, 0x5151u), 0x5C005C00u);  // sc1 / 4
+    } else {
+        r.slo = hsub2(__byte_perm(sc, 0x6C6Cu, 0x4040u), 0x6C006C00u);  // 4 sc0
+        r.shi = hsub2(__byte_perm(sc, 0x6C6Cu, 0x5151u), 0x6C006C00u);  // 4 sc1
+    }
     r.amin = __byte_perm(mn, 0u, 0x4140u);
     const float d = __half2float(__ushort_as_half((unsigned short)(h.x & 0xffffu)));
     const float dmin = __half2float(__ushort_as_half((unsigned short)(h.x >> 16)));
-    r.dd = d * 16384.0f;
+    r.dd = d * 4194304.0f;
     r.dm = -dmin * 16777216.0f;
     return r;
 }
 
 // ---------------------------------------------------------------------------
 // Per-super-block compute, one function per format.  wsl: this warp's first
-// weight row in shared memory (row pitch Fmt<T>::RB); xsl: this super-block's
-// staged x for token 0 (token stride xtok).  acc is [MT][G][4] in the mma
-// C-fragment layout: c0/c1 row g tokens 2t/2t+1, c2/c3 row g+8.
+// weight row in shared memory (row pitch RBP); xsl: this super-block's staged
+// x for token 0 (token stride xtok).  acc is [MT][G][4] in the mma C-fragment
+// layout: c0/c1 row g tokens 2t/2t+1, c2/c3 row g+8.
 // ---------------------------------------------------------------------------
-template <int T, int MT, int G>
+template <int T, int MT, int G, int RBP = Fmt<T>::RB>
 __device__ __forceinline__ void compute_kquant(uint32_t wsl, uint32_t xsl, int xtok, int g, int t,
-                                               int ntok, float (&acc)[MT][G][4])
+                                               int ntok, const KSel &ksel, float (&acc)[MT][G][4])
 {
-    constexpr int RB = Fmt<T>::RB;
     constexpr int QS = (T == T_Q4K) ? 16 : 48;  // qs offset in the block
     KRow rc[MT][2];
     uint4 q[MT][2][2];
@@ -280,9 +309,9 @@ __device__ __forceinline__ void compute_kquant(uint32_t wsl, uint32_t xsl, int x
     for (int mt = 0; mt < MT; ++mt) {
 #pragma unroll
         for (int rr = 0; rr < 2; ++rr) {
-            const uint32_t ra = wsl + (mt * 16 + g + 8 * rr) * RB;
+            const uint32_t ra = wsl + (mt * 16 + g + 8 * rr) * RBP;
             const uint4 h = lds128(ra);
-            rc[mt][rr] = k_row_consts<T>(h, t);
+            rc[mt][rr] = k_row_consts<T>(h, ksel);
             q[mt][rr][0] = lds128(ra + QS + 32 * t);
             q[mt][rr][1] = lds128(ra + QS + 32 * t + 16);
             if (T == T_Q5K) {
@@ -292,17 +321,6 @@ __device__ __forceinline__ void compute_kquant(uint32_t wsl, uint32_t xsl, int x
         }
     }
     float d1[2][MT][G][4];
-#pragma unroll
-    for (int e = 0; e < 2; ++e)
-#pragma unroll
-        for (int mt = 0; mt < MT; ++mt)
-#pragma unroll
-            for (int gi = 0; gi < G; ++gi)
-#pragma unroll
-                for (int c = 0; c < 4; ++c) d1[e][mt][gi][c] = 0.0f;
-
-    const bool tokok[G] = {};
-    (void)tokok;
 #pragma unroll
     for (int jp = 0; jp < 4; ++jp) {
 #pragma unroll
@@ -346,9 +364,13 @@ __device__ __forceinline__ void compute_kquant(uint32_t wsl, uint32_t xsl, int x
                     const uint32_t a2 = hmul2(p[0][1], s0);
                     const uint32_t a3 = hmul2(p[1][1], s1);
 #pragma unroll
-                    for (int gi = 0; gi < G; ++gi)
-                        mma16816(d1[e][mt][gi], a0, a1, a2, a3, jj ? B[gi].z : B[gi].x,
-                                 jj ? B[gi].w : B[gi].y);
+                    for (int gi = 0; gi < G; ++gi) {
+                        const uint32_t b0 = jj ? B[gi].z : B[gi].x, b1 = jj ? B[gi].w : B[gi].y;
+                        if (j == 0)
+                            mma16816_zc(d1[e][mt][gi], a0, a1, a2, a3, b0, b1);
+                        else
+                            mma16816(d1[e][mt][gi], a0, a1, a2, a3, b0, b1);
+                    }
                 }
             }
         }
@@ -541,7 +563,8 @@ __device__ __forceinline__ void compute_sb(Acc<T, MT, G> &A, uint32_t wsl, uint3
                                            int cp = Fmt<T>::RB, uint32_t fsc = 0)
 {
     if (T == T_Q4K || T == T_Q5K) {
-        compute_kquant<T, MT, G>(wsl, xsl, xtok, g, t, ntok, A.a[0]);
+        compute_kquant<T, MT, G>(wsl, xsl, xtok, g, t, ntok, k_sel(t), A.a[0]);
+        (void)cp;  // K-quant rows use the same pitch in both kernels
     } else if (T == T_Q6K) {
         int boff[MT][2];
 #pragma unroll
@@ -757,6 +780,7 @@ __global__ void __launch_bounds__(kThreads) skinny_kernel(const __grid_constant_
 // 576 bytes, token stride p.xtok].
 // ===========================================================================
 constexpr int kGemvStages = 4;
+constexpr int kGemvMT = 2;  // m16 tiles per consumer warp (32 rows)
 
 // Slot layout of one stage (R rows of one super-block):
 //   Q4_K / Q5_K : R rows x BB bytes (one 2-D tensor copy)
@@ -772,7 +796,8 @@ __device__ __forceinline__ void gemv_tile(const Params &p, const Mat &m, int rti
     constexpr bool TMA = (T != T_Q6K);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int g = lane >> 2, t = lane & 3;
-    const int R = p.rows_cta;                  // CW * 16 (or fewer for small launches)
+    constexpr int MTG = kGemvMT;
+    const int R = p.rows_cta;                  // CW * 32
     const int rank = blockIdx.x;
     const int ks = p.ks;
     const int sb0 = (rank * p.nb) / ks;
@@ -856,10 +881,10 @@ __device__ __forceinline__ void gemv_tile(const Params &p, const Mat &m, int rti
     }
     __syncthreads();
 
-    Acc<T, 1, 1> A;
+    Acc<T, MTG, 1> A;
     A.zero();
     const int c = warp - 1;
-    const int row_w = row0 + c * 16;
+    const int row_w = row0 + c * 16 * MTG;
     if (warp == 0) {
         for (int i = STAGES; i < nsb; ++i) {
             const int slot = i % STAGES;
@@ -870,7 +895,7 @@ __device__ __forceinline__ void gemv_tile(const Params &p, const Mat &m, int rti
             }
             produce(i);
         }
-    } else if (c * 16 < R) {
+    } else if (c * 16 * MTG < R) {
         for (int i = 0; i < nsb; ++i) {
             const int slot = i % STAGES;
             const uint32_t par = (i / STAGES) & 1;
@@ -880,11 +905,12 @@ __device__ __forceinline__ void gemv_tile(const Params &p, const Mat &m, int rti
             }
             const uint32_t sl = slots + slot * slot_bytes;
             if (T == T_FP4)
-                compute_sb<T, 1, 1>(A, sl + c * 16 * 128, xreg + i * kXTok, p.xtok, g, t, ntok, m,
-                                    row_w, sb0 + i, 128, sl + R * 128 + c * 16 * 16);
+                compute_sb<T, MTG, 1>(A, sl + c * 16 * MTG * 128, xreg + i * kXTok, p.xtok, g, t,
+                                      ntok, m, row_w, sb0 + i, 128,
+                                      sl + R * 128 + c * 16 * MTG * 16);
             else
-                compute_sb<T, 1, 1>(A, sl + c * 16 * F::RBG, xreg + i * kXTok, p.xtok, g, t, ntok,
-                                    m, row_w, sb0 + i, F::RBG);
+                compute_sb<T, MTG, 1>(A, sl + c * 16 * MTG * F::RBG, xreg + i * kXTok, p.xtok, g,
+                                      t, ntok, m, row_w, sb0 + i, F::RBG);
             __syncwarp();
             if (lane == 0) mbar_arrive(bar_empty + 8 * slot);
         }
@@ -902,8 +928,8 @@ __device__ __forceinline__ void gemv_tile(const Params &p, const Mat &m, int rti
     }
     if (err && p.err) atomicOr(p.err, err);
     __syncthreads();
-    const bool consumer = warp > 0 && c * 16 < R;
-    reduce_and_store<T, 1, 1>(A, reinterpret_cast<float *>(smem + 128), rank, ks,
+    const bool consumer = warp > 0 && c * 16 * MTG < R;
+    reduce_and_store<T, MTG, 1>(A, reinterpret_cast<float *>(smem + 128), rank, ks,
                               threadIdx.x - 32, blockDim.x - 32, consumer, p, m, row_w, 0, g, t);
 }
 
@@ -932,7 +958,7 @@ __host__ __device__ inline int gemv_smem_bytes(int rbg, int R, int N, int nsbr)
 {
     const int stages = kGemvStages * R * rbg;
     const int x = N * gemv_xtok(nsbr);
-    const int red = 4 * 4 * R * 2;  // reduction buffer overlays stages+x
+    const int red = 4 * 4 * R * 2;  // reduction buffer (R consumer threads x 8 floats)
     const int body = stages + x > red ? stages + x : red;
     return 128 + body;
 }
