@@ -26,11 +26,11 @@ struct qg_handle {
     int64_t row_bytes, sc_row_bytes, w_bytes;
     uint32_t flags;
     int max_tokens;
-    int ks;        // K-split ranks, fixed by K
+    int kw;        // K slices, fixed by (M, K)
     int layout;    // staged-x layout this format reads
     uint8_t *xs;   // staging buffer: max_tokens * nb * kXTok bytes
     unsigned int *err;  // device error word written by the kernels (timeouts)
-    CUtensorMap tmw[3], tms[3];  // 2-D maps for 32, 64, 128 rows per CTA
+    CUtensorMap tmw, tms;  // 3-D maps [block][row][bytes] for the N <= 8 kernel
     int device;
     void *hx;      // device buffers of the host-pointer entry point
     size_t hx_cap;
@@ -102,15 +102,16 @@ int tset_bit(qg_type t)
     }
 }
 
-// K-split: about six super-blocks per rank, at most 8 ranks (one cluster).
-// Depends on K only, so every row's reduction order is fixed by the shape.
-int plan_ks(int nb)
+// K slices: the smallest of 1, 2, 4, 8 that gives this matrix alone at least
+// 148 row tiles of 128 / kw rows (one CTA per SM of the N <= 8 kernel), and
+// never more than the super-blocks.  Depends on (M, K) only, so every row's
+// reduction order is fixed by the shape.
+int plan_kw(int64_t M, int nb)
 {
-    int ks = (nb + 5) / 6;
-    if (ks < 1) ks = 1;
-    if (ks > 8) ks = 8;
-    if (ks > nb) ks = nb;
-    return ks;
+    int kw = 1;
+    while (kw < 8 && kw < nb && (M + kGemvRows / kw - 1) / (kGemvRows / kw) < 148) kw *= 2;
+    if (kw > nb) kw = nb;
+    return kw;
 }
 
 int groups_for(int64_t n) { return n >= 32 ? 4 : (int)((n + 7) / 8); }
@@ -127,43 +128,34 @@ int rb_of_tset(int tset)
     return rb;
 }
 
-// Rows per CTA of the N <= 8 kernel: 128 (four consumer warps) while the
-// weight ring stays within ~100 KB, halved while the grid would leave SMs idle.
-// Any choice gives the same bits: it only moves rows between CTAs.
-int gemv_rows(int tset, const int64_t *Ms, int nm, int ks)
+// Stage bytes of the N <= 8 kernel for a format and slice count.
+int gemv_stage_bytes_host(qg_type t, int kw)
 {
-    int R = (kGemvStages * 128 * rb_of_tset(tset) <= 100 * 1024) ? 128 : 64;
-    auto ctas = [&](int r) {
-        int64_t c = 0;
-        for (int i = 0; i < nm; ++i) c += (Ms[i] + r - 1) / r;
-        return c * ks;
-    };
-    while (R > 32 && ctas(R) < 148) R /= 2;
-    return R;
+    const int R = kGemvRows / kw;
+    if (t == QG_Q6_K) return R * q6_pitch(kw);
+    if (t == QG_NVFP4_W4A16) return kw * R * (128 + 16);
+    return kw * R * block_bytes(t);
 }
 
-cudaError_t launch_gemv_tset(int tset, int cw, const Params &p, dim3 grid, int smem, cudaStream_t s)
+cudaError_t launch_gemv_tset(int tset, const Params &p, dim3 grid, int smem, cudaStream_t s)
 {
     switch (tset) {
-    case TS_Q4K: return launch_gemv_q4k(cw, p, grid, smem, s);
-    case TS_Q5K: return launch_gemv_q5k(cw, p, grid, smem, s);
-    case TS_Q6K: return launch_gemv_q6k(cw, p, grid, smem, s);
-    case TS_FP4: return launch_gemv_fp4(cw, p, grid, smem, s);
-    case TS_Q4K | TS_Q6K: return launch_gemv_q4k_q6k(cw, p, grid, smem, s);
+    case TS_Q4K: return launch_gemv_q4k(p, grid, smem, s);
+    case TS_Q5K: return launch_gemv_q5k(p, grid, smem, s);
+    case TS_Q6K: return launch_gemv_q6k(p, grid, smem, s);
+    case TS_FP4: return launch_gemv_fp4(p, grid, smem, s);
+    case TS_Q4K | TS_Q6K: return launch_gemv_q4k_q6k(p, grid, smem, s);
     default: return cudaErrorInvalidValue;
     }
 }
 
-int map_index(int R) { return R <= 32 ? 0 : (R <= 64 ? 1 : 2); }
-
-Mat mat_of(const qg_handle *h, void *y, const __half *res, int R = 0)
+Mat mat_of(const qg_handle *h, void *y, const __half *res)
 {
     Mat m;
     memset(&m, 0, sizeof m);
-    if (R > 0) {
-        m.tmw = h->tmw[map_index(R)];
-        m.tms = h->tms[map_index(R)];
-    }
+    m.tmw = h->tmw;
+    m.tms = h->tms;
+    m.kw = h->kw;
     m.w = h->w;
     m.sc = h->sc;
     m.y = y;
@@ -214,18 +206,19 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn()
     return fn;
 }
 
-// 2-D map over rows of `row_bytes` bytes viewed as 8-byte elements; box of
-// box_bytes x box_rows.
-bool encode_rows(CUtensorMap *m, const void *base, int64_t row_bytes, int64_t rows, int box_bytes,
-                 int box_rows)
+// 3-D map of a matrix of `rows` rows (row stride row_bytes) made of blocks of
+// `bb` bytes (viewed as 8-byte elements): dims (bytes of a block, row, block),
+// box (bb, box_rows, box_blocks), so a copy lands as [block][row][bytes].
+bool encode_blocks(CUtensorMap *m, const void *base, int64_t row_bytes, int64_t rows, int bb,
+                   int box_rows, int box_blocks)
 {
     PFN_cuTensorMapEncodeTiled_v12000 fn = encode_fn();
     if (!fn) return false;
-    cuuint64_t dims[2] = {(cuuint64_t)(row_bytes / 8), (cuuint64_t)rows};
-    cuuint64_t strides[1] = {(cuuint64_t)row_bytes};
-    cuuint32_t box[2] = {(cuuint32_t)(box_bytes / 8), (cuuint32_t)box_rows};
-    cuuint32_t estr[2] = {1, 1};
-    return fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT64, 2, const_cast<void *>(base), dims, strides, box,
+    cuuint64_t dims[3] = {(cuuint64_t)(bb / 8), (cuuint64_t)rows, (cuuint64_t)(row_bytes / bb)};
+    cuuint64_t strides[2] = {(cuuint64_t)row_bytes, (cuuint64_t)bb};
+    cuuint32_t box[3] = {(cuuint32_t)(bb / 8), (cuuint32_t)box_rows, (cuuint32_t)box_blocks};
+    cuuint32_t estr[3] = {1, 1, 1};
+    return fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT64, 3, const_cast<void *>(base), dims, strides, box,
               estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
@@ -274,25 +267,33 @@ qg_status run_product(qg_handle *const *hs, int nh, const __half *x, int64_t N, 
                 gsize[ng++] = 1;
             }
         }
+        // N <= 8 with the whole x of the call fitting in shared memory: one
+        // kernel per group, x staged inside the kernel.
+        int gemv_smem = 0, gemv_stages = 1;
         if (n <= 8) {
-            // N <= 8: one kernel per group, x staged inside the kernel.
+            int sbytes = 0, nst = 1;
+            for (int i = 0; i < nh; ++i) {
+                const int b = gemv_stage_bytes_host(hs[i]->type, hs[i]->kw);
+                if (b > sbytes) sbytes = b;
+                const int st = (h0->nb + hs[i]->kw - 1) / hs[i]->kw;
+                if (st > nst) nst = st;
+            }
+            gemv_stages = nst < kGemvStagesMax ? nst : kGemvStagesMax;
+            gemv_smem = gemv_smem_bytes(sbytes, gemv_stages, n, h0->nb);
+        }
+        if (n <= 8 && gemv_smem <= kGemvMaxSmem) {
             for (int gidx = 0; gidx < ng; ++gidx) {
                 Params p;
                 memset(&p, 0, sizeof p);
-                int gts = 0;
-                int64_t Ms[3];
-                for (int j = 0; j < gsize[gidx]; ++j) {
-                    gts |= tset_bit(hs[groups[gidx][j]]->type);
-                    Ms[j] = hs[groups[gidx][j]]->M;
-                }
-                const int R = gemv_rows(gts, Ms, gsize[gidx], h0->ks);
-                int tiles = 0;
+                int gts = 0, tiles = 0;
                 for (int j = 0; j < gsize[gidx]; ++j) {
                     const int idx = groups[gidx][j];
                     const qg_handle *h = hs[idx];
+                    gts |= tset_bit(h->type);
                     p.mat[j] = mat_of(h, (uint8_t *)ys[idx] + c0 * h->M * (out_f32 ? 4 : 2),
-                                      res ? res + c0 * h->M : nullptr, R);
+                                      res ? res + c0 * h->M : nullptr);
                     p.mat[j].tile_begin = tiles;
+                    const int R = kGemvRows / h->kw;
                     tiles += (int)((h->M + R - 1) / R);
                 }
                 p.nmat = gsize[gidx];
@@ -300,17 +301,14 @@ qg_status run_product(qg_handle *const *hs, int nh, const __half *x, int64_t N, 
                 p.N = n;
                 p.K = (int)h0->K;
                 p.nb = h0->nb;
-                p.ks = h0->ks;
-                p.rows_cta = R;
-                const int nsbr = (h0->nb + h0->ks - 1) / h0->ks;
-                p.xtok = gemv_xtok(nsbr);
+                p.ks = 1;
+                p.stages = gemv_stages;
+                p.xtok = gemv_xtok(h0->nb);
                 p.out_f32 = out_f32;
                 p.err = h0->err;
-                const int smem = gemv_smem_bytes(rb_of_tset(gts), R, n, nsbr);
-                const dim3 grid((unsigned)p.ks, (unsigned)tiles, 1u);
-                cudaError_t le = fault_at("launch")
-                                     ? cudaErrorLaunchOutOfResources
-                                     : launch_gemv_tset(gts, R / (16 * kGemvMT), p, grid, smem, s);
+                const dim3 grid(1u, (unsigned)tiles, 1u);
+                cudaError_t le = fault_at("launch") ? cudaErrorLaunchOutOfResources
+                                                    : launch_gemv_tset(gts, p, grid, gemv_smem, s);
                 if (le != cudaSuccess) {
                     cudaGetLastError();
                     if (flags & QG_FLAG_NO_FALLBACK) {
@@ -340,6 +338,16 @@ qg_status run_product(qg_handle *const *hs, int nh, const __half *x, int64_t N, 
 
         const int G = groups_for(n);
         const int rows = rows_per_cta(G);
+        // One launch serves handles of one cluster shape (equal kw).
+        bool same_kw = true;
+        for (int i = 1; i < nh; ++i) same_kw = same_kw && hs[i]->kw == h0->kw;
+        if (ng == 1 && !same_kw) {
+            ng = 0;
+            for (int i = 0; i < nh; ++i) {
+                groups[ng][0] = i;
+                gsize[ng++] = 1;
+            }
+        }
         for (int gidx = 0; gidx < ng; ++gidx) {
             Params p;
             memset(&p, 0, sizeof p);
@@ -359,7 +367,7 @@ qg_status run_product(qg_handle *const *hs, int nh, const __half *x, int64_t N, 
             p.N = n;
             p.tok_base = 0;
             p.nb = h0->nb;
-            p.ks = h0->ks;
+            p.ks = hs[groups[gidx][0]]->kw;
             p.K = (int)h0->K;
             p.out_f32 = out_f32;
             p.err = h0->err;
@@ -482,7 +490,7 @@ qg_status qgemv_create(qg_handle **out, qg_type t, int64_t M, int64_t K, const v
     h->w_bytes = h->row_bytes * M;
     h->flags = flags;
     h->max_tokens = max_tokens;
-    h->ks = plan_ks(nb);
+    h->kw = plan_kw(M, nb);
     h->layout = layout_of(t);
     h->device = dev;
     const size_t xs_bytes = (size_t)max_tokens * nb * kXTok;
@@ -494,16 +502,14 @@ qg_status qgemv_create(qg_handle **out, qg_type t, int64_t M, int64_t K, const v
     }
     if (t != QG_Q6_K) {
         const int bb = (t == QG_NVFP4_W4A16) ? 128 : block_bytes(t);
-        for (int i = 0; i < 3; ++i) {
-            const int R = 32 << i;
-            bool ok = encode_rows(&h->tmw[i], w_dev, h->row_bytes, M, bb, R);
-            if (ok && t == QG_NVFP4_W4A16)
-                ok = encode_rows(&h->tms[i], scales_dev, h->sc_row_bytes, M, 16, R);
-            if (!ok) {
-                cudaFree(h->xs);
-                delete h;
-                return fail(QG_ECUDA, "tensor map encoding failed");
-            }
+        const int R = kGemvRows / h->kw;
+        bool ok = encode_blocks(&h->tmw, w_dev, h->row_bytes, M, bb, R, h->kw);
+        if (ok && t == QG_NVFP4_W4A16)
+            ok = encode_blocks(&h->tms, scales_dev, h->sc_row_bytes, M, 16, R, h->kw);
+        if (!ok) {
+            cudaFree(h->xs);
+            delete h;
+            return fail(QG_ECUDA, "tensor map encoding failed");
         }
     }
     e = cudaMalloc((void **)&h->err, sizeof(unsigned int));
@@ -653,21 +659,22 @@ qg_status qgemv_plan_info(const qg_handle *h, int64_t N, int32_t *ksplit, int32_
     if (N < 1) return fail(QG_EINVAL, "N must be >= 1");
     const int64_t chunks = (N + h->max_tokens - 1) / h->max_tokens;
     const int64_t nfirst = N < h->max_tokens ? N : h->max_tokens;
-    if (ksplit) *ksplit = h->ks;
+    if (ksplit) *ksplit = h->kw;
     if (rows_cta) *rows_cta = rows_per_cta(groups_for(nfirst));
     if (launches) {
         int64_t l = 0;
         for (int64_t c = 0; c < chunks; ++c) {
             const int64_t n = (N - c * h->max_tokens) < h->max_tokens ? (N - c * h->max_tokens)
                                                                       : h->max_tokens;
-            l += ((h->flags & QG_FLAG_FORCE_REFERENCE) || n <= 8) ? 1 : 2;
+            const bool gemv = n <= 8 && gemv_smem_bytes(gemv_stage_bytes_host(h->type, h->kw),
+                                                        kGemvStagesMax, (int)n,
+                                                        h->nb) <= kGemvMaxSmem;
+            l += ((h->flags & QG_FLAG_FORCE_REFERENCE) || gemv) ? 1 : 2;
         }
         *launches = (int32_t)l;
     }
-    if (rows_cta && nfirst <= 8 && !(h->flags & QG_FLAG_FORCE_REFERENCE)) {
-        const int64_t Ms[1] = {h->M};
-        *rows_cta = gemv_rows(tset_bit(h->type), Ms, 1, h->ks);
-    }
+    if (rows_cta && nfirst <= 8 && !(h->flags & QG_FLAG_FORCE_REFERENCE))
+        *rows_cta = kGemvRows / h->kw;
     return QG_OK;
 }
 

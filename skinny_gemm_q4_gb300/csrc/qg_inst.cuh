@@ -41,9 +41,8 @@ static cudaError_t launch_one(const Params &p, dim3 grid, cudaStream_t stream)
     return cudaLaunchKernelEx(&cfg, skinny_kernel<TSET, G>, p);
 }
 
-constexpr int kGemvMaxSmem = 200 * 1024;
 
-template <int TSET, int CW>
+template <int TSET>
 static cudaError_t launch_gemv_one(const Params &p, dim3 grid, int smem, cudaStream_t stream)
 {
     static int configured[64] = {0};
@@ -53,31 +52,22 @@ static cudaError_t launch_gemv_one(const Params &p, dim3 grid, int smem, cudaStr
     if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
     if (smem > kGemvMaxSmem) return cudaErrorInvalidValue;
     if (!configured[dev]) {
-        e = cudaFuncSetAttribute(gemv_kernel<TSET, CW>,
-                                 cudaFuncAttributeMaxDynamicSharedMemorySize, kGemvMaxSmem);
+        e = cudaFuncSetAttribute(gemv_kernel<TSET>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 kGemvMaxSmem);
         if (e != cudaSuccess) return e;
         configured[dev] = 1;
     }
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = grid;
-    cfg.blockDim = dim3(32 * (CW + 1));
+    cfg.blockDim = dim3(32 * (kGemvCW + 1));
     cfg.dynamicSmemBytes = smem;
     cfg.stream = stream;
-    cudaLaunchAttribute attr[2];
-    int na = 0;
-    attr[na].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[na].val.programmaticStreamSerializationAllowed = 1;
-    ++na;
-    if (p.ks > 1) {
-        attr[na].id = cudaLaunchAttributeClusterDimension;
-        attr[na].val.clusterDim.x = (unsigned)p.ks;
-        attr[na].val.clusterDim.y = 1;
-        attr[na].val.clusterDim.z = 1;
-        ++na;
-    }
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
-    cfg.numAttrs = na;
-    return cudaLaunchKernelEx(&cfg, gemv_kernel<TSET, CW>, p);
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, gemv_kernel<TSET>, p);
 }
 
 }  // namespace qg
@@ -104,13 +94,8 @@ static cudaError_t launch_gemv_one(const Params &p, dim3 grid, int smem, cudaStr
         default: return 0;                                                                  \
         }                                                                                   \
     }                                                                                       \
-    cudaError_t launch_gemv_##NAME(int cw, const Params &p, dim3 grid, int smem, cudaStream_t s) \
+    cudaError_t launch_gemv_##NAME(const Params &p, dim3 grid, int smem, cudaStream_t s)  \
     {                                                                                       \
-        switch (cw) {                                                                       \
-        case 1: return launch_gemv_one<TSET, 1>(p, grid, smem, s);                          \
-        case 2: return launch_gemv_one<TSET, 2>(p, grid, smem, s);                          \
-        case 4: return launch_gemv_one<TSET, 4>(p, grid, smem, s);                          \
-        default: return cudaErrorInvalidValue;                                              \
-        }                                                                                   \
+        return launch_gemv_one<TSET>(p, grid, smem, s);                                     \
     }                                                                                       \
     }

@@ -69,6 +69,8 @@ struct Mat {
     int M;
     int type;
     int tile_begin;        // first row tile of this matrix in blockIdx.y
+    int kw;                // K slices (fixed by M and K): super-block sb belongs to
+                           // slice sb % kw; slice partial sums are added in slice order
     float gscale;          // NVFP4 per-tensor scale
 };
 
@@ -82,8 +84,8 @@ struct Params {
     int tok_base;                 // first token of blockIdx.z == 0
     int K;
     int nb;                       // 256-wide super-blocks along K
-    int ks;                       // K-split ranks (cluster size along x)
-    int rows_cta;                 // rows per CTA (gemv_kernel)
+    int ks;                       // cluster size along x (skinny_kernel: the matrices' kw)
+    int stages;                   // ring depth (gemv_kernel)
     int xtok;                     // token stride of the in-kernel x region (gemv_kernel)
     int out_f32;
     unsigned int *err;            // error word (timeouts)
@@ -397,11 +399,10 @@ __device__ __forceinline__ void compute_kquant(uint32_t wsl, uint32_t xsl, int x
 }
 
 template <int MT, int G>
-__device__ __forceinline__ void compute_q6k(uint32_t wsl, uint32_t xsl, int xtok, int g, int t,
-                                            int ntok, const int (&boff)[MT][2],
+__device__ __forceinline__ void compute_q6k(uint32_t wsl, int RB, uint32_t xsl, int xtok, int g,
+                                            int t, int ntok, const int (&boff)[MT][2],
                                             float (&acc)[MT][G][4])
 {
-    constexpr int RB = Fmt<T_Q6K>::RB;
     uint32_t sw[MT][2][4];  // int8 scales, 4 per word
     float dq[MT][2];
 #pragma unroll
@@ -560,12 +561,16 @@ struct Acc {
 template <int T, int MT, int G>
 __device__ __forceinline__ void compute_sb(Acc<T, MT, G> &A, uint32_t wsl, uint32_t xsl, int xtok,
                                            int g, int t, int ntok, const Mat &m, int row_w, int sb,
-                                           int cp = Fmt<T>::RB, uint32_t fsc = 0)
+                                           int cp = Fmt<T>::RB, uint32_t fsc = 0, int sb0q = -1)
 {
+    if (sb0q < 0) sb0q = sb;
     if (T == T_Q4K || T == T_Q5K) {
         compute_kquant<T, MT, G>(wsl, xsl, xtok, g, t, ntok, k_sel(t), A.a[0]);
         (void)cp;  // K-quant rows use the same pitch in both kernels
     } else if (T == T_Q6K) {
+        // The slot row holds the 16-byte aligned superset of a run of blocks
+        // starting at block sb0q; this block sits (address & 15) + (sb - sb0q)
+        // * 210 bytes into it.
         int boff[MT][2];
 #pragma unroll
         for (int mt = 0; mt < MT; ++mt)
@@ -573,9 +578,11 @@ __device__ __forceinline__ void compute_sb(Acc<T, MT, G> &A, uint32_t wsl, uint3
             for (int rr = 0; rr < 2; ++rr) {
                 const int row = min(row_w + mt * 16 + g + 8 * rr, m.M - 1);
                 boff[mt][rr] =
-                    (int)((uintptr_t)(m.w + (int64_t)row * m.row_bytes + (int64_t)sb * 210) & 15);
+                    (int)((uintptr_t)(m.w + (int64_t)row * m.row_bytes + (int64_t)sb0q * 210) &
+                          15) +
+                    (sb - sb0q) * 210;
             }
-        compute_q6k<MT, G>(wsl, xsl, xtok, g, t, ntok, boff, A.a[0]);
+        compute_q6k<MT, G>(wsl, cp, xsl, xtok, g, t, ntok, boff, A.a[0]);
     } else {
         compute_fp4<MT, G>(wsl, cp, fsc ? fsc : wsl + 128, fsc ? 16 : cp, xsl, xtok, g, t, ntok,
                            *reinterpret_cast<float(*)[2][MT][G][4]>(&A.a));
@@ -669,10 +676,9 @@ __device__ __forceinline__ void run_tile(const Params &p, const Mat &m, int rtil
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int g = lane >> 2, t = lane & 3;
     const int rank = blockIdx.x;
-    const int ks = p.ks;
-    const int sb0 = (rank * p.nb) / ks;
-    const int sb1 = ((rank + 1) * p.nb) / ks;
-    const int nsb = sb1 - sb0;
+    const int ks = p.ks;                       // == m.kw
+    // K slice `rank`: super-blocks rank, rank + ks, rank + 2 ks, ...
+    const int nsb = (p.nb - rank + ks - 1) / ks;
     const int tok0 = p.tok_base + blockIdx.z * kTokChunk;
     const int ntok = min(8 * G, p.N - tok0);
     const int row_w = rtile * Cfg<G>::ROWS + warp * MT * 16;
@@ -680,7 +686,7 @@ __device__ __forceinline__ void run_tile(const Params &p, const Mat &m, int rtil
     const uint8_t *xs = p.xs[F::XL] + (int64_t)tok0 * p.xs_tok_stride;
 
     auto issue_w = [&](int i) {
-        const int sb = sb0 + i;
+        const int sb = rank + i * ks;
         const uint32_t dst = sbase + (i % STAGES) * S::STAGE + warp * S::WSLOT;
 #pragma unroll 1
         for (int v = lane; v < MT * 16 * F::VPR; v += 32) {
@@ -707,7 +713,7 @@ __device__ __forceinline__ void run_tile(const Params &p, const Mat &m, int rtil
         }
     };
     auto issue_x = [&](int i) {
-        const int sb = sb0 + i;
+        const int sb = rank + i * ks;
         const uint32_t dst = sbase + (i % STAGES) * S::STAGE + S::WPART;
 #pragma unroll 1
         for (int v = threadIdx.x; v < ntok * F::XV; v += kThreads) {
@@ -745,7 +751,7 @@ __device__ __forceinline__ void run_tile(const Params &p, const Mat &m, int rtil
         cp_async_commit();
         const uint32_t stage = sbase + (i % STAGES) * S::STAGE;
         compute_sb<T, MT, G>(A, stage + warp * S::WSLOT, stage + S::WPART, kXTok, g, t, ntok, m,
-                             row_w, sb0 + i);
+                             row_w, rank + i * ks);
     }
     cp_async_wait<0>();
     __syncthreads();
@@ -779,42 +785,51 @@ __global__ void __launch_bounds__(kThreads) skinny_kernel(const __grid_constant_
 // of rows_cta * RB bytes | x region: N tokens x (this rank's super-blocks) x
 // 576 bytes, token stride p.xtok].
 // ===========================================================================
-constexpr int kGemvStages = 4;
-constexpr int kGemvMT = 2;  // m16 tiles per consumer warp (32 rows)
+constexpr int kGemvStagesMax = 4;
+constexpr int kGemvCW = 8;        // consumer warps per CTA
+constexpr int kGemvRows = 16 * kGemvCW;  // rows per CTA when kw == 1
 
-// Slot layout of one stage (R rows of one super-block):
-//   Q4_K / Q5_K : R rows x BB bytes (one 2-D tensor copy)
-//   NVFP4       : R x 128 code bytes, then R x 16 scale bytes (two copies)
-//   Q6_K        : R rows x 224 bytes, the 16-byte aligned superset of each
-//                 210-byte block (cp.async by the producer lanes; the block
-//                 starts (address & 15) bytes into its row)
-template <int T, int CW>
+// Bytes of one stage row for Q6_K: the 16-byte aligned superset of kw
+// consecutive 210-byte blocks.
+__host__ __device__ inline int q6_pitch(int kw) { return ((14 + 210 * kw) + 15) & ~15; }
+
+// Slot layout of one stage (R = 128 / kw rows, kw super-blocks: one per slice):
+//   Q4_K / Q5_K : [kw][R][BB]                 one 3-D tensor copy
+//   NVFP4       : [kw][R][128] codes, then [kw][R][16] scales (two copies)
+//   Q6_K        : [R][q6_pitch(kw)]          one 1-D bulk copy per row
+// Consumer warp c takes row tile c / kw and K slice c % kw.
+template <int T>
+__device__ __forceinline__ int gemv_stage_bytes(int kw)
+{
+    const int R = kGemvRows / kw;
+    if (T == T_Q6K) return R * q6_pitch(kw);
+    if (T == T_FP4) return kw * R * (128 + 16);
+    return kw * R * Fmt<T>::BB;
+}
+
+template <int T>
 __device__ __forceinline__ void gemv_tile(const Params &p, const Mat &m, int rtile, uint8_t *smem)
 {
     using F = Fmt<T>;
-    constexpr int STAGES = kGemvStages;
     constexpr bool TMA = (T != T_Q6K);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int g = lane >> 2, t = lane & 3;
-    constexpr int MTG = kGemvMT;
-    const int R = p.rows_cta;                  // CW * 32
-    const int rank = blockIdx.x;
-    const int ks = p.ks;
-    const int sb0 = (rank * p.nb) / ks;
-    const int sb1 = ((rank + 1) * p.nb) / ks;
-    const int nsb = sb1 - sb0;
+    const int kw = m.kw;
+    const int R = kGemvRows / kw;
+    const int STAGES = p.stages;
+    const int nst = (p.nb + kw - 1) / kw;      // stages of this CTA
     const int ntok = p.N;                      // <= 8
     const int row0 = rtile * R;
     const uint32_t sbase = smem_u32(smem);
-    const uint32_t bar_full = sbase, bar_empty = sbase + 8 * STAGES;
-    const int slot_bytes = R * F::RBG;
+    const uint32_t bar_full = sbase, bar_empty = sbase + 8 * kGemvStagesMax;
+    const int slot_bytes = gemv_stage_bytes<T>(kw);
     const uint32_t slots = sbase + 128;
     const uint32_t xreg = slots + STAGES * slot_bytes;
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < STAGES; ++s) {
             mbar_init(bar_full + 8 * s, TMA ? 1 : 32);
-            mbar_init(bar_empty + 8 * s, CW);
+            mbar_init(bar_empty + 8 * s, kGemvCW);
         }
         mbar_fence_init();
     }
@@ -824,69 +839,89 @@ __device__ __forceinline__ void gemv_tile(const Params &p, const Mat &m, int rti
     }
     __syncthreads();
 
-    // Producer: fill the slot of stage i (super-block sb0 + i).
+    // Producer: fill the slot of stage i (super-blocks i*kw .. i*kw + kw - 1).
     auto produce = [&](int i) {
         const int slot = i % STAGES;
-        const int sb = sb0 + i;
+        const int sbq = i * kw;
         const uint32_t dst = slots + slot * slot_bytes;
         const uint32_t fb = bar_full + 8 * slot;
         if (TMA) {
             if (lane == 0) {
+                mbar_arrive_expect_tx(fb, (uint32_t)slot_bytes);
                 if (T == T_FP4) {
-                    mbar_arrive_expect_tx(fb, (uint32_t)(R * (128 + 16)));
-                    tma_load_2d(dst, &m.tmw, sb * 16, row0, fb);
-                    tma_load_2d(dst + R * 128, &m.tms, sb * 2, row0, fb);
+                    tma_load_3d(dst, &m.tmw, 0, row0, sbq, fb);
+                    tma_load_3d(dst + kw * R * 128, &m.tms, 0, row0, sbq, fb);
                 } else {
-                    mbar_arrive_expect_tx(fb, (uint32_t)(R * F::BB));
-                    tma_load_2d(dst, &m.tmw, sb * (F::BB / 8), row0, fb);
+                    tma_load_3d(dst, &m.tmw, 0, row0, sbq, fb);
                 }
             }
         } else {
+            // Q6_K: per row, the aligned superset of the stage's blocks;
+            // anything past the end of the matrix is not read.
+            const int nv = min(kw, p.nb - sbq);
+            const int pitch = q6_pitch(kw);
             const uint8_t *end = m.w + m.w_bytes;
-            for (int v = lane; v < R * 14; v += 32) {
-                const int r = v / 14, c = v - r * 14;
+            uint32_t bytes = 0;
+            for (int r = lane; r < R; r += 32) {
                 const int row = row0 + r;
-                const uint8_t *src = m.w;
-                int n = 0;
-                if (row < m.M) {
-                    const uint8_t *blk = m.w + (int64_t)row * m.row_bytes + (int64_t)sb * 210;
-                    src = (const uint8_t *)((uintptr_t)blk & ~(uintptr_t)15) + c * 16;
-                    const int64_t left = end - src;
-                    n = left >= 16 ? 16 : (left > 0 ? (int)left : 0);
+                if (row >= m.M) continue;
+                const uint8_t *blk = m.w + (int64_t)row * m.row_bytes + (int64_t)sbq * 210;
+                const uint8_t *al = (const uint8_t *)((uintptr_t)blk & ~(uintptr_t)15);
+                const uint8_t *stop = blk + 210 * nv;
+                uint32_t n = (uint32_t)(((stop - al) + 15) & ~(int64_t)15);
+                if (al + n > end) {
+                    n = (uint32_t)((end - al) & ~(int64_t)15);
+                    uint8_t *d = smem + (dst - sbase) + r * pitch;
+                    for (uint32_t b = n; al + b < stop; ++b) d[b] = al[b];
                 }
-                cp_async16(dst + r * 224 + c * 16, src, n);
+                bytes += n;
             }
-            cp_async_mbar_arrive(fb);
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) bytes += __shfl_xor_sync(0xffffffffu, bytes, o);
+            __syncwarp();
+            if (lane == 0) mbar_arrive_expect_tx(fb, bytes);
+            __syncwarp();
+            for (int r = lane; r < R; r += 32) {
+                const int row = row0 + r;
+                if (row >= m.M) continue;
+                const uint8_t *blk = m.w + (int64_t)row * m.row_bytes + (int64_t)sbq * 210;
+                const uint8_t *al = (const uint8_t *)((uintptr_t)blk & ~(uintptr_t)15);
+                const uint8_t *stop = blk + 210 * nv;
+                uint32_t n = (uint32_t)(((stop - al) + 15) & ~(int64_t)15);
+                if (al + n > end) n = (uint32_t)((end - al) & ~(int64_t)15);
+                if (n) bulk_g2s(dst + r * pitch, al, n, fb);
+            }
         }
     };
 
     unsigned int err = 0;
     if (warp == 0) {
-        for (int i = 0; i < STAGES && i < nsb; ++i) produce(i);
+        for (int i = 0; i < STAGES && i < nst; ++i) produce(i);
     }
 
-    // x for this rank's super-blocks, staged by every warp (after the
-    // programmatic dependency: x may be written by the previous kernel).
+    // x for the whole K range, staged by every warp after the programmatic
+    // dependency (x may be written by the previous kernel).
     pdl_wait();
     {
         const int nwarps = blockDim.x >> 5;
-        for (int it = warp; it < ntok * nsb; it += nwarps) {
-            const int n = it / nsb, i = it - n * nsb;
+        for (int it = warp; it < ntok * p.nb; it += nwarps) {
+            const int n = it / p.nb, sb = it - n * p.nb;
             const uint4 v = *reinterpret_cast<const uint4 *>(
-                p.x + (int64_t)n * p.K + 256 * (sb0 + i) + 8 * lane);
-            uint8_t *dst = smem + (xreg - sbase) + n * p.xtok + i * kXTok;
+                p.x + (int64_t)n * p.K + 256 * sb + 8 * lane);
+            uint8_t *dst = smem + (xreg - sbase) + n * p.xtok + sb * kXTok;
             stage_sb(v, lane, F::XL == XL_Q4 ? dst : nullptr, F::XL == XL_Q6 ? dst : nullptr,
                      F::XL == XL_FP4 ? dst : nullptr);
         }
     }
     __syncthreads();
 
-    Acc<T, MTG, 1> A;
+    Acc<T, 1, 1> A;
     A.zero();
     const int c = warp - 1;
-    const int row_w = row0 + c * 16 * MTG;
+    const int mg = c / kw, ks = c - mg * kw;
+    const int row_w = row0 + 16 * mg;
     if (warp == 0) {
-        for (int i = STAGES; i < nsb; ++i) {
+        for (int i = STAGES; i < nst; ++i) {
             const int slot = i % STAGES;
             const uint32_t par = ((i / STAGES) - 1) & 1;
             if (!mbar_wait(bar_empty + 8 * slot, par)) {
@@ -895,32 +930,29 @@ __device__ __forceinline__ void gemv_tile(const Params &p, const Mat &m, int rti
             }
             produce(i);
         }
-    } else if (c * 16 * MTG < R) {
-        for (int i = 0; i < nsb; ++i) {
+    } else {
+        for (int i = 0; i < nst; ++i) {
             const int slot = i % STAGES;
             const uint32_t par = (i / STAGES) & 1;
             if (!mbar_wait(bar_full + 8 * slot, par)) {
                 err |= ERR_FULL_TIMEOUT;
                 break;
             }
-            const uint32_t sl = slots + slot * slot_bytes;
-            if (T == T_FP4)
-                compute_sb<T, MTG, 1>(A, sl + c * 16 * MTG * 128, xreg + i * kXTok, p.xtok, g, t,
-                                      ntok, m, row_w, sb0 + i, 128,
-                                      sl + R * 128 + c * 16 * MTG * 16);
-            else
-                compute_sb<T, MTG, 1>(A, sl + c * 16 * MTG * F::RBG, xreg + i * kXTok, p.xtok, g,
-                                      t, ntok, m, row_w, sb0 + i, F::RBG);
-            __syncwarp();
-            if (lane == 0) mbar_arrive(bar_empty + 8 * slot);
-        }
-    } else {
-        // idle consumer warp (fewer rows than warps): still releases slots
-        for (int i = 0; i < nsb; ++i) {
-            const int slot = i % STAGES;
-            if (!mbar_wait(bar_full + 8 * slot, (i / STAGES) & 1)) {
-                err |= ERR_FULL_TIMEOUT;
-                break;
+            const int sb = i * kw + ks;
+            if (sb < p.nb) {
+                const uint32_t sl = slots + slot * slot_bytes;
+                const uint32_t xsl = xreg + sb * kXTok;
+                if (T == T_FP4) {
+                    compute_sb<T, 1, 1>(A, sl + (ks * R + 16 * mg) * 128, xsl, p.xtok, g, t, ntok,
+                                        m, row_w, sb, 128,
+                                        sl + kw * R * 128 + (ks * R + 16 * mg) * 16);
+                } else if (T == T_Q6K) {
+                    compute_sb<T, 1, 1>(A, sl + 16 * mg * q6_pitch(kw), xsl, p.xtok, g, t, ntok,
+                                        m, row_w, sb, q6_pitch(kw), 0u, i * kw);
+                } else {
+                    compute_sb<T, 1, 1>(A, sl + (ks * R + 16 * mg) * F::BB, xsl, p.xtok, g, t,
+                                        ntok, m, row_w, sb);
+                }
             }
             __syncwarp();
             if (lane == 0) mbar_arrive(bar_empty + 8 * slot);
@@ -928,13 +960,40 @@ __device__ __forceinline__ void gemv_tile(const Params &p, const Mat &m, int rti
     }
     if (err && p.err) atomicOr(p.err, err);
     __syncthreads();
-    const bool consumer = warp > 0 && c * 16 * MTG < R;
-    reduce_and_store<T, MTG, 1>(A, reinterpret_cast<float *>(smem + 128), rank, ks,
-                              threadIdx.x - 32, blockDim.x - 32, consumer, p, m, row_w, 0, g, t);
+
+    // Slice partials: slices 1..kw-1 publish, slice 0 adds them in slice order.
+    float *red = reinterpret_cast<float *>(smem + 128);
+    float v[4];
+#pragma unroll
+    for (int cc = 0; cc < 4; ++cc) v[cc] = A.partial(0, 0, cc);
+    if (warp > 0 && ks > 0) {
+#pragma unroll
+        for (int cc = 0; cc < 4; ++cc) red[(c * 4 + cc) * 32 + lane] = v[cc];
+    }
+    __syncthreads();
+    if (warp == 0 || ks != 0) return;
+    for (int q = 1; q < kw; ++q) {
+#pragma unroll
+        for (int cc = 0; cc < 4; ++cc) v[cc] += red[((c + q) * 4 + cc) * 32 + lane];
+    }
+#pragma unroll
+    for (int cc = 0; cc < 4; ++cc) {
+        const int row = row_w + g + 8 * (cc >> 1);
+        const int tok = 2 * t + (cc & 1);
+        if (row >= m.M || tok >= p.N) continue;
+        float val = v[cc];
+        if (T == T_FP4) val = val * m.gscale;
+        const int64_t o = (int64_t)tok * m.M + row;
+        if (m.res) val = __fadd_rn(__half2float(m.res[o]), val);
+        if (p.out_f32)
+            reinterpret_cast<float *>(m.y)[o] = val;
+        else
+            reinterpret_cast<__half *>(m.y)[o] = __float2half_rn(val);
+    }
 }
 
-template <int TSET, int CW>
-__global__ void __launch_bounds__(32 * (CW + 1)) gemv_kernel(const __grid_constant__ Params p)
+template <int TSET>
+__global__ void __launch_bounds__(32 * (kGemvCW + 1)) gemv_kernel(const __grid_constant__ Params p)
 {
     extern __shared__ __align__(128) uint8_t smem[];
     pdl_trigger();
@@ -942,25 +1001,23 @@ __global__ void __launch_bounds__(32 * (CW + 1)) gemv_kernel(const __grid_consta
     const Mat &m = p.mat[select_mat(p, tile)];
     const int rtile = tile - m.tile_begin;
     if constexpr ((TSET & TS_Q4K) != 0)
-        if (m.type == T_Q4K) return gemv_tile<T_Q4K, CW>(p, m, rtile, smem);
+        if (m.type == T_Q4K) return gemv_tile<T_Q4K>(p, m, rtile, smem);
     if constexpr ((TSET & TS_Q5K) != 0)
-        if (m.type == T_Q5K) return gemv_tile<T_Q5K, CW>(p, m, rtile, smem);
+        if (m.type == T_Q5K) return gemv_tile<T_Q5K>(p, m, rtile, smem);
     if constexpr ((TSET & TS_Q6K) != 0)
-        if (m.type == T_Q6K) return gemv_tile<T_Q6K, CW>(p, m, rtile, smem);
+        if (m.type == T_Q6K) return gemv_tile<T_Q6K>(p, m, rtile, smem);
     if constexpr ((TSET & TS_FP4) != 0)
-        if (m.type == T_FP4) return gemv_tile<T_FP4, CW>(p, m, rtile, smem);
+        if (m.type == T_FP4) return gemv_tile<T_FP4>(p, m, rtile, smem);
 }
 
-// Dynamic shared memory of gemv_kernel for R rows per CTA, N tokens and nsbr
-// super-blocks per rank.
-__host__ __device__ inline int gemv_xtok(int nsbr) { return nsbr * kXTok + ((nsbr & 1) ? 0 : 64); }
-__host__ __device__ inline int gemv_smem_bytes(int rbg, int R, int N, int nsbr)
+// Dynamic shared memory of gemv_kernel: barriers, `stages` ring slots of
+// `stage_bytes`, and the x region of N tokens x nb super-blocks.
+__host__ __device__ inline int gemv_xtok(int nb) { return nb * kXTok + ((nb & 1) ? 0 : 64); }
+__host__ __device__ inline int gemv_smem_bytes(int stage_bytes, int stages, int N, int nb)
 {
-    const int stages = kGemvStages * R * rbg;
-    const int x = N * gemv_xtok(nsbr);
-    const int red = 4 * 4 * R * 2;  // reduction buffer (R consumer threads x 8 floats)
-    const int body = stages + x > red ? stages + x : red;
-    return 128 + body;
+    const int body = stages * stage_bytes + N * gemv_xtok(nb);
+    const int red = kGemvCW * 4 * 32 * 4;  // slice partials overlay the ring
+    return 128 + (body > red ? body : red);
 }
 
 }  // namespace qg

@@ -9,6 +9,7 @@ namespace qg {
 // Launch skinny_kernel<TSET, G> with `ks` CTAs per cluster along x and
 // programmatic dependent launch enabled.  Returns the launch status.
 cudaError_t launch_skinny(int tset, int G, const Params &p, dim3 grid, cudaStream_t stream);
+constexpr int kGemvMaxSmem = 200 * 1024;
 // Dynamic shared memory of skinny_kernel<TSET, G>.
 int skinny_smem_bytes(int tset, int G);
 
@@ -22,7 +23,7 @@ cudaError_t launch_ref_gemv(const Mat &m, int K, const __half *x, int N, int out
 #define QG_DECLARE_TSET(NAME)                                                           \
     cudaError_t launch_skinny_##NAME(int G, const Params &p, dim3 grid, cudaStream_t s); \
     int smem_skinny_##NAME(int G);                                                      \
-    cudaError_t launch_gemv_##NAME(int cw, const Params &p, dim3 grid, int smem, cudaStream_t s);
+    cudaError_t launch_gemv_##NAME(const Params &p, dim3 grid, int smem, cudaStream_t s);
 QG_DECLARE_TSET(q4k)
 QG_DECLARE_TSET(q5k)
 QG_DECLARE_TSET(q6k)

@@ -259,3 +259,18 @@ __device__ __forceinline__ void cp_async_mbar_arrive(uint32_t mbar)
 }
 
 }  // namespace qg
+
+namespace qg {
+
+// 3-D tiled tensor copy global->shared, completing on an mbarrier.
+__device__ __forceinline__ void tma_load_3d(uint32_t dst, const void *tmap, int x, int y, int z,
+                                            uint32_t mbar)
+{
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes "
+        "[%0], [%1, {%2, %3, %4}], [%5];\n" ::"r"(dst),
+        "l"(tmap), "r"(x), "r"(y), "r"(z), "r"(mbar)
+        : "memory");
+}
+
+}  // namespace qg

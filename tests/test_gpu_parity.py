@@ -209,8 +209,8 @@ def test_argument_errors_are_statuses():
     other, _, _, _ = make_matrix(qg.Q4_K, 64, 4096, seed=14)
     assert lib.qgemv_pair_run(h.h, other.h, x.data_ptr(), 1, y.data_ptr(), x.data_ptr(), 0,
                               None) == -1
-    ks, rows, launches = h.plan_info(1)
-    assert ks == 2 and rows == 32 and launches == 1      # N <= 8: one kernel
-    ks, rows, launches = h.plan_info(16)
-    assert ks == 2 and rows == 64 and launches == 2      # staging + product
+    kw, rows, launches = h.plan_info(1)
+    assert kw == 8 and rows == 16 and launches == 1      # N <= 8: one kernel
+    kw, rows, launches = h.plan_info(16)
+    assert kw == 8 and rows == 64 and launches == 2      # staging + product
     assert h.device_status() == 0
