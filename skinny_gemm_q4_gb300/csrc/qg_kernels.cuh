@@ -828,7 +828,7 @@ __device__ __forceinline__ void gemv_tile(const Params &p, const Mat &m, int rti
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < STAGES; ++s) {
-            mbar_init(bar_full + 8 * s, TMA ? 1 : 32);
+            mbar_init(bar_full + 8 * s, 1);
             mbar_init(bar_empty + 8 * s, kGemvCW);
         }
         mbar_fence_init();

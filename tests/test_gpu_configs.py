@@ -77,6 +77,8 @@ def test_decode_layer_fused_calls(N):
     rows = _sample_rows(2560, seed=7)
     yref, mag = oracle.qgemv(oracle.Q6_K, wd, 2560, 9728, xdn, rows=rows)
     check_close(yd.float().cpu().numpy()[:, rows], yref, mag, fp16_out=True, what="down")
+    for role in mats:
+        assert mats[role][0].device_status() == 0, role
 
 
 @pytest.mark.parametrize("qtype,M,K", synth.SWEEP_SHAPES)
