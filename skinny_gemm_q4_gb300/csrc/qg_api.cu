@@ -102,15 +102,14 @@ int tset_bit(qg_type t)
     }
 }
 
-// K slices: the smallest of 1, 2, 4, 8 that gives this matrix alone at least
+// K slices: the smallest power of two up to 8 that gives this matrix alone at least
 // 148 row tiles of 128 / kw rows (one CTA per SM of the N <= 8 kernel), and
 // never more than the super-blocks.  Depends on (M, K) only, so every row's
 // reduction order is fixed by the shape.
 int plan_kw(int64_t M, int nb)
 {
-    int kw = 1;
-    while (kw < 8 && kw < nb && (M + kGemvRows / kw - 1) / (kGemvRows / kw) < 148) kw *= 2;
-    if (kw > nb) kw = nb;
+    int kw = 1;  // a power of two: kGemvRows / kw rows are whole 16-row tiles
+    while (kw < 8 && 2 * kw <= nb && (M + kGemvRows / kw - 1) / (kGemvRows / kw) < 148) kw *= 2;
     return kw;
 }
 
