@@ -903,14 +903,32 @@ __device__ __forceinline__ void gemv_tile(const Params &p, const Mat &m, int rti
     // dependency (x may be written by the previous kernel).
     pdl_wait();
     {
+        // Loads for up to four items are in flight at once (one L2 round trip
+        // per four items instead of one per item).
+        constexpr int XU = 4;
         const int nwarps = blockDim.x >> 5;
-        for (int it = warp; it < ntok * p.nb; it += nwarps) {
-            const int n = it / p.nb, sb = it - n * p.nb;
-            const uint4 v = *reinterpret_cast<const uint4 *>(
-                p.x + (int64_t)n * p.K + 256 * sb + 8 * lane);
-            uint8_t *dst = smem + (xreg - sbase) + n * p.xtok + sb * kXTok;
-            stage_sb(v, lane, F::XL == XL_Q4 ? dst : nullptr, F::XL == XL_Q6 ? dst : nullptr,
-                     F::XL == XL_FP4 ? dst : nullptr);
+        const int total = ntok * p.nb;
+        for (int base = warp; base < total; base += XU * nwarps) {
+            uint4 v[XU];
+#pragma unroll
+            for (int u = 0; u < XU; ++u) {
+                const int it = base + u * nwarps;
+                if (it < total) {
+                    const int n = it / p.nb, sb = it - n * p.nb;
+                    v[u] = __ldg(reinterpret_cast<const uint4 *>(p.x + (int64_t)n * p.K +
+                                                                 256 * sb + 8 * lane));
+                }
+            }
+#pragma unroll
+            for (int u = 0; u < XU; ++u) {
+                const int it = base + u * nwarps;
+                if (it < total) {
+                    const int n = it / p.nb, sb = it - n * p.nb;
+                    uint8_t *dst = smem + (xreg - sbase) + n * p.xtok + sb * kXTok;
+                    stage_sb(v[u], lane, F::XL == XL_Q4 ? dst : nullptr,
+                             F::XL == XL_Q6 ? dst : nullptr, F::XL == XL_FP4 ? dst : nullptr);
+                }
+            }
         }
     }
     __syncthreads();
