@@ -278,6 +278,9 @@ qg_status run_product(qg_handle *const *hs, int nh, const __half *x, int64_t N, 
                 if (st > nst) nst = st;
             }
             gemv_stages = nst < kGemvStagesMax ? nst : kGemvStagesMax;
+            // Two CTAs per SM when a shallower ring allows it (never below 3).
+            while (gemv_stages > 3 && gemv_smem_bytes(sbytes, gemv_stages, n, h0->nb) > 110 * 1024)
+                --gemv_stages;
             gemv_smem = gemv_smem_bytes(sbytes, gemv_stages, n, h0->nb);
         }
         if (n <= 8 && gemv_smem <= kGemvMaxSmem) {

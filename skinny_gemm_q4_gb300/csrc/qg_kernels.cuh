@@ -398,11 +398,17 @@ __device__ __forceinline__ void compute_kquant(uint32_t wsl, uint32_t xsl, int x
     }
 }
 
-template <int MT, int G>
-__device__ __forceinline__ void compute_q6k(uint32_t wsl, int RB, uint32_t xsl, int xtok, int g,
-                                            int t, int ntok, const int (&boff)[MT][2],
-                                            float (&acc)[MT][G][4])
+// Q6_K: A = q - 32 (exact), one MMA per 16-weight scale group (C = 0), the
+// group's int8 scale applied in fp32 (accs += sc * D), the block's d once per
+// super-block (acc += d * accs).  Rows sit at byte offset boff[mt][rr] of
+// their row in shared memory (row pitch RB); ALIGNED: every such block start
+// is 4-byte aligned, so plain 32-bit loads read it.
+template <int MT, int G, bool ALIGNED>
+__device__ __forceinline__ void q6k_body(uint32_t wsl, int RB, uint32_t xsl, int xtok, int g, int t,
+                                         int ntok, const int (&boff)[MT][2],
+                                         float (&acc)[MT][G][4])
 {
+    auto ld = [&](uint32_t a) -> uint32_t { return ALIGNED ? lds32(a) : lds32_any(a); };
     uint32_t sw[MT][2][4];  // int8 scales, 4 per word
     float dq[MT][2];
 #pragma unroll
@@ -411,11 +417,11 @@ __device__ __forceinline__ void compute_q6k(uint32_t wsl, int RB, uint32_t xsl, 
         for (int rr = 0; rr < 2; ++rr) {
             const uint32_t ba = wsl + (mt * 16 + g + 8 * rr) * RB + boff[mt][rr];
 #pragma unroll
-            for (int i = 0; i < 4; ++i) sw[mt][rr][i] = lds32_any(ba + 192 + 4 * i);
-            dq[mt][rr] =
-                __half2float(__ushort_as_half((unsigned short)(lds32_any(ba + 208) & 0xffffu)));
+            for (int i = 0; i < 4; ++i) sw[mt][rr][i] = ld(ba + 192 + 4 * i);
+            dq[mt][rr] = __half2float(__ushort_as_half((unsigned short)(ld(ba + 208) & 0xffffu)));
         }
     }
+    float accs[MT][G][4];
 #pragma unroll
     for (int h = 0; h < 2; ++h) {
 #pragma unroll
@@ -427,9 +433,9 @@ __device__ __forceinline__ void compute_q6k(uint32_t wsl, int RB, uint32_t xsl, 
                 for (int rr = 0; rr < 2; ++rr) {
                     const uint32_t ba = wsl + (mt * 16 + g + 8 * rr) * RB + boff[mt][rr];
                     const uint32_t lo = 64 * h + 16 * i + 4 * t;
-                    ql0[mt][rr] = lds32_any(ba + lo);
-                    ql1[mt][rr] = lds32_any(ba + lo + 32);
-                    qh[mt][rr] = lds32_any(ba + 128 + 32 * h + 16 * i + 4 * t);
+                    ql0[mt][rr] = ld(ba + lo);
+                    ql1[mt][rr] = ld(ba + lo + 32);
+                    qh[mt][rr] = ld(ba + 128 + 32 * h + 16 * i + 4 * t);
                 }
             }
 #pragma unroll
@@ -444,10 +450,11 @@ __device__ __forceinline__ void compute_q6k(uint32_t wsl, int RB, uint32_t xsl, 
                                 : make_uint2(0u, 0u);
                 }
                 const int grp = 8 * h + i + 2 * s;  // scale index
+                const bool first = (h == 0 && i == 0 && s == 0);
 #pragma unroll
                 for (int mt = 0; mt < MT; ++mt) {
                     uint32_t a[2][2];
-                    float dsc[2];
+                    float scf[2];
 #pragma unroll
                     for (int rr = 0; rr < 2; ++rr) {
                         const uint32_t ql = (s & 1) ? ql1[mt][rr] : ql0[mt][rr];
@@ -457,9 +464,7 @@ __device__ __forceinline__ void compute_q6k(uint32_t wsl, int RB, uint32_t xsl, 
                         const uint32_t v = nw | (hw & 0x30303030u);
                         a[rr][0] = hsub2(__byte_perm(v, 0x6464u, 0x5240u), 0x64206420u);
                         a[rr][1] = hsub2(__byte_perm(v, 0x6464u, 0x5341u), 0x64206420u);
-                        const int scv =
-                            (int)(int8_t)((sw[mt][rr][grp >> 2] >> (8 * (grp & 3))) & 0xffu);
-                        dsc[rr] = dq[mt][rr] * (float)scv;
+                        scf[rr] = (float)(int8_t)((sw[mt][rr][grp >> 2] >> (8 * (grp & 3))) & 0xffu);
                     }
 #pragma unroll
                     for (int gi = 0; gi < G; ++gi) {
@@ -467,12 +472,37 @@ __device__ __forceinline__ void compute_q6k(uint32_t wsl, int RB, uint32_t xsl, 
                         mma16816_zc(d, a[0][0], a[1][0], a[0][1], a[1][1], B[gi].x, B[gi].y);
 #pragma unroll
                         for (int c = 0; c < 4; ++c)
-                            acc[mt][gi][c] = __fmaf_rn(dsc[c >> 1], d[c], acc[mt][gi][c]);
+                            accs[mt][gi][c] = first ? __fmul_rn(scf[c >> 1], d[c])
+                                                    : __fmaf_rn(scf[c >> 1], d[c], accs[mt][gi][c]);
                     }
                 }
             }
         }
     }
+#pragma unroll
+    for (int mt = 0; mt < MT; ++mt)
+#pragma unroll
+        for (int gi = 0; gi < G; ++gi)
+#pragma unroll
+            for (int c = 0; c < 4; ++c)
+                acc[mt][gi][c] = __fmaf_rn(dq[mt][c >> 1], accs[mt][gi][c], acc[mt][gi][c]);
+}
+
+template <int MT, int G>
+__device__ __forceinline__ void compute_q6k(uint32_t wsl, int RB, uint32_t xsl, int xtok, int g,
+                                            int t, int ntok, const int (&boff)[MT][2],
+                                            float (&acc)[MT][G][4])
+{
+    bool al = true;
+#pragma unroll
+    for (int mt = 0; mt < MT; ++mt)
+#pragma unroll
+        for (int rr = 0; rr < 2; ++rr) al = al && (((wsl + (mt * 16 + g + 8 * rr) * RB +
+                                                      boff[mt][rr]) & 3u) == 0);
+    if (__all_sync(0xffffffffu, al))
+        q6k_body<MT, G, true>(wsl, RB, xsl, xtok, g, t, ntok, boff, acc);
+    else
+        q6k_body<MT, G, false>(wsl, RB, xsl, xtok, g, t, ntok, boff, acc);
 }
 
 // NVFP4: acc is [2][MT][G][4] (two chains: even and odd steps).
