@@ -43,52 +43,70 @@ def _peaks():
 
 
 class ClockSampler:
-    """nvidia-smi clocks and throttle reasons sampled during the timed region."""
+    """nvidia-smi clocks and throttle reasons sampled every 20 ms by one
+    background nvidia-smi process; only samples taken inside the timed window
+    (mark_start / mark_end) are summarised."""
 
-    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+    FIELDS = ("timestamp,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
     def __init__(self, index: int):
         self.index = index
-        self.samples = []
-        self._stop = threading.Event()
-        self._t = None
-
-    def _run(self):
-        while not self._stop.is_set():
-            try:
-                out = subprocess.run(
-                    ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
-                     "--format=csv,noheader,nounits"], capture_output=True, text=True, timeout=5)
-                if out.returncode == 0 and out.stdout.strip():
-                    self.samples.append([v.strip() for v in out.stdout.strip().split(",")])
-            except Exception:
-                pass
-            self._stop.wait(0.1)
+        self.lines = []
+        self.proc = None
+        self.t0 = self.t1 = None
+        self._reader = None
 
     def __enter__(self):
-        self._t = threading.Thread(target=self._run, daemon=True)
-        self._t.start()
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "20"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+
+            def read():
+                for line in self.proc.stdout:
+                    self.lines.append((time.time(), line.strip()))
+            self._reader = threading.Thread(target=read, daemon=True)
+            self._reader.start()
+            time.sleep(0.3)  # first samples before the timed window opens
+        except Exception:
+            self.proc = None
         return self
 
+    def mark_start(self):
+        self.t0 = time.time()
+
+    def mark_end(self):
+        self.t1 = time.time()
+        # keep sampling briefly so the window's last interval is covered
+        time.sleep(0.05)
+
     def __exit__(self, *a):
-        self._stop.set()
-        if self._t:
-            self._t.join(timeout=10)
+        if self.proc:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
 
     def summary(self):
-        if not self.samples:
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"]}
-        sm = sorted(float(s[0]) for s in self.samples)
+        inside = [l for (t, l) in self.lines if self.t0 is not None and self.t0 - 0.03 <= t <= (self.t1 or 0) + 0.03]
+        rows = [[v.strip() for v in l.split(",")] for l in inside]
+        rows = [r for r in rows if len(r) >= 9]
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"], "samples": 0}
+        sm = sorted(float(r[1]) for r in rows)
         reasons = set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for s in self.samples:
-            for name, v in zip(names, s[4:8]):
+        for r in rows:
+            for name, v in zip(names, r[5:9]):
                 if v.lower().startswith("active"):
                     reasons.add(name)
-        return {"sm_mhz": sm[len(sm) // 2], "sm_max_mhz": float(self.samples[0][1]),
-                "reasons": sorted(reasons), "samples": len(self.samples)}
+        return {"sm_mhz": sm[len(sm) // 2], "sm_max_mhz": float(rows[0][2]),
+                "reasons": sorted(reasons), "samples": len(rows),
+                "power_w_max": max(float(r[3]) for r in rows if r[3].replace('.', '', 1).isdigit())}
 
 
 def _kernel_source_sha():
@@ -132,24 +150,37 @@ def run_reference(args):
     if rank != 0:
         return
     oracle.build()
-    frac = 16  # every 16th row of every matrix of the layer
-    mats = []
+    # Bounded sample: every frac-th row of each matrix of one layer, frac chosen
+    # so that warmup + steps take about a minute on this host in total.
+    full = []
     for i, (role, qt, M, K) in enumerate(synth.LAYER):
         w, sc, g = synth.weights(qt, M, K, seed=0, stream=100 + i)
-        rows = np.arange(0, M, frac)
         x = synth.activations(1, K, seed=0, stream=200 + i)
-        mats.append((qt, w, M, K, rows, x))
-    sample_bytes = sum(len(r) * synth.row_bytes(qt, K) for qt, w, M, K, r, x in mats)
+        full.append((qt, w, M, K, x))
 
-    def step():
+    def make(frac):
+        mats = [(qt, w, M, K, np.arange(0, M, frac), x) for qt, w, M, K, x in full]
+        nbytes = sum(len(r) * synth.row_bytes(qt, K) for qt, w, M, K, r, x in mats)
+        return mats, nbytes
+
+    def step(mats):
         for qt, w, M, K, rows, x in mats:
             oracle.qgemv(qt, w, M, K, x, rows=rows)
 
+    probe, probe_bytes = make(256)
+    t0 = time.perf_counter()
+    step(probe)
+    sec_per_byte = (time.perf_counter() - t0) / probe_bytes
+    budget = 60.0 / (args.steps + args.warmup)
+    frac = 16
+    while frac < 4096 and make(frac)[1] * sec_per_byte > budget:
+        frac *= 2
+    mats, sample_bytes = make(frac)
     for _ in range(args.warmup):
-        step()
+        step(mats)
     t0 = time.perf_counter()
     for _ in range(args.steps):
-        step()
+        step(mats)
     dt = (time.perf_counter() - t0) / args.steps
     gbs = sample_bytes / dt / 1e9
     line = {
@@ -198,7 +229,6 @@ def run_ours(args):
             w, sc, g = synth.device_weights(qt, M, K, seed=rank, stream=1000 * L + i, device=dev)
             hs[role] = qg.QGemv(qt, M, K, w, sc, g, max_tokens=32)
         layers.append(hs)
-    wbytes = layer_weight_bytes()
     x_qkv = synth.device_activations(1, 2560, 0, 1, dev)
     x_o = synth.device_activations(1, 4096, 0, 2, dev)
     res = synth.device_activations(1, 2560, 0, 3, dev)
@@ -213,17 +243,27 @@ def run_ours(args):
     yu = torch.empty((1, 9728), dtype=f16, device=dev)
     yd = torch.empty((1, 2560), dtype=f16, device=dev)
 
+    part = args.part
+
     def step(L):
         h = layers[L]
         s = torch.cuda.current_stream().cuda_stream
-        qg.qgemv_triple_run(h["wq"].h, h["wk"].h, h["wv"].h, x_qkv.data_ptr(), 1,
-                            yq.data_ptr(), yk.data_ptr(), yv.data_ptr(), qg.OUT_F16, s)
-        qg.qgemv_run_add(h["wo"].h, x_o.data_ptr(), 1, res.data_ptr(), yo.data_ptr(), s)
-        qg.qgemv_pair_run(h["gate"].h, h["up"].h, x_ffn.data_ptr(), 1, yg.data_ptr(),
-                          yu.data_ptr(), qg.OUT_F16, s)
-        qg.qgemv_run(h["down"].h, x_dn.data_ptr(), 1, yd.data_ptr(), qg.OUT_F16, s)
+        if part in ("layer", "qkv"):
+            qg.qgemv_triple_run(h["wq"].h, h["wk"].h, h["wv"].h, x_qkv.data_ptr(), 1,
+                                yq.data_ptr(), yk.data_ptr(), yv.data_ptr(), qg.OUT_F16, s)
+        if part in ("layer", "wo"):
+            qg.qgemv_run_add(h["wo"].h, x_o.data_ptr(), 1, res.data_ptr(), yo.data_ptr(), s)
+        if part in ("layer", "pair"):
+            qg.qgemv_pair_run(h["gate"].h, h["up"].h, x_ffn.data_ptr(), 1, yg.data_ptr(),
+                              yu.data_ptr(), qg.OUT_F16, s)
+        if part in ("layer", "down"):
+            qg.qgemv_run(h["down"].h, x_dn.data_ptr(), 1, yd.data_ptr(), qg.OUT_F16, s)
 
-    launches_per_step = 8  # 4 staging + 4 product kernels
+    roles = {"layer": [r for r, _, _, _ in synth.LAYER], "qkv": ["wq", "wk", "wv"],
+             "wo": ["wo"], "pair": ["gate", "up"], "down": ["down"]}[part]
+    wbytes = sum(M * synth.row_bytes(qt, K) for r, qt, M, K in synth.LAYER if r in roles)
+    # N = 1: one product kernel per call (x staged in-kernel)
+    launches_per_step = 4 if part == "layer" else 1
 
     for i in range(args.warmup):
         step(i % N_LAYERS)
@@ -248,10 +288,12 @@ def run_ours(args):
     with ClockSampler(local) as clk:
         barrier()
         torch.cuda.synchronize()
+        clk.mark_start()
         start.record()
         graph.replay()
         end.record()
         torch.cuda.synchronize()
+        clk.mark_end()
         barrier()
     ms = start.elapsed_time(end)
     if dist is not None:
@@ -286,14 +328,14 @@ def run_ours(args):
 
     # End to end through the host-buffer entry point: per matrix, x from
     # pinned host memory, y back to pinned host memory, synchronized.
-    e2e_steps = min(args.steps, N_LAYERS)
+    e2e_steps = min(args.steps, N_LAYERS) if part == "layer" else 0
     hx = {K: torch.from_numpy(np.random.default_rng(K).standard_normal((1, K)).astype(np.float16))
           .pin_memory() for K in (2560, 4096, 9728)}
     hy = {M: torch.empty((1, M), dtype=f16).pin_memory() for M in (4096, 1024, 2560, 9728)}
     h2d = sum(K * 2 for _, _, M, K in synth.LAYER)
     d2h = sum(M * 2 for _, _, M, K in synth.LAYER)
     s = torch.cuda.current_stream().cuda_stream
-    for L in range(2):
+    for L in range(2 if e2e_steps else 0):
         for role, qt, M, K in synth.LAYER:
             qg.qgemv_run_host(layers[L][role].h, hx[K].data_ptr(), 1, hy[M].data_ptr(),
                               qg.OUT_F16, s)
@@ -303,15 +345,15 @@ def run_ours(args):
         for role, qt, M, K in synth.LAYER:
             qg.qgemv_run_host(layers[i % N_LAYERS][role].h, hx[K].data_ptr(), 1,
                               hy[M].data_ptr(), qg.OUT_F16, s)
-    e2e_s = (time.perf_counter() - t0) / e2e_steps
+    e2e_s = (time.perf_counter() - t0) / max(e2e_steps, 1)
     barrier()
-    e2e_val = world * wbytes / e2e_s / 1e9
+    e2e_val = world * wbytes / e2e_s / 1e9 if e2e_steps else None
 
     if rank != 0:
         return
     # CPU baseline: the oracle on one whole layer (N = 1), single thread.
     cpu = None
-    if not args.no_cpu_baseline and world == 1:
+    if not args.no_cpu_baseline and world == 1 and part == "layer":
         import oracle
         oracle.build()
         t_cpu = 0.0
@@ -341,7 +383,8 @@ def run_ours(args):
         "vs_baseline": None,
         "dtype": "f16 x, fp32 accumulate, 4-bit weights",
         "data": "synthetic",
-        "config": {"workload": WORKLOAD, "N": 1, "layers_rotated": N_LAYERS,
+        "config": {"workload": WORKLOAD if part == "layer" else WORKLOAD + ":" + part, "N": 1,
+                   "layers_rotated": N_LAYERS,
                    "weight_bytes_per_step": wbytes,
                    "cold": "36 distinct layers (2.3 GB) > L2; no flush needed",
                    "pct_of_nominal_8TBps": round(100 * value / world / 8000.0, 2),
@@ -349,11 +392,11 @@ def run_ours(args):
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak,
                      "unit": "GB/s", "frac": round(achieved / peak, 4),
                      "traffic": _traffic_record(),
-                     "kernel": "gate/up pair call (staging + skinny_kernel<Q4_K, G=1>)",
+                     "kernel": "gate/up pair call: gemv_kernel<Q4_K> (one launch, N=1)",
                      "per_launch_us": round(pair_us, 3), "bytes_per_launch": pair_bytes,
                      "peak_kind": peak_kind},
         "cpu_baseline": cpu,
-        "e2e": {"value": round(e2e_val, 3), "unit": "GB/s", "h2d_bytes_per_step": h2d,
+        "e2e": None if e2e_val is None else {"value": round(e2e_val, 3), "unit": "GB/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h,
                 "how": "qgemv_run_host per matrix (pinned host x and y, synchronized)"},
         "gpu_launches": launches_per_step * args.steps,
@@ -365,10 +408,12 @@ def run_ours(args):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--steps", type=int, default=3600)
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--part", default="layer", choices=["layer", "qkv", "wo", "pair", "down"],
+                    help="time one call of the layer only (profiling); default: the whole layer")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
