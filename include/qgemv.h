@@ -160,6 +160,28 @@ qg_status qgemv_device_status(qg_handle *h, uint32_t *flags_out, int clear);
 qg_status qgemv_plan_info(const qg_handle *h, int64_t N, int32_t *ksplit,
                           int32_t *rows_per_cta, int32_t *launches);
 
+/* Allocation-free form of qgemv_run, for callers that may not allocate device
+ * memory while they run (for example a serving runtime that hands all device
+ * memory to its own pool at start-up, or a library that must keep its host
+ * process's device footprint fixed).  It needs no handle: the weights are
+ * described by the same arguments as qgemv_create (t, M, K, w_dev, scales_dev,
+ * global_scale; 16-byte aligned), x and y as in qgemv_run.  The pages have no
+ * counterpart: this is a library-usage variant of the staging + product path.
+ * Scratch: one 2 MiB array in the library's device memory (held by every GPU
+ * that loads the library until exit) holds the staged x; N is processed in
+ * chunks of min(32, 2 MiB / (K/256 * 576)) tokens and K above 931,840 is
+ * rejected with QG_EUNSUPPORTED.  It never calls cudaMalloc or cudaFree.  All
+ * calls on a device share the array and it keeps the last call's contents;
+ * every byte a call reads it has written first, so nothing needs clearing,
+ * but calls that overlap on the GPU (unordered streams) race and must be
+ * ordered.  The first call on a device looks up the array's address
+ * (cudaGetSymbolAddress) with that device current; make it before any stream
+ * capture.  Results equal qgemv_run's for the same weights.
+ * Errors: QG_EINVAL, QG_EALIGN, QG_EUNSUPPORTED, QG_ECUDA. */
+qg_status qgemv_run_noalloc(qg_type t, int64_t M, int64_t K, const void *w_dev,
+                            const void *scales_dev, float global_scale, const void *x,
+                            int64_t N, void *y, qg_out ydt, void *stream);
+
 /* Human-readable description of the options in effect (flags, environment
  * overrides QGEMV_FORCE_REFERENCE, QGEMV_DEBUG_SYNC, QGEMV_FAULT_INJECT). */
 const char *qgemv_describe(void);

@@ -422,6 +422,11 @@ qg_status check_run_args(const qg_handle *h, const void *x, int64_t N, const voi
 
 }  // namespace
 
+namespace qg {
+// Sets the calling thread's qgemv_last_error text (used by qg_noalloc.cu).
+void set_last_error(const char *msg) { g_err = msg; }
+}  // namespace qg
+
 extern "C" {
 
 int64_t qgemv_row_bytes(qg_type t, int64_t K)

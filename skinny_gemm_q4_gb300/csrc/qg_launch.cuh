@@ -6,9 +6,6 @@
 
 namespace qg {
 
-// Launch skinny_kernel<TSET, G> with `ks` CTAs per cluster along x and
-// programmatic dependent launch enabled.  Returns the launch status.
-cudaError_t launch_skinny(int tset, int G, const Params &p, dim3 grid, cudaStream_t stream);
 constexpr int kGemvMaxSmem = 200 * 1024;
 // Dynamic shared memory of skinny_kernel<TSET, G>.
 int skinny_smem_bytes(int tset, int G);

@@ -35,7 +35,8 @@ STATUS_NAMES = {0: "QG_OK", -1: "QG_EINVAL", -2: "QG_EUNSUPPORTED", -3: "QG_EALI
 #: every symbol include/qgemv.h declares
 EXPORTS = ["qgemv_create", "qgemv_run", "qgemv_run_add", "qgemv_pair_run", "qgemv_triple_run",
            "qgemv_run_host", "qgemv_dequantize", "qgemv_destroy", "qgemv_last_error",
-           "qgemv_row_bytes", "qgemv_plan_info", "qgemv_describe", "qgemv_device_status"]
+           "qgemv_row_bytes", "qgemv_plan_info", "qgemv_describe", "qgemv_device_status",
+           "qgemv_run_noalloc"]
 
 
 class QgOpts(ctypes.Structure):
@@ -158,6 +159,19 @@ def qgemv_device_status(h, clear: bool = False) -> int:
     _check(load().qgemv_device_status(h, ctypes.byref(w), 1 if clear else 0),
            "qgemv_device_status")
     return w.value
+
+
+def qgemv_run_noalloc(qtype, M, K, w_ptr, scales_ptr, global_scale, x_ptr, N, y_ptr, ydt,
+                      stream):
+    """Allocation-free product (no handle; scratch in a fixed device array)."""
+    lib = load()
+    f = lib.qgemv_run_noalloc
+    f.argtypes = [ctypes.c_int, ctypes.c_int64, ctypes.c_int64, ctypes.c_void_p, ctypes.c_void_p,
+                  ctypes.c_float, ctypes.c_void_p, ctypes.c_int64, ctypes.c_void_p, ctypes.c_int,
+                  ctypes.c_void_p]
+    f.restype = ctypes.c_int
+    _check(f(qtype, M, K, w_ptr or None, scales_ptr or None, global_scale, x_ptr, N, y_ptr, ydt,
+             stream), "qgemv_run_noalloc")
 
 
 # ----------------------------------------------------- torch convenience
