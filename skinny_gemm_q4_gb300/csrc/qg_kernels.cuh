@@ -591,11 +591,12 @@ struct Acc {
 template <int T, int MT, int G>
 __device__ __forceinline__ void compute_sb(Acc<T, MT, G> &A, uint32_t wsl, uint32_t xsl, int xtok,
                                            int g, int t, int ntok, const Mat &m, int row_w, int sb,
-                                           int cp = Fmt<T>::RB, uint32_t fsc = 0, int sb0q = -1)
+                                           const KSel &ksel, int cp = Fmt<T>::RB,
+                                           uint32_t fsc = 0, int sb0q = -1)
 {
     if (sb0q < 0) sb0q = sb;
     if (T == T_Q4K || T == T_Q5K) {
-        compute_kquant<T, MT, G>(wsl, xsl, xtok, g, t, ntok, k_sel(t), A.a[0]);
+        compute_kquant<T, MT, G>(wsl, xsl, xtok, g, t, ntok, ksel, A.a[0]);
         (void)cp;  // K-quant rows use the same pitch in both kernels
     } else if (T == T_Q6K) {
         // The slot row holds the 16-byte aligned superset of a run of blocks
@@ -767,6 +768,7 @@ __device__ __forceinline__ void run_tile(const Params &p, const Mat &m, int rtil
 
     Acc<T, MT, G> A;
     A.zero();
+    const KSel ksel = k_sel(t);
 #pragma unroll 1
     for (int i = 0; i < nsb; ++i) {
         if (i == 0)
@@ -781,7 +783,7 @@ __device__ __forceinline__ void run_tile(const Params &p, const Mat &m, int rtil
         cp_async_commit();
         const uint32_t stage = sbase + (i % STAGES) * S::STAGE;
         compute_sb<T, MT, G>(A, stage + warp * S::WSLOT, stage + S::WPART, kXTok, g, t, ntok, m,
-                             row_w, rank + i * ks);
+                             row_w, rank + i * ks, ksel);
     }
     cp_async_wait<0>();
     __syncthreads();
@@ -869,9 +871,8 @@ __device__ __forceinline__ void gemv_tile(const Params &p, const Mat &m, int rti
     }
     __syncthreads();
 
-    // Producer: fill the slot of stage i (super-blocks i*kw .. i*kw + kw - 1).
-    auto produce = [&](int i) {
-        const int slot = i % STAGES;
+    // Producer: fill slot `slot` with stage i (super-blocks i*kw .. i*kw + kw - 1).
+    auto produce = [&](int i, int slot) {
         const int sbq = i * kw;
         const uint32_t dst = slots + slot * slot_bytes;
         const uint32_t fb = bar_full + 8 * slot;
@@ -926,7 +927,7 @@ __device__ __forceinline__ void gemv_tile(const Params &p, const Mat &m, int rti
 
     unsigned int err = 0;
     if (warp == 0) {
-        for (int i = 0; i < STAGES && i < nst; ++i) produce(i);
+        for (int i = 0; i < STAGES && i < nst; ++i) produce(i, i);
     }
 
     // x for the whole K range, staged by every warp after the programmatic
@@ -968,20 +969,30 @@ __device__ __forceinline__ void gemv_tile(const Params &p, const Mat &m, int rti
     const int c = warp - 1;
     const int mg = c / kw, ks = c - mg * kw;
     const int row_w = row0 + 16 * mg;
+    const KSel ksel = k_sel(t);
     if (warp == 0) {
+        // stage i reuses slot i % STAGES after its consumers released it
+        int slot = 0;
+        uint32_t par = 0;
         for (int i = STAGES; i < nst; ++i) {
-            const int slot = i % STAGES;
-            const uint32_t par = ((i / STAGES) - 1) & 1;
             if (!mbar_wait(bar_empty + 8 * slot, par)) {
                 err |= ERR_EMPTY_TIMEOUT;
                 break;
             }
-            produce(i);
+            produce(i, slot);
+            if (++slot == STAGES) {
+                slot = 0;
+                par ^= 1u;
+            }
         }
     } else {
+        int slot = 0;
+        uint32_t par = 0;
+        const uint32_t wrow = (T == T_Q6K) ? (uint32_t)(16 * mg * q6_pitch(kw))
+                            : (T == T_FP4) ? (uint32_t)((ks * R + 16 * mg) * 128)
+                                           : (uint32_t)((ks * R + 16 * mg) * F::BB);
+        const uint32_t srow = (uint32_t)(kw * R * 128 + (ks * R + 16 * mg) * 16);
         for (int i = 0; i < nst; ++i) {
-            const int slot = i % STAGES;
-            const uint32_t par = (i / STAGES) & 1;
             if (!mbar_wait(bar_full + 8 * slot, par)) {
                 err |= ERR_FULL_TIMEOUT;
                 break;
@@ -991,19 +1002,21 @@ __device__ __forceinline__ void gemv_tile(const Params &p, const Mat &m, int rti
                 const uint32_t sl = slots + slot * slot_bytes;
                 const uint32_t xsl = xreg + sb * kXTok;
                 if (T == T_FP4) {
-                    compute_sb<T, 1, 1>(A, sl + (ks * R + 16 * mg) * 128, xsl, p.xtok, g, t, ntok,
-                                        m, row_w, sb, 128,
-                                        sl + kw * R * 128 + (ks * R + 16 * mg) * 16);
+                    compute_sb<T, 1, 1>(A, sl + wrow, xsl, p.xtok, g, t, ntok, m, row_w, sb, ksel,
+                                        128, sl + srow);
                 } else if (T == T_Q6K) {
-                    compute_sb<T, 1, 1>(A, sl + 16 * mg * q6_pitch(kw), xsl, p.xtok, g, t, ntok,
-                                        m, row_w, sb, q6_pitch(kw), 0u, i * kw);
+                    compute_sb<T, 1, 1>(A, sl + wrow, xsl, p.xtok, g, t, ntok, m, row_w, sb, ksel,
+                                        q6_pitch(kw), 0u, i * kw);
                 } else {
-                    compute_sb<T, 1, 1>(A, sl + (ks * R + 16 * mg) * F::BB, xsl, p.xtok, g, t,
-                                        ntok, m, row_w, sb);
+                    compute_sb<T, 1, 1>(A, sl + wrow, xsl, p.xtok, g, t, ntok, m, row_w, sb, ksel);
                 }
             }
             __syncwarp();
             if (lane == 0) mbar_arrive(bar_empty + 8 * slot);
+            if (++slot == STAGES) {
+                slot = 0;
+                par ^= 1u;
+            }
         }
     }
     if (err && p.err) atomicOr(p.err, err);
