@@ -52,8 +52,11 @@ static cudaError_t launch_gemv_one(const Params &p, dim3 grid, int smem, cudaStr
     if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
     if (smem > kGemvMaxSmem) return cudaErrorInvalidValue;
     if (!configured[dev]) {
-        e = cudaFuncSetAttribute(gemv_kernel<TSET>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 kGemvMaxSmem);
+        e = cudaFuncSetAttribute(gemv_kernel<TSET, false>,
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize, kGemvMaxSmem);
+        if (e != cudaSuccess) return e;
+        e = cudaFuncSetAttribute(gemv_kernel<TSET, true>,
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize, kGemvMaxSmem);
         if (e != cudaSuccess) return e;
         configured[dev] = 1;
     }
@@ -67,7 +70,8 @@ static cudaError_t launch_gemv_one(const Params &p, dim3 grid, int smem, cudaStr
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, gemv_kernel<TSET>, p);
+    if (p.N == 1) return cudaLaunchKernelEx(&cfg, gemv_kernel<TSET, true>, p);
+    return cudaLaunchKernelEx(&cfg, gemv_kernel<TSET, false>, p);
 }
 
 }  // namespace qg

@@ -299,7 +299,7 @@ __device__ __forceinline__ KRow k_row_consts(const uint4 &h, const KSel &ks)
 // x for token 0 (token stride xtok).  acc is [MT][G][4] in the mma C-fragment
 // layout: c0/c1 row g tokens 2t/2t+1, c2/c3 row g+8.
 // ---------------------------------------------------------------------------
-template <int T, int MT, int G, int RBP = Fmt<T>::RB>
+template <int T, int MT, int G, bool ODD = true, int RBP = Fmt<T>::RB>
 __device__ __forceinline__ void compute_kquant(uint32_t wsl, uint32_t xsl, int xtok, int g, int t,
                                                int ntok, const KSel &ksel, float (&acc)[MT][G][4])
 {
@@ -322,18 +322,19 @@ __device__ __forceinline__ void compute_kquant(uint32_t wsl, uint32_t xsl, int x
             }
         }
     }
-    float d1[2][MT][G][4];
+    // Token columns past ntok read the last real token (their results are
+    // never stored), so the B loads need no predicate.
+    uint32_t xb[G];
+#pragma unroll
+    for (int gi = 0; gi < G; ++gi) xb[gi] = xsl + min(8 * gi + g, ntok - 1) * xtok;
+    float d1[MT][G][4];
 #pragma unroll
     for (int jp = 0; jp < 4; ++jp) {
 #pragma unroll
         for (int e = 0; e < 2; ++e) {
             uint4 B[G];
 #pragma unroll
-            for (int gi = 0; gi < G; ++gi) {
-                const int tok = 8 * gi + g;
-                B[gi] = (tok < ntok) ? lds128(xsl + tok * xtok + ((jp * 2 + e) * 4 + t) * 16)
-                                     : make_uint4(0u, 0u, 0u, 0u);
-            }
+            for (int gi = 0; gi < G; ++gi) B[gi] = lds128(xb[gi] + ((jp * 2 + e) * 4 + t) * 16);
 #pragma unroll
             for (int jj = 0; jj < 2; ++jj) {
                 const int j = 2 * jp + jj;
@@ -368,10 +369,10 @@ __device__ __forceinline__ void compute_kquant(uint32_t wsl, uint32_t xsl, int x
 #pragma unroll
                     for (int gi = 0; gi < G; ++gi) {
                         const uint32_t b0 = jj ? B[gi].z : B[gi].x, b1 = jj ? B[gi].w : B[gi].y;
-                        if (j == 0)
-                            mma16816_zc(d1[e][mt][gi], a0, a1, a2, a3, b0, b1);
+                        if (j == 0 && e == 0)
+                            mma16816_zc(d1[mt][gi], a0, a1, a2, a3, b0, b1);
                         else
-                            mma16816(d1[e][mt][gi], a0, a1, a2, a3, b0, b1);
+                            mma16816(d1[mt][gi], a0, a1, a2, a3, b0, b1);
                     }
                 }
             }
@@ -380,8 +381,7 @@ __device__ __forceinline__ void compute_kquant(uint32_t wsl, uint32_t xsl, int x
     // Mins: one MMA against the per-sub-block sums of x, then the fold.
 #pragma unroll
     for (int gi = 0; gi < G; ++gi) {
-        const int tok = 8 * gi + g;
-        const uint2 bm = (tok < ntok) ? lds64(xsl + tok * xtok + 512 + 8 * t) : make_uint2(0u, 0u);
+        const uint2 bm = lds64(xb[gi] + 512 + 8 * t);
 #pragma unroll
         for (int mt = 0; mt < MT; ++mt) {
             float d2[4];
@@ -389,9 +389,9 @@ __device__ __forceinline__ void compute_kquant(uint32_t wsl, uint32_t xsl, int x
                         bm.y);
 #pragma unroll
             for (int c = 0; c < 4; ++c) {
+                if (!ODD && (c & 1)) continue;
                 const KRow &r = rc[mt][c >> 1];
-                acc[mt][gi][c] = __fmaf_rn(r.dd, d1[0][mt][gi][c], acc[mt][gi][c]);
-                acc[mt][gi][c] = __fmaf_rn(r.dd, d1[1][mt][gi][c], acc[mt][gi][c]);
+                acc[mt][gi][c] = __fmaf_rn(r.dd, d1[mt][gi][c], acc[mt][gi][c]);
                 acc[mt][gi][c] = __fmaf_rn(r.dm, d2[c], acc[mt][gi][c]);
             }
         }
@@ -403,11 +403,14 @@ __device__ __forceinline__ void compute_kquant(uint32_t wsl, uint32_t xsl, int x
 // super-block (acc += d * accs).  Rows sit at byte offset boff[mt][rr] of
 // their row in shared memory (row pitch RB); ALIGNED: every such block start
 // is 4-byte aligned, so plain 32-bit loads read it.
-template <int MT, int G, bool ALIGNED>
+template <int MT, int G, bool ALIGNED, bool ODD>
 __device__ __forceinline__ void q6k_body(uint32_t wsl, int RB, uint32_t xsl, int xtok, int g, int t,
                                          int ntok, const int (&boff)[MT][2],
                                          float (&acc)[MT][G][4])
 {
+    uint32_t xb[G];
+#pragma unroll
+    for (int gi = 0; gi < G; ++gi) xb[gi] = xsl + min(8 * gi + g, ntok - 1) * xtok;
     auto ld = [&](uint32_t a) -> uint32_t { return ALIGNED ? lds32(a) : lds32_any(a); };
     uint32_t sw[MT][2][4];  // int8 scales, 4 per word
     float dq[MT][2];
@@ -441,14 +444,10 @@ __device__ __forceinline__ void q6k_body(uint32_t wsl, int RB, uint32_t xsl, int
 #pragma unroll
             for (int s = 0; s < 4; ++s) {
                 uint2 B[G];
+                // unit (h, s, t) holds the 4-groups i = 0 and 1
 #pragma unroll
-                for (int gi = 0; gi < G; ++gi) {
-                    const int tok = 8 * gi + g;
-                    // unit (h, s, t) holds the 4-groups i = 0 and 1
-                    B[gi] = (tok < ntok)
-                                ? lds64(xsl + tok * xtok + ((h * 4 + s) * 4 + t) * 16 + 8 * i)
-                                : make_uint2(0u, 0u);
-                }
+                for (int gi = 0; gi < G; ++gi)
+                    B[gi] = lds64(xb[gi] + ((h * 4 + s) * 4 + t) * 16 + 8 * i);
                 const int grp = 8 * h + i + 2 * s;  // scale index
                 const bool first = (h == 0 && i == 0 && s == 0);
 #pragma unroll
@@ -471,9 +470,11 @@ __device__ __forceinline__ void q6k_body(uint32_t wsl, int RB, uint32_t xsl, int
                         float d[4];
                         mma16816_zc(d, a[0][0], a[1][0], a[0][1], a[1][1], B[gi].x, B[gi].y);
 #pragma unroll
-                        for (int c = 0; c < 4; ++c)
+                        for (int c = 0; c < 4; ++c) {
+                            if (!ODD && (c & 1)) continue;
                             accs[mt][gi][c] = first ? __fmul_rn(scf[c >> 1], d[c])
                                                     : __fmaf_rn(scf[c >> 1], d[c], accs[mt][gi][c]);
+                        }
                     }
                 }
             }
@@ -484,11 +485,13 @@ __device__ __forceinline__ void q6k_body(uint32_t wsl, int RB, uint32_t xsl, int
 #pragma unroll
         for (int gi = 0; gi < G; ++gi)
 #pragma unroll
-            for (int c = 0; c < 4; ++c)
+            for (int c = 0; c < 4; ++c) {
+                if (!ODD && (c & 1)) continue;
                 acc[mt][gi][c] = __fmaf_rn(dq[mt][c >> 1], accs[mt][gi][c], acc[mt][gi][c]);
+            }
 }
 
-template <int MT, int G>
+template <int MT, int G, bool ODD>
 __device__ __forceinline__ void compute_q6k(uint32_t wsl, int RB, uint32_t xsl, int xtok, int g,
                                             int t, int ntok, const int (&boff)[MT][2],
                                             float (&acc)[MT][G][4])
@@ -500,9 +503,9 @@ __device__ __forceinline__ void compute_q6k(uint32_t wsl, int RB, uint32_t xsl, 
         for (int rr = 0; rr < 2; ++rr) al = al && (((wsl + (mt * 16 + g + 8 * rr) * RB +
                                                       boff[mt][rr]) & 3u) == 0);
     if (__all_sync(0xffffffffu, al))
-        q6k_body<MT, G, true>(wsl, RB, xsl, xtok, g, t, ntok, boff, acc);
+        q6k_body<MT, G, true, ODD>(wsl, RB, xsl, xtok, g, t, ntok, boff, acc);
     else
-        q6k_body<MT, G, false>(wsl, RB, xsl, xtok, g, t, ntok, boff, acc);
+        q6k_body<MT, G, false, ODD>(wsl, RB, xsl, xtok, g, t, ntok, boff, acc);
 }
 
 // NVFP4: acc is [2][MT][G][4] (two chains: even and odd steps).
@@ -534,11 +537,9 @@ __device__ __forceinline__ void compute_fp4(uint32_t cbase, int cp, uint32_t sba
         for (int sp = 0; sp < 4; ++sp) {
             uint4 B[G];
 #pragma unroll
-            for (int gi = 0; gi < G; ++gi) {
-                const int tok = 8 * gi + g;
-                B[gi] = (tok < ntok) ? lds128(xsl + tok * xtok + ((hf * 4 + sp) * 4 + t) * 16)
-                                     : make_uint4(0u, 0u, 0u, 0u);
-            }
+            for (int gi = 0; gi < G; ++gi)
+                B[gi] = lds128(xsl + min(8 * gi + g, ntok - 1) * xtok +
+                               ((hf * 4 + sp) * 4 + t) * 16);
 #pragma unroll
             for (int jj = 0; jj < 2; ++jj) {
                 const int s = 2 * sp + jj;  // step: bytes 2s, 2s+1 of the thread's 16
@@ -588,7 +589,7 @@ struct Acc {
 // wsl: the warp's first weight row; for NVFP4 the codes use pitch `cp` and
 // the scales start at `fsc` with a 16-byte pitch when fsc != 0 (else they
 // follow each code row at +128 with the same pitch).
-template <int T, int MT, int G>
+template <int T, int MT, int G, bool ODD = true>
 __device__ __forceinline__ void compute_sb(Acc<T, MT, G> &A, uint32_t wsl, uint32_t xsl, int xtok,
                                            int g, int t, int ntok, const Mat &m, int row_w, int sb,
                                            const KSel &ksel, int cp = Fmt<T>::RB,
@@ -596,7 +597,7 @@ __device__ __forceinline__ void compute_sb(Acc<T, MT, G> &A, uint32_t wsl, uint3
 {
     if (sb0q < 0) sb0q = sb;
     if (T == T_Q4K || T == T_Q5K) {
-        compute_kquant<T, MT, G>(wsl, xsl, xtok, g, t, ntok, ksel, A.a[0]);
+        compute_kquant<T, MT, G, ODD>(wsl, xsl, xtok, g, t, ntok, ksel, A.a[0]);
         (void)cp;  // K-quant rows use the same pitch in both kernels
     } else if (T == T_Q6K) {
         // The slot row holds the 16-byte aligned superset of a run of blocks
@@ -613,7 +614,7 @@ __device__ __forceinline__ void compute_sb(Acc<T, MT, G> &A, uint32_t wsl, uint3
                           15) +
                     (sb - sb0q) * 210;
             }
-        compute_q6k<MT, G>(wsl, cp, xsl, xtok, g, t, ntok, boff, A.a[0]);
+        compute_q6k<MT, G, ODD>(wsl, cp, xsl, xtok, g, t, ntok, boff, A.a[0]);
     } else {
         compute_fp4<MT, G>(wsl, cp, fsc ? fsc : wsl + 128, fsc ? 16 : cp, xsl, xtok, g, t, ntok,
                            *reinterpret_cast<float(*)[2][MT][G][4]>(&A.a));
@@ -839,7 +840,7 @@ __device__ __forceinline__ int gemv_stage_bytes(int kw)
     return kw * R * Fmt<T>::BB;
 }
 
-template <int T>
+template <int T, bool ODD>
 __device__ __forceinline__ void gemv_tile(const Params &p, const Mat &m, int rtile, uint8_t *smem)
 {
     using F = Fmt<T>;
@@ -936,28 +937,39 @@ __device__ __forceinline__ void gemv_tile(const Params &p, const Mat &m, int rti
     {
         // Loads for up to four items are in flight at once (one L2 round trip
         // per four items instead of one per item).
+        // Item it = n * nb + sb; this warp takes it = warp, warp + nwarps, ...
+        // and steps (n, sb) without dividing.
         constexpr int XU = 4;
         const int nwarps = blockDim.x >> 5;
-        const int total = ntok * p.nb;
+        const int nb = p.nb;
+        const int total = ntok * nb;
+        int n = 0, sb = warp;
+        while (sb >= nb) {
+            sb -= nb;
+            ++n;
+        }
         for (int base = warp; base < total; base += XU * nwarps) {
             uint4 v[XU];
+            uint32_t dst[XU];
 #pragma unroll
             for (int u = 0; u < XU; ++u) {
-                const int it = base + u * nwarps;
-                if (it < total) {
-                    const int n = it / p.nb, sb = it - n * p.nb;
+                if (base + u * nwarps < total) {
                     v[u] = __ldg(reinterpret_cast<const uint4 *>(p.x + (int64_t)n * p.K +
                                                                  256 * sb + 8 * lane));
+                    dst[u] = (uint32_t)(n * p.xtok + sb * kXTok);
+                }
+                sb += nwarps;
+                while (sb >= nb) {
+                    sb -= nb;
+                    ++n;
                 }
             }
 #pragma unroll
             for (int u = 0; u < XU; ++u) {
-                const int it = base + u * nwarps;
-                if (it < total) {
-                    const int n = it / p.nb, sb = it - n * p.nb;
-                    uint8_t *dst = smem + (xreg - sbase) + n * p.xtok + sb * kXTok;
-                    stage_sb(v[u], lane, F::XL == XL_Q4 ? dst : nullptr,
-                             F::XL == XL_Q6 ? dst : nullptr, F::XL == XL_FP4 ? dst : nullptr);
+                if (base + u * nwarps < total) {
+                    uint8_t *d = smem + (xreg - sbase) + dst[u];
+                    stage_sb(v[u], lane, F::XL == XL_Q4 ? d : nullptr,
+                             F::XL == XL_Q6 ? d : nullptr, F::XL == XL_FP4 ? d : nullptr);
                 }
             }
         }
@@ -1002,13 +1014,14 @@ __device__ __forceinline__ void gemv_tile(const Params &p, const Mat &m, int rti
                 const uint32_t sl = slots + slot * slot_bytes;
                 const uint32_t xsl = xreg + sb * kXTok;
                 if (T == T_FP4) {
-                    compute_sb<T, 1, 1>(A, sl + wrow, xsl, p.xtok, g, t, ntok, m, row_w, sb, ksel,
-                                        128, sl + srow);
+                    compute_sb<T, 1, 1, ODD>(A, sl + wrow, xsl, p.xtok, g, t, ntok, m, row_w, sb,
+                                             ksel, 128, sl + srow);
                 } else if (T == T_Q6K) {
-                    compute_sb<T, 1, 1>(A, sl + wrow, xsl, p.xtok, g, t, ntok, m, row_w, sb, ksel,
-                                        q6_pitch(kw), 0u, i * kw);
+                    compute_sb<T, 1, 1, ODD>(A, sl + wrow, xsl, p.xtok, g, t, ntok, m, row_w, sb,
+                                             ksel, q6_pitch(kw), 0u, i * kw);
                 } else {
-                    compute_sb<T, 1, 1>(A, sl + wrow, xsl, p.xtok, g, t, ntok, m, row_w, sb, ksel);
+                    compute_sb<T, 1, 1, ODD>(A, sl + wrow, xsl, p.xtok, g, t, ntok, m, row_w, sb,
+                                             ksel);
                 }
             }
             __syncwarp();
@@ -1053,7 +1066,10 @@ __device__ __forceinline__ void gemv_tile(const Params &p, const Mat &m, int rti
     }
 }
 
-template <int TSET>
+// ONE: N == 1, so only the even token column of each accumulator pair is
+// folded (the odd columns are never stored; the even ones get the same
+// arithmetic as for any other N).
+template <int TSET, bool ONE>
 __global__ void __launch_bounds__(32 * (kGemvCW + 1)) gemv_kernel(const __grid_constant__ Params p)
 {
     extern __shared__ __align__(128) uint8_t smem[];
@@ -1062,13 +1078,13 @@ __global__ void __launch_bounds__(32 * (kGemvCW + 1)) gemv_kernel(const __grid_c
     const Mat &m = p.mat[select_mat(p, tile)];
     const int rtile = tile - m.tile_begin;
     if constexpr ((TSET & TS_Q4K) != 0)
-        if (m.type == T_Q4K) return gemv_tile<T_Q4K>(p, m, rtile, smem);
+        if (m.type == T_Q4K) return gemv_tile<T_Q4K, !ONE>(p, m, rtile, smem);
     if constexpr ((TSET & TS_Q5K) != 0)
-        if (m.type == T_Q5K) return gemv_tile<T_Q5K>(p, m, rtile, smem);
+        if (m.type == T_Q5K) return gemv_tile<T_Q5K, !ONE>(p, m, rtile, smem);
     if constexpr ((TSET & TS_Q6K) != 0)
-        if (m.type == T_Q6K) return gemv_tile<T_Q6K>(p, m, rtile, smem);
+        if (m.type == T_Q6K) return gemv_tile<T_Q6K, !ONE>(p, m, rtile, smem);
     if constexpr ((TSET & TS_FP4) != 0)
-        if (m.type == T_FP4) return gemv_tile<T_FP4>(p, m, rtile, smem);
+        if (m.type == T_FP4) return gemv_tile<T_FP4, !ONE>(p, m, rtile, smem);
 }
 
 // Dynamic shared memory of gemv_kernel: barriers, `stages` ring slots of
