@@ -31,6 +31,8 @@ struct qg_handle {
     uint8_t *xs;   // staging buffer: max_tokens * nb * kXTok bytes
     unsigned int *err;  // device error word written by the kernels (timeouts)
     CUtensorMap tmw, tms;  // 3-D maps [block][row][bytes] for the N <= 8 kernel
+    CUtensorMap tmw1, tms1;  // the same with a 128-row x 1-block box (sk_kernel)
+    CUtensorMap xmap[4];   // 2-D maps of this handle's staging buffer, box 8 (G) tokens
     int device;
     void *hx;      // device buffers of the host-pointer entry point
     size_t hx_cap;
@@ -154,6 +156,8 @@ Mat mat_of(const qg_handle *h, void *y, const __half *res)
     memset(&m, 0, sizeof m);
     m.tmw = h->tmw;
     m.tms = h->tms;
+    m.tmw1 = h->tmw1;
+    m.tms1 = h->tms1;
     m.kw = h->kw;
     m.w = h->w;
     m.sc = h->sc;
@@ -220,6 +224,44 @@ bool encode_blocks(CUtensorMap *m, const void *base, int64_t row_bytes, int64_t 
     return fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT64, 3, const_cast<void *>(base), dims, strides, box,
               estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// 2-D map of the staging buffer: rows are tokens (stride nb * 576 bytes), a
+// row is nb units of 576 bytes (72 8-byte elements); box = one unit x
+// box_rows tokens.
+bool encode_staged(CUtensorMap *m, const void *base, int nb, int64_t rows, int box_rows)
+{
+    PFN_cuTensorMapEncodeTiled_v12000 fn = encode_fn();
+    if (!fn) return false;
+    const cuuint64_t unit = kXTok / 8;
+    cuuint64_t dims[2] = {(cuuint64_t)nb * unit, (cuuint64_t)rows};
+    cuuint64_t strides[1] = {(cuuint64_t)nb * kXTok};
+    cuuint32_t box[2] = {(cuuint32_t)unit, (cuuint32_t)box_rows};
+    cuuint32_t estr[2] = {1, 1};
+    return fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT64, 2, const_cast<void *>(base), dims, strides, box,
+              estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+int sk_tset_smem(int wbytes, int G, bool q6, int *stages)
+{
+    int st = kSkStagesMax;
+    while (st > 2 && sk_smem_bytes(wbytes, G, st) > 110 * 1024) --st;
+    if (q6 && st < 3) st = 3;  // Q6_K weights run two stages ahead
+    *stages = st;
+    return sk_smem_bytes(wbytes, G, st);
+}
+
+cudaError_t launch_sk_tset(int tset, int G, const Params &p, dim3 grid, int smem, cudaStream_t s)
+{
+    switch (tset) {
+    case TS_Q4K: return launch_sk_q4k(G, p, grid, smem, s);
+    case TS_Q5K: return launch_sk_q5k(G, p, grid, smem, s);
+    case TS_Q6K: return launch_sk_q6k(G, p, grid, smem, s);
+    case TS_FP4: return launch_sk_fp4(G, p, grid, smem, s);
+    case TS_Q4K | TS_Q6K: return launch_sk_q4k_q6k(G, p, grid, smem, s);
+    default: return cudaErrorInvalidValue;
+    }
 }
 
 // The whole path for 1..3 handles that share x: staging, then one product
@@ -330,8 +372,12 @@ qg_status run_product(qg_handle *const *hs, int nh, const __half *x, int64_t N, 
         }
         // Stage x once per layout.
         uint8_t *xl[XL_COUNT] = {nullptr, nullptr, nullptr};
+        const qg_handle *xh[XL_COUNT] = {nullptr, nullptr, nullptr};
         for (int i = 0; i < nh; ++i)
-            if (!xl[hs[i]->layout]) xl[hs[i]->layout] = hs[i]->xs;
+            if (!xl[hs[i]->layout]) {
+                xl[hs[i]->layout] = hs[i]->xs;
+                xh[hs[i]->layout] = hs[i];
+            }
         if (fault_at("stage")) return fail(QG_EFAULT_INJECTED, "injected fault: staging launch");
         const int64_t tok_stride = (int64_t)h0->nb * kXTok;
         cudaError_t e = launch_stage(xc, n, (int)h0->K, h0->nb, tok_stride, xl[XL_Q4], xl[XL_Q6],
@@ -339,7 +385,7 @@ qg_status run_product(qg_handle *const *hs, int nh, const __half *x, int64_t N, 
         if (e != cudaSuccess) return cuda_fail(e, "staging kernel launch");
 
         const int G = groups_for(n);
-        const int rows = rows_per_cta(G);
+        const int rows = kSkRows;
         // One launch serves handles of one cluster shape (equal kw).
         bool same_kw = true;
         for (int i = 1; i < nh; ++i) same_kw = same_kw && hs[i]->kw == h0->kw;
@@ -354,6 +400,8 @@ qg_status run_product(qg_handle *const *hs, int nh, const __half *x, int64_t N, 
             Params p;
             memset(&p, 0, sizeof p);
             int tiles = 0, gts = 0;
+            int wbytes = 0;
+            bool q6 = false;
             for (int j = 0; j < gsize[gidx]; ++j) {
                 const qg_handle *h = hs[groups[gidx][j]];
                 const int idx = groups[gidx][j];
@@ -362,7 +410,15 @@ qg_status run_product(qg_handle *const *hs, int nh, const __half *x, int64_t N, 
                 p.mat[j].tile_begin = tiles;
                 tiles += (int)((h->M + rows - 1) / rows);
                 gts |= tset_bit(h->type);
+                const int wb = sk_wbytes((int)h->type);
+                if (wb > wbytes) wbytes = wb;
+                q6 = q6 || h->type == QG_Q6_K;
             }
+            for (int l = 0; l < XL_COUNT; ++l)
+                if (xh[l]) p.xm[l] = xh[l]->xmap[G - 1];
+            int stages = 0;
+            const int smem = sk_tset_smem(wbytes, G, q6, &stages);
+            p.stages = stages;
             p.nmat = gsize[gidx];
             for (int l = 0; l < XL_COUNT; ++l) p.xs[l] = xl[l];
             p.xs_tok_stride = tok_stride;
@@ -378,7 +434,7 @@ qg_status run_product(qg_handle *const *hs, int nh, const __half *x, int64_t N, 
             if (fault_at("launch")) {
                 le = cudaErrorLaunchOutOfResources;  // simulated, nothing was launched
             } else {
-                le = launch_tset(gts, G, p, grid, s);
+                le = launch_sk_tset(gts, G, p, grid, smem, s);
             }
             if (le != cudaSuccess) {
                 cudaGetLastError();  // launch-time errors are not sticky
@@ -513,10 +569,20 @@ qg_status qgemv_create(qg_handle **out, qg_type t, int64_t M, int64_t K, const v
         bool ok = encode_blocks(&h->tmw, w_dev, h->row_bytes, M, bb, R, h->kw);
         if (ok && t == QG_NVFP4_W4A16)
             ok = encode_blocks(&h->tms, scales_dev, h->sc_row_bytes, M, 16, R, h->kw);
+        if (ok) ok = encode_blocks(&h->tmw1, w_dev, h->row_bytes, M, bb, kSkRows, 1);
+        if (ok && t == QG_NVFP4_W4A16)
+            ok = encode_blocks(&h->tms1, scales_dev, h->sc_row_bytes, M, 16, kSkRows, 1);
         if (!ok) {
             cudaFree(h->xs);
             delete h;
             return fail(QG_ECUDA, "tensor map encoding failed");
+        }
+    }
+    for (int G = 1; G <= 4; ++G) {
+        if (!encode_staged(&h->xmap[G - 1], h->xs, nb, max_tokens, 8 * G)) {
+            cudaFree(h->xs);
+            delete h;
+            return fail(QG_ECUDA, "tensor map encoding failed (staging buffer)");
         }
     }
     e = cudaMalloc((void **)&h->err, sizeof(unsigned int));
@@ -667,7 +733,7 @@ qg_status qgemv_plan_info(const qg_handle *h, int64_t N, int32_t *ksplit, int32_
     const int64_t chunks = (N + h->max_tokens - 1) / h->max_tokens;
     const int64_t nfirst = N < h->max_tokens ? N : h->max_tokens;
     if (ksplit) *ksplit = h->kw;
-    if (rows_cta) *rows_cta = rows_per_cta(groups_for(nfirst));
+    if (rows_cta) *rows_cta = kSkRows;
     if (launches) {
         int64_t l = 0;
         for (int64_t c = 0; c < chunks; ++c) {

@@ -74,6 +74,43 @@ static cudaError_t launch_gemv_one(const Params &p, dim3 grid, int smem, cudaStr
     return cudaLaunchKernelEx(&cfg, gemv_kernel<TSET, false>, p);
 }
 
+template <int TSET, int G>
+static cudaError_t launch_sk_one(const Params &p, dim3 grid, int smem, cudaStream_t stream)
+{
+    static int configured[64] = {0};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+    if (smem > kGemvMaxSmem) return cudaErrorInvalidValue;
+    if (!configured[dev]) {
+        e = cudaFuncSetAttribute(sk_kernel<TSET, G>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 kGemvMaxSmem);
+        if (e != cudaSuccess) return e;
+        configured[dev] = 1;
+    }
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = dim3(kSkThreads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[2];
+    int na = 0;
+    attr[na].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[na].val.programmaticStreamSerializationAllowed = 1;
+    ++na;
+    if (p.ks > 1) {
+        attr[na].id = cudaLaunchAttributeClusterDimension;
+        attr[na].val.clusterDim.x = (unsigned)p.ks;
+        attr[na].val.clusterDim.y = 1;
+        attr[na].val.clusterDim.z = 1;
+        ++na;
+    }
+    cfg.attrs = attr;
+    cfg.numAttrs = na;
+    return cudaLaunchKernelEx(&cfg, sk_kernel<TSET, G>, p);
+}
+
 }  // namespace qg
 
 #define QG_DEFINE_TSET(NAME, TSET)                                                          \
@@ -101,5 +138,15 @@ static cudaError_t launch_gemv_one(const Params &p, dim3 grid, int smem, cudaStr
     cudaError_t launch_gemv_##NAME(const Params &p, dim3 grid, int smem, cudaStream_t s)  \
     {                                                                                       \
         return launch_gemv_one<TSET>(p, grid, smem, s);                                     \
+    }                                                                                       \
+    cudaError_t launch_sk_##NAME(int G, const Params &p, dim3 grid, int smem, cudaStream_t s) \
+    {                                                                                       \
+        switch (G) {                                                                        \
+        case 1: return launch_sk_one<TSET, 1>(p, grid, smem, s);                            \
+        case 2: return launch_sk_one<TSET, 2>(p, grid, smem, s);                            \
+        case 3: return launch_sk_one<TSET, 3>(p, grid, smem, s);                            \
+        case 4: return launch_sk_one<TSET, 4>(p, grid, smem, s);                            \
+        default: return cudaErrorInvalidValue;                                              \
+        }                                                                                   \
     }                                                                                       \
     }

@@ -57,8 +57,10 @@ constexpr int kMaxMats = 3;
 enum { ERR_FULL_TIMEOUT = 1, ERR_EMPTY_TIMEOUT = 2 };
 
 struct Mat {
-    CUtensorMap tmw;       // 2-D map of the packed rows (Q4_K, Q5_K, NVFP4 codes)
-    CUtensorMap tms;       // 2-D map of the NVFP4 scale rows
+    CUtensorMap tmw;       // 3-D map of the packed rows (Q4_K, Q5_K, NVFP4 codes), gemv box
+    CUtensorMap tms;       // 3-D map of the NVFP4 scale rows, gemv box
+    CUtensorMap tmw1;      // the same maps with a box of 128 rows x 1 block (sk_kernel)
+    CUtensorMap tms1;
     const uint8_t *w;      // packed weights (codes for NVFP4)
     const uint8_t *sc;     // NVFP4 e4m3 scales [M][K/16]
     void *y;               // output [N][M]
@@ -77,6 +79,8 @@ struct Mat {
 struct Params {
     Mat mat[kMaxMats];
     int nmat;
+    CUtensorMap xm[XL_COUNT];     // 2-D maps (576-byte super-block units, token) of the staged x
+                                  // per layout, box 8G tokens (sk_kernel)
     const uint8_t *xs[XL_COUNT];  // staged x per layout (skinny_kernel)
     int64_t xs_tok_stride;        // bytes per token in the staged buffers (nb * kXTok)
     const __half *x;              // raw x [N][K] (gemv_kernel stages it itself)
@@ -1095,6 +1099,209 @@ __host__ __device__ inline int gemv_smem_bytes(int stage_bytes, int stages, int 
     const int body = stages * stage_bytes + N * gemv_xtok(nb);
     const int red = kGemvCW * 4 * 32 * 4;  // slice partials overlay the ring
     return 128 + (body > red ? body : red);
+}
+
+}  // namespace qg
+
+namespace qg {
+
+// ===========================================================================
+// sk_kernel (N > 8, and N <= 8 when x does not fit gemv_kernel's shared
+// memory): warp 0 streams, per super-block of this cluster rank's K slice,
+// the weights of 128 rows (one 3-D tensor copy; Q6_K rows are loaded by
+// their consumer warp with 16-byte cp.async) and the staged x of up to 32
+// tokens (one 2-D tensor copy) into an mbarrier ring; warps 1..8 each decode
+// and multiply 16 rows against G column groups.  The slices and their
+// rank-order sum through distributed shared memory are those of
+// skinny_kernel, so every row gets the same bits as on any other path.
+// Shared memory: [full[4], empty[4] | ring | (after the loop) rank partials].
+// ===========================================================================
+constexpr int kSkCons = 8;
+constexpr int kSkRows = 16 * kSkCons;
+constexpr int kSkThreads = 32 * (kSkCons + 1);
+constexpr int kSkStagesMax = 4;
+
+__host__ __device__ inline int sk_wbytes(int type)
+{
+    return kSkRows * (type == T_Q6K ? 224 : type == T_Q5K ? 176 : 144);
+}
+__host__ __device__ inline int sk_stage_bytes(int wbytes, int G) { return wbytes + 8 * G * kXTok; }
+__host__ __device__ inline int sk_smem_bytes(int wbytes, int G, int stages)
+{
+    const int ring = stages * sk_stage_bytes(wbytes, G);
+    const int red = kSkCons * 32 * G * 4 * 4;
+    return 128 + (ring > red ? ring : red);
+}
+
+template <int T, int G>
+__device__ __forceinline__ void sk_tile(const Params &p, const Mat &m, int rtile, uint8_t *smem,
+                                        int wbytes)
+{
+    using F = Fmt<T>;
+    constexpr int WP = (T == T_Q6K) ? 224 : (T == T_FP4) ? 128 : F::BB;  // weight row pitch
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int g = lane >> 2, t = lane & 3;
+    const int rank = blockIdx.x, ks = p.ks;
+    const int nsb = (p.nb - rank + ks - 1) / ks;  // super-blocks rank, rank + ks, ...
+    const int tok0 = p.tok_base + blockIdx.z * kTokChunk;
+    const int ntok = min(8 * G, p.N - tok0);
+    const int row0 = rtile * kSkRows;
+    const int STAGES = p.stages;
+    const int sbytes = sk_stage_bytes(wbytes, G);
+    const uint32_t sbase = smem_u32(smem);
+    const uint32_t bar_full = sbase, bar_empty = sbase + 8 * kSkStagesMax;
+    const uint32_t ring = sbase + 128;
+    const uint32_t xbytes = (uint32_t)(8 * G * kXTok);
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < STAGES; ++s) {
+            mbar_init(bar_full + 8 * s, 1);
+            mbar_init(bar_empty + 8 * s, kSkCons);
+        }
+        mbar_fence_init();
+    }
+    if (warp == 0 && lane == 0) {
+        if (T != T_Q6K) prefetch_tmap(&m.tmw1);
+        if (T == T_FP4) prefetch_tmap(&m.tms1);
+        prefetch_tmap(&p.xm[F::XL]);
+    }
+    __syncthreads();
+
+    unsigned int err = 0;
+    Acc<T, 1, G> A;
+    A.zero();
+    if (warp == 0) {
+        if (lane == 0) {
+            // Weights need nothing from earlier kernels: the first stages'
+            // weight copies go out before the dependency wait, their x after.
+            const int pre = min(STAGES, nsb);
+            for (int i = 0; i < pre; ++i) {
+                const int sb = rank + i * ks;
+                const uint32_t dst = ring + i * sbytes, fb = bar_full + 8 * i;
+                mbar_arrive_expect_tx(fb, (T == T_Q6K ? 0u : (uint32_t)sk_wbytes(T)) + xbytes);
+                if (T != T_Q6K) tma_load_3d(dst, &m.tmw1, 0, row0, sb, fb);
+                if (T == T_FP4) tma_load_3d(dst + kSkRows * 128, &m.tms1, 0, row0, sb, fb);
+            }
+            pdl_wait();
+            for (int i = 0; i < pre; ++i)
+                tma_load_2d(ring + i * sbytes + wbytes, &p.xm[F::XL], 72 * (rank + i * ks), tok0,
+                            bar_full + 8 * i);
+            int slot = 0;
+            uint32_t par = 0;
+            for (int i = STAGES; i < nsb; ++i) {
+                if (!mbar_wait(bar_empty + 8 * slot, par)) {
+                    err |= ERR_EMPTY_TIMEOUT;
+                    break;
+                }
+                const int sb = rank + i * ks;
+                const uint32_t dst = ring + slot * sbytes, fb = bar_full + 8 * slot;
+                mbar_arrive_expect_tx(fb, (T == T_Q6K ? 0u : (uint32_t)sk_wbytes(T)) + xbytes);
+                if (T != T_Q6K) tma_load_3d(dst, &m.tmw1, 0, row0, sb, fb);
+                if (T == T_FP4) tma_load_3d(dst + kSkRows * 128, &m.tms1, 0, row0, sb, fb);
+                tma_load_2d(dst + wbytes, &p.xm[F::XL], 72 * sb, tok0, fb);
+                if (++slot == STAGES) {
+                    slot = 0;
+                    par ^= 1u;
+                }
+            }
+        }
+    } else {
+        const int cw = warp - 1;
+        const int row_w = row0 + 16 * cw;
+        const KSel ksel = k_sel(t);
+        pdl_wait();  // the residual and y may belong to earlier kernels
+        // Q6_K: this warp's 16 rows of stage i, each the 16-byte aligned
+        // 224-byte superset of its 210-byte block (bytes past the end of the
+        // matrix are zero-filled, not read).
+        auto q6_issue = [&](int i) {
+            const int sb = rank + i * ks;
+            const uint32_t dst = ring + (i % STAGES) * sbytes + 16 * cw * 224;
+            const uint8_t *end = m.w + m.w_bytes;
+#pragma unroll 1
+            for (int v = lane; v < 16 * 14; v += 32) {
+                const int r = v / 14, c = v - r * 14;
+                const int row = row_w + r;
+                const uint8_t *src = m.w;
+                int nbytes = 0;
+                if (row < m.M) {
+                    const uint8_t *blk = m.w + (int64_t)row * m.row_bytes + (int64_t)sb * 210;
+                    src = (const uint8_t *)((uintptr_t)blk & ~(uintptr_t)15) + 16 * c;
+                    const int64_t left = end - src;
+                    nbytes = left >= 16 ? 16 : (left > 0 ? (int)left : 0);
+                    if (!nbytes) src = m.w;
+                }
+                cp_async16(dst + r * 224 + 16 * c, src, nbytes);
+            }
+        };
+        // Q6_K weights run two stages ahead of this warp (the ring has at
+        // least three slots for Q6_K, so the slot refilled is one this warp
+        // has finished with).
+        if (T == T_Q6K) {
+            for (int i = 0; i < 2; ++i) {
+                if (i < nsb) q6_issue(i);
+                cp_async_commit();
+            }
+        }
+        int slot = 0;
+        uint32_t par = 0;
+#pragma unroll 1
+        for (int i = 0; i < nsb; ++i) {
+            const int sb = rank + i * ks;
+            if (T == T_Q6K) {
+                if (i + 2 < nsb) q6_issue(i + 2);
+                cp_async_commit();
+                cp_async_wait<2>();  // stage i's group has landed
+            }
+            if (!mbar_wait(bar_full + 8 * slot, par)) {
+                err |= ERR_FULL_TIMEOUT;
+                break;
+            }
+            if (T == T_Q6K) __syncwarp();
+            const uint32_t sl = ring + slot * sbytes;
+            const uint32_t xsl = sl + wbytes;
+            if (T == T_FP4) {
+                compute_sb<T, 1, G>(A, sl + 16 * cw * 128, xsl, kXTok, g, t, ntok, m, row_w, sb, ksel,
+                                    128, sl + kSkRows * 128 + 16 * cw * 16);
+            } else if (T == T_Q6K) {
+                compute_sb<T, 1, G>(A, sl + 16 * cw * 224, xsl, kXTok, g, t, ntok, m, row_w, sb, ksel,
+                                    224, 0u, sb);
+            } else {
+                compute_sb<T, 1, G>(A, sl + 16 * cw * WP, xsl, kXTok, g, t, ntok, m, row_w, sb, ksel);
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar_empty + 8 * slot);
+            if (++slot == STAGES) {
+                slot = 0;
+                par ^= 1u;
+            }
+        }
+        if (T == T_Q6K) cp_async_wait<0>();
+    }
+    if (err && p.err) atomicOr(p.err, err);
+    __syncthreads();
+    reduce_and_store<T, 1, G>(A, reinterpret_cast<float *>(smem + 128), rank, ks,
+                              threadIdx.x - 32, kSkCons * 32, warp > 0, p, m, row0 + 16 * (warp - 1),
+                              tok0, g, t);
+}
+
+template <int TSET, int G>
+__global__ void __launch_bounds__(kSkThreads) sk_kernel(const __grid_constant__ Params p)
+{
+    extern __shared__ __align__(128) uint8_t smem[];
+    pdl_trigger();
+    int wbytes = 0;
+    for (int i = 0; i < p.nmat; ++i) wbytes = max(wbytes, sk_wbytes(p.mat[i].type));
+    const int tile = blockIdx.y;
+    const Mat &m = p.mat[select_mat(p, tile)];
+    const int rtile = tile - m.tile_begin;
+    if constexpr ((TSET & TS_Q4K) != 0)
+        if (m.type == T_Q4K) return sk_tile<T_Q4K, G>(p, m, rtile, smem, wbytes);
+    if constexpr ((TSET & TS_Q5K) != 0)
+        if (m.type == T_Q5K) return sk_tile<T_Q5K, G>(p, m, rtile, smem, wbytes);
+    if constexpr ((TSET & TS_Q6K) != 0)
+        if (m.type == T_Q6K) return sk_tile<T_Q6K, G>(p, m, rtile, smem, wbytes);
+    if constexpr ((TSET & TS_FP4) != 0)
+        if (m.type == T_FP4) return sk_tile<T_FP4, G>(p, m, rtile, smem, wbytes);
 }
 
 }  // namespace qg

@@ -20,7 +20,8 @@ cudaError_t launch_ref_gemv(const Mat &m, int K, const __half *x, int N, int out
 #define QG_DECLARE_TSET(NAME)                                                           \
     cudaError_t launch_skinny_##NAME(int G, const Params &p, dim3 grid, cudaStream_t s); \
     int smem_skinny_##NAME(int G);                                                      \
-    cudaError_t launch_gemv_##NAME(const Params &p, dim3 grid, int smem, cudaStream_t s);
+    cudaError_t launch_gemv_##NAME(const Params &p, dim3 grid, int smem, cudaStream_t s); \
+    cudaError_t launch_sk_##NAME(int G, const Params &p, dim3 grid, int smem, cudaStream_t s);
 QG_DECLARE_TSET(q4k)
 QG_DECLARE_TSET(q5k)
 QG_DECLARE_TSET(q6k)

@@ -212,5 +212,5 @@ def test_argument_errors_are_statuses():
     kw, rows, launches = h.plan_info(1)
     assert kw == 8 and rows == 16 and launches == 1      # N <= 8: one kernel
     kw, rows, launches = h.plan_info(16)
-    assert kw == 8 and rows == 64 and launches == 2      # staging + product
+    assert kw == 8 and rows == 128 and launches == 2     # staging + product
     assert h.device_status() == 0
