@@ -16,6 +16,10 @@ static cudaError_t launch_one(const Params &p, dim3 grid, cudaStream_t stream)
     if (!configured[dev]) {
         e = cudaFuncSetAttribute(skinny_kernel<TSET, G>,
                                  cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+        if (e == cudaSuccess)
+            e = cudaFuncSetAttribute(skinny_kernel<TSET, G>,
+                                     cudaFuncAttributePreferredSharedMemoryCarveout,
+                                     cudaSharedmemCarveoutMaxShared);
         if (e != cudaSuccess) return e;
         configured[dev] = 1;
     }
@@ -52,11 +56,20 @@ static cudaError_t launch_gemv_one(const Params &p, dim3 grid, int smem, cudaStr
     if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
     if (smem > kGemvMaxSmem) return cudaErrorInvalidValue;
     if (!configured[dev]) {
+        // Largest shared-memory carveout, so two ~110 KB CTAs share an SM.
         e = cudaFuncSetAttribute(gemv_kernel<TSET, false>,
                                  cudaFuncAttributeMaxDynamicSharedMemorySize, kGemvMaxSmem);
-        if (e != cudaSuccess) return e;
-        e = cudaFuncSetAttribute(gemv_kernel<TSET, true>,
-                                 cudaFuncAttributeMaxDynamicSharedMemorySize, kGemvMaxSmem);
+        if (e == cudaSuccess)
+            e = cudaFuncSetAttribute(gemv_kernel<TSET, true>,
+                                     cudaFuncAttributeMaxDynamicSharedMemorySize, kGemvMaxSmem);
+        if (e == cudaSuccess)
+            e = cudaFuncSetAttribute(gemv_kernel<TSET, false>,
+                                     cudaFuncAttributePreferredSharedMemoryCarveout,
+                                     cudaSharedmemCarveoutMaxShared);
+        if (e == cudaSuccess)
+            e = cudaFuncSetAttribute(gemv_kernel<TSET, true>,
+                                     cudaFuncAttributePreferredSharedMemoryCarveout,
+                                     cudaSharedmemCarveoutMaxShared);
         if (e != cudaSuccess) return e;
         configured[dev] = 1;
     }
@@ -86,6 +99,10 @@ static cudaError_t launch_sk_one(const Params &p, dim3 grid, int smem, cudaStrea
     if (!configured[dev]) {
         e = cudaFuncSetAttribute(sk_kernel<TSET, G>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  kGemvMaxSmem);
+        if (e == cudaSuccess)
+            e = cudaFuncSetAttribute(sk_kernel<TSET, G>,
+                                     cudaFuncAttributePreferredSharedMemoryCarveout,
+                                     cudaSharedmemCarveoutMaxShared);
         if (e != cudaSuccess) return e;
         configured[dev] = 1;
     }
