@@ -117,6 +117,11 @@ int plan_kw(int64_t M, int nb)
 
 int groups_for(int64_t n) { return n >= 32 ? 4 : (int)((n + 7) / 8); }
 
+// gemv_kernel keeps x for the whole K in shared memory; beyond about 48 KB of
+// it the smaller ring costs more than sk_kernel's per-stage x copies
+// (measured crossover on the sweep shapes: 34-46 KB).
+bool gemv_x_fits(int64_t n, int nb) { return n * nb * kXTok <= 48 * 1024; }
+
 int rows_per_cta(int G) { return G <= 2 ? Cfg<1>::ROWS : Cfg<4>::ROWS; }
 
 int rb_of_tset(int tset)
@@ -246,8 +251,10 @@ bool encode_staged(CUtensorMap *m, const void *base, int nb, int64_t rows, int b
 int sk_tset_smem(int wbytes, int G, bool q6, int *stages)
 {
     int st = kSkStagesMax;
+    // Two CTAs per SM where the ring allows it; Q6_K (weights two stages
+    // ahead, by cp.async from the consumers) needs at least three slots.
     while (st > 2 && sk_smem_bytes(wbytes, G, st) > 110 * 1024) --st;
-    if (q6 && st < 3) st = 3;  // Q6_K weights run two stages ahead
+    if (q6 && st < 3) st = 3;
     *stages = st;
     return sk_smem_bytes(wbytes, G, st);
 }
@@ -325,7 +332,7 @@ qg_status run_product(qg_handle *const *hs, int nh, const __half *x, int64_t N, 
                 --gemv_stages;
             gemv_smem = gemv_smem_bytes(sbytes, gemv_stages, n, h0->nb);
         }
-        if (n <= 8 && gemv_smem <= kGemvMaxSmem) {
+        if (n <= 8 && gemv_smem <= kGemvMaxSmem && gemv_x_fits(n, h0->nb)) {
             for (int gidx = 0; gidx < ng; ++gidx) {
                 Params p;
                 memset(&p, 0, sizeof p);
@@ -725,6 +732,13 @@ qg_status qgemv_device_status(qg_handle *h, uint32_t *flags_out, int clear)
     return QG_OK;
 }
 
+static bool gv_x_ok(const qg_handle *h, int64_t n)
+{
+    return gemv_smem_bytes(gemv_stage_bytes_host(h->type, h->kw), kGemvStagesMax, (int)n, h->nb) <=
+               kGemvMaxSmem &&
+           gemv_x_fits(n, h->nb);
+}
+
 qg_status qgemv_plan_info(const qg_handle *h, int64_t N, int32_t *ksplit, int32_t *rows_cta,
                           int32_t *launches)
 {
@@ -739,14 +753,12 @@ qg_status qgemv_plan_info(const qg_handle *h, int64_t N, int32_t *ksplit, int32_
         for (int64_t c = 0; c < chunks; ++c) {
             const int64_t n = (N - c * h->max_tokens) < h->max_tokens ? (N - c * h->max_tokens)
                                                                       : h->max_tokens;
-            const bool gemv = n <= 8 && gemv_smem_bytes(gemv_stage_bytes_host(h->type, h->kw),
-                                                        kGemvStagesMax, (int)n,
-                                                        h->nb) <= kGemvMaxSmem;
+            const bool gemv = n <= 8 && gv_x_ok(h, n);
             l += ((h->flags & QG_FLAG_FORCE_REFERENCE) || gemv) ? 1 : 2;
         }
         *launches = (int32_t)l;
     }
-    if (rows_cta && nfirst <= 8 && !(h->flags & QG_FLAG_FORCE_REFERENCE))
+    if (rows_cta && nfirst <= 8 && gv_x_ok(h, nfirst) && !(h->flags & QG_FLAG_FORCE_REFERENCE))
         *rows_cta = kGemvRows / h->kw;
     return QG_OK;
 }

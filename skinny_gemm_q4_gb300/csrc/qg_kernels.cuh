@@ -1233,11 +1233,11 @@ __device__ __forceinline__ void sk_tile(const Params &p, const Mat &m, int rtile
                 cp_async16(dst + r * 224 + 16 * c, src, nbytes);
             }
         };
-        // Q6_K weights run two stages ahead of this warp (the ring has at
-        // least three slots for Q6_K, so the slot refilled is one this warp
-        // has finished with).
+        // Q6_K weights run STAGES - 1 (2 or 3) stages ahead of this warp; the
+        // slot refilled is one this warp has finished with.
+        const int q6_ahead = (STAGES >= 4) ? 3 : 2;
         if (T == T_Q6K) {
-            for (int i = 0; i < 2; ++i) {
+            for (int i = 0; i < q6_ahead; ++i) {
                 if (i < nsb) q6_issue(i);
                 cp_async_commit();
             }
@@ -1248,9 +1248,13 @@ __device__ __forceinline__ void sk_tile(const Params &p, const Mat &m, int rtile
         for (int i = 0; i < nsb; ++i) {
             const int sb = rank + i * ks;
             if (T == T_Q6K) {
-                if (i + 2 < nsb) q6_issue(i + 2);
+                if (i + q6_ahead < nsb) q6_issue(i + q6_ahead);
                 cp_async_commit();
-                cp_async_wait<2>();  // stage i's group has landed
+                // stage i's group has landed
+                if (q6_ahead == 3)
+                    cp_async_wait<3>();
+                else
+                    cp_async_wait<2>();
             }
             if (!mbar_wait(bar_full + 8 * slot, par)) {
                 err |= ERR_FULL_TIMEOUT;
