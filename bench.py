@@ -326,6 +326,34 @@ def run_ours(args):
     peak, peak_kind = _peaks()
     achieved = pair_bytes / (pair_us * 1e-6) / 1e9
 
+    # Skinny sweep on the gate matrices (Q4_K 9728 x 2560): one call per
+    # layer, N rows, graph replay over the 36 layers (cold), CUDA events.
+    sweep = None
+    if part == "layer" and not args.no_sweep:
+        sweep = {"matrix": "Q4_K 9728x2560 (gate of each layer)", "unit": "GB/s", "points": []}
+        xs = synth.device_activations(32, 2560, 0, 6, dev)
+        ys = torch.empty((32, 9728), dtype=f16, device=dev)
+        gbytes = 9728 * synth.row_bytes(synth.Q4_K, 2560)
+        for n in (1, 2, 4, 8, 16, 32):
+            sg = torch.cuda.CUDAGraph()
+            with torch.cuda.stream(side):
+                with torch.cuda.graph(sg, stream=side):
+                    for i in range(reps):
+                        qg.qgemv_run(layers[i % N_LAYERS]["gate"].h, xs.data_ptr(), n,
+                                     ys.data_ptr(), qg.OUT_F16,
+                                     torch.cuda.current_stream().cuda_stream)
+            sg.replay()
+            torch.cuda.synchronize()
+            e0.record()
+            sg.replay()
+            e1.record()
+            torch.cuda.synchronize()
+            us = e0.elapsed_time(e1) * 1e3 / reps
+            sweep["points"].append({"N": n, "us_per_call": round(us, 3),
+                                    "GBps": round(gbytes / (us * 1e-6) / 1e9, 1),
+                                    "frac_of_measured": round(gbytes / (us * 1e-6) / 1e9 / peak, 4)})
+            del sg
+
     # End to end through the host-buffer entry point: per matrix, x from
     # pinned host memory, y back to pinned host memory, synchronized.
     e2e_steps = min(args.steps, N_LAYERS) if part == "layer" else 0
@@ -399,6 +427,7 @@ def run_ours(args):
         "e2e": None if e2e_val is None else {"value": round(e2e_val, 3), "unit": "GB/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h,
                 "how": "qgemv_run_host per matrix (pinned host x and y, synchronized)"},
+        "sweep": sweep,
         "gpu_launches": launches_per_step * args.steps,
         "clocks": clocks,
     }
@@ -412,6 +441,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-sweep", action="store_true", help="skip the N = 1..32 sweep line")
     ap.add_argument("--part", default="layer", choices=["layer", "qkv", "wo", "pair", "down"],
                     help="time one call of the layer only (profiling); default: the whole layer")
     args = ap.parse_args()
