@@ -7,34 +7,38 @@
 //     instruction); x is the B operand (8 tokens per n8 column group).  N only
 //     sets how many column groups an A fragment is multiplied with.
 //   * A is decoded in registers straight from the packed bytes, exactly:
-//       Q4_K  A = sc*q * 2^-14           (nibble as an fp16 subnormal times sc*2^k)
-//       Q5_K  A = sc*q5 * 2^-14          (fifth bit merged into the subnormal)
-//       Q6_K  A = q - 32                 (magic-number decode)
-//       NVFP4 A = e2m1 * e4m3            (hardware cvt, exact in fp16: six bits)
+//       Q4_K  A = sc*q * 2^-22          (nibble as an fp16 subnormal times sc*2^k)
+//       Q5_K  A = sc*q5 * 2^-22         (fifth bit merged into the subnormal)
+//       Q6_K  A = q - 32                (magic-number decode)
+//       NVFP4 A = e2m1 * e4m3           (hardware cvt, exact in fp16: six bits)
 //     (reflex-llm "docs/kernels.md": dequantize in registers, never write fp16
 //     weights; TandemLLM "Kernels", NVFP4 matrix products: e2m1*e4m3 is exact.)
-//   * Q4_K/Q5_K: per super-block two MMA chains D1a (low nibbles, sub-block
-//     2t) and D1b (high nibbles, 2t+1) plus one MMA of the 6-bit mins against
-//     the per-sub-block sums of x (split hi+lo in fp16), folded as
-//       acc = fma(d*2^14, D1a, acc); acc = fma(d*2^14, D1b, acc);
-//       acc = fma(-dmin*2^24, D2, acc).
-//     Q6_K: one MMA per 16-weight scale group, acc = fma(d*sc, D, acc).
+//   * Q4_K/Q5_K: per super-block one MMA chain D1 over both nibble halves
+//     (thread t owns sub-blocks 2t and 2t+1) plus one MMA of the 6-bit mins
+//     against the per-sub-block sums of x (split hi+lo in fp16), folded as
+//       acc = fma(d*2^22, D1, acc); acc = fma(-dmin*2^24, D2, acc).
+//     Q6_K: one MMA per 16-weight scale group, accs += sc*D, acc += d*accs.
 //     NVFP4: two MMA chains over all of K (even / odd steps), added at the
 //     end and multiplied by the global scale.
-//   * The K range is split over a cluster of `ks` CTAs fixed by K alone; the
-//     ranks' partial sums are added in rank order through distributed shared
-//     memory.  No atomics in the arithmetic.
+//   * The K range is cut into kw slices fixed by (M, K) (super-block sb goes
+//     to slice sb mod kw); slice partials are added in slice order (shared
+//     memory inside a CTA, or distributed shared memory across the cluster
+//     ranks of one row tile).  No atomics in the arithmetic.
 //   * x arrives in the B-fragment order of each format (stage_sb below), so
 //     every B load is one conflict-free 16-byte shared load.
 //
-// Two data-movement variants share the arithmetic above bit for bit:
-//   gemv_kernel   (N <= 8): a producer warp streams the weight tiles into an
-//                 mbarrier ring with one 2-D tensor copy (TMA) per stage (Q6_K,
-//                 whose 210-byte rows cannot be described by a tensor map: by
-//                 producer-lane cp.async); consumer warps decode and multiply;
-//                 x is staged inside the kernel.
-//   skinny_kernel (N > 8): 16-byte cp.async ring, x staged by a separate
-//                 kernel (qg_stage.cu) once per call.
+// Three data-movement variants share the arithmetic above bit for bit:
+//   gemv_kernel   (N <= 8, x for the whole K within 48 KB): a producer warp
+//                 streams the weight tiles into an mbarrier ring with one 3-D
+//                 tensor copy (TMA) per stage (Q6_K, whose 210-byte blocks
+//                 are not 16-byte aligned: one 1-D bulk copy per row of the
+//                 aligned superset); 8 consumer warps decode and multiply; x
+//                 is staged inside the kernel.
+//   sk_kernel     (the rest): x staged once per call by qg_stage.cu; a
+//                 producer warp streams 128 weight rows and the staged x of
+//                 one super-block per stage by TMA; cluster ranks are slices.
+//   skinny_kernel (the allocation-free entry point): 16-byte cp.async ring,
+//                 4 warps, same slices and cluster ranks.
 #pragma once
 
 #include <cuda.h>
