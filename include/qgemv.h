@@ -68,8 +68,15 @@ enum {
     QG_FLAG_FORCE_REFERENCE = 1u << 0, /* always use the simple reference kernel */
     QG_FLAG_DEBUG_SYNC = 1u << 1,      /* synchronize the stream after each call and
                                           report asynchronous errors              */
-    QG_FLAG_NO_FALLBACK = 1u << 2      /* return the fast path's launch error instead
+    QG_FLAG_NO_FALLBACK = 1u << 2,     /* return the fast path's launch error instead
                                           of retrying on the reference kernel      */
+    QG_FLAG_TCGEN05_PREFILL = 1u << 3  /* Q4_K only: calls with N >= 33 run on the
+                                          tcgen05 / tensor-memory engine (128 rows x
+                                          up to 64 tokens per MMA) instead of the
+                                          mma.sync kernels.  Results stay within the
+                                          tolerance but are not bit-identical to the
+                                          default path; measured slower on GB300 at
+                                          N = 33..128, so off by default.          */
 };
 
 typedef struct {

@@ -12,6 +12,7 @@
 #include <string>
 
 #include "qg_launch.cuh"
+#include "qg_tc.cuh"
 #include "qgemv.h"
 
 using namespace qg;
@@ -274,8 +275,8 @@ cudaError_t launch_sk_tset(int tset, int G, const Params &p, dim3 grid, int smem
 // The whole path for 1..3 handles that share x: staging, then one product
 // launch per chunk of at most max_tokens rows (several launches only when the
 // formats have no common kernel).
-qg_status run_product(qg_handle *const *hs, int nh, const __half *x, int64_t N, void *const *ys,
-                      const __half *res, int out_f32, cudaStream_t s)
+qg_status run_product_mma(qg_handle *const *hs, int nh, const __half *x, int64_t N,
+                          void *const *ys, const __half *res, int out_f32, cudaStream_t s)
 {
     const qg_handle *h0 = hs[0];
     uint32_t flags = 0;
@@ -459,14 +460,130 @@ qg_status run_product(qg_handle *const *hs, int nh, const __half *x, int64_t N, 
             }
         }
     }
+    return QG_OK;
+}
+
+// Q4_K handles sharing x, N >= 33, on the tensor core (tc_kernel): x staged
+// once per chunk by stage_tc4_kernel, one product launch per group of equal
+// chunk count (cluster size).
+qg_status run_product_tc(qg_handle *const *hs, int nh, const __half *x, int64_t N,
+                         void *const *ys, const __half *res, int out_f32, cudaStream_t s)
+{
+    const qg_handle *h0 = hs[0];
+    uint32_t flags = 0;
+    int max_tokens = h0->max_tokens;
+    for (int i = 0; i < nh; ++i) {
+        flags |= hs[i]->flags;
+        if (hs[i]->max_tokens < max_tokens) max_tokens = hs[i]->max_tokens;
+    }
+    const int nb = h0->nb;
+    const int64_t chunk_stride = tc_chunk_bytes(nb);
+    for (int64_t c0 = 0; c0 < N; c0 += max_tokens) {
+        const int n = (int)((N - c0) < max_tokens ? (N - c0) : max_tokens);
+        const __half *xc = x + c0 * h0->K;
+        if (fault_at("stage")) return fail(QG_EFAULT_INJECTED, "injected fault: staging launch");
+        cudaError_t e = launch_stage_tc4(xc, n, (int)h0->K, nb, chunk_stride, h0->xs, s);
+        if (e != cudaSuccess) return cuda_fail(e, "staging kernel launch");
+        const int G = n >= kTcTok ? 8 : (n + 7) / 8;
+        bool done[3] = {false, false, false};
+        for (int a = 0; a < nh; ++a) {
+            if (done[a]) continue;
+            const int kw = hs[a]->kw;
+            Params p;
+            memset(&p, 0, sizeof p);
+            int tiles = 0;
+            for (int j = a; j < nh; ++j) {
+                if (done[j] || hs[j]->kw != kw) continue;
+                done[j] = true;
+                const qg_handle *h = hs[j];
+                Mat &m = p.mat[p.nmat++];
+                m = mat_of(h, (uint8_t *)ys[j] + c0 * h->M * (out_f32 ? 4 : 2),
+                           res ? res + c0 * h->M : nullptr);
+                m.tile_begin = tiles;
+                tiles += (int)((h->M + kTcRows - 1) / kTcRows);
+            }
+            p.xs[XL_TC4] = h0->xs;
+            p.xs_tok_stride = chunk_stride;
+            p.x = xc;
+            p.N = n;
+            p.tok_base = 0;
+            p.K = (int)h0->K;
+            p.nb = nb;
+            p.ks = kw;
+            p.out_f32 = out_f32;
+            p.err = h0->err;
+            int stages = kTcStagesMax;
+            while (stages > 2 && tc_smem_bytes(G, stages) > 200 * 1024) --stages;
+            p.stages = stages;
+            const int smem = tc_smem_bytes(G, stages);
+            const dim3 grid((unsigned)kw, (unsigned)tiles, (unsigned)((n + kTcTok - 1) / kTcTok));
+            cudaError_t le = fault_at("launch") ? cudaErrorLaunchOutOfResources
+                                                : launch_tc(G, p, grid, smem, s);
+            if (le != cudaSuccess) {
+                cudaGetLastError();
+                if (flags & QG_FLAG_NO_FALLBACK) {
+                    if (fault_at("launch"))
+                        return fail(QG_EFAULT_INJECTED, "injected fault: product launch");
+                    return cuda_fail(le, "product kernel launch");
+                }
+                for (int j = 0; j < p.nmat; ++j) {
+                    cudaError_t re = launch_ref_gemv(p.mat[j], (int)h0->K, xc, n, out_f32, s);
+                    if (re != cudaSuccess) return cuda_fail(re, "reference kernel launch");
+                }
+                fail(QG_OK, "fast path launch failed (%s); used the reference kernel",
+                     cudaGetErrorName(le));
+            }
+        }
+    }
+    return QG_OK;
+}
+
+// Every product call: with QG_FLAG_TCGEN05_PREFILL, Q4_K handles of calls
+// with N >= 33 (prefill chunks; rows need not keep their bits across N
+// there) go to the tensor-core engine; everything else runs on the mma.sync
+// kernels.
+qg_status run_product(qg_handle *const *hs, int nh, const __half *x, int64_t N, void *const *ys,
+                      const __half *res, int out_f32, cudaStream_t s)
+{
+    g_err.clear();
+    uint32_t flags = 0;
+    for (int i = 0; i < nh; ++i) flags |= hs[i]->flags;
+    qg_handle *tc[3], *mm[3];
+    void *ytc[3], *ymm[3];
+    int ntc = 0, nmm = 0;
+    for (int i = 0; i < nh; ++i) {
+        if (hs[i]->type == QG_Q4_K && N >= kTcMinN && (flags & QG_FLAG_TCGEN05_PREFILL) &&
+            !(flags & QG_FLAG_FORCE_REFERENCE)) {
+            tc[ntc] = hs[i];
+            ytc[ntc++] = ys[i];
+        } else {
+            mm[nmm] = hs[i];
+            ymm[nmm++] = ys[i];
+        }
+    }
+    qg_status st = QG_OK;
+    std::string note;
+    if (ntc) {
+        st = run_product_tc(tc, ntc, x, N, ytc, res, out_f32, s);
+        if (st != QG_OK) return st;
+        note = g_err;
+    }
+    if (nmm) {
+        st = run_product_mma(mm, nmm, x, N, ymm, res, out_f32, s);
+        if (st != QG_OK) return st;
+        if (note.empty()) note = g_err;
+    }
+    g_err = note;
     if (flags & QG_FLAG_DEBUG_SYNC) {
         cudaError_t e = cudaStreamSynchronize(s);
         if (e == cudaSuccess) e = cudaGetLastError();
         if (e != cudaSuccess) return cuda_fail(e, "debug synchronize");
-        unsigned int w = 0;
-        e = cudaMemcpy(&w, h0->err, sizeof w, cudaMemcpyDeviceToHost);
-        if (e != cudaSuccess) return cuda_fail(e, "error word read");
-        if (w) return fail(QG_ECUDA, "kernel reported a bounded-wait timeout (0x%x)", w);
+        for (int i = 0; i < nh; ++i) {
+            unsigned int w = 0;
+            e = cudaMemcpy(&w, hs[i]->err, sizeof w, cudaMemcpyDeviceToHost);
+            if (e != cudaSuccess) return cuda_fail(e, "error word read");
+            if (w) return fail(QG_ECUDA, "kernel reported a bounded-wait timeout (0x%x)", w);
+        }
     }
     return QG_OK;
 }
@@ -506,7 +623,8 @@ const char *qgemv_describe(void)
     static thread_local std::string d;
     const char *fi = getenv("QGEMV_FAULT_INJECT");
     d = std::string("qgemv: GB300 (sm_103a) fused 4-bit GEMV; formats Q4_K=12 Q5_K=13 Q6_K=14 "
-                    "NVFP4_W4A16=256; flags FORCE_REFERENCE=1 DEBUG_SYNC=2 NO_FALLBACK=4; ") +
+                    "NVFP4_W4A16=256; flags FORCE_REFERENCE=1 DEBUG_SYNC=2 NO_FALLBACK=4 "
+                    "TCGEN05_PREFILL=8; ") +
         "env QGEMV_FORCE_REFERENCE=" + (env_on("QGEMV_FORCE_REFERENCE") ? "1" : "0") +
         " QGEMV_DEBUG_SYNC=" + (env_on("QGEMV_DEBUG_SYNC") ? "1" : "0") +
         " QGEMV_FAULT_INJECT=" + (fi ? fi : "") +
@@ -563,7 +681,14 @@ qg_status qgemv_create(qg_handle **out, qg_type t, int64_t M, int64_t K, const v
     h->kw = plan_kw(M, nb);
     h->layout = layout_of(t);
     h->device = dev;
-    const size_t xs_bytes = (size_t)max_tokens * nb * kXTok;
+    // staged x: [token][super-block][576] for the mma.sync kernels; Q4_K
+    // prefill chunks use the same buffer as [64-token chunk][super-block][8
+    // groups][kTcXBlk] (tc_kernel)
+    size_t xs_bytes = (size_t)max_tokens * nb * kXTok;
+    if (t == QG_Q4_K) {
+        const size_t tc = (size_t)((max_tokens + kTcTok - 1) / kTcTok) * tc_chunk_bytes(nb);
+        if (tc > xs_bytes) xs_bytes = tc;
+    }
     e = cudaMalloc((void **)&h->xs, xs_bytes);
     if (e != cudaSuccess) {
         cudaGetLastError();
@@ -747,6 +872,13 @@ qg_status qgemv_plan_info(const qg_handle *h, int64_t N, int32_t *ksplit, int32_
     const int64_t chunks = (N + h->max_tokens - 1) / h->max_tokens;
     const int64_t nfirst = N < h->max_tokens ? N : h->max_tokens;
     if (ksplit) *ksplit = h->kw;
+    if (h->type == QG_Q4_K && N >= kTcMinN && (h->flags & QG_FLAG_TCGEN05_PREFILL) &&
+        !(h->flags & QG_FLAG_FORCE_REFERENCE)) {
+        // tc_kernel: 128 rows per CTA, one staging launch per chunk
+        if (rows_cta) *rows_cta = kTcRows;
+        if (launches) *launches = (int32_t)(2 * chunks);
+        return QG_OK;
+    }
     if (rows_cta) *rows_cta = kSkRows;
     if (launches) {
         int64_t l = 0;

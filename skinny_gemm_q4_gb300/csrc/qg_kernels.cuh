@@ -49,7 +49,9 @@ namespace qg {
 
 enum { T_Q4K = 12, T_Q5K = 13, T_Q6K = 14, T_FP4 = 256 };
 enum { TS_Q4K = 1, TS_Q5K = 2, TS_Q6K = 4, TS_FP4 = 8 };
-enum { XL_Q4 = 0, XL_Q6 = 1, XL_FP4 = 2, XL_COUNT = 3 };
+// Staged-x layouts: B-fragment orders of the mma.sync kernels, and the
+// tensor-core core-matrix layout of tc_kernel (qg_tc.cuh).
+enum { XL_Q4 = 0, XL_Q6 = 1, XL_FP4 = 2, XL_TC4 = 3, XL_COUNT = 4 };
 
 constexpr int kWarps = 4;
 constexpr int kThreads = 32 * kWarps;

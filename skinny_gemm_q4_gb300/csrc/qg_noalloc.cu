@@ -125,18 +125,18 @@ extern "C" qg_status qgemv_run_noalloc(qg_type t, int64_t M, int64_t K, const vo
     int kw = 1;
     while (kw < 8 && 2 * kw <= nb && (M + kGemvRows / kw - 1) / (kGemvRows / kw) < 148) kw *= 2;
 
+    cudaStream_t s = (cudaStream_t)stream;
+    const int esize = (ydt == QG_OUT_F32) ? 4 : 2;
     const int layout = (t == QG_Q6_K) ? XL_Q6 : (t == QG_NVFP4_W4A16 ? XL_FP4 : XL_Q4);
     const int tset = (t == QG_Q4_K) ? TS_Q4K
                    : (t == QG_Q5_K) ? TS_Q5K
                    : (t == QG_Q6_K) ? TS_Q6K
                                     : TS_FP4;
     const int64_t row_bytes = (t == QG_NVFP4_W4A16) ? K / 2 : (int64_t)nb * bb;
-    cudaStream_t s = (cudaStream_t)stream;
-    const int esize = (ydt == QG_OUT_F32) ? 4 : 2;
     for (int64_t c0 = 0; c0 < N; c0 += chunk) {
         const int n = (int)((N - c0) < chunk ? (N - c0) : chunk);
         const __half *xc = (const __half *)x + c0 * K;
-        uint8_t *xl[XL_COUNT] = {nullptr, nullptr, nullptr};
+        uint8_t *xl[XL_COUNT] = {nullptr, nullptr, nullptr, nullptr};
         xl[layout] = scratch;
         cudaError_t e = launch_stage(xc, n, (int)K, nb, (int64_t)tok_bytes, xl[XL_Q4], xl[XL_Q6],
                                      xl[XL_FP4], s);

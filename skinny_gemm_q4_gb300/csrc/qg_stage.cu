@@ -8,6 +8,7 @@
 // stage_sb in qg_kernels.cuh, the same function the N <= 8 kernel uses for
 // its in-kernel staging, so both paths see identical x and sub-block sums.
 #include "qg_kernels.cuh"
+#include "qg_tc.cuh"
 
 namespace qg {
 
@@ -43,6 +44,41 @@ cudaError_t launch_stage(const __half *x, int N, int K, int nb, int64_t tok_stri
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     return cudaLaunchKernelEx(&cfg, stage_x_kernel, x, N, K, nb, tok_stride, xq4, xq6, xfp4);
+}
+
+// The same for tc_kernel's layout: token n of a 64-token chunk goes to row
+// n % 8 of 8-token group (n % 64) / 8; per chunk [super-block][8 groups][kTcXBlk].
+__global__ void __launch_bounds__(128)
+    stage_tc4_kernel(const __half *__restrict__ x, int N, int K, int nb, int64_t chunk_stride,
+                     uint8_t *out)
+{
+    pdl_trigger();
+    pdl_wait();
+    const int warp = (int)((blockIdx.x * blockDim.x + threadIdx.x) >> 5);
+    const int lane = threadIdx.x & 31;
+    if (warp >= N * nb) return;
+    const int n = warp / nb, sb = warp - n * nb;
+    const uint4 v = *reinterpret_cast<const uint4 *>(x + (int64_t)n * K + 256 * sb + 8 * lane);
+    uint8_t *blk = out + (int64_t)(n / kTcTok) * chunk_stride + (int64_t)sb * (8 * kTcXBlk) +
+                   ((n % kTcTok) / 8) * kTcXBlk;
+    stage_tc4(v, lane, blk, n % 8);
+}
+
+cudaError_t launch_stage_tc4(const __half *x, int N, int K, int nb, int64_t chunk_stride,
+                             uint8_t *out, cudaStream_t stream)
+{
+    const int warps = N * nb;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)((warps + 3) / 4));
+    cfg.blockDim = dim3(128);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, stage_tc4_kernel, x, N, K, nb, chunk_stride, out);
 }
 
 }  // namespace qg

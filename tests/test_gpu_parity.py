@@ -90,10 +90,43 @@ def test_row_invariance_twins(qtype, M, K):
         assert np.array_equal(yN.view(np.uint32), one[:N].view(np.uint32)), f"N={N}"
     # duplicated inputs give duplicated outputs
     assert np.array_equal(one[2], one[0])
-    # N >= 33 (next chunking regime) keeps the same bits too
+    # N >= 33 (next chunking regime) keeps the same bits too on the default path
     y40 = h.run(to_dev(np.concatenate([x, x[:8]])), out_f32=True).cpu().numpy()
     assert np.array_equal(y40[:32].view(np.uint32), one.view(np.uint32))
     assert h.device_status() == 0
+
+
+@pytest.mark.parametrize("M,K", [(9728, 2560), (300, 2560), (77, 4096)])
+@pytest.mark.parametrize("N", [33, 40, 64, 100, 128])
+def test_tcgen05_prefill_engine(M, K, N):
+    """Opt-in tcgen05 / tensor-memory engine for Q4_K prefill chunks (N >= 33):
+    within the tolerance of the oracle, duplicated rows bit-identical, fp16
+    output the fp32 result rounded once, residual variant and fused pair."""
+    t = torch()
+    w, sc, g = synth.weights(qg.Q4_K, M, K, seed=21, stream=qg.Q4_K)
+    wd = t.from_numpy(np.ascontiguousarray(w)).cuda()
+    h = qg.QGemv(qg.Q4_K, M, K, wd, flags=qg.FLAG_TCGEN05_PREFILL)
+    ks, rows, launches = h.plan_info(N)
+    assert rows == 128 and launches == 2 * ((N + 127) // 128)
+    x = synth.activations(N, K, seed=21, duplicate_rows=True)
+    yref, mag = oracle.qgemv(oracle.Q4_K, w, M, K, x)
+    xd = to_dev(x)
+    y32 = h.run(xd, out_f32=True)
+    y16 = h.run(xd, out_f32=False)
+    check_close(y32.cpu().numpy(), yref, mag, what=f"tcgen05 Q4_K {M}x{K} N={N}")
+    assert np.array_equal(y16.cpu().numpy(), y32.half().cpu().numpy())
+    yc = y32.cpu().numpy()
+    assert np.array_equal(yc[2].view(np.uint32), yc[0].view(np.uint32))  # row 2 repeats row 0
+    r = synth.residual(N, M, seed=21)
+    ya = h.run_add(xd, to_dev(r)).float().cpu().numpy()
+    yref_a, mag_a = oracle.qgemv(oracle.Q4_K, w, M, K, x, residual=r)
+    check_close(ya, yref_a, mag_a, fp16_out=True, what="tcgen05 run_add")
+    # the pair call gives each matrix the same bits as its own call
+    h2 = qg.QGemv(qg.Q4_K, M, K, wd, flags=qg.FLAG_TCGEN05_PREFILL)
+    pa, pb = qg.pair_run(h, h2, xd, out_f32=True)
+    assert np.array_equal(pa.cpu().numpy().view(np.uint32), yc.view(np.uint32))
+    assert np.array_equal(pb.cpu().numpy().view(np.uint32), yc.view(np.uint32))
+    assert h.device_status() == 0 and h2.device_status() == 0
 
 
 @pytest.mark.parametrize("qtype", [qg.Q4_K, qg.Q6_K, qg.NVFP4_W4A16])
@@ -211,6 +244,8 @@ def test_argument_errors_are_statuses():
                               None) == -1
     kw, rows, launches = h.plan_info(1)
     assert kw == 8 and rows == 16 and launches == 1      # N <= 8: one kernel
+    kw, rows, launches = h.plan_info(40)
+    assert rows == 128 and launches == 2                 # staging + product
     kw, rows, launches = h.plan_info(16)
     assert kw == 8 and rows == 128 and launches == 2     # staging + product
     assert h.device_status() == 0
