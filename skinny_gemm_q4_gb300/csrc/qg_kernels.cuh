@@ -13,10 +13,11 @@
 //       NVFP4 A = e2m1 * e4m3           (hardware cvt, exact in fp16: six bits)
 //     (reflex-llm "docs/kernels.md": dequantize in registers, never write fp16
 //     weights; TandemLLM "Kernels", NVFP4 matrix products: e2m1*e4m3 is exact.)
-//   * Q4_K/Q5_K: per super-block one MMA chain D1 over both nibble halves
-//     (thread t owns sub-blocks 2t and 2t+1) plus one MMA of the 6-bit mins
-//     against the per-sub-block sums of x (split hi+lo in fp16), folded as
-//       acc = fma(d*2^22, D1, acc); acc = fma(-dmin*2^24, D2, acc).
+//   * Q4_K/Q5_K: per super-block two MMA chains, D1a (low nibbles, sub-block
+//     2t of thread t) and D1b (high nibbles, 2t+1), plus one MMA of the 6-bit
+//     mins against the per-sub-block sums of x (split hi+lo in fp16), folded as
+//       acc = fma(d*2^22, D1a, acc); acc = fma(d*2^22, D1b, acc);
+//       acc = fma(-dmin*2^24, D2, acc).
 //     Q6_K: one MMA per 16-weight scale group, accs += sc*D, acc += d*accs.
 //     NVFP4: two MMA chains over all of K (even / odd steps), added at the
 //     end and multiplied by the global scale.
@@ -337,7 +338,10 @@ __device__ __forceinline__ void compute_kquant(uint32_t wsl, uint32_t xsl, int x
     uint32_t xb[G];
 #pragma unroll
     for (int gi = 0; gi < G; ++gi) xb[gi] = xsl + min(8 * gi + g, ntok - 1) * xtok;
-    float d1[MT][G][4];
+    // Two MMA chains (low and high nibbles) halve the dependent-MMA latency
+    // per super-block; the same for every G, so a row's bits do not depend on N.
+    constexpr int NC = 2;
+    float d1[NC][MT][G][4];
 #pragma unroll
     for (int jp = 0; jp < 4; ++jp) {
 #pragma unroll
@@ -379,10 +383,11 @@ __device__ __forceinline__ void compute_kquant(uint32_t wsl, uint32_t xsl, int x
 #pragma unroll
                     for (int gi = 0; gi < G; ++gi) {
                         const uint32_t b0 = jj ? B[gi].z : B[gi].x, b1 = jj ? B[gi].w : B[gi].y;
-                        if (j == 0 && e == 0)
-                            mma16816_zc(d1[mt][gi], a0, a1, a2, a3, b0, b1);
+                        const int ch = (NC == 2) ? e : 0;
+                        if (j == 0 && (NC == 2 || e == 0))
+                            mma16816_zc(d1[ch][mt][gi], a0, a1, a2, a3, b0, b1);
                         else
-                            mma16816(d1[mt][gi], a0, a1, a2, a3, b0, b1);
+                            mma16816(d1[ch][mt][gi], a0, a1, a2, a3, b0, b1);
                     }
                 }
             }
@@ -401,7 +406,9 @@ __device__ __forceinline__ void compute_kquant(uint32_t wsl, uint32_t xsl, int x
             for (int c = 0; c < 4; ++c) {
                 if (!ODD && (c & 1)) continue;
                 const KRow &r = rc[mt][c >> 1];
-                acc[mt][gi][c] = __fmaf_rn(r.dd, d1[mt][gi][c], acc[mt][gi][c]);
+#pragma unroll
+                for (int ch = 0; ch < NC; ++ch)
+                    acc[mt][gi][c] = __fmaf_rn(r.dd, d1[ch][mt][gi][c], acc[mt][gi][c]);
                 acc[mt][gi][c] = __fmaf_rn(r.dm, d2[c], acc[mt][gi][c]);
             }
         }
