@@ -948,24 +948,28 @@ __device__ __forceinline__ void gemv_tile(const Params &p, const Mat &m, int rti
         for (int i = 0; i < STAGES && i < nst; ++i) produce(i, i);
     }
 
-    // x for the whole K range, staged by every warp after the programmatic
-    // dependency (x may be written by the previous kernel).
+    // x for the whole K range, staged after the programmatic dependency (x
+    // may be written by the previous kernel): by every warp, except that the
+    // Q6_K producer (still issuing its per-row copies) leaves it to the
+    // consumer warps.
     pdl_wait();
     {
         // Loads for up to four items are in flight at once (one L2 round trip
         // per four items instead of one per item).
-        // Item it = n * nb + sb; this warp takes it = warp, warp + nwarps, ...
-        // and steps (n, sb) without dividing.
+        // Item it = n * nb + sb; staging warp xw takes it = xw, xw + nwarps,
+        // ... and steps (n, sb) without dividing.
         constexpr int XU = 4;
-        const int nwarps = blockDim.x >> 5;
+        constexpr int W0 = TMA ? 0 : 1;  // first staging warp
+        const int nwarps = (blockDim.x >> 5) - W0;
+        const int xw = warp - W0;
         const int nb = p.nb;
-        const int total = ntok * nb;
-        int n = 0, sb = warp;
+        const int total = xw < 0 ? 0 : ntok * nb;
+        int n = 0, sb = xw < 0 ? 0 : xw;
         while (sb >= nb) {
             sb -= nb;
             ++n;
         }
-        for (int base = warp; base < total; base += XU * nwarps) {
+        for (int base = xw; base < total; base += XU * nwarps) {
             uint4 v[XU];
             uint32_t dst[XU];
 #pragma unroll
