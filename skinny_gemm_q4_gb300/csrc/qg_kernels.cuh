@@ -890,6 +890,8 @@ __device__ __forceinline__ void gemv_tile(const Params &p, const Mat &m, int rti
     __syncthreads();
 
     // Producer: fill slot `slot` with stage i (super-blocks i*kw .. i*kw + kw - 1).
+    // The weights are read once per call: evict-first in L2.
+    const uint64_t wpol = l2_evict_first_policy();
     auto produce = [&](int i, int slot) {
         const int sbq = i * kw;
         const uint32_t dst = slots + slot * slot_bytes;
@@ -898,10 +900,10 @@ __device__ __forceinline__ void gemv_tile(const Params &p, const Mat &m, int rti
             if (lane == 0) {
                 mbar_arrive_expect_tx(fb, (uint32_t)slot_bytes);
                 if (T == T_FP4) {
-                    tma_load_3d(dst, &m.tmw, 0, row0, sbq, fb);
-                    tma_load_3d(dst + kw * R * 128, &m.tms, 0, row0, sbq, fb);
+                    tma_load_3d_ef(dst, &m.tmw, 0, row0, sbq, fb, wpol);
+                    tma_load_3d_ef(dst + kw * R * 128, &m.tms, 0, row0, sbq, fb, wpol);
                 } else {
-                    tma_load_3d(dst, &m.tmw, 0, row0, sbq, fb);
+                    tma_load_3d_ef(dst, &m.tmw, 0, row0, sbq, fb, wpol);
                 }
             }
         } else {
@@ -938,7 +940,7 @@ __device__ __forceinline__ void gemv_tile(const Params &p, const Mat &m, int rti
                 const uint8_t *stop = blk + 210 * nv;
                 uint32_t n = (uint32_t)(((stop - al) + 15) & ~(int64_t)15);
                 if (al + n > end) n = (uint32_t)((end - al) & ~(int64_t)15);
-                if (n) bulk_g2s(dst + r * pitch, al, n, fb);
+                if (n) bulk_g2s_ef(dst + r * pitch, al, n, fb, wpol);
             }
         }
     };

@@ -263,6 +263,35 @@ __device__ __forceinline__ void cp_async_mbar_arrive(uint32_t mbar)
 namespace qg {
 
 // 3-D tiled tensor copy global->shared, completing on an mbarrier.
+// L2 policy for data read once (streamed weights): evicted first, so that
+// activations and other reused data stay in L2.
+__device__ __forceinline__ uint64_t l2_evict_first_policy()
+{
+    uint64_t pol;
+    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;\n" : "=l"(pol));
+    return pol;
+}
+
+__device__ __forceinline__ void tma_load_3d_ef(uint32_t dst, const void *tmap, int x, int y, int z,
+                                               uint32_t mbar, uint64_t pol)
+{
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        ".L2::cache_hint [%0], [%1, {%2, %3, %4}], [%5], %6;\n" ::"r"(dst),
+        "l"(tmap), "r"(x), "r"(y), "r"(z), "r"(mbar), "l"(pol)
+        : "memory");
+}
+
+__device__ __forceinline__ void bulk_g2s_ef(uint32_t dst, const void *src, uint32_t bytes,
+                                            uint32_t mbar, uint64_t pol)
+{
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], "
+        "[%1], %2, [%3], %4;\n" ::"r"(dst),
+        "l"(src), "r"(bytes), "r"(mbar), "l"(pol)
+        : "memory");
+}
+
 __device__ __forceinline__ void tma_load_3d(uint32_t dst, const void *tmap, int x, int y, int z,
                                             uint32_t mbar)
 {
