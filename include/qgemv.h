@@ -70,13 +70,14 @@ enum {
                                           report asynchronous errors              */
     QG_FLAG_NO_FALLBACK = 1u << 2,     /* return the fast path's launch error instead
                                           of retrying on the reference kernel      */
-    QG_FLAG_TCGEN05_PREFILL = 1u << 3  /* Q4_K only: calls with N >= 33 run on the
-                                          tcgen05 / tensor-memory engine (128 rows x
-                                          up to 64 tokens per MMA) instead of the
-                                          mma.sync kernels.  Results stay within the
-                                          tolerance but are not bit-identical to the
-                                          default path; measured slower on GB300 at
-                                          N = 33..128, so off by default.          */
+    QG_FLAG_MMA_SYNC_PREFILL = 1u << 3 /* Q4_K calls with N >= 33 (prefill chunks)
+                                          run on the mma.sync kernels, whose rows
+                                          keep the bits of N <= 32 calls, instead of
+                                          the default tcgen05 / tensor-memory engine
+                                          (128 rows x up to 64 tokens per MMA; within
+                                          the tolerance, not bit-identical to N <= 32
+                                          rows; measured 1.1-1.5x faster at N = 33,
+                                          64 and 128 on the decode-layer shapes).   */
 };
 
 typedef struct {

@@ -538,10 +538,10 @@ qg_status run_product_tc(qg_handle *const *hs, int nh, const __half *x, int64_t 
     return QG_OK;
 }
 
-// Every product call: with QG_FLAG_TCGEN05_PREFILL, Q4_K handles of calls
-// with N >= 33 (prefill chunks; rows need not keep their bits across N
-// there) go to the tensor-core engine; everything else runs on the mma.sync
-// kernels.
+// Every product call: Q4_K handles of calls with N >= 33 (prefill chunks;
+// rows need not keep their bits across N there) go to the tcgen05 engine
+// unless QG_FLAG_MMA_SYNC_PREFILL is set; everything else runs on the
+// mma.sync kernels.
 qg_status run_product(qg_handle *const *hs, int nh, const __half *x, int64_t N, void *const *ys,
                       const __half *res, int out_f32, cudaStream_t s)
 {
@@ -552,7 +552,7 @@ qg_status run_product(qg_handle *const *hs, int nh, const __half *x, int64_t N, 
     void *ytc[3], *ymm[3];
     int ntc = 0, nmm = 0;
     for (int i = 0; i < nh; ++i) {
-        if (hs[i]->type == QG_Q4_K && N >= kTcMinN && (flags & QG_FLAG_TCGEN05_PREFILL) &&
+        if (hs[i]->type == QG_Q4_K && N >= kTcMinN && !(flags & QG_FLAG_MMA_SYNC_PREFILL) &&
             !(flags & QG_FLAG_FORCE_REFERENCE)) {
             tc[ntc] = hs[i];
             ytc[ntc++] = ys[i];
@@ -624,12 +624,13 @@ const char *qgemv_describe(void)
     const char *fi = getenv("QGEMV_FAULT_INJECT");
     d = std::string("qgemv: GB300 (sm_103a) fused 4-bit GEMV; formats Q4_K=12 Q5_K=13 Q6_K=14 "
                     "NVFP4_W4A16=256; flags FORCE_REFERENCE=1 DEBUG_SYNC=2 NO_FALLBACK=4 "
-                    "TCGEN05_PREFILL=8; ") +
+                    "MMA_SYNC_PREFILL=8; ") +
         "env QGEMV_FORCE_REFERENCE=" + (env_on("QGEMV_FORCE_REFERENCE") ? "1" : "0") +
         " QGEMV_DEBUG_SYNC=" + (env_on("QGEMV_DEBUG_SYNC") ? "1" : "0") +
         " QGEMV_FAULT_INJECT=" + (fi ? fi : "") +
         "; staging " + std::to_string(kXTok) + " B per token per 256 columns; " +
-        "K split over ceil(K/1536) (<= 8) cluster ranks";
+        "K slices kw in {1,2,4,8} fixed by (M, K); Q4_K N >= 33 on the tcgen05 engine "
+        "unless MMA_SYNC_PREFILL";
     return d.c_str();
 }
 
@@ -872,7 +873,7 @@ qg_status qgemv_plan_info(const qg_handle *h, int64_t N, int32_t *ksplit, int32_
     const int64_t chunks = (N + h->max_tokens - 1) / h->max_tokens;
     const int64_t nfirst = N < h->max_tokens ? N : h->max_tokens;
     if (ksplit) *ksplit = h->kw;
-    if (h->type == QG_Q4_K && N >= kTcMinN && (h->flags & QG_FLAG_TCGEN05_PREFILL) &&
+    if (h->type == QG_Q4_K && N >= kTcMinN && !(h->flags & QG_FLAG_MMA_SYNC_PREFILL) &&
         !(h->flags & QG_FLAG_FORCE_REFERENCE)) {
         // tc_kernel: 128 rows per CTA, one staging launch per chunk
         if (rows_cta) *rows_cta = kTcRows;

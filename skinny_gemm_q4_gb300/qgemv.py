@@ -27,7 +27,7 @@ OUT_F32 = 1
 FLAG_FORCE_REFERENCE = 1
 FLAG_DEBUG_SYNC = 2
 FLAG_NO_FALLBACK = 4
-FLAG_TCGEN05_PREFILL = 8
+FLAG_MMA_SYNC_PREFILL = 8
 
 OK = 0
 STATUS_NAMES = {0: "QG_OK", -1: "QG_EINVAL", -2: "QG_EUNSUPPORTED", -3: "QG_EALIGN",

@@ -18,13 +18,13 @@ def torch():
     return t
 
 
-def make_matrix(qtype, M, K, seed=0, stream=None, device="cuda"):
+def make_matrix(qtype, M, K, seed=0, stream=None, device="cuda", flags=0):
     """(QGemv handle, host bytes, host scales, global scale)."""
     t = torch()
     w, sc, g = synth.weights(qtype, M, K, seed=seed, stream=qtype if stream is None else stream)
     wd = t.from_numpy(np.ascontiguousarray(w)).to(device)
     sd = None if sc is None else t.from_numpy(np.ascontiguousarray(sc)).to(device)
-    h = qg.QGemv(qtype, M, K, wd, sd, g)
+    h = qg.QGemv(qtype, M, K, wd, sd, g, flags=flags)
     return h, w, sc, g
 
 

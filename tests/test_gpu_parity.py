@@ -80,7 +80,9 @@ def test_product_matches_oracle(qtype, M, K, N):
 def test_row_invariance_twins(qtype, M, K):
     """TandemLLM verify-twin rule: an N-row call equals N one-row calls bit
     for bit, N = 2..32, with rows that share inputs."""
-    h, w, sc, g = make_matrix(qtype, M, K, seed=6)
+    # N >= 33 Q4_K calls default to the tcgen05 engine (tolerance only); the
+    # mma.sync prefill path is the one that keeps the N <= 32 bits
+    h, w, sc, g = make_matrix(qtype, M, K, seed=6, flags=qg.FLAG_MMA_SYNC_PREFILL)
     x = synth.activations(32, K, seed=6, duplicate_rows=True)
     xd = to_dev(x)
     singles = [h.run(xd[n:n + 1], out_f32=True) for n in range(32)]
@@ -90,7 +92,7 @@ def test_row_invariance_twins(qtype, M, K):
         assert np.array_equal(yN.view(np.uint32), one[:N].view(np.uint32)), f"N={N}"
     # duplicated inputs give duplicated outputs
     assert np.array_equal(one[2], one[0])
-    # N >= 33 (next chunking regime) keeps the same bits too on the default path
+    # N >= 33 (next chunking regime) keeps the same bits too on the mma.sync path
     y40 = h.run(to_dev(np.concatenate([x, x[:8]])), out_f32=True).cpu().numpy()
     assert np.array_equal(y40[:32].view(np.uint32), one.view(np.uint32))
     assert h.device_status() == 0
@@ -99,21 +101,25 @@ def test_row_invariance_twins(qtype, M, K):
 @pytest.mark.parametrize("M,K", [(9728, 2560), (300, 2560), (77, 4096)])
 @pytest.mark.parametrize("N", [33, 40, 64, 100, 128])
 def test_tcgen05_prefill_engine(M, K, N):
-    """Opt-in tcgen05 / tensor-memory engine for Q4_K prefill chunks (N >= 33):
-    within the tolerance of the oracle, duplicated rows bit-identical, fp16
-    output the fp32 result rounded once, residual variant and fused pair."""
+    """tcgen05 / tensor-memory engine, the default for Q4_K prefill chunks
+    (N >= 33): within the tolerance of the oracle, duplicated rows
+    bit-identical, fp16 output the fp32 result rounded once, residual variant
+    and fused pair; QG_FLAG_MMA_SYNC_PREFILL selects the mma.sync kernels."""
     t = torch()
     w, sc, g = synth.weights(qg.Q4_K, M, K, seed=21, stream=qg.Q4_K)
     wd = t.from_numpy(np.ascontiguousarray(w)).cuda()
-    h = qg.QGemv(qg.Q4_K, M, K, wd, flags=qg.FLAG_TCGEN05_PREFILL)
+    h = qg.QGemv(qg.Q4_K, M, K, wd)
     ks, rows, launches = h.plan_info(N)
     assert rows == 128 and launches == 2 * ((N + 127) // 128)
+    hm = qg.QGemv(qg.Q4_K, M, K, wd, flags=qg.FLAG_MMA_SYNC_PREFILL)
+    ym = hm.run(to_dev(synth.activations(N, K, seed=21, duplicate_rows=True)), out_f32=True)
     x = synth.activations(N, K, seed=21, duplicate_rows=True)
     yref, mag = oracle.qgemv(oracle.Q4_K, w, M, K, x)
     xd = to_dev(x)
     y32 = h.run(xd, out_f32=True)
     y16 = h.run(xd, out_f32=False)
     check_close(y32.cpu().numpy(), yref, mag, what=f"tcgen05 Q4_K {M}x{K} N={N}")
+    check_close(ym.cpu().numpy(), yref, mag, what=f"mma.sync prefill Q4_K {M}x{K} N={N}")
     assert np.array_equal(y16.cpu().numpy(), y32.half().cpu().numpy())
     yc = y32.cpu().numpy()
     assert np.array_equal(yc[2].view(np.uint32), yc[0].view(np.uint32))  # row 2 repeats row 0
@@ -122,7 +128,7 @@ def test_tcgen05_prefill_engine(M, K, N):
     yref_a, mag_a = oracle.qgemv(oracle.Q4_K, w, M, K, x, residual=r)
     check_close(ya, yref_a, mag_a, fp16_out=True, what="tcgen05 run_add")
     # the pair call gives each matrix the same bits as its own call
-    h2 = qg.QGemv(qg.Q4_K, M, K, wd, flags=qg.FLAG_TCGEN05_PREFILL)
+    h2 = qg.QGemv(qg.Q4_K, M, K, wd)
     pa, pb = qg.pair_run(h, h2, xd, out_f32=True)
     assert np.array_equal(pa.cpu().numpy().view(np.uint32), yc.view(np.uint32))
     assert np.array_equal(pb.cpu().numpy().view(np.uint32), yc.view(np.uint32))
