@@ -638,70 +638,97 @@ __device__ __forceinline__ void compute_sb(Acc<T, MT, G> &A, uint32_t wsl, uint3
     }
 }
 
+// Epilogue of one output element: NVFP4 global scale, residual (fp32 add
+// before the single rounding), fp16 RN or fp32 store.
+template <int T>
+__device__ __forceinline__ void store_out(const Params &p, const Mat &m, int row, int tok, float val)
+{
+    if (row >= m.M || tok >= p.N) return;
+    if (T == T_FP4) val = val * m.gscale;
+    const int64_t o = (int64_t)tok * m.M + row;
+    if (m.res) val = __fadd_rn(__half2float(m.res[o]), val);
+    if (p.out_f32)
+        reinterpret_cast<float *>(m.y)[o] = val;
+    else
+        reinterpret_cast<__half *>(m.y)[o] = __float2half_rn(val);
+}
+
 // Rank-ordered K-split reduction through distributed shared memory, then the
-// epilogue (rank 0 only).  `red` is free shared memory of at least
-// nthreads * MT * G * 4 floats; every thread of every CTA in the cluster must
-// call this.  cid/ncons: this thread's index among the consumer threads.
+// epilogue.  Every rank publishes its partial tile in `red` (free shared
+// memory of at least ncons * MT * G * 4 floats); after a cluster barrier rank
+// q sums the q-th 1/ks of the tile over ranks 0, 1, .., ks-1 in that order
+// (all ks remote loads in flight at once, so one distributed-shared-memory
+// round trip instead of one per rank) and stores it; a second, relaxed
+// barrier keeps every rank's shared memory alive until all reads are done.  The sum order
+// per element is the same for every rank split and every N.  Every thread of
+// every CTA in the cluster must call this.  cid/ncons: this thread's index
+// among the consumer threads; row_cta: the tile's first row (consumer warp w
+// holds rows row_cta + 16 MT w ..).
 template <int T, int MT, int G>
 __device__ __forceinline__ void reduce_and_store(const Acc<T, MT, G> &A, float *red, int rank,
                                                  int ks, int cid, int ncons, bool consumer,
-                                                 const Params &p, const Mat &m, int row_w,
+                                                 const Params &p, const Mat &m, int row_cta,
                                                  int tok0, int g, int t)
 {
-    float v[MT][G][4];
-#pragma unroll
-    for (int mt = 0; mt < MT; ++mt)
-#pragma unroll
-        for (int gi = 0; gi < G; ++gi)
-#pragma unroll
-            for (int c = 0; c < 4; ++c) v[mt][gi][c] = A.partial(mt, gi, c);
+    constexpr int E = MT * G * 4;  // partial floats per consumer thread
     if (ks > 1) {
-        if (consumer && rank != 0) {
+        if (consumer) {
 #pragma unroll
             for (int mt = 0; mt < MT; ++mt)
 #pragma unroll
                 for (int gi = 0; gi < G; ++gi)
 #pragma unroll
                     for (int c = 0; c < 4; ++c)
-                        red[((mt * G + gi) * 4 + c) * ncons + cid] = v[mt][gi][c];
+                        red[((mt * G + gi) * 4 + c) * ncons + cid] = A.partial(mt, gi, c);
         }
         cluster_sync();
-        if (consumer && rank == 0) {
-            for (int r = 1; r < ks; ++r) {
-                const uint32_t ra = map_shared_rank(smem_u32(red), (uint32_t)r);
+        const int per = E * ncons / ks;  // floats of this rank's share (a multiple of 4)
+        const uint32_t rbase = smem_u32(red);
+        for (int q4 = threadIdx.x; 4 * q4 < per; q4 += blockDim.x) {
+            const int idx0 = rank * per + 4 * q4;
+            float4 part[8];
 #pragma unroll
-                for (int mt = 0; mt < MT; ++mt)
+            for (int r = 0; r < 8; ++r)
+                if (r < ks) part[r] = ld_dsmem_v4(map_shared_rank(rbase + 4 * idx0, (uint32_t)r));
+            float4 sum = part[0];
 #pragma unroll
-                    for (int gi = 0; gi < G; ++gi)
+            for (int r = 1; r < 8; ++r) {
+                if (r < ks) {
+                    sum.x += part[r].x;
+                    sum.y += part[r].y;
+                    sum.z += part[r].z;
+                    sum.w += part[r].w;
+                }
+            }
+            const float sv[4] = {sum.x, sum.y, sum.z, sum.w};
 #pragma unroll
-                        for (int c = 0; c < 4; ++c)
-                            v[mt][gi][c] += ld_dsmem_f32(
-                                ra + (((mt * G + gi) * 4 + c) * ncons + cid) * 4);
+            for (int e = 0; e < 4; ++e) {
+                const int idx = idx0 + e;
+                const int rest = idx / ncons, ec = idx - rest * ncons;
+                const int c = rest & 3, mg = rest >> 2;
+                const int gi = mg % G, mt = mg / G;
+                const int el = ec & 31, eg = el >> 2, et = el & 3;
+                const int row = row_cta + ((ec >> 5) * MT + mt) * 16 + eg + 8 * (c >> 1);
+                const int tok = tok0 + 8 * gi + 2 * et + (c & 1);
+                store_out<T>(p, m, row, tok, sv[e]);
             }
         }
-        cluster_sync();
+        // every remote read has returned (its value was summed): the other
+        // CTAs may exit once all have arrived; the y stores need no wait
+        cluster_arrive_relaxed();
+        cluster_wait();
+        return;
     }
-    if (!consumer || rank != 0) return;
+    if (!consumer) return;
+    const int row_w = row_cta + (cid >> 5) * MT * 16;
 #pragma unroll
-    for (int mt = 0; mt < MT; ++mt) {
+    for (int mt = 0; mt < MT; ++mt)
 #pragma unroll
-        for (int gi = 0; gi < G; ++gi) {
+        for (int gi = 0; gi < G; ++gi)
 #pragma unroll
-            for (int c = 0; c < 4; ++c) {
-                const int row = row_w + mt * 16 + g + 8 * (c >> 1);
-                const int tok = tok0 + 8 * gi + 2 * t + (c & 1);
-                if (row >= m.M || tok >= p.N) continue;
-                float val = v[mt][gi][c];
-                if (T == T_FP4) val = val * m.gscale;
-                const int64_t o = (int64_t)tok * m.M + row;
-                if (m.res) val = __fadd_rn(__half2float(m.res[o]), val);
-                if (p.out_f32)
-                    reinterpret_cast<float *>(m.y)[o] = val;
-                else
-                    reinterpret_cast<__half *>(m.y)[o] = __float2half_rn(val);
-            }
-        }
-    }
+            for (int c = 0; c < 4; ++c)
+                store_out<T>(p, m, row_w + mt * 16 + g + 8 * (c >> 1),
+                             tok0 + 8 * gi + 2 * t + (c & 1), A.partial(mt, gi, c));
 }
 
 __device__ __forceinline__ int select_mat(const Params &p, int tile)
@@ -806,7 +833,7 @@ __device__ __forceinline__ void run_tile(const Params &p, const Mat &m, int rtil
     cp_async_wait<0>();
     __syncthreads();
     reduce_and_store<T, MT, G>(A, reinterpret_cast<float *>(smem), rank, ks, threadIdx.x, kThreads,
-                               true, p, m, row_w, tok0, g, t);
+                               true, p, m, rtile * Cfg<G>::ROWS, tok0, g, t);
 }
 
 template <int TSET, int G>
@@ -1303,8 +1330,7 @@ __device__ __forceinline__ void sk_tile(const Params &p, const Mat &m, int rtile
     if (err && p.err) atomicOr(p.err, err);
     __syncthreads();
     reduce_and_store<T, 1, G>(A, reinterpret_cast<float *>(smem + 128), rank, ks,
-                              threadIdx.x - 32, kSkCons * 32, warp > 0, p, m, row0 + 16 * (warp - 1),
-                              tok0, g, t);
+                              threadIdx.x - 32, kSkCons * 32, warp > 0, p, m, row0, tok0, g, t);
 }
 
 template <int TSET, int G>

@@ -148,11 +148,35 @@ __device__ __forceinline__ void cluster_sync()
 }
 
 // Address of the same shared-memory location in CTA `rank` of the cluster.
+// Split cluster barrier without memory ordering: arrive (relaxed) once this
+// thread's reads of other CTAs' shared memory have returned, wait before
+// the CTA may exit.  Unlike cluster_sync() it does not wait for this
+// thread's earlier global stores to complete.
+__device__ __forceinline__ void cluster_arrive_relaxed()
+{
+    asm volatile("barrier.cluster.arrive.relaxed.aligned;\n" ::: "memory");
+}
+
+__device__ __forceinline__ void cluster_wait()
+{
+    asm volatile("barrier.cluster.wait.aligned;\n" ::: "memory");
+}
+
 __device__ __forceinline__ uint32_t map_shared_rank(uint32_t addr, uint32_t rank)
 {
     uint32_t r;
     asm volatile("mapa.shared::cluster.u32 %0, %1, %2;\n" : "=r"(r) : "r"(addr), "r"(rank));
     return r;
+}
+
+__device__ __forceinline__ float4 ld_dsmem_v4(uint32_t addr)
+{
+    float4 v;
+    asm volatile("ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%4];\n"
+                 : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+                 : "r"(addr)
+                 : "memory");
+    return v;
 }
 
 __device__ __forceinline__ float ld_dsmem_f32(uint32_t addr)

@@ -157,6 +157,19 @@ __host__ __device__ inline int tc_smem_bytes(int G, int stages)
 // Staged x of tc_kernel: [64-token chunk][super-block][8 groups][kTcXBlk].
 __host__ __device__ inline int64_t tc_chunk_bytes(int nb) { return (int64_t)nb * 8 * kTcXBlk; }
 
+// Epilogue of one output element: residual (fp32 add before the single
+// rounding), fp16 RN or fp32 store.
+__device__ __forceinline__ void tc_store(const Params &p, const Mat &m, int row, int tok, float val)
+{
+    if (row >= m.M || tok >= p.N) return;
+    const int64_t o = (int64_t)tok * m.M + row;
+    if (m.res) val = __fadd_rn(__half2float(m.res[o]), val);
+    if (p.out_f32)
+        reinterpret_cast<float *>(m.y)[o] = val;
+    else
+        reinterpret_cast<__half *>(m.y)[o] = __float2half_rn(val);
+}
+
 template <int G>
 __global__ void __launch_bounds__(kTcThreads) tc_kernel(const __grid_constant__ Params p)
 {
@@ -389,13 +402,16 @@ __global__ void __launch_bounds__(kTcThreads) tc_kernel(const __grid_constant__ 
     tc_fence_after();
     if (warp == 9) tmem_dealloc(tbase, kTcCols);
 
-    // Rank partials through distributed shared memory, added in rank order.
+    // Rank partials through distributed shared memory, added in rank order:
+    // every rank publishes its tile [group][token][row]; rank q then sums the
+    // q-th 1/ks of it over ranks 0..ks-1 (all remote loads in flight at once)
+    // and stores it.
     float *red = reinterpret_cast<float *>(smem + 256);
     const bool rowt = warp < 8;
     const int r = threadIdx.x & 127;
     const int gbeg = (warp >= 4) ? G0 : 0, gcnt = (warp >= 4) ? G - G0 : G0;
     if (ks > 1) {
-        if (rowt && rank != 0) {
+        if (rowt) {
 #pragma unroll
             for (int g = 0; g < G0; ++g)
                 if (g < gcnt)
@@ -403,38 +419,42 @@ __global__ void __launch_bounds__(kTcThreads) tc_kernel(const __grid_constant__ 
                     for (int n = 0; n < 8; ++n) red[((gbeg + g) * 8 + n) * kTcRows + r] = acc[g][n];
         }
         cluster_sync();
-        if (rowt && rank == 0) {
-            for (int q = 1; q < ks; ++q) {
-                const uint32_t ra = map_shared_rank(smem_u32(red), (uint32_t)q);
+        const int per = G * 8 * kTcRows / ks;  // floats of this rank's share (a multiple of 4)
+        const uint32_t rbase = smem_u32(red);
+        for (int q4 = threadIdx.x; 4 * q4 < per; q4 += blockDim.x) {
+            const int idx0 = rank * per + 4 * q4;
+            float4 part[8];
 #pragma unroll
-                for (int g = 0; g < G0; ++g)
-                    if (g < gcnt)
+            for (int q = 0; q < 8; ++q)
+                if (q < ks) part[q] = ld_dsmem_v4(map_shared_rank(rbase + 4 * idx0, (uint32_t)q));
+            float4 sum = part[0];
 #pragma unroll
-                        for (int n = 0; n < 8; ++n)
-                            acc[g][n] = __fadd_rn(
-                                acc[g][n], ld_dsmem_f32(ra + (((gbeg + g) * 8 + n) * kTcRows + r) * 4));
+            for (int q = 1; q < 8; ++q) {
+                if (q < ks) {
+                    sum.x = __fadd_rn(sum.x, part[q].x);
+                    sum.y = __fadd_rn(sum.y, part[q].y);
+                    sum.z = __fadd_rn(sum.z, part[q].z);
+                    sum.w = __fadd_rn(sum.w, part[q].w);
+                }
+            }
+            const float sv[4] = {sum.x, sum.y, sum.z, sum.w};
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const int idx = idx0 + e;
+                const int er = idx % kTcRows, gn = idx / kTcRows;
+                tc_store(p, m, row0 + er, tok0 + gn, sv[e]);
             }
         }
-        cluster_sync();
+        cluster_arrive_relaxed();
+        cluster_wait();
+        return;
     }
-    if (!rowt || rank != 0) return;
-    const int row = row0 + r;
-    if (row >= m.M) return;
+    if (!rowt) return;
 #pragma unroll
     for (int g = 0; g < G0; ++g) {
         if (g >= gcnt) break;
 #pragma unroll
-        for (int n = 0; n < 8; ++n) {
-            const int tok = tok0 + 8 * (gbeg + g) + n;
-            if (tok >= p.N) continue;
-            float val = acc[g][n];
-            const int64_t o = (int64_t)tok * m.M + row;
-            if (m.res) val = __fadd_rn(__half2float(m.res[o]), val);
-            if (p.out_f32)
-                reinterpret_cast<float *>(m.y)[o] = val;
-            else
-                reinterpret_cast<__half *>(m.y)[o] = __float2half_rn(val);
-        }
+        for (int n = 0; n < 8; ++n) tc_store(p, m, row0 + r, tok0 + 8 * (gbeg + g) + n, acc[g][n]);
     }
 }
 
