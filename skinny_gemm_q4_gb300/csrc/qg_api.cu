@@ -35,6 +35,7 @@ struct qg_handle {
     CUtensorMap tmw1, tms1;  // the same with a 128-row x 1-block box (sk_kernel)
     CUtensorMap xmap[4];   // 2-D maps of this handle's staging buffer, box 8 (G) tokens
     int device;
+    int sms = 0;           // SM count of that device
     void *hx;      // device buffers of the host-pointer entry point
     size_t hx_cap;
     void *hy;
@@ -328,8 +329,17 @@ qg_status run_product_mma(qg_handle *const *hs, int nh, const __half *x, int64_t
                 if (st > nst) nst = st;
             }
             gemv_stages = nst < kGemvStagesMax ? nst : kGemvStagesMax;
-            // Two CTAs per SM when a shallower ring allows it (never below 3).
-            while (gemv_stages > 3 && gemv_smem_bytes(sbytes, gemv_stages, n, h0->nb) > 110 * 1024)
+            // Two CTAs per SM when a shallower ring allows it: never below 3
+            // stages, or 2 when the grid has more row tiles than SMs (one
+            // CTA per SM would run it as two waves).
+            int tiles = 0;
+            for (int i = 0; i < nh; ++i) {
+                const int R = kGemvRows / hs[i]->kw;
+                tiles += (int)((hs[i]->M + R - 1) / R);
+            }
+            const int min_stages = (h0->sms > 0 && tiles > h0->sms) ? 2 : 3;
+            while (gemv_stages > min_stages &&
+                   gemv_smem_bytes(sbytes, gemv_stages, n, h0->nb) > 110 * 1024)
                 --gemv_stages;
             gemv_smem = gemv_smem_bytes(sbytes, gemv_stages, n, h0->nb);
         }
@@ -682,6 +692,10 @@ qg_status qgemv_create(qg_handle **out, qg_type t, int64_t M, int64_t K, const v
     h->kw = plan_kw(M, nb);
     h->layout = layout_of(t);
     h->device = dev;
+    if (cudaDeviceGetAttribute(&h->sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
+        cudaGetLastError();
+        h->sms = 0;
+    }
     // staged x: [token][super-block][576] for the mma.sync kernels; Q4_K
     // prefill chunks use the same buffer as [64-token chunk][super-block][8
     // groups][kTcXBlk] (tc_kernel)
