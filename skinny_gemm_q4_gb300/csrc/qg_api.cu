@@ -124,6 +124,19 @@ int groups_for(int64_t n) { return n >= 32 ? 4 : (int)((n + 7) / 8); }
 // (measured crossover on the sweep shapes: 34-46 KB).
 bool gemv_x_fits(int64_t n, int nb) { return n * nb * kXTok <= 48 * 1024; }
 
+// For N >= 2, Q4_K / Q5_K matrices of at most 2560 rows run faster on
+// sk_kernel than on gemv_kernel (measured at N = 2..8: Wo 2560 x 4096 5.2-5.4
+// vs 6.2-7.7 us, K/V 1024 x 2560 4.5-4.8 vs 4.8-6.7 us, Q5_K 2560 x 9728
+// 12.1-12.4 vs 12.2-12.6 us); larger matrices, Q6_K and NVFP4 do not.  Both
+// kernels give the same bits, so this only moves time.
+bool sk_preferred(const qg_handle *const *hs, int nh, int64_t n)
+{
+    if (n < 2) return false;
+    for (int i = 0; i < nh; ++i)
+        if ((hs[i]->type != QG_Q4_K && hs[i]->type != QG_Q5_K) || hs[i]->M > 2560) return false;
+    return true;
+}
+
 int rows_per_cta(int G) { return G <= 2 ? Cfg<1>::ROWS : Cfg<4>::ROWS; }
 
 int rb_of_tset(int tset)
@@ -343,7 +356,8 @@ qg_status run_product_mma(qg_handle *const *hs, int nh, const __half *x, int64_t
                 --gemv_stages;
             gemv_smem = gemv_smem_bytes(sbytes, gemv_stages, n, h0->nb);
         }
-        if (n <= 8 && gemv_smem <= kGemvMaxSmem && gemv_x_fits(n, h0->nb)) {
+        if (n <= 8 && gemv_smem <= kGemvMaxSmem && gemv_x_fits(n, h0->nb) &&
+            !sk_preferred(hs, nh, n)) {
             for (int gidx = 0; gidx < ng; ++gidx) {
                 Params p;
                 memset(&p, 0, sizeof p);
@@ -876,7 +890,7 @@ static bool gv_x_ok(const qg_handle *h, int64_t n)
 {
     return gemv_smem_bytes(gemv_stage_bytes_host(h->type, h->kw), kGemvStagesMax, (int)n, h->nb) <=
                kGemvMaxSmem &&
-           gemv_x_fits(n, h->nb);
+           gemv_x_fits(n, h->nb) && !sk_preferred(&h, 1, n);
 }
 
 qg_status qgemv_plan_info(const qg_handle *h, int64_t N, int32_t *ksplit, int32_t *rows_cta,
