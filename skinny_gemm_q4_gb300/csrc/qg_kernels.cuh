@@ -1255,7 +1255,6 @@ __device__ __forceinline__ void sk_tile(const Params &p, const Mat &m, int rtile
         const int cw = warp - 1;
         const int row_w = row0 + 16 * cw;
         const KSel ksel = k_sel(t);
-        pdl_wait();  // the residual and y may belong to earlier kernels
         // Q6_K: this warp's 16 rows of stage i, each the 16-byte aligned
         // 224-byte superset of its 210-byte block (bytes past the end of the
         // matrix are zero-filled, not read).
@@ -1288,6 +1287,9 @@ __device__ __forceinline__ void sk_tile(const Params &p, const Mat &m, int rtile
                 cp_async_commit();
             }
         }
+        // The weights need nothing from earlier kernels (their first stages
+        // are on their way already); the residual and y may.
+        pdl_wait();
         int slot = 0;
         uint32_t par = 0;
 #pragma unroll 1
