@@ -47,7 +47,8 @@ uint8_t *g_scratch_ptr[kMaxDevices] = {nullptr};
 }  // namespace
 
 namespace qg {
-void set_last_error(const char *msg);  // qg_api.cu: the text qgemv_last_error returns
+void set_last_error(const char *msg);    // qg_api.cu: the text qgemv_last_error returns
+int plan_k_slices(int64_t M, int nb);   // qg_api.cu: a handle's K slices for (M, K/256)
 }
 
 namespace {
@@ -122,8 +123,7 @@ extern "C" qg_status qgemv_run_noalloc(qg_type t, int64_t M, int64_t K, const vo
 
     // Same plan as a handle for (t, M, K): K slices of 1, 2, 4 or 8, so the
     // results equal qgemv_run's bit for bit.
-    int kw = 1;
-    while (kw < 8 && 2 * kw <= nb && (M + kGemvRows / kw - 1) / (kGemvRows / kw) < 148) kw *= 2;
+    const int kw = plan_k_slices(M, nb);
 
     cudaStream_t s = (cudaStream_t)stream;
     const int esize = (ydt == QG_OUT_F32) ? 4 : 2;

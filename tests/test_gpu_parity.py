@@ -75,8 +75,9 @@ def test_product_matches_oracle(qtype, M, K, N):
     assert np.array_equal(y16.cpu().numpy(), y32.half().cpu().numpy())
 
 
-@pytest.mark.parametrize("qtype,M,K", [(qg.Q4_K, 9728, 2560), (qg.Q4_K, 2560, 4096),
-                                       (qg.Q4_K, 1024, 2560), (qg.Q5_K, 2560, 9728),
+@pytest.mark.parametrize("qtype,M,K", [(qg.Q4_K, 9728, 2560), (qg.Q4_K, 4096, 2560),
+                                       (qg.Q4_K, 2560, 4096), (qg.Q4_K, 1024, 2560),
+                                       (qg.Q5_K, 2560, 9728),
                                        (qg.Q6_K, 1024, 2560), (qg.NVFP4_W4A16, 7168, 5120)])
 def test_row_invariance_twins(qtype, M, K):
     """TandemLLM verify-twin rule: an N-row call equals N one-row calls bit
