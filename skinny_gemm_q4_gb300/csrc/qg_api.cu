@@ -126,16 +126,17 @@ int groups_for(int64_t n) { return n >= 32 ? 4 : (int)((n + 7) / 8); }
 // (measured crossover on the sweep shapes: 34-46 KB).
 bool gemv_x_fits(int64_t n, int nb) { return n * nb * kXTok <= 48 * 1024; }
 
-// For N >= 2, Q4_K / Q5_K matrices of at most 2560 rows run faster on
+// For N >= 2, Q4_K / Q5_K matrices of at most 4096 rows run faster on
 // sk_kernel than on gemv_kernel (measured at N = 2..8: Wo 2560 x 4096 5.2-5.4
-// vs 6.2-7.7 us, K/V 1024 x 2560 4.5-4.8 vs 4.8-6.7 us, Q5_K 2560 x 9728
-// 12.1-12.4 vs 12.2-12.6 us); larger matrices, Q6_K and NVFP4 do not.  Both
-// kernels give the same bits, so this only moves time.
+// vs 6.2-7.7 us, K/V 1024 x 2560 4.5-4.8 vs 4.8-6.7 us, Q 4096 x 2560
+// 5.9-6.0 vs 6.1-7.5 us, Q5_K 2560 x 9728 12.1-12.4 vs 12.2-12.6 us); the
+// 9728-row matrices, Q6_K and NVFP4 do not.  Both kernels give the same
+// bits, so this only moves time.
 bool sk_preferred(const qg_handle *const *hs, int nh, int64_t n)
 {
     if (n < 2) return false;
     for (int i = 0; i < nh; ++i)
-        if ((hs[i]->type != QG_Q4_K && hs[i]->type != QG_Q5_K) || hs[i]->M > 2560) return false;
+        if ((hs[i]->type != QG_Q4_K && hs[i]->type != QG_Q5_K) || hs[i]->M > 4096) return false;
     return true;
 }
 
