@@ -29,15 +29,17 @@
 //     every B load is one conflict-free 16-byte shared load.
 //
 // Three data-movement variants share the arithmetic above bit for bit:
-//   gemv_kernel   (N <= 8, x for the whole K within 48 KB): a producer warp
-//                 streams the weight tiles into an mbarrier ring with one 3-D
-//                 tensor copy (TMA) per stage (Q6_K, whose 210-byte blocks
+//   gemv_kernel   (N <= 8, x for the whole K within 48 KB; for N >= 2 not
+//                 for Q4_K/Q5_K matrices of at most 4096 rows): a producer
+//                 warp streams the weight tiles into an mbarrier ring with one
+//                 3-D tensor copy (TMA) per stage (Q6_K, whose 210-byte blocks
 //                 are not 16-byte aligned: one 1-D bulk copy per row of the
 //                 aligned superset); 8 consumer warps decode and multiply; x
 //                 is staged inside the kernel.
-//   sk_kernel     (the rest): x staged once per call by qg_stage.cu; a
-//                 producer warp streams 128 weight rows and the staged x of
-//                 one super-block per stage by TMA; cluster ranks are slices.
+//   sk_kernel     (the rest up to N = 32, and N >= 33 except Q4_K): x staged
+//                 once per call by qg_stage.cu; a producer warp streams 128
+//                 weight rows and the staged x of one super-block per stage by
+//                 TMA; cluster ranks are slices.
 //   skinny_kernel (the allocation-free entry point): 16-byte cp.async ring,
 //                 4 warps, same slices and cluster ranks.
 #pragma once
@@ -1153,7 +1155,7 @@ namespace qg {
 
 // ===========================================================================
 // sk_kernel (N > 8, and N <= 8 when x does not fit gemv_kernel's shared
-// memory): warp 0 streams, per super-block of this cluster rank's K slice,
+// memory or the matrix is a Q4_K/Q5_K one of at most 4096 rows): warp 0 streams, per super-block of this cluster rank's K slice,
 // the weights of 128 rows (one 3-D tensor copy; Q6_K rows are loaded by
 // their consumer warp with 16-byte cp.async) and the staged x of up to 32
 // tokens (one 2-D tensor copy) into an mbarrier ring; warps 1..8 each decode
