@@ -655,6 +655,52 @@ __device__ __forceinline__ void store_out(const Params &p, const Mat &m, int row
         reinterpret_cast<__half *>(m.y)[o] = __float2half_rn(val);
 }
 
+// The epilogue of four consecutive rows row .. row + 3 of token tok: one
+// 8-byte (fp16) or 16-byte (fp32) store when all four rows exist and the y
+// (and residual) addresses are aligned for it, else four scalar stores.
+template <int T>
+__device__ __forceinline__ void store_out4(const Params &p, const Mat &m, int row, int tok,
+                                           float4 v)
+{
+    if (tok >= p.N) return;
+    const int64_t o = (int64_t)tok * m.M + row;
+    const uintptr_t ya = p.out_f32 ? (uintptr_t)(reinterpret_cast<float *>(m.y) + o)
+                                   : (uintptr_t)(reinterpret_cast<__half *>(m.y) + o);
+    const bool vec = row + 3 < m.M && (ya & (p.out_f32 ? 15u : 7u)) == 0 &&
+                     (!m.res || ((uintptr_t)(m.res + o) & 7u) == 0);
+    if (vec) {
+        float a[4] = {v.x, v.y, v.z, v.w};
+        if (T == T_FP4)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) a[e] = a[e] * m.gscale;
+        if (m.res) {
+            const uint2 r = *reinterpret_cast<const uint2 *>(m.res + o);
+            const __half2 r01 = *reinterpret_cast<const __half2 *>(&r.x);
+            const __half2 r23 = *reinterpret_cast<const __half2 *>(&r.y);
+            a[0] = __fadd_rn(__low2float(r01), a[0]);
+            a[1] = __fadd_rn(__high2float(r01), a[1]);
+            a[2] = __fadd_rn(__low2float(r23), a[2]);
+            a[3] = __fadd_rn(__high2float(r23), a[3]);
+        }
+        if (p.out_f32) {
+            *reinterpret_cast<float4 *>(reinterpret_cast<float *>(m.y) + o) =
+                make_float4(a[0], a[1], a[2], a[3]);
+        } else {
+            const __half2 h01 = __halves2half2(__float2half_rn(a[0]), __float2half_rn(a[1]));
+            const __half2 h23 = __halves2half2(__float2half_rn(a[2]), __float2half_rn(a[3]));
+            uint2 u;
+            u.x = *reinterpret_cast<const uint32_t *>(&h01);
+            u.y = *reinterpret_cast<const uint32_t *>(&h23);
+            *reinterpret_cast<uint2 *>(reinterpret_cast<__half *>(m.y) + o) = u;
+        }
+        return;
+    }
+    store_out<T>(p, m, row, tok, v.x);
+    store_out<T>(p, m, row + 1, tok, v.y);
+    store_out<T>(p, m, row + 2, tok, v.z);
+    store_out<T>(p, m, row + 3, tok, v.w);
+}
+
 // Rank-ordered K-split reduction through distributed shared memory, then the
 // epilogue.  Every rank publishes its partial tile in `red` (free shared
 // memory of at least ncons * MT * G * 4 floats); after a cluster barrier rank
@@ -674,14 +720,19 @@ __device__ __forceinline__ void reduce_and_store(const Acc<T, MT, G> &A, float *
 {
     constexpr int E = MT * G * 4;  // partial floats per consumer thread
     if (ks > 1) {
+        // partials published token-major, [token][row] of the tile, so that
+        // a float4 of the share is four consecutive rows of one token
+        const int nrows = (ncons >> 5) * MT * 16;
         if (consumer) {
+            const int rw = (cid >> 5) * MT * 16;
 #pragma unroll
             for (int mt = 0; mt < MT; ++mt)
 #pragma unroll
                 for (int gi = 0; gi < G; ++gi)
 #pragma unroll
                     for (int c = 0; c < 4; ++c)
-                        red[((mt * G + gi) * 4 + c) * ncons + cid] = A.partial(mt, gi, c);
+                        red[(8 * gi + 2 * t + (c & 1)) * nrows + rw + mt * 16 + g + 8 * (c >> 1)] =
+                            A.partial(mt, gi, c);
         }
         cluster_sync();
         const int per = E * ncons / ks;  // floats of this rank's share (a multiple of 4)
@@ -702,18 +753,8 @@ __device__ __forceinline__ void reduce_and_store(const Acc<T, MT, G> &A, float *
                     sum.w += part[r].w;
                 }
             }
-            const float sv[4] = {sum.x, sum.y, sum.z, sum.w};
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                const int idx = idx0 + e;
-                const int rest = idx / ncons, ec = idx - rest * ncons;
-                const int c = rest & 3, mg = rest >> 2;
-                const int gi = mg % G, mt = mg / G;
-                const int el = ec & 31, eg = el >> 2, et = el & 3;
-                const int row = row_cta + ((ec >> 5) * MT + mt) * 16 + eg + 8 * (c >> 1);
-                const int tok = tok0 + 8 * gi + 2 * et + (c & 1);
-                store_out<T>(p, m, row, tok, sv[e]);
-            }
+            const int tl = idx0 / nrows, rl = idx0 - tl * nrows;
+            store_out4<T>(p, m, row_cta + rl, tok0 + tl, sum);
         }
         // every remote read has returned (its value was summed): the other
         // CTAs may exit once all have arrived; the y stores need no wait

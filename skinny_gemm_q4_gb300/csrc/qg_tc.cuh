@@ -437,13 +437,8 @@ __global__ void __launch_bounds__(kTcThreads) tc_kernel(const __grid_constant__ 
                     sum.w = __fadd_rn(sum.w, part[q].w);
                 }
             }
-            const float sv[4] = {sum.x, sum.y, sum.z, sum.w};
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                const int idx = idx0 + e;
-                const int er = idx % kTcRows, gn = idx / kTcRows;
-                tc_store(p, m, row0 + er, tok0 + gn, sv[e]);
-            }
+            // four consecutive rows of one token
+            store_out4<T_Q4K>(p, m, row0 + idx0 % kTcRows, tok0 + idx0 / kTcRows, sum);
         }
         cluster_arrive_relaxed();
         cluster_wait();

@@ -165,8 +165,11 @@ def test_q4k_all_q_zero_min_term():
 
 
 @pytest.mark.parametrize("inplace", [False, True])
-def test_run_add_residual(inplace):
-    M, K, N = 2560, 4096, 3
+@pytest.mark.parametrize("M,N", [(2560, 3), (77, 12), (2560, 40)])
+def test_run_add_residual(inplace, M, N):
+    """Residual added in fp32 before one rounding; M = 77 gives rows whose
+    y addresses are not 8-byte aligned (scalar epilogue stores)."""
+    K = 4096
     h, w, sc, g = make_matrix(qg.Q4_K, M, K, seed=9)
     x = synth.activations(N, K, seed=9)
     r = synth.residual(N, M, seed=9)
