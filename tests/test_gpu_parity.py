@@ -260,3 +260,33 @@ def test_argument_errors_are_statuses():
     kw, rows, launches = h.plan_info(16)
     assert kw == 8 and rows == 128 and launches == 2     # staging + product
     assert h.device_status() == 0
+
+
+EDGE = [  # (M, K, N, max_tokens): one row, one super-block, chunked N, ragged tails
+    (1, 256, 1, 0), (1, 256, 40, 0), (17, 256, 9, 0), (1, 2560, 33, 0),
+    (33, 512, 20, 8), (130, 1024, 70, 32), (5, 768, 3, 1),
+]
+
+
+@pytest.mark.parametrize("qtype", TYPES)
+@pytest.mark.parametrize("M,K,N,mt", EDGE)
+def test_edge_shapes(qtype, M, K, N, mt):
+    """Degenerate and ragged shapes: a single row, a single super-block
+    (K = 256), N processed in max_tokens chunks, ragged row and token tails.
+    Within the tolerance of the oracle, and rows computed in chunks of at
+    most 32 equal one-row calls bit for bit."""
+    t = torch()
+    w, sc, g = synth.weights(qtype, M, K, seed=30, stream=qtype)
+    wd = t.from_numpy(np.ascontiguousarray(w)).cuda()
+    sd = None if sc is None else t.from_numpy(np.ascontiguousarray(sc)).cuda()
+    h = qg.QGemv(qtype, M, K, wd, sd, g, max_tokens=mt,
+                 flags=qg.FLAG_MMA_SYNC_PREFILL)
+    x = synth.activations(N, K, seed=30, duplicate_rows=True)
+    xd = to_dev(x)
+    y = h.run(xd, out_f32=True).cpu().numpy()
+    yref, mag = oracle.qgemv(ORTYPE[qtype], w, M, K, x, scales=sc, global_scale=g)
+    check_close(y, yref, mag, what=f"edge {qtype} {M}x{K} N={N} max_tokens={mt}")
+    if N <= 32 or (0 < mt <= 32):
+        one = np.concatenate([h.run(xd[n:n + 1], out_f32=True).cpu().numpy() for n in range(N)])
+        assert np.array_equal(y.view(np.uint32), one.view(np.uint32))
+    assert h.device_status() == 0
