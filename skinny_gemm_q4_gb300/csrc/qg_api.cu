@@ -126,6 +126,10 @@ int groups_for(int64_t n) { return n >= 32 ? 4 : (int)((n + 7) / 8); }
 // (measured crossover on the sweep shapes: 34-46 KB).
 bool gemv_x_fits(int64_t n, int nb) { return n * nb * kXTok <= 48 * 1024; }
 
+// Dynamic shared memory that keeps sk_kernel at one CTA per SM (more than
+// half of the 228 KB an SM has).
+constexpr int kSkSpreadSmem = 120 * 1024;
+
 // For N >= 2, Q4_K / Q5_K matrices of at most 4096 rows run faster on
 // sk_kernel than on gemv_kernel (measured at N = 2..8: Wo 2560 x 4096 5.2-5.4
 // vs 6.2-7.7 us, K/V 1024 x 2560 4.5-4.8 vs 4.8-6.7 us, Q 4096 x 2560
@@ -465,11 +469,18 @@ qg_status run_product_mma(qg_handle *const *hs, int nh, const __half *x, int64_t
             p.out_f32 = out_f32;
             p.err = h0->err;
             const dim3 grid((unsigned)p.ks, (unsigned)tiles, (unsigned)((n + kTokChunk - 1) / kTokChunk));
+            // With no more CTAs than SMs, ask for more than half an SM's shared
+            // memory: otherwise both CTAs of a cluster may be placed on one SM
+            // and leave another idle (measured: Q4_K 9728 x 2560 at N = 9..16
+            // 7.8 us with this, 7.9-9.8 us without, varying from run to run).
+            const int64_t ctas = (int64_t)grid.x * grid.y * grid.z;
+            const int smem_launch =
+                (h0->sms > 0 && ctas <= h0->sms && smem < kSkSpreadSmem) ? kSkSpreadSmem : smem;
             cudaError_t le;
             if (fault_at("launch")) {
                 le = cudaErrorLaunchOutOfResources;  // simulated, nothing was launched
             } else {
-                le = launch_sk_tset(gts, G, p, grid, smem, s);
+                le = launch_sk_tset(gts, G, p, grid, smem_launch, s);
             }
             if (le != cudaSuccess) {
                 cudaGetLastError();  // launch-time errors are not sticky
