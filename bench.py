@@ -244,6 +244,9 @@ def run_ours(args):
     yd = torch.empty((1, 2560), dtype=f16, device=dev)
 
     part = args.part
+    rows = max(1, args.rows) if part == "gate" else 1
+    x_g = synth.device_activations(rows, 2560, 0, 7, dev)
+    y_g = torch.empty((rows, 9728), dtype=f16, device=dev)
 
     def step(L):
         h = layers[L]
@@ -258,12 +261,16 @@ def run_ours(args):
                               yu.data_ptr(), qg.OUT_F16, s)
         if part in ("layer", "down"):
             qg.qgemv_run(h["down"].h, x_dn.data_ptr(), 1, yd.data_ptr(), qg.OUT_F16, s)
+        if part == "gate":
+            qg.qgemv_run(h["gate"].h, x_g.data_ptr(), rows, y_g.data_ptr(), qg.OUT_F16, s)
 
     roles = {"layer": [r for r, _, _, _ in synth.LAYER], "qkv": ["wq", "wk", "wv"],
-             "wo": ["wo"], "pair": ["gate", "up"], "down": ["down"]}[part]
+             "wo": ["wo"], "pair": ["gate", "up"], "down": ["down"], "gate": ["gate"]}[part]
     wbytes = sum(M * synth.row_bytes(qt, K) for r, qt, M, K in synth.LAYER if r in roles)
     # N = 1: one product kernel per call (x staged in-kernel)
     launches_per_step = 4 if part == "layer" else 1
+    if part == "gate":
+        launches_per_step = layers[0]["gate"].plan_info(rows)[2]
 
     for i in range(args.warmup):
         step(i % N_LAYERS)
@@ -411,7 +418,7 @@ def run_ours(args):
         "vs_baseline": None,
         "dtype": "f16 x, fp32 accumulate, 4-bit weights",
         "data": "synthetic",
-        "config": {"workload": WORKLOAD if part == "layer" else WORKLOAD + ":" + part, "N": 1,
+        "config": {"workload": WORKLOAD if part == "layer" else WORKLOAD + ":" + part, "N": rows,
                    "layers_rotated": N_LAYERS,
                    "weight_bytes_per_step": wbytes,
                    "cold": "36 distinct layers (2.3 GB) > L2; no flush needed",
@@ -442,8 +449,11 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-sweep", action="store_true", help="skip the N = 1..32 sweep line")
-    ap.add_argument("--part", default="layer", choices=["layer", "qkv", "wo", "pair", "down"],
+    ap.add_argument("--part", default="layer", choices=["layer", "qkv", "wo", "pair", "down", "gate"],
                     help="time one call of the layer only (profiling); default: the whole layer")
+    ap.add_argument("--rows", type=int, default=1,
+                    help="N for --part gate (the gate matrix alone at N rows: the skinny and "
+                         "prefill kernels, for profiling)")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
