@@ -281,6 +281,32 @@ int sk_tset_smem(int wbytes, int G, bool q6, int *stages)
     return sk_smem_bytes(wbytes, G, st);
 }
 
+// sk_kernel with x staged inside (p.xin): ring of weights only, then this
+// rank's x for all its super-blocks (ceil(nb / ks) x 8 G tokens x 576 B).
+// Two CTAs per SM where the ring allows it, as above.  Returns 0 when the x
+// region would be too large (the staging kernel is used instead).
+constexpr int kSkXinMax = 100 * 1024;
+bool sk_xin_ok(int64_t n, int nb, int kw)
+{
+    const int64_t nsb = (nb + kw - 1) / kw;  // super-blocks of the largest rank
+    return n <= 8 && n * nsb <= 32 && nsb * 8 * groups_for(n) * kXTok <= kSkXinMax;
+}
+int sk_xin_smem(int wbytes, int G, bool q6, int nb, int ks, int *stages)
+{
+    const int xreg = ((nb + ks - 1) / ks) * 8 * G * kXTok;
+    if (xreg > kSkXinMax) return 0;
+    const int red = kSkCons * 32 * G * 4 * 4;
+    auto total = [&](int st) {
+        const int body = st * wbytes + xreg;
+        return 128 + (body > red ? body : red);
+    };
+    int st = kSkStagesMax;
+    while (st > 2 && total(st) > 110 * 1024) --st;
+    if (q6 && st < 3) st = 3;
+    *stages = st;
+    return total(st);
+}
+
 cudaError_t launch_sk_tset(int tset, int G, const Params &p, dim3 grid, int smem, cudaStream_t s)
 {
     switch (tset) {
@@ -417,22 +443,41 @@ qg_status run_product_mma(qg_handle *const *hs, int nh, const __half *x, int64_t
                 xl[hs[i]->layout] = hs[i]->xs;
                 xh[hs[i]->layout] = hs[i];
             }
+        const int G = groups_for(n);
+        // N <= 8 with at most 32 (token, super-block) items per CTA: x staged
+        // inside sk_kernel (no staging launch; the smallest kw gives the
+        // largest per-rank x).  With more items every CTA staging its slice
+        // of x costs more than the launch it saves (measured: Q4_K 9728 x 2560
+        // N = 16 9.5 vs 7.9 us, Q6_K 2560 x 9728 N = 8 16.2 vs 15.7 us; at
+        // N = 2..8 it saves 0.2-1.0 us on the 1024-4096-row Q4_K matrices).
+        int kw_min = 8;
+        for (int i = 0; i < nh; ++i) kw_min = hs[i]->kw < kw_min ? hs[i]->kw : kw_min;
+        const bool xin = sk_xin_ok(n, h0->nb, kw_min);
         if (fault_at("stage")) return fail(QG_EFAULT_INJECTED, "injected fault: staging launch");
         const int64_t tok_stride = (int64_t)h0->nb * kXTok;
-        cudaError_t e = launch_stage(xc, n, (int)h0->K, h0->nb, tok_stride, xl[XL_Q4], xl[XL_Q6],
-                                     xl[XL_FP4], s);
-        if (e != cudaSuccess) return cuda_fail(e, "staging kernel launch");
+        if (!xin) {
+            cudaError_t e = launch_stage(xc, n, (int)h0->K, h0->nb, tok_stride, xl[XL_Q4],
+                                         xl[XL_Q6], xl[XL_FP4], s);
+            if (e != cudaSuccess) return cuda_fail(e, "staging kernel launch");
+        }
 
-        const int G = groups_for(n);
         const int rows = kSkRows;
-        // One launch serves handles of one cluster shape (equal kw).
-        bool same_kw = true;
-        for (int i = 1; i < nh; ++i) same_kw = same_kw && hs[i]->kw == h0->kw;
-        if (ng == 1 && !same_kw) {
-            ng = 0;
+        // One launch serves handles of one cluster shape (equal kw): split
+        // the group by kw, keeping the call order within each part.
+        if (ng == 1) {
+            int kws[3], nk = 0;
             for (int i = 0; i < nh; ++i) {
-                groups[ng][0] = i;
-                gsize[ng++] = 1;
+                bool seen = false;
+                for (int q = 0; q < nk; ++q) seen = seen || kws[q] == hs[i]->kw;
+                if (!seen) kws[nk++] = hs[i]->kw;
+            }
+            if (nk > 1) {
+                ng = nk;
+                for (int q = 0; q < nk; ++q) {
+                    gsize[q] = 0;
+                    for (int i = 0; i < nh; ++i)
+                        if (hs[i]->kw == kws[q]) groups[q][gsize[q]++] = i;
+                }
             }
         }
         for (int gidx = 0; gidx < ng; ++gidx) {
@@ -456,8 +501,12 @@ qg_status run_product_mma(qg_handle *const *hs, int nh, const __half *x, int64_t
             for (int l = 0; l < XL_COUNT; ++l)
                 if (xh[l]) p.xm[l] = xh[l]->xmap[G - 1];
             int stages = 0;
-            const int smem = sk_tset_smem(wbytes, G, q6, &stages);
+            const int smem = xin ? sk_xin_smem(wbytes, G, q6, h0->nb,
+                                               hs[groups[gidx][0]]->kw, &stages)
+                                 : sk_tset_smem(wbytes, G, q6, &stages);
             p.stages = stages;
+            p.xin = xin ? 1 : 0;
+            p.x = xc;
             p.nmat = gsize[gidx];
             for (int l = 0; l < XL_COUNT; ++l) p.xs[l] = xl[l];
             p.xs_tok_stride = tok_stride;
@@ -932,7 +981,8 @@ qg_status qgemv_plan_info(const qg_handle *h, int64_t N, int32_t *ksplit, int32_
             const int64_t n = (N - c * h->max_tokens) < h->max_tokens ? (N - c * h->max_tokens)
                                                                       : h->max_tokens;
             const bool gemv = n <= 8 && gv_x_ok(h, n);
-            l += ((h->flags & QG_FLAG_FORCE_REFERENCE) || gemv) ? 1 : 2;
+            const bool xin = sk_xin_ok(n, h->nb, h->kw);
+            l += ((h->flags & QG_FLAG_FORCE_REFERENCE) || gemv || xin) ? 1 : 2;
         }
         *launches = (int32_t)l;
     }

@@ -87,7 +87,7 @@ static cudaError_t launch_gemv_one(const Params &p, dim3 grid, int smem, cudaStr
     return cudaLaunchKernelEx(&cfg, gemv_kernel<TSET, false>, p);
 }
 
-template <int TSET, int G>
+template <int TSET, int G, bool XIN = false>
 static cudaError_t launch_sk_one(const Params &p, dim3 grid, int smem, cudaStream_t stream)
 {
     static int configured[64] = {0};
@@ -97,10 +97,10 @@ static cudaError_t launch_sk_one(const Params &p, dim3 grid, int smem, cudaStrea
     if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
     if (smem > kGemvMaxSmem) return cudaErrorInvalidValue;
     if (!configured[dev]) {
-        e = cudaFuncSetAttribute(sk_kernel<TSET, G>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        e = cudaFuncSetAttribute(sk_kernel<TSET, G, XIN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  kGemvMaxSmem);
         if (e == cudaSuccess)
-            e = cudaFuncSetAttribute(sk_kernel<TSET, G>,
+            e = cudaFuncSetAttribute(sk_kernel<TSET, G, XIN>,
                                      cudaFuncAttributePreferredSharedMemoryCarveout,
                                      cudaSharedmemCarveoutMaxShared);
         if (e != cudaSuccess) return e;
@@ -125,7 +125,7 @@ static cudaError_t launch_sk_one(const Params &p, dim3 grid, int smem, cudaStrea
     }
     cfg.attrs = attr;
     cfg.numAttrs = na;
-    return cudaLaunchKernelEx(&cfg, sk_kernel<TSET, G>, p);
+    return cudaLaunchKernelEx(&cfg, sk_kernel<TSET, G, XIN>, p);
 }
 
 }  // namespace qg
@@ -159,7 +159,8 @@ static cudaError_t launch_sk_one(const Params &p, dim3 grid, int smem, cudaStrea
     cudaError_t launch_sk_##NAME(int G, const Params &p, dim3 grid, int smem, cudaStream_t s) \
     {                                                                                       \
         switch (G) {                                                                        \
-        case 1: return launch_sk_one<TSET, 1>(p, grid, smem, s);                            \
+        case 1: return p.xin ? launch_sk_one<TSET, 1, true>(p, grid, smem, s)                \
+                             : launch_sk_one<TSET, 1>(p, grid, smem, s);                     \
         case 2: return launch_sk_one<TSET, 2>(p, grid, smem, s);                            \
         case 3: return launch_sk_one<TSET, 3>(p, grid, smem, s);                            \
         case 4: return launch_sk_one<TSET, 4>(p, grid, smem, s);                            \

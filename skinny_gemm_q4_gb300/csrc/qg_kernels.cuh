@@ -102,6 +102,7 @@ struct Params {
     int xtok;                     // token stride of the in-kernel x region (gemv_kernel)
     int out_f32;
     unsigned int *err;            // error word (timeouts)
+    int xin;                      // sk_kernel: x staged inside the kernel from p.x
 };
 
 template <int T>
@@ -1222,7 +1223,7 @@ __host__ __device__ inline int sk_smem_bytes(int wbytes, int G, int stages)
     return 128 + (ring > red ? ring : red);
 }
 
-template <int T, int G>
+template <int T, int G, bool XIN>
 __device__ __forceinline__ void sk_tile(const Params &p, const Mat &m, int rtile, uint8_t *smem,
                                         int wbytes)
 {
@@ -1236,11 +1237,17 @@ __device__ __forceinline__ void sk_tile(const Params &p, const Mat &m, int rtile
     const int ntok = min(8 * G, p.N - tok0);
     const int row0 = rtile * kSkRows;
     const int STAGES = p.stages;
-    const int sbytes = sk_stage_bytes(wbytes, G);
+    // xin: this rank's x, for all its super-blocks, is staged by the consumer
+    // warps into a region after the ring (no staging launch); otherwise each
+    // slot carries the stage's staged x, brought by TMA.
+    constexpr bool xin = XIN;
+    const int sbytes = xin ? wbytes : sk_stage_bytes(wbytes, G);
     const uint32_t sbase = smem_u32(smem);
     const uint32_t bar_full = sbase, bar_empty = sbase + 8 * kSkStagesMax;
     const uint32_t ring = sbase + 128;
-    const uint32_t xbytes = (uint32_t)(8 * G * kXTok);
+    const uint32_t xreg = ring + STAGES * sbytes;
+    const uint32_t xbytes = xin ? 0u : (uint32_t)(8 * G * kXTok);
+    (void)xreg;
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < STAGES; ++s) {
@@ -1252,7 +1259,7 @@ __device__ __forceinline__ void sk_tile(const Params &p, const Mat &m, int rtile
     if (warp == 0 && lane == 0) {
         if (T != T_Q6K) prefetch_tmap(&m.tmw1);
         if (T == T_FP4) prefetch_tmap(&m.tms1);
-        prefetch_tmap(&p.xm[F::XL]);
+        if (!xin) prefetch_tmap(&p.xm[F::XL]);
     }
     __syncthreads();
 
@@ -1272,9 +1279,10 @@ __device__ __forceinline__ void sk_tile(const Params &p, const Mat &m, int rtile
                 if (T == T_FP4) tma_load_3d(dst + kSkRows * 128, &m.tms1, 0, row0, sb, fb);
             }
             pdl_wait();
-            for (int i = 0; i < pre; ++i)
-                tma_load_2d(ring + i * sbytes + wbytes, &p.xm[F::XL], 72 * (rank + i * ks), tok0,
-                            bar_full + 8 * i);
+            if (!xin)
+                for (int i = 0; i < pre; ++i)
+                    tma_load_2d(ring + i * sbytes + wbytes, &p.xm[F::XL], 72 * (rank + i * ks),
+                                tok0, bar_full + 8 * i);
             int slot = 0;
             uint32_t par = 0;
             for (int i = STAGES; i < nsb; ++i) {
@@ -1287,7 +1295,7 @@ __device__ __forceinline__ void sk_tile(const Params &p, const Mat &m, int rtile
                 mbar_arrive_expect_tx(fb, (T == T_Q6K ? 0u : (uint32_t)sk_wbytes(T)) + xbytes);
                 if (T != T_Q6K) tma_load_3d(dst, &m.tmw1, 0, row0, sb, fb);
                 if (T == T_FP4) tma_load_3d(dst + kSkRows * 128, &m.tms1, 0, row0, sb, fb);
-                tma_load_2d(dst + wbytes, &p.xm[F::XL], 72 * sb, tok0, fb);
+                if (!xin) tma_load_2d(dst + wbytes, &p.xm[F::XL], 72 * sb, tok0, fb);
                 if (++slot == STAGES) {
                     slot = 0;
                     par ^= 1u;
@@ -1331,8 +1339,37 @@ __device__ __forceinline__ void sk_tile(const Params &p, const Mat &m, int rtile
             }
         }
         // The weights need nothing from earlier kernels (their first stages
-        // are on their way already); the residual and y may.
+        // are on their way already); x, the residual and y may.
         pdl_wait();
+        if constexpr (XIN) {
+            // Items (j, n): super-block rank + j ks of token tok0 + n; four
+            // loads in flight per warp, then the same staging as everywhere.
+            constexpr int XU = 4;
+            const int total = nsb * ntok;
+            for (int base = cw; base < total; base += XU * kSkCons) {
+                uint4 v[XU];
+                uint32_t dst[XU];
+#pragma unroll
+                for (int u = 0; u < XU; ++u) {
+                    const int it = base + u * kSkCons;
+                    if (it < total) {
+                        const int j = it / ntok, n = it - j * ntok;
+                        v[u] = __ldg(reinterpret_cast<const uint4 *>(
+                            p.x + (int64_t)(tok0 + n) * p.K + 256 * (rank + j * ks) + 8 * lane));
+                        dst[u] = (uint32_t)((j * 8 * G + n) * kXTok);
+                    }
+                }
+#pragma unroll
+                for (int u = 0; u < XU; ++u) {
+                    if (base + u * kSkCons < total) {
+                        uint8_t *d = smem + (xreg - sbase) + dst[u];
+                        stage_sb(v[u], lane, F::XL == XL_Q4 ? d : nullptr,
+                                 F::XL == XL_Q6 ? d : nullptr, F::XL == XL_FP4 ? d : nullptr);
+                    }
+                }
+            }
+            bar_sync_named(3, kSkCons * 32);  // the consumer warps only
+        }
         int slot = 0;
         uint32_t par = 0;
 #pragma unroll 1
@@ -1353,7 +1390,7 @@ __device__ __forceinline__ void sk_tile(const Params &p, const Mat &m, int rtile
             }
             if (T == T_Q6K) __syncwarp();
             const uint32_t sl = ring + slot * sbytes;
-            const uint32_t xsl = sl + wbytes;
+            const uint32_t xsl = xin ? xreg + (uint32_t)(i * 8 * G * kXTok) : sl + wbytes;
             if (T == T_FP4) {
                 compute_sb<T, 1, G>(A, sl + 16 * cw * 128, xsl, kXTok, g, t, ntok, m, row_w, sb, ksel,
                                     128, sl + kSkRows * 128 + 16 * cw * 16);
@@ -1378,7 +1415,7 @@ __device__ __forceinline__ void sk_tile(const Params &p, const Mat &m, int rtile
                               threadIdx.x - 32, kSkCons * 32, warp > 0, p, m, row0, tok0, g, t);
 }
 
-template <int TSET, int G>
+template <int TSET, int G, bool XIN = false>
 __global__ void __launch_bounds__(kSkThreads) sk_kernel(const __grid_constant__ Params p)
 {
     extern __shared__ __align__(128) uint8_t smem[];
@@ -1389,13 +1426,13 @@ __global__ void __launch_bounds__(kSkThreads) sk_kernel(const __grid_constant__ 
     const Mat &m = p.mat[select_mat(p, tile)];
     const int rtile = tile - m.tile_begin;
     if constexpr ((TSET & TS_Q4K) != 0)
-        if (m.type == T_Q4K) return sk_tile<T_Q4K, G>(p, m, rtile, smem, wbytes);
+        if (m.type == T_Q4K) return sk_tile<T_Q4K, G, XIN>(p, m, rtile, smem, wbytes);
     if constexpr ((TSET & TS_Q5K) != 0)
-        if (m.type == T_Q5K) return sk_tile<T_Q5K, G>(p, m, rtile, smem, wbytes);
+        if (m.type == T_Q5K) return sk_tile<T_Q5K, G, XIN>(p, m, rtile, smem, wbytes);
     if constexpr ((TSET & TS_Q6K) != 0)
-        if (m.type == T_Q6K) return sk_tile<T_Q6K, G>(p, m, rtile, smem, wbytes);
+        if (m.type == T_Q6K) return sk_tile<T_Q6K, G, XIN>(p, m, rtile, smem, wbytes);
     if constexpr ((TSET & TS_FP4) != 0)
-        if (m.type == T_FP4) return sk_tile<T_FP4, G>(p, m, rtile, smem, wbytes);
+        if (m.type == T_FP4) return sk_tile<T_FP4, G, XIN>(p, m, rtile, smem, wbytes);
 }
 
 }  // namespace qg

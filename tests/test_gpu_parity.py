@@ -180,8 +180,11 @@ def test_run_add_residual(inplace, M, N):
     check_close(y.float().cpu().numpy(), yref, mag, fp16_out=True, what="run_add")
 
 
-def test_pair_and_mixed_triple_equal_separate_calls():
-    K, N = 2560, 5
+@pytest.mark.parametrize("N", [5, 12, 40])
+def test_pair_and_mixed_triple_equal_separate_calls(N):
+    """The fused calls give each matrix the bits of its own call; the triple
+    mixes formats and K-slice counts (Q 4096 rows: 4 slices, K/V: 8)."""
+    K = 2560
     a, wa, _, _ = make_matrix(qg.Q4_K, 4096, K, seed=10, stream=1)
     b, wb, _, _ = make_matrix(qg.Q4_K, 1024, K, seed=10, stream=2)
     c, wc, _, _ = make_matrix(qg.Q6_K, 1024, K, seed=10, stream=3)
@@ -256,9 +259,11 @@ def test_argument_errors_are_statuses():
     kw, rows, launches = h.plan_info(1)
     assert kw == 8 and rows == 16 and launches == 1      # N <= 8: one kernel
     kw, rows, launches = h.plan_info(40)
-    assert rows == 128 and launches == 2                 # staging + product
+    assert rows == 128 and launches == 2                 # staging + tcgen05 product
     kw, rows, launches = h.plan_info(16)
     assert kw == 8 and rows == 128 and launches == 2     # staging + product
+    kw, rows, launches = h.plan_info(4)
+    assert kw == 8 and rows == 128 and launches == 1     # sk_kernel stages x itself
     assert h.device_status() == 0
 
 
