@@ -132,6 +132,18 @@ def _traffic_record():
     return rec.get("dram_bytes_per_launch")
 
 
+def aggregate_ranks(ms_local, world, wbytes, steps, dist=None, device=None):
+    """Whole-job timing of a replicated run: the slowest rank's time (max
+    over ranks) and the bytes all ranks streamed divided by it, in GB/s."""
+    import torch
+    ms = float(ms_local)
+    if dist is not None:
+        t = torch.tensor([ms], dtype=torch.float64, device=device)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+    return ms, world * wbytes * steps / (ms / 1e3) / 1e9
+
+
 def layer_weight_bytes():
     from skinny_gemm_q4_gb300 import synth
     return sum(M * synth.row_bytes(qt, K) for _, qt, M, K in synth.LAYER)
@@ -302,13 +314,8 @@ def run_ours(args):
         torch.cuda.synchronize()
         clk.mark_end()
         barrier()
-    ms = start.elapsed_time(end)
-    if dist is not None:
-        t = torch.tensor([ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
+    ms, value = aggregate_ranks(start.elapsed_time(end), world, wbytes, args.steps, dist, dev)
     ms_step = ms / args.steps
-    value = world * wbytes * args.steps / (ms / 1e3) / 1e9
 
     # Dominant kernel: the gate/up pair product (44% of the layer's bytes),
     # timed alone back to back over the 36 layers (graph), CUDA events on the
