@@ -71,8 +71,6 @@ def _load():
         lib.or_unpack_scale_min.restype = None
         lib.or_dequant_rows.argtypes = [i32, vp, vp, f32, i64, i64, vp, i64, vp]
         lib.or_dequant_rows.restype = i32
-        lib.or_gemv.argtypes = [vp, i64, i64, vp, i64, vp, vp, vp]
-        lib.or_gemv.restype = None
         lib.or_qgemv_rows.argtypes = [i32, vp, vp, f32, i64, i64, vp, i64, vp, i64,
                                       vp, vp, vp, vp]
         lib.or_qgemv_rows.restype = i32
@@ -136,19 +134,6 @@ def dequantize(qtype: int, w, M: int, K: int, scales=None, global_scale: float =
     if rc != 0:
         raise ValueError(f"oracle dequantize failed (rc={rc})")
     return out
-
-
-def gemv_dense(wf32: np.ndarray, x, residual=None):
-    """y, mag (float64 [N][M]) of a dense float32 W [M][K] and fp16 x [N][K]."""
-    wf32 = np.ascontiguousarray(wf32, dtype=np.float32)
-    M, K = wf32.shape
-    xb = _f16bits(x).reshape(-1, K)
-    N = xb.shape[0]
-    rb = None if residual is None else _f16bits(residual).reshape(N, M)
-    y = np.empty((N, M), dtype=np.float64)
-    mag = np.empty((N, M), dtype=np.float64)
-    _load().or_gemv(_ptr(wf32), M, K, _ptr(xb), N, _ptr(rb), _ptr(y), _ptr(mag))
-    return y, mag
 
 
 def qgemv(qtype: int, w, M: int, K: int, x, scales=None, global_scale: float = 1.0,

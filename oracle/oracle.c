@@ -293,34 +293,6 @@ int or_dequant(int type, const uint8_t *w, const uint8_t *scales, float g,
 /* The product.                                                             */
 /* ------------------------------------------------------------------------ */
 
-/* y[n][m] = sum_k w[m][k] * x[n][k] in increasing k, float64; mag likewise
- * with absolute products.  w is the float32 dequantized matrix [M][K], x is
- * fp16 bits [N][K], residual (nullable) fp16 bits [N][M]. */
-void or_gemv(const float *w, int64_t M, int64_t K, const uint16_t *x, int64_t N,
-             const uint16_t *residual, double *y, double *mag)
-{
-    for (int64_t n = 0; n < N; ++n) {
-        const uint16_t *xn = x + n * K;
-        for (int64_t m = 0; m < M; ++m) {
-            const float *wm = w + m * K;
-            double acc = 0.0, a = 0.0;
-            for (int64_t k = 0; k < K; ++k) {
-                double p = (double)wm[k] * or_f16_to_f64(xn[k]);
-                acc += p;
-                a += fabs(p);
-            }
-            if (residual) {
-                double r = or_f16_to_f64(residual[n * M + m]);
-                acc += r;
-                a += fabs(r);
-            }
-            y[n * M + m] = acc;
-            if (mag)
-                mag[n * M + m] = a;
-        }
-    }
-}
-
 /* The whole path for one weight matrix on selected rows: dequantize the rows
  * and multiply.  rows == NULL means rows 0..nrows-1.  y and mag are
  * [N][nrows]; residual (nullable) is [N][M] and indexed by the real row. */

@@ -28,8 +28,6 @@ int or_dequant(int type, const uint8_t *w, const uint8_t *scales, float g,
 int or_dequant_rows(int type, const uint8_t *w, const uint8_t *scales, float g,
                     int64_t M, int64_t K, const int64_t *rows, int64_t nrows,
                     float *out);
-void or_gemv(const float *w, int64_t M, int64_t K, const uint16_t *x, int64_t N,
-             const uint16_t *residual, double *y, double *mag);
 int or_qgemv_rows(int type, const uint8_t *w, const uint8_t *scales, float g,
                   int64_t M, int64_t K, const int64_t *rows, int64_t nrows,
                   const uint16_t *x, int64_t N, const uint16_t *residual,
