@@ -88,10 +88,18 @@ typedef struct {
 
 typedef struct qg_handle qg_handle;
 
-/* Create a handle for one weight matrix.
+/* Create a handle for one weight matrix and fix its launch plan.
+ * Defining passages: TandemLLM "Kernels", Row invariance (the tile table is
+ * keyed by the weight's shape, never by the row count: here the K split and
+ * rows per CTA are a function of (t, M, K) only) and NVFP4 matrix products (a
+ * tile table per shape); reflex-llm "docs/kernels.md", K-quant GEMV (the
+ * dispatcher selects the kernel by GGML tensor type).
  *   t            format
  *   M, K         rows (outputs) and columns (reduction length); M >= 1,
- *                K >= 256 and K % 256 == 0 for every format
+ *                K >= 256 and K % 256 == 0 for every format (NVFP4 too: the
+ *                pages' 32-element granularity is not served; every workload
+ *                here has K % 256 == 0); M up to 2^30 rows with
+ *                ceil(M / 64) <= 65535, K up to 2^24
  *   w_dev        device pointer to the packed matrix (row-major rows of
  *                qgemv_row_bytes(t, K) bytes), 16-byte aligned.  (Inside a
  *                Q6_K matrix the 210-byte blocks are not aligned; they are
@@ -108,7 +116,13 @@ qg_status qgemv_create(qg_handle **h, qg_type t, int64_t M, int64_t K,
                        const void *w_dev, const void *scales_dev, float global_scale,
                        const qg_opts *opts);
 
-/* y = x . W^T.  x: fp16 [N][K] device, 16-byte aligned; y: [N][M] device of
+/* y = x . W^T (reflex-llm "docs/kernels.md", K-quant GEMV for N = 1 and the
+ * batched K-quant GEMM section for N > 1, output token-outer; TandemLLM
+ * "Kernels", NVFP4 matrix products).  N = 1..32 rows are row-invariant
+ * (TandemLLM "Kernels", Verify twins); N >= 33 Q4_K calls run on the tcgen05
+ * prefill engine unless QG_FLAG_MMA_SYNC_PREFILL (TandemLLM "Kernels",
+ * Prefill kernels: prompt chunks have no twin contract).
+ * x: fp16 [N][K] device, 16-byte aligned; y: [N][M] device of
  * type ydt (fp16 rounded to nearest-even, or fp32), 4-byte aligned.
  * N >= 1.  Work is enqueued on stream (a cudaStream_t; NULL = legacy default
  * stream); the call does not synchronize unless QG_FLAG_DEBUG_SYNC is set.
@@ -118,80 +132,122 @@ qg_status qgemv_run(qg_handle *h, const void *x, int64_t N, void *y, qg_out ydt,
                     void *stream);
 
 /* y = residual + x . W^T, added in fp32 before one rounding to fp16
- * (reflex-llm "docs/kernels.md": Wo fused with the residual add).
+ * (reflex-llm "docs/kernels.md", uint32-loads section: the residual-fused Wo
+ * kernel gemv_quant_add; "docs/performance.md", Path C, PR #25).
  * residual, y: fp16 [N][M] device; y may equal residual (in place). */
 qg_status qgemv_run_add(qg_handle *h, const void *x, int64_t N, const void *residual,
                         void *y, void *stream);
 
-/* Two matrices with the same K sharing x (gate/up pair), one launch.
- * ya is [N][Ma], yb is [N][Mb]. */
+/* Two matrices with the same K sharing x (gate/up pair), one launch
+ * (reflex-llm "docs/kernels.md", uint32-loads section: gemv_quant_pair, the
+ * gate/up pair, ~44 % of decode).  ya is [N][Ma], yb is [N][Mb]; the handles'
+ * checks and errors are those of qgemv_run, plus QG_EINVAL when K differs or
+ * ya == yb.  Each matrix's rows have the bits of its own qgemv_run call. */
 qg_status qgemv_pair_run(qg_handle *a, qg_handle *b, const void *x, int64_t N,
                          void *ya, void *yb, qg_out ydt, void *stream);
 
 /* Three matrices with the same K sharing x (QKV triple); formats may differ
- * (e.g. Q4_K, Q4_K, Q6_K).  One staging pass and one product launch. */
+ * (e.g. Q4_K, Q4_K, Q6_K) (reflex-llm "docs/kernels.md", uint32-loads
+ * section: gemv_quant_triple_uint32_q4k_q4k_q6k, the QKV triple of
+ * Qwen3-4B).  One staging pass and one product launch where one kernel serves
+ * the formats.  QG_EINVAL when the Ks differ or two outputs are equal. */
 qg_status qgemv_triple_run(qg_handle *a, qg_handle *b, qg_handle *c, const void *x,
                            int64_t N, void *ya, void *yb, void *yc, qg_out ydt,
                            void *stream);
 
-/* Host-buffer form of qgemv_run: x_host (fp16 [N][K]) and y_host ([N][M] of
+/* Host-buffer form of qgemv_run (the same operation as qgemv_run; the pages
+ * time kernels with their inputs resident, TandemLLM "Kernels", How a kernel
+ * gets in -- this entry times the whole round trip).
+ * x_host (fp16 [N][K]) and y_host ([N][M] of
  * ydt) are host memory (pinned memory gives the fastest copies).  Copies x to
  * the device, runs, copies y back and synchronizes the stream before
  * returning.  The device buffers are owned by the handle and grow on demand. */
 qg_status qgemv_run_host(qg_handle *h, const void *x_host, int64_t N, void *y_host,
                          qg_out ydt, void *stream);
 
-/* Dequantize the whole matrix to fp32 w_out[M][K] (device, 4-byte aligned)
- * with the same decoders the product uses.  A test path, not a hot path. */
+/* Dequantize the whole matrix to fp32 w_out[M][K] (device, 4-byte aligned):
+ * w = d * sc * q - dmin * m (Q4_K/Q5_K), d * sc * (q - 32) (Q6_K), e2m1 *
+ * e4m3 * global scale (NVFP4), each rounded once to fp32 (reflex-llm
+ * "docs/performance.md", Path E "What worked": the Q4_K weight formula;
+ * TandemLLM "Kernels", NVFP4 matrix products).  It runs the product kernels'
+ * own decoder functions on their thread mapping, with the product's rounding
+ * steps for a one-hot x, so its output checks those decoders bit for bit;
+ * with QG_FLAG_FORCE_REFERENCE it uses the simple per-element reference
+ * decoder instead.  A test path, not a hot path (the product never writes
+ * weights back: reflex-llm "docs/kernels.md", K-quant GEMV).
+ * Errors: QG_EINVAL (null), QG_EALIGN, QG_ECUDA. */
 qg_status qgemv_dequantize(qg_handle *h, float *w_out, void *stream);
 
-/* Free the handle (does not free the borrowed weights).  NULL is a no-op. */
+/* Free the handle and the device buffers it owns (staging buffer, error word,
+ * the host-entry buffers); the borrowed weights are not freed, as the pages'
+ * kernels read weights where the caller keeps them (reflex-llm
+ * "docs/kernels.md", K-quant GEMV: weights stay in the caller's mapping).
+ * NULL is a no-op.  No call on h may be in flight. */
 void qgemv_destroy(qg_handle *h);
 
-/* Message of the last error on the calling thread ("" if none). */
+/* Message of the last error on the calling thread ("" if none); also the
+ * note left when a fast-path launch failure fell back to the reference
+ * kernel (reflex-llm "docs/kernels.md", uint32-loads section: any cudaError
+ * falls through to the typed byte-load kernel). */
 const char *qgemv_last_error(void);
 
 /* Bytes per row of the packed matrix (codes only for NVFP4); -1 if K is not
- * supported for the format.  Pure host function. */
+ * supported for the format.  Pure host function.  Block sizes: Q4_K 144 and
+ * Q6_K 210 bytes (reflex-llm "docs/kernels.md", uint32-loads section), Q5_K
+ * 176, NVFP4 K/2 code bytes (TandemLLM "Kernels", NVFP4 matrix products). */
 int64_t qgemv_row_bytes(qg_type t, int64_t K);
 
-/* Read (and with clear != 0, reset) the handle's device error word.  The
+/* Read (and with clear != 0, reset) the handle's device error word; with
+ * h == NULL, the error word of qgemv_run_noalloc on the current device.  The
  * kernels never trap: a bounded wait that runs out (a pipeline that stopped
  * making progress) sets bit 1 (consumer side) or bit 2 (producer side) and
- * the kernel returns with undefined results.  Synchronous (a device-to-host
- * copy of 4 bytes).  *flags_out == 0 means no kernel reported a problem. */
+ * the kernel returns with undefined results (reflex-llm "docs/kernels.md",
+ * uint32-loads section: a fault must never crash generation;
+ * "docs/performance.md", Path C #29: a faulting kernel leaves the context
+ * sticky).  Synchronous (a device-to-host copy of 4 bytes).  *flags_out == 0
+ * means no kernel reported a problem.  Errors: QG_ECUDA. */
 qg_status qgemv_device_status(qg_handle *h, uint32_t *flags_out, int clear);
 
 /* Launch plan of a handle, for tests and profiling: number of K-split ranks
- * (a cluster of CTAs per row tile, combined in rank order), rows per CTA for
- * the given N, and how many kernels one qgemv_run launches.  Pure host. */
+ * (a cluster of CTAs per row tile, combined in rank order: TandemLLM
+ * "Kernels", Row invariance, partial sums added in a fixed order), rows per
+ * CTA for the given N, and how many kernels one qgemv_run launches.  Pure
+ * host.  Errors: QG_EINVAL (null h, N < 1). */
 qg_status qgemv_plan_info(const qg_handle *h, int64_t N, int32_t *ksplit,
                           int32_t *rows_per_cta, int32_t *launches);
 
 /* Allocation-free form of qgemv_run, for callers that may not allocate device
  * memory while they run (for example a serving runtime that hands all device
- * memory to its own pool at start-up, or a library that must keep its host
- * process's device footprint fixed).  It needs no handle: the weights are
- * described by the same arguments as qgemv_create (t, M, K, w_dev, scales_dev,
- * global_scale; 16-byte aligned), x and y as in qgemv_run.  The pages have no
- * counterpart: this is a library-usage variant of the staging + product path.
+ * memory to its own pool at start-up, so any cudaMalloc behind its back can
+ * fail or fragment that pool, or a library that must keep its host process's
+ * device footprint fixed).  The pages have no counterpart: this is a
+ * library-usage variant of the staging + product path.  It needs no handle:
+ * the weights are described by the same arguments as qgemv_create (t, M, K,
+ * w_dev, scales_dev, global_scale; checked the same way), x and y as in
+ * qgemv_run; every argument is checked before the device is touched.
  * Scratch: one 2 MiB array in the library's device memory (held by every GPU
- * that loads the library until exit) holds the staged x; N is processed in
- * chunks of min(32, 2 MiB / (K/256 * 576)) tokens and K above 931,840 is
- * rejected with QG_EUNSUPPORTED.  It never calls cudaMalloc or cudaFree.  All
- * calls on a device share the array and it keeps the last call's contents;
- * every byte a call reads it has written first, so nothing needs clearing,
- * but calls that overlap on the GPU (unordered streams) race and must be
- * ordered.  The first call on a device looks up the array's address
+ * that loads the library until exit) holds the staged x and the kernels'
+ * error word; N is processed in chunks of min(32, about 2 MiB / (K/256 * 576))
+ * tokens and K above 931,840 is rejected with QG_EUNSUPPORTED.  It never calls
+ * cudaMalloc or cudaFree.  All calls on a device share the array and it keeps
+ * the last call's contents; every staged byte a call reads it has written
+ * first, and the error word starts at zero, so nothing needs clearing, but
+ * calls that overlap on the GPU (unordered streams) race and must be ordered.
+ * The error word is read (and cleared) with qgemv_device_status(NULL, ..).
+ * The first call on a device looks up the array's address
  * (cudaGetSymbolAddress) with that device current; make it before any stream
- * capture.  Results equal qgemv_run's for the same weights.
- * Errors: QG_EINVAL, QG_EALIGN, QG_EUNSUPPORTED, QG_ECUDA. */
+ * capture.  Results equal qgemv_run's bit for bit for N <= 32, and for every
+ * N those of a handle created with QG_FLAG_MMA_SYNC_PREFILL (Q4_K calls with
+ * N >= 33 under default flags run on the tcgen05 engine and agree only within
+ * the tolerance).  Errors: QG_EINVAL, QG_EALIGN, QG_EUNSUPPORTED, QG_ECUDA. */
 qg_status qgemv_run_noalloc(qg_type t, int64_t M, int64_t K, const void *w_dev,
                             const void *scales_dev, float global_scale, const void *x,
                             int64_t N, void *y, qg_out ydt, void *stream);
 
 /* Human-readable description of the options in effect (flags, environment
- * overrides QGEMV_FORCE_REFERENCE, QGEMV_DEBUG_SYNC, QGEMV_FAULT_INJECT). */
+ * overrides QGEMV_FORCE_REFERENCE, QGEMV_DEBUG_SYNC, QGEMV_FAULT_INJECT)
+ * (TandemLLM "Kernels", Knobs: every switch and the values in effect can be
+ * printed).  Never fails; the string is owned by the library. */
 const char *qgemv_describe(void);
 
 #ifdef __cplusplus

@@ -17,6 +17,10 @@
 
 using namespace qg;
 
+namespace qg {
+unsigned int *noalloc_error_word();  // qg_noalloc.cu (null on failure, message set)
+}
+
 struct qg_handle {
     qg_type type;
     int64_t M, K;
@@ -32,7 +36,7 @@ struct qg_handle {
     uint8_t *xs;   // staging buffer: max_tokens * nb * kXTok bytes
     unsigned int *err;  // device error word written by the kernels (timeouts)
     CUtensorMap tmw, tms;  // 3-D maps [block][row][bytes] for the N <= 8 kernel
-    CUtensorMap tmw1, tms1;  // the same with a 128-row x 1-block box (sk_kernel)
+    CUtensorMap tmw1, tms1;  // the same with a 128-row x 1-block box (qg_sk_kernel)
     CUtensorMap xmap[4];   // 2-D maps of this handle's staging buffer, box 8 (G) tokens
     int device;
     int sms = 0;           // SM count of that device
@@ -40,6 +44,7 @@ struct qg_handle {
     size_t hx_cap;
     void *hy;
     size_t hy_cap;
+    bool owns_buffers;     // xs and err were allocated by qgemv_create
 };
 
 namespace {
@@ -121,17 +126,17 @@ int plan_kw(int64_t M, int nb)
 
 int groups_for(int64_t n) { return n >= 32 ? 4 : (int)((n + 7) / 8); }
 
-// gemv_kernel keeps x for the whole K in shared memory; beyond about 48 KB of
-// it the smaller ring costs more than sk_kernel's per-stage x copies
+// qg_n8_kernel keeps x for the whole K in shared memory; beyond about 48 KB of
+// it the smaller ring costs more than qg_sk_kernel's per-stage x copies
 // (measured crossover on the sweep shapes: 34-46 KB).
 bool gemv_x_fits(int64_t n, int nb) { return n * nb * kXTok <= 48 * 1024; }
 
-// Dynamic shared memory that keeps sk_kernel at one CTA per SM (more than
+// Dynamic shared memory that keeps qg_sk_kernel at one CTA per SM (more than
 // half of the 228 KB an SM has).
 constexpr int kSkSpreadSmem = 120 * 1024;
 
 // For N >= 2, Q4_K / Q5_K matrices of at most 4096 rows run faster on
-// sk_kernel than on gemv_kernel (measured at N = 2..8: Wo 2560 x 4096 5.2-5.4
+// qg_sk_kernel than on qg_n8_kernel (measured at N = 2..8: Wo 2560 x 4096 5.2-5.4
 // vs 6.2-7.7 us, K/V 1024 x 2560 4.5-4.8 vs 4.8-6.7 us, Q 4096 x 2560
 // 5.9-6.0 vs 6.1-7.5 us, Q5_K 2560 x 9728 12.1-12.4 vs 12.2-12.6 us); the
 // 9728-row matrices, Q6_K and NVFP4 do not.  Both kernels give the same
@@ -142,18 +147,6 @@ bool sk_preferred(const qg_handle *const *hs, int nh, int64_t n)
     for (int i = 0; i < nh; ++i)
         if ((hs[i]->type != QG_Q4_K && hs[i]->type != QG_Q5_K) || hs[i]->M > 4096) return false;
     return true;
-}
-
-int rows_per_cta(int G) { return G <= 2 ? Cfg<1>::ROWS : Cfg<4>::ROWS; }
-
-int rb_of_tset(int tset)
-{
-    int rb = 0;
-    if (tset & TS_Q4K) rb = rb > Fmt<T_Q4K>::RBG ? rb : Fmt<T_Q4K>::RBG;
-    if (tset & TS_Q5K) rb = rb > Fmt<T_Q5K>::RBG ? rb : Fmt<T_Q5K>::RBG;
-    if (tset & TS_Q6K) rb = rb > Fmt<T_Q6K>::RBG ? rb : Fmt<T_Q6K>::RBG;
-    if (tset & TS_FP4) rb = rb > Fmt<T_FP4>::RBG ? rb : Fmt<T_FP4>::RBG;
-    return rb;
 }
 
 // Stage bytes of the N <= 8 kernel for a format and slice count.
@@ -198,18 +191,6 @@ Mat mat_of(const qg_handle *h, void *y, const __half *res)
     m.tile_begin = 0;
     m.gscale = h->gscale;
     return m;
-}
-
-cudaError_t launch_tset(int tset, int G, const Params &p, dim3 grid, cudaStream_t s)
-{
-    switch (tset) {
-    case TS_Q4K: return launch_skinny_q4k(G, p, grid, s);
-    case TS_Q5K: return launch_skinny_q5k(G, p, grid, s);
-    case TS_Q6K: return launch_skinny_q6k(G, p, grid, s);
-    case TS_FP4: return launch_skinny_fp4(G, p, grid, s);
-    case TS_Q4K | TS_Q6K: return launch_skinny_q4k_q6k(G, p, grid, s);
-    default: return cudaErrorInvalidValue;
-    }
 }
 
 bool tset_supported(int tset)
@@ -281,7 +262,7 @@ int sk_tset_smem(int wbytes, int G, bool q6, int *stages)
     return sk_smem_bytes(wbytes, G, st);
 }
 
-// sk_kernel with x staged inside (p.xin): ring of weights only, then this
+// qg_sk_kernel with x staged inside (p.xin): ring of weights only, then this
 // rank's x for all its super-blocks (ceil(nb / ks) x 8 G tokens x 576 B).
 // Two CTAs per SM where the ring allows it, as above.  Returns 0 when the x
 // region would be too large (the staging kernel is used instead).
@@ -445,7 +426,7 @@ qg_status run_product_mma(qg_handle *const *hs, int nh, const __half *x, int64_t
             }
         const int G = groups_for(n);
         // N <= 8 with at most 32 (token, super-block) items per CTA: x staged
-        // inside sk_kernel (no staging launch; the smallest kw gives the
+        // inside qg_sk_kernel (no staging launch; the smallest kw gives the
         // largest per-rank x).  With more items every CTA staging its slice
         // of x costs more than the launch it saves (measured: Q4_K 9728 x 2560
         // N = 16 9.5 vs 7.9 us, Q6_K 2560 x 9728 N = 8 16.2 vs 15.7 us; at
@@ -550,8 +531,8 @@ qg_status run_product_mma(qg_handle *const *hs, int nh, const __half *x, int64_t
     return QG_OK;
 }
 
-// Q4_K handles sharing x, N >= 33, on the tensor core (tc_kernel): x staged
-// once per chunk by stage_tc4_kernel, one product launch per group of equal
+// Q4_K handles sharing x, N >= 33, on the tensor core (qg_tc_kernel): x staged
+// once per chunk by qg_stage_tc_kernel, one product launch per group of equal
 // chunk count (cluster size).
 qg_status run_product_tc(qg_handle *const *hs, int nh, const __half *x, int64_t N,
                          void *const *ys, const __half *res, int out_f32, cudaStream_t s)
@@ -687,14 +668,128 @@ qg_status check_run_args(const qg_handle *h, const void *x, int64_t N, const voi
     return QG_OK;
 }
 
+// Argument checks of a weight matrix, before any CUDA call (qgemv_create and
+// the allocation-free entry point).
+qg_status check_matrix(qg_type t, int64_t M, int64_t K, const void *w_dev, const void *scales_dev,
+                       float global_scale)
+{
+    if (!type_known(t)) return fail(QG_EUNSUPPORTED, "unknown weight type %d", (int)t);
+    if (M < 1) return fail(QG_EINVAL, "M must be >= 1");
+    if (K < 256 || K % 256 != 0) return fail(QG_EUNSUPPORTED, "K must be a positive multiple of 256");
+    if (M > (int64_t)1 << 30 || K > (int64_t)1 << 24) return fail(QG_EUNSUPPORTED, "shape too large");
+    if (!w_dev) return fail(QG_EINVAL, "null weight pointer");
+    if (!aligned(w_dev, 16)) return fail(QG_EALIGN, "weights must be 16-byte aligned");
+    if (t == QG_NVFP4_W4A16) {
+        if (!scales_dev) return fail(QG_EINVAL, "NVFP4 needs the e4m3 scale array");
+        if (!aligned(scales_dev, 16)) return fail(QG_EALIGN, "scales must be 16-byte aligned");
+        if (!std::isfinite(global_scale)) return fail(QG_EINVAL, "global scale must be finite");
+    }
+    const int64_t rows_needed = (M + 63) / 64;
+    if (rows_needed > 65535) return fail(QG_EUNSUPPORTED, "too many rows for one grid");
+    return QG_OK;
+}
+
+// Everything of a handle that needs no device allocation: the plan (K
+// slices, layout), the device's SM count and the tensor maps (encoded on the
+// host) of the weights and of the given staging buffer xs; err is the device
+// error word the kernels report to.
+qg_status init_handle(qg_handle *h, qg_type t, int64_t M, int64_t K, const void *w_dev,
+                      const void *scales_dev, float global_scale, uint32_t flags, int max_tokens,
+                      uint8_t *xs, unsigned int *err)
+{
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+    const int nb = (int)(K / 256);
+    h->type = t;
+    h->M = M;
+    h->K = K;
+    h->nb = nb;
+    h->w = (const uint8_t *)w_dev;
+    h->sc = (const uint8_t *)scales_dev;
+    h->gscale = (t == QG_NVFP4_W4A16) ? global_scale : 1.0f;
+    h->row_bytes = qgemv_row_bytes(t, K);
+    h->sc_row_bytes = (t == QG_NVFP4_W4A16) ? K / 16 : 0;
+    h->w_bytes = h->row_bytes * M;
+    h->flags = flags;
+    h->max_tokens = max_tokens;
+    h->kw = plan_kw(M, nb);
+    h->layout = layout_of(t);
+    h->device = dev;
+    h->xs = xs;
+    h->err = err;
+    if (cudaDeviceGetAttribute(&h->sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
+        cudaGetLastError();
+        h->sms = 0;
+    }
+    if (t != QG_Q6_K) {
+        const int bb = (t == QG_NVFP4_W4A16) ? 128 : block_bytes(t);
+        const int R = kGemvRows / h->kw;
+        bool ok = encode_blocks(&h->tmw, w_dev, h->row_bytes, M, bb, R, h->kw);
+        if (ok && t == QG_NVFP4_W4A16)
+            ok = encode_blocks(&h->tms, scales_dev, h->sc_row_bytes, M, 16, R, h->kw);
+        if (ok) ok = encode_blocks(&h->tmw1, w_dev, h->row_bytes, M, bb, kSkRows, 1);
+        if (ok && t == QG_NVFP4_W4A16)
+            ok = encode_blocks(&h->tms1, scales_dev, h->sc_row_bytes, M, 16, kSkRows, 1);
+        if (!ok) return fail(QG_ECUDA, "tensor map encoding failed");
+    }
+    for (int G = 1; G <= 4; ++G)
+        if (!encode_staged(&h->xmap[G - 1], xs, nb, max_tokens, 8 * G))
+            return fail(QG_ECUDA, "tensor map encoding failed (staging buffer)");
+    return QG_OK;
+}
+
 }  // namespace
 
 namespace qg {
+// The path of qgemv_run with caller-provided device memory and no handle
+// (qgemv_run_noalloc, qg_noalloc.cu): the matrix is checked as qgemv_create
+// checks it, a handle is filled on the stack (plan and host-encoded tensor
+// maps; nothing is allocated), the staged x goes to the scratch memory that
+// get_scratch() returns (at most scratch_bytes; called only after every
+// argument check passed) in chunks of up to 32 tokens, and the kernels report
+// bounded-wait timeouts to the word at scratch + err_offset.  Q4_K calls with N >= 33 stay on the
+// mma.sync kernels (as with QG_FLAG_MMA_SYNC_PREFILL), so every row keeps
+// the bits of an N <= 32 call.
+qg_status run_with_scratch(qg_type t, int64_t M, int64_t K, const void *w_dev,
+                           const void *scales_dev, float global_scale, const void *x, int64_t N,
+                           void *y, qg_out ydt, cudaStream_t s, uint8_t *(*get_scratch)(),
+                           size_t scratch_bytes, size_t err_offset)
+{
+    g_err.clear();
+    qg_status st = check_matrix(t, M, K, w_dev, scales_dev, global_scale);
+    if (st != QG_OK) return st;
+    if (!x || !y) return fail(QG_EINVAL, "null x or y");
+    if (N < 1) return fail(QG_EINVAL, "N must be >= 1 (got %lld)", (long long)N);
+    if (N > (int64_t)1 << 24) return fail(QG_EUNSUPPORTED, "N too large");
+    if (ydt != QG_OUT_F16 && ydt != QG_OUT_F32) return fail(QG_EINVAL, "bad output type");
+    if (!aligned(x, 16)) return fail(QG_EALIGN, "x must be 16-byte aligned");
+    if (!aligned(y, ydt == QG_OUT_F32 ? 4 : 2)) return fail(QG_EALIGN, "y misaligned");
+    const size_t tok_bytes = (size_t)(K / 256) * kXTok;
+    const size_t fit = scratch_bytes / tok_bytes;
+    if (fit < 1)
+        return fail(QG_EUNSUPPORTED,
+                    "K too large: one token's staged x (%zu bytes) exceeds the %zu-byte scratch "
+                    "array",
+                    tok_bytes, scratch_bytes);
+    const int chunk = (int)(fit < 32 ? fit : 32);
+    // Every argument has been checked: now the device.
+    uint8_t *scratch = get_scratch();
+    if (!scratch) return QG_ECUDA;
+    unsigned int *err_word = reinterpret_cast<unsigned int *>(scratch + err_offset);
+    uint32_t flags = QG_FLAG_MMA_SYNC_PREFILL;
+    if (env_on("QGEMV_FORCE_REFERENCE")) flags |= QG_FLAG_FORCE_REFERENCE;
+    if (env_on("QGEMV_DEBUG_SYNC")) flags |= QG_FLAG_DEBUG_SYNC;
+    qg_handle h = {};
+    st = init_handle(&h, t, M, K, w_dev, scales_dev, global_scale, flags, chunk, scratch, err_word);
+    if (st != QG_OK) return st;
+    qg_handle *hp = &h;
+    void *ys[1] = {y};
+    return run_product(&hp, 1, (const __half *)x, N, ys, nullptr, ydt == QG_OUT_F32, s);
+}
+
 // Sets the calling thread's qgemv_last_error text (used by qg_noalloc.cu).
 void set_last_error(const char *msg) { g_err = msg; }
-// The K-slice plan of a (M, K/256) shape (used by qg_noalloc.cu, whose
-// results must equal qgemv_run's).
-int plan_k_slices(int64_t M, int nb) { return plan_kw(M, nb); }
 }  // namespace qg
 
 extern "C" {
@@ -729,17 +824,8 @@ qg_status qgemv_create(qg_handle **out, qg_type t, int64_t M, int64_t K, const v
 {
     if (!out) return fail(QG_EINVAL, "null output handle pointer");
     *out = nullptr;
-    if (!type_known(t)) return fail(QG_EUNSUPPORTED, "unknown weight type %d", (int)t);
-    if (M < 1) return fail(QG_EINVAL, "M must be >= 1");
-    if (K < 256 || K % 256 != 0) return fail(QG_EUNSUPPORTED, "K must be a positive multiple of 256");
-    if (M > (int64_t)1 << 30 || K > (int64_t)1 << 24) return fail(QG_EUNSUPPORTED, "shape too large");
-    if (!w_dev) return fail(QG_EINVAL, "null weight pointer");
-    if (!aligned(w_dev, 16)) return fail(QG_EALIGN, "weights must be 16-byte aligned");
-    if (t == QG_NVFP4_W4A16) {
-        if (!scales_dev) return fail(QG_EINVAL, "NVFP4 needs the e4m3 scale array");
-        if (!aligned(scales_dev, 16)) return fail(QG_EALIGN, "scales must be 16-byte aligned");
-        if (!std::isfinite(global_scale)) return fail(QG_EINVAL, "global scale must be finite");
-    }
+    qg_status st = check_matrix(t, M, K, w_dev, scales_dev, global_scale);
+    if (st != QG_OK) return st;
     const int max_tokens = (opts && opts->max_tokens > 0) ? opts->max_tokens : 128;
     if (max_tokens > (1 << 20)) return fail(QG_EUNSUPPORTED, "max_tokens too large");
     uint32_t flags = opts ? opts->flags : 0u;
@@ -747,79 +833,42 @@ qg_status qgemv_create(qg_handle **out, qg_type t, int64_t M, int64_t K, const v
     if (env_on("QGEMV_DEBUG_SYNC")) flags |= QG_FLAG_DEBUG_SYNC;
     if (fault_at("create")) return fail(QG_EFAULT_INJECTED, "injected fault: create");
 
-    const int nb = (int)(K / 256);
-    const int64_t rows_needed = (M + Cfg<1>::ROWS - 1) / Cfg<1>::ROWS;
-    if (rows_needed > 65535) return fail(QG_EUNSUPPORTED, "too many rows for one grid");
-
-    int dev = 0;
-    cudaError_t e = cudaGetDevice(&dev);
-    if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
-
     qg_handle *h = new (std::nothrow) qg_handle();
     if (!h) return fail(QG_ENOMEM, "host allocation failed");
-    h->type = t;
-    h->M = M;
-    h->K = K;
-    h->nb = nb;
-    h->w = (const uint8_t *)w_dev;
-    h->sc = (const uint8_t *)scales_dev;
-    h->gscale = (t == QG_NVFP4_W4A16) ? global_scale : 1.0f;
-    h->row_bytes = qgemv_row_bytes(t, K);
-    h->sc_row_bytes = (t == QG_NVFP4_W4A16) ? K / 16 : 0;
-    h->w_bytes = h->row_bytes * M;
-    h->flags = flags;
-    h->max_tokens = max_tokens;
-    h->kw = plan_kw(M, nb);
-    h->layout = layout_of(t);
-    h->device = dev;
-    if (cudaDeviceGetAttribute(&h->sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
-        cudaGetLastError();
-        h->sms = 0;
-    }
     // staged x: [token][super-block][576] for the mma.sync kernels; Q4_K
     // prefill chunks use the same buffer as [64-token chunk][super-block][8
-    // groups][kTcXBlk] (tc_kernel)
+    // groups][kTcXBlk] (qg_tc_kernel)
+    const int nb = (int)(K / 256);
     size_t xs_bytes = (size_t)max_tokens * nb * kXTok;
     if (t == QG_Q4_K) {
         const size_t tc = (size_t)((max_tokens + kTcTok - 1) / kTcTok) * tc_chunk_bytes(nb);
         if (tc > xs_bytes) xs_bytes = tc;
     }
-    e = cudaMalloc((void **)&h->xs, xs_bytes);
+    uint8_t *xs = nullptr;
+    cudaError_t e = cudaMalloc((void **)&xs, xs_bytes);
     if (e != cudaSuccess) {
         cudaGetLastError();
         delete h;
         return fail(QG_ENOMEM, "staging buffer allocation of %zu bytes failed", xs_bytes);
     }
-    if (t != QG_Q6_K) {
-        const int bb = (t == QG_NVFP4_W4A16) ? 128 : block_bytes(t);
-        const int R = kGemvRows / h->kw;
-        bool ok = encode_blocks(&h->tmw, w_dev, h->row_bytes, M, bb, R, h->kw);
-        if (ok && t == QG_NVFP4_W4A16)
-            ok = encode_blocks(&h->tms, scales_dev, h->sc_row_bytes, M, 16, R, h->kw);
-        if (ok) ok = encode_blocks(&h->tmw1, w_dev, h->row_bytes, M, bb, kSkRows, 1);
-        if (ok && t == QG_NVFP4_W4A16)
-            ok = encode_blocks(&h->tms1, scales_dev, h->sc_row_bytes, M, 16, kSkRows, 1);
-        if (!ok) {
-            cudaFree(h->xs);
-            delete h;
-            return fail(QG_ECUDA, "tensor map encoding failed");
-        }
-    }
-    for (int G = 1; G <= 4; ++G) {
-        if (!encode_staged(&h->xmap[G - 1], h->xs, nb, max_tokens, 8 * G)) {
-            cudaFree(h->xs);
-            delete h;
-            return fail(QG_ECUDA, "tensor map encoding failed (staging buffer)");
-        }
-    }
-    e = cudaMalloc((void **)&h->err, sizeof(unsigned int));
-    if (e == cudaSuccess) e = cudaMemset(h->err, 0, sizeof(unsigned int));
+    unsigned int *err = nullptr;
+    e = cudaMalloc((void **)&err, sizeof(unsigned int));
+    if (e == cudaSuccess) e = cudaMemset(err, 0, sizeof(unsigned int));
     if (e != cudaSuccess) {
         cudaGetLastError();
-        cudaFree(h->xs);
+        if (err) cudaFree(err);
+        cudaFree(xs);
         delete h;
         return fail(QG_ENOMEM, "error word allocation failed");
     }
+    st = init_handle(h, t, M, K, w_dev, scales_dev, global_scale, flags, max_tokens, xs, err);
+    if (st != QG_OK) {
+        cudaFree(xs);
+        cudaFree(err);
+        delete h;
+        return st;
+    }
+    h->owns_buffers = true;
     *out = h;
     return QG_OK;
 }
@@ -827,8 +876,8 @@ qg_status qgemv_create(qg_handle **out, qg_type t, int64_t M, int64_t K, const v
 void qgemv_destroy(qg_handle *h)
 {
     if (!h) return;
-    if (h->xs) cudaFree(h->xs);
-    if (h->err) cudaFree(h->err);
+    if (h->owns_buffers && h->xs) cudaFree(h->xs);
+    if (h->owns_buffers && h->err) cudaFree(h->err);
     if (h->hx) cudaFree(h->hx);
     if (h->hy) cudaFree(h->hy);
     delete h;
@@ -929,7 +978,11 @@ qg_status qgemv_dequantize(qg_handle *h, float *w_out, void *stream)
     if (!w_out) return fail(QG_EINVAL, "null output");
     if (!aligned(w_out, 4)) return fail(QG_EALIGN, "output must be 4-byte aligned");
     Mat m = mat_of(h, nullptr, nullptr);
-    cudaError_t e = launch_dequant(m, (int)h->K, w_out, (cudaStream_t)stream);
+    // The product kernels' own decoders; FORCE_REFERENCE selects the simple
+    // per-element reference decoder instead.
+    cudaError_t e = (h->flags & QG_FLAG_FORCE_REFERENCE)
+                        ? launch_dequant(m, (int)h->K, w_out, (cudaStream_t)stream)
+                        : launch_dequant_fast(m, (int)h->K, w_out, (cudaStream_t)stream);
     if (e != cudaSuccess) return cuda_fail(e, "dequantize kernel launch");
     if (h->flags & QG_FLAG_DEBUG_SYNC) {
         e = cudaStreamSynchronize((cudaStream_t)stream);
@@ -940,12 +993,14 @@ qg_status qgemv_dequantize(qg_handle *h, float *w_out, void *stream)
 
 qg_status qgemv_device_status(qg_handle *h, uint32_t *flags_out, int clear)
 {
-    if (!h) return fail(QG_EINVAL, "null handle");
+    // NULL: the allocation-free entry point's error word on the current device.
+    unsigned int *word = h ? h->err : noalloc_error_word();
+    if (!word) return QG_ECUDA;
     unsigned int w = 0;
-    cudaError_t e = cudaMemcpy(&w, h->err, sizeof w, cudaMemcpyDeviceToHost);
+    cudaError_t e = cudaMemcpy(&w, word, sizeof w, cudaMemcpyDeviceToHost);
     if (e != cudaSuccess) return cuda_fail(e, "error word read");
     if (clear && w) {
-        e = cudaMemset(h->err, 0, sizeof(unsigned int));
+        e = cudaMemset(word, 0, sizeof(unsigned int));
         if (e != cudaSuccess) return cuda_fail(e, "error word reset");
     }
     if (flags_out) *flags_out = w;
@@ -969,7 +1024,7 @@ qg_status qgemv_plan_info(const qg_handle *h, int64_t N, int32_t *ksplit, int32_
     if (ksplit) *ksplit = h->kw;
     if (h->type == QG_Q4_K && N >= kTcMinN && !(h->flags & QG_FLAG_MMA_SYNC_PREFILL) &&
         !(h->flags & QG_FLAG_FORCE_REFERENCE)) {
-        // tc_kernel: 128 rows per CTA, one staging launch per chunk
+        // qg_tc_kernel: 128 rows per CTA, one staging launch per chunk
         if (rows_cta) *rows_cta = kTcRows;
         if (launches) *launches = (int32_t)(2 * chunks);
         return QG_OK;

@@ -1,50 +1,9 @@
-// Instantiation helper: defines launch_skinny_<NAME>(G, ...) for one type set.
+// Instantiation helper: defines launch_gemv_<NAME> and launch_sk_<NAME>(G, ...)
+// for one type set.
 #pragma once
 #include "qg_launch.cuh"
 
 namespace qg {
-
-template <int TSET, int G>
-static cudaError_t launch_one(const Params &p, dim3 grid, cudaStream_t stream)
-{
-    constexpr int smem = SmemMax<TSET, G>::TOTAL;
-    static int configured[64] = {0};
-    int dev = 0;
-    cudaError_t e = cudaGetDevice(&dev);
-    if (e != cudaSuccess) return e;
-    if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
-    if (!configured[dev]) {
-        e = cudaFuncSetAttribute(skinny_kernel<TSET, G>,
-                                 cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-        if (e == cudaSuccess)
-            e = cudaFuncSetAttribute(skinny_kernel<TSET, G>,
-                                     cudaFuncAttributePreferredSharedMemoryCarveout,
-                                     cudaSharedmemCarveoutMaxShared);
-        if (e != cudaSuccess) return e;
-        configured[dev] = 1;
-    }
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = grid;
-    cfg.blockDim = dim3(kThreads);
-    cfg.dynamicSmemBytes = smem;
-    cfg.stream = stream;
-    cudaLaunchAttribute attr[2];
-    int na = 0;
-    attr[na].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[na].val.programmaticStreamSerializationAllowed = 1;
-    ++na;
-    if (p.ks > 1) {
-        attr[na].id = cudaLaunchAttributeClusterDimension;
-        attr[na].val.clusterDim.x = (unsigned)p.ks;
-        attr[na].val.clusterDim.y = 1;
-        attr[na].val.clusterDim.z = 1;
-        ++na;
-    }
-    cfg.attrs = attr;
-    cfg.numAttrs = na;
-    return cudaLaunchKernelEx(&cfg, skinny_kernel<TSET, G>, p);
-}
-
 
 template <int TSET>
 static cudaError_t launch_gemv_one(const Params &p, dim3 grid, int smem, cudaStream_t stream)
@@ -57,17 +16,17 @@ static cudaError_t launch_gemv_one(const Params &p, dim3 grid, int smem, cudaStr
     if (smem > kGemvMaxSmem) return cudaErrorInvalidValue;
     if (!configured[dev]) {
         // Largest shared-memory carveout, so two ~110 KB CTAs share an SM.
-        e = cudaFuncSetAttribute(gemv_kernel<TSET, false>,
+        e = cudaFuncSetAttribute(qg_n8_kernel<TSET, false>,
                                  cudaFuncAttributeMaxDynamicSharedMemorySize, kGemvMaxSmem);
         if (e == cudaSuccess)
-            e = cudaFuncSetAttribute(gemv_kernel<TSET, true>,
+            e = cudaFuncSetAttribute(qg_n8_kernel<TSET, true>,
                                      cudaFuncAttributeMaxDynamicSharedMemorySize, kGemvMaxSmem);
         if (e == cudaSuccess)
-            e = cudaFuncSetAttribute(gemv_kernel<TSET, false>,
+            e = cudaFuncSetAttribute(qg_n8_kernel<TSET, false>,
                                      cudaFuncAttributePreferredSharedMemoryCarveout,
                                      cudaSharedmemCarveoutMaxShared);
         if (e == cudaSuccess)
-            e = cudaFuncSetAttribute(gemv_kernel<TSET, true>,
+            e = cudaFuncSetAttribute(qg_n8_kernel<TSET, true>,
                                      cudaFuncAttributePreferredSharedMemoryCarveout,
                                      cudaSharedmemCarveoutMaxShared);
         if (e != cudaSuccess) return e;
@@ -83,8 +42,8 @@ static cudaError_t launch_gemv_one(const Params &p, dim3 grid, int smem, cudaStr
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    if (p.N == 1) return cudaLaunchKernelEx(&cfg, gemv_kernel<TSET, true>, p);
-    return cudaLaunchKernelEx(&cfg, gemv_kernel<TSET, false>, p);
+    if (p.N == 1) return cudaLaunchKernelEx(&cfg, qg_n8_kernel<TSET, true>, p);
+    return cudaLaunchKernelEx(&cfg, qg_n8_kernel<TSET, false>, p);
 }
 
 template <int TSET, int G, bool XIN = false>
@@ -97,10 +56,10 @@ static cudaError_t launch_sk_one(const Params &p, dim3 grid, int smem, cudaStrea
     if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
     if (smem > kGemvMaxSmem) return cudaErrorInvalidValue;
     if (!configured[dev]) {
-        e = cudaFuncSetAttribute(sk_kernel<TSET, G, XIN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        e = cudaFuncSetAttribute(qg_sk_kernel<TSET, G, XIN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  kGemvMaxSmem);
         if (e == cudaSuccess)
-            e = cudaFuncSetAttribute(sk_kernel<TSET, G, XIN>,
+            e = cudaFuncSetAttribute(qg_sk_kernel<TSET, G, XIN>,
                                      cudaFuncAttributePreferredSharedMemoryCarveout,
                                      cudaSharedmemCarveoutMaxShared);
         if (e != cudaSuccess) return e;
@@ -125,33 +84,13 @@ static cudaError_t launch_sk_one(const Params &p, dim3 grid, int smem, cudaStrea
     }
     cfg.attrs = attr;
     cfg.numAttrs = na;
-    return cudaLaunchKernelEx(&cfg, sk_kernel<TSET, G, XIN>, p);
+    return cudaLaunchKernelEx(&cfg, qg_sk_kernel<TSET, G, XIN>, p);
 }
 
 }  // namespace qg
 
 #define QG_DEFINE_TSET(NAME, TSET)                                                          \
     namespace qg {                                                                          \
-    cudaError_t launch_skinny_##NAME(int G, const Params &p, dim3 grid, cudaStream_t s)     \
-    {                                                                                       \
-        switch (G) {                                                                        \
-        case 1: return launch_one<TSET, 1>(p, grid, s);                                     \
-        case 2: return launch_one<TSET, 2>(p, grid, s);                                     \
-        case 3: return launch_one<TSET, 3>(p, grid, s);                                     \
-        case 4: return launch_one<TSET, 4>(p, grid, s);                                     \
-        default: return cudaErrorInvalidValue;                                              \
-        }                                                                                   \
-    }                                                                                       \
-    int smem_skinny_##NAME(int G)                                                           \
-    {                                                                                       \
-        switch (G) {                                                                        \
-        case 1: return SmemMax<TSET, 1>::TOTAL;                                             \
-        case 2: return SmemMax<TSET, 2>::TOTAL;                                             \
-        case 3: return SmemMax<TSET, 3>::TOTAL;                                             \
-        case 4: return SmemMax<TSET, 4>::TOTAL;                                             \
-        default: return 0;                                                                  \
-        }                                                                                   \
-    }                                                                                       \
     cudaError_t launch_gemv_##NAME(const Params &p, dim3 grid, int smem, cudaStream_t s)  \
     {                                                                                       \
         return launch_gemv_one<TSET>(p, grid, smem, s);                                     \

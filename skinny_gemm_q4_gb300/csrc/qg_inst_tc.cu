@@ -1,4 +1,4 @@
-// Launchers of tc_kernel (Q4_K prefill chunks on the 5th-generation tensor core).
+// Launchers of qg_tc_kernel (Q4_K prefill chunks on the 5th-generation tensor core).
 #include "qg_launch.cuh"
 #include "qg_tc.cuh"
 
@@ -14,10 +14,10 @@ static cudaError_t launch_tc_one(const Params &p, dim3 grid, int smem, cudaStrea
     if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
     if (smem > kGemvMaxSmem) return cudaErrorInvalidValue;
     if (!configured[dev]) {
-        e = cudaFuncSetAttribute(tc_kernel<G>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        e = cudaFuncSetAttribute(qg_tc_kernel<G>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  kGemvMaxSmem);
         if (e == cudaSuccess)
-            e = cudaFuncSetAttribute(tc_kernel<G>,
+            e = cudaFuncSetAttribute(qg_tc_kernel<G>,
                                      cudaFuncAttributePreferredSharedMemoryCarveout,
                                      cudaSharedmemCarveoutMaxShared);
         if (e != cudaSuccess) return e;
@@ -42,7 +42,7 @@ static cudaError_t launch_tc_one(const Params &p, dim3 grid, int smem, cudaStrea
     }
     cfg.attrs = attr;
     cfg.numAttrs = na;
-    return cudaLaunchKernelEx(&cfg, tc_kernel<G>, p);
+    return cudaLaunchKernelEx(&cfg, qg_tc_kernel<G>, p);
 }
 
 cudaError_t launch_tc(int G, const Params &p, dim3 grid, int smem, cudaStream_t s)

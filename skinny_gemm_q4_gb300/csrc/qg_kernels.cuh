@@ -15,7 +15,8 @@
 //     weights; TandemLLM "Kernels", NVFP4 matrix products: e2m1*e4m3 is exact.)
 //   * Q4_K/Q5_K: per super-block two MMA chains, D1a (low nibbles, sub-block
 //     2t of thread t) and D1b (high nibbles, 2t+1), plus one MMA of the 6-bit
-//     mins against the per-sub-block sums of x (split hi+lo in fp16), folded as
+//     mins against the per-sub-block sums of x (split S = 32 hi + lo in fp16,
+//     so every finite fp16 x fits), folded as
 //       acc = fma(d*2^22, D1a, acc); acc = fma(d*2^22, D1b, acc);
 //       acc = fma(-dmin*2^24, D2, acc).
 //     Q6_K: one MMA per 16-weight scale group, accs += sc*D, acc += d*accs.
@@ -28,20 +29,18 @@
 //   * x arrives in the B-fragment order of each format (stage_sb below), so
 //     every B load is one conflict-free 16-byte shared load.
 //
-// Three data-movement variants share the arithmetic above bit for bit:
-//   gemv_kernel   (N <= 8, x for the whole K within 48 KB; for N >= 2 not
+// Two data-movement variants share the arithmetic above bit for bit:
+//   qg_n8_kernel  (N <= 8, x for the whole K within 48 KB; for N >= 2 not
 //                 for Q4_K/Q5_K matrices of at most 4096 rows): a producer
 //                 warp streams the weight tiles into an mbarrier ring with one
 //                 3-D tensor copy (TMA) per stage (Q6_K, whose 210-byte blocks
 //                 are not 16-byte aligned: one 1-D bulk copy per row of the
 //                 aligned superset); 8 consumer warps decode and multiply; x
 //                 is staged inside the kernel.
-//   sk_kernel     (the rest up to N = 32, and N >= 33 except Q4_K): x staged
+//   qg_sk_kernel  (the rest up to N = 32, and N >= 33 except Q4_K): x staged
 //                 once per call by qg_stage.cu; a producer warp streams 128
 //                 weight rows and the staged x of one super-block per stage by
 //                 TMA; cluster ranks are slices.
-//   skinny_kernel (the allocation-free entry point): 16-byte cp.async ring,
-//                 4 warps, same slices and cluster ranks.
 #pragma once
 
 #include <cuda.h>
@@ -53,13 +52,11 @@ namespace qg {
 enum { T_Q4K = 12, T_Q5K = 13, T_Q6K = 14, T_FP4 = 256 };
 enum { TS_Q4K = 1, TS_Q5K = 2, TS_Q6K = 4, TS_FP4 = 8 };
 // Staged-x layouts: B-fragment orders of the mma.sync kernels, and the
-// tensor-core core-matrix layout of tc_kernel (qg_tc.cuh).
+// tensor-core core-matrix layout of qg_tc_kernel (qg_tc.cuh).
 enum { XL_Q4 = 0, XL_Q6 = 1, XL_FP4 = 2, XL_TC4 = 3, XL_COUNT = 4 };
 
-constexpr int kWarps = 4;
-constexpr int kThreads = 32 * kWarps;
 constexpr int kXTok = 576;     // staged bytes per (token, super-block): 512 x + 32 sums + pad
-constexpr int kTokChunk = 32;  // tokens per launch chunk (skinny_kernel)
+constexpr int kTokChunk = 32;  // tokens per blockIdx.z chunk (qg_sk_kernel)
 constexpr int kMaxMats = 3;
 
 // Error bits written to Params::err by a kernel (never trap).
@@ -68,7 +65,7 @@ enum { ERR_FULL_TIMEOUT = 1, ERR_EMPTY_TIMEOUT = 2 };
 struct Mat {
     CUtensorMap tmw;       // 3-D map of the packed rows (Q4_K, Q5_K, NVFP4 codes), gemv box
     CUtensorMap tms;       // 3-D map of the NVFP4 scale rows, gemv box
-    CUtensorMap tmw1;      // the same maps with a box of 128 rows x 1 block (sk_kernel)
+    CUtensorMap tmw1;      // the same maps with a box of 128 rows x 1 block (qg_sk_kernel)
     CUtensorMap tms1;
     const uint8_t *w;      // packed weights (codes for NVFP4)
     const uint8_t *sc;     // NVFP4 e4m3 scales [M][K/16]
@@ -89,20 +86,20 @@ struct Params {
     Mat mat[kMaxMats];
     int nmat;
     CUtensorMap xm[XL_COUNT];     // 2-D maps (576-byte super-block units, token) of the staged x
-                                  // per layout, box 8G tokens (sk_kernel)
-    const uint8_t *xs[XL_COUNT];  // staged x per layout (skinny_kernel)
+                                  // per layout, box 8G tokens (qg_sk_kernel)
+    const uint8_t *xs[XL_COUNT];  // staged x per layout (qg_tc_kernel)
     int64_t xs_tok_stride;        // bytes per token in the staged buffers (nb * kXTok)
-    const __half *x;              // raw x [N][K] (gemv_kernel stages it itself)
+    const __half *x;              // raw x [N][K] (qg_n8_kernel stages it itself)
     int N;                        // tokens of this launch
     int tok_base;                 // first token of blockIdx.z == 0
     int K;
     int nb;                       // 256-wide super-blocks along K
-    int ks;                       // cluster size along x (skinny_kernel: the matrices' kw)
-    int stages;                   // ring depth (gemv_kernel)
-    int xtok;                     // token stride of the in-kernel x region (gemv_kernel)
+    int ks;                       // cluster size along x (the matrices' kw)
+    int stages;                   // ring depth (qg_n8_kernel)
+    int xtok;                     // token stride of the in-kernel x region (qg_n8_kernel)
     int out_f32;
     unsigned int *err;            // error word (timeouts)
-    int xin;                      // sk_kernel: x staged inside the kernel from p.x
+    int xin;                      // qg_sk_kernel: x staged inside the kernel from p.x
 };
 
 template <int T>
@@ -126,44 +123,6 @@ struct Fmt<T_FP4> {
     static constexpr int BB = 128, RB = 192, VPR = 9, XL = XL_FP4, XV = 32, RBG = 144;
 };
 
-template <int G>
-struct Cfg {
-    static constexpr int MT = (G <= 2) ? 1 : 2;      // m16 tiles per warp
-    static constexpr int STAGES = (G <= 2) ? 4 : 3;  // ring depth
-    static constexpr int ROWS = kWarps * MT * 16;    // rows per CTA
-};
-
-template <int T, int G>
-struct Smem {
-    static constexpr int WSLOT = Cfg<G>::MT * 16 * Fmt<T>::RB;
-    static constexpr int WPART = kWarps * WSLOT;
-    static constexpr int XPART = 8 * G * kXTok;
-    static constexpr int STAGE = WPART + XPART;
-    static constexpr int TOTAL = Cfg<G>::STAGES * STAGE;
-};
-
-template <int TSET, int G>
-struct SmemMax {
-    static constexpr int a = (TSET & TS_Q4K) ? Smem<T_Q4K, G>::TOTAL : 0;
-    static constexpr int b = (TSET & TS_Q5K) ? Smem<T_Q5K, G>::TOTAL : 0;
-    static constexpr int c = (TSET & TS_Q6K) ? Smem<T_Q6K, G>::TOTAL : 0;
-    static constexpr int d = (TSET & TS_FP4) ? Smem<T_FP4, G>::TOTAL : 0;
-    static constexpr int ab = a > b ? a : b;
-    static constexpr int cd = c > d ? c : d;
-    static constexpr int TOTAL = ab > cd ? ab : cd;
-};
-
-template <int TSET>
-struct RBMax {
-    static constexpr int a = (TSET & TS_Q4K) ? Fmt<T_Q4K>::RB : 0;
-    static constexpr int b = (TSET & TS_Q5K) ? Fmt<T_Q5K>::RB : 0;
-    static constexpr int c = (TSET & TS_Q6K) ? Fmt<T_Q6K>::RB : 0;
-    static constexpr int d = (TSET & TS_FP4) ? Fmt<T_FP4>::RB : 0;
-    static constexpr int ab = a > b ? a : b;
-    static constexpr int cd = c > d ? c : d;
-    static constexpr int V = ab > cd ? ab : cd;
-};
-
 __device__ __forceinline__ uint32_t word_of(const uint4 &v, int i)
 {
     return i == 0 ? v.x : i == 1 ? v.y : i == 2 ? v.z : v.w;
@@ -184,7 +143,12 @@ __device__ __forceinline__ uint32_t lds32_any(uint32_t addr)
 //        j&1, stored (x0, x2, x1, x3); bytes 512..543: for t = 0..3 the fp16
 //        (hi[2t], hi[2t+1], lo[2t], lo[2t+1]) of the sub-block sums
 //        S_s = sum of the 32 x of sub-block s (fp32: sequential within the
-//        lane, then a fixed butterfly), hi = fp16(S), lo = fp16(S - hi).
+//        lane, then a fixed butterfly), hi = fp16(S * 2^-5),
+//        lo = fp16(S - 32 hi).  The 2^-5 keeps hi finite for every finite
+//        fp16 x (|S| <= 32 * 65504, so |hi| <= 65504) and |lo| <= 512; the
+//        min MMA multiplies hi by m * 2^-19 and lo by m * 2^-24.  (hi is an
+//        fp16 normal, and power-of-two scaling of x scales the pair exactly,
+//        while |S| >= 2^-9.)
 //   Q6 : 4-group q = 32h + 8s + 4i + t -> unit (h*4 + s)*4 + t, half i,
 //        stored (x0, x2, x1, x3).
 //   FP4: the raw 8 values of lane l -> unit ((l/16)*4 + (l&3))*4 + ((l/4)&3).
@@ -208,8 +172,8 @@ __device__ __forceinline__ void stage_sb(uint4 v, int lane, uint8_t *q4, uint8_t
         }
         s = __fadd_rn(s, __shfl_xor_sync(0xffffffffu, s, 1));
         s = __fadd_rn(s, __shfl_xor_sync(0xffffffffu, s, 2));
-        const __half hi = __float2half_rn(s);
-        const __half lo = __float2half_rn(__fsub_rn(s, __half2float(hi)));
+        const __half hi = __float2half_rn(__fmul_rn(s, 0.03125f));
+        const __half lo = __float2half_rn(__fsub_rn(s, __fmul_rn(__half2float(hi), 32.0f)));
         const uint32_t hib = __half_as_ushort(hi), lob = __half_as_ushort(lo);
         const uint32_t hin = __shfl_down_sync(0xffffffffu, hib, 4);
         const uint32_t lon = __shfl_down_sync(0xffffffffu, lob, 4);
@@ -250,7 +214,8 @@ __device__ __forceinline__ void stage_sb(uint4 v, int lane, uint8_t *q4, uint8_t
 // ---------------------------------------------------------------------------
 struct KRow {
     uint32_t slo, shi;  // fp16x2 broadcast scale for the two sub-blocks
-    uint32_t amin;      // fp16x2 (m_2t, m_2t+1) * 2^-24 (subnormals)
+    uint32_t amin;      // fp16x2 (m_2t, m_2t+1) * 2^-24 (subnormals): times the lo sums,
+                        // and times 32 (exact) against the hi sums (S = 32 hi + lo)
     float dd, dm;       // d * 2^22 and -dmin * 2^24
 };
 
@@ -308,6 +273,73 @@ __device__ __forceinline__ KRow k_row_consts(const uint4 &h, const KSel &ks)
 }
 
 // ---------------------------------------------------------------------------
+// Exact decoders of one 32-bit word of packed weights into the two fp16x2
+// A-operand registers it feeds: x02 holds the elements of bytes 0 and 2 of
+// the word (low half, high half), x13 those of bytes 1 and 3.  The product
+// kernels and the dequantize entry (qg_dequant.cu) call the same functions.
+// ---------------------------------------------------------------------------
+// Q4_K / Q5_K: qs word w of thread t, nibble half e (0: low nibbles, sub-block
+// 2t; 1: high nibbles, sub-block 2t + 1); Q5_K also takes the qh word hj at
+// the same byte offset.  slo / shi: the k_row_consts scales.  Result
+// sc * q * 2^-22, exact.
+template <int T>
+__device__ __forceinline__ void kq_decode(uint32_t w, uint32_t hj, int t, int e, uint32_t slo,
+                                          uint32_t shi, uint32_t &x02, uint32_t &x13)
+{
+    uint32_t p0, p1;
+    if (T == T_Q4K) {
+        (void)hj;
+        (void)t;
+        if (e == 0) {
+            p0 = w & 0x000f000fu;
+            p1 = (w >> 8) & 0x000f000fu;
+        } else {
+            p0 = w & 0x00f000f0u;
+            p1 = (w >> 8) & 0x00f000f0u;
+        }
+    } else {
+        const uint32_t hb = hj >> (2 * t + e);
+        const uint32_t ws = e ? (w >> 4) : w;
+        p0 = (ws & 0x000f000fu) | ((hb << 4) & 0x00100010u);
+        p1 = ((ws >> 8) & 0x000f000fu) | ((hb >> 4) & 0x00100010u);
+    }
+    const uint32_t sc = e ? shi : slo;
+    x02 = hmul2(p0, sc);
+    x13 = hmul2(p1, sc);
+}
+
+// Q6_K: the ql word (its low nibbles for s < 2, high for s >= 2) and the qh
+// word (bits 2s, 2s + 1 of each byte) of scale step s.  Result q - 32, exact.
+__device__ __forceinline__ void q6_decode(uint32_t ql, uint32_t qh, int s, uint32_t &x02,
+                                          uint32_t &x13)
+{
+    const uint32_t nw = ((s >> 1) ? (ql >> 4) : ql) & 0x0f0f0f0fu;
+    const uint32_t hw = (s <= 2) ? (qh << (4 - 2 * s)) : (qh >> 2);
+    const uint32_t v = nw | (hw & 0x30303030u);
+    x02 = hsub2(__byte_perm(v, 0x6464u, 0x5240u), 0x64206420u);
+    x13 = hsub2(__byte_perm(v, 0x6464u, 0x5341u), 0x64206420u);
+}
+
+// NVFP4 group scales of thread t from the scale word sw holding bytes
+// 4 (t / 2) .. + 3 of a 64-element half: bytes 2t, 2t + 1 (mod 4), the scales
+// of its code bytes 0..7 (sA) and 8..15 (sB), as fp16x2 broadcasts.
+__device__ __forceinline__ void fp4_scales(uint32_t sw, int t, uint32_t &sA, uint32_t &sB)
+{
+    const uint32_t s2 = e4m3x2_to_h2((sw >> (16 * (t & 1))) & 0xffffu);
+    sA = __byte_perm(s2, 0u, 0x1010u);
+    sB = __byte_perm(s2, 0u, 0x3232u);
+}
+
+// NVFP4: two code bytes (low 16 bits of w: elements 2B .. 2B + 3 of code
+// byte B, B + 1) times the fp16x2 broadcast group scale.  Result e2m1 * e4m3,
+// exact in fp16.
+__device__ __forceinline__ void fp4_decode(uint32_t w, uint32_t sc, uint32_t &x02, uint32_t &x13)
+{
+    x02 = hmul2(e2m1x2_to_h2(w & 0xffu), sc);
+    x13 = hmul2(e2m1x2_to_h2((w >> 8) & 0xffu), sc);
+}
+
+// ---------------------------------------------------------------------------
 // Per-super-block compute, one function per format.  wsl: this warp's first
 // weight row in shared memory (row pitch RBP); xsl: this super-block's staged
 // x for token 0 (token stride xtok).  acc is [MT][G][4] in the mma C-fragment
@@ -357,32 +389,13 @@ __device__ __forceinline__ void compute_kquant(uint32_t wsl, uint32_t xsl, int x
                 const int j = 2 * jp + jj;
 #pragma unroll
                 for (int mt = 0; mt < MT; ++mt) {
-                    uint32_t p[2][2];  // [row][pair 02/13]
-#pragma unroll
-                    for (int rr = 0; rr < 2; ++rr) {
-                        const uint32_t w = word_of(q[mt][rr][j >> 2], j & 3);
-                        if (T == T_Q4K) {
-                            if (e == 0) {
-                                p[rr][0] = w & 0x000f000fu;
-                                p[rr][1] = (w >> 8) & 0x000f000fu;
-                            } else {
-                                p[rr][0] = w & 0x00f000f0u;
-                                p[rr][1] = (w >> 8) & 0x00f000f0u;
-                            }
-                        } else {
-                            const uint32_t hj = word_of(qh[mt][rr][j >> 2], j & 3);
-                            const uint32_t hb = hj >> (2 * t + e);
-                            const uint32_t ws = e ? (w >> 4) : w;
-                            p[rr][0] = (ws & 0x000f000fu) | ((hb << 4) & 0x00100010u);
-                            p[rr][1] = ((ws >> 8) & 0x000f000fu) | ((hb >> 4) & 0x00100010u);
-                        }
-                    }
-                    const uint32_t s0 = e ? rc[mt][0].shi : rc[mt][0].slo;
-                    const uint32_t s1 = e ? rc[mt][1].shi : rc[mt][1].slo;
-                    const uint32_t a0 = hmul2(p[0][0], s0);
-                    const uint32_t a1 = hmul2(p[1][0], s1);
-                    const uint32_t a2 = hmul2(p[0][1], s0);
-                    const uint32_t a3 = hmul2(p[1][1], s1);
+                    uint32_t a0, a1, a2, a3;
+                    kq_decode<T>(word_of(q[mt][0][j >> 2], j & 3),
+                                 T == T_Q5K ? word_of(qh[mt][0][j >> 2], j & 3) : 0u, t, e,
+                                 rc[mt][0].slo, rc[mt][0].shi, a0, a2);
+                    kq_decode<T>(word_of(q[mt][1][j >> 2], j & 3),
+                                 T == T_Q5K ? word_of(qh[mt][1][j >> 2], j & 3) : 0u, t, e,
+                                 rc[mt][1].slo, rc[mt][1].shi, a1, a3);
 #pragma unroll
                     for (int gi = 0; gi < G; ++gi) {
                         const uint32_t b0 = jj ? B[gi].z : B[gi].x, b1 = jj ? B[gi].w : B[gi].y;
@@ -403,7 +416,8 @@ __device__ __forceinline__ void compute_kquant(uint32_t wsl, uint32_t xsl, int x
 #pragma unroll
         for (int mt = 0; mt < MT; ++mt) {
             float d2[4];
-            mma16816_zc(d2, rc[mt][0].amin, rc[mt][1].amin, rc[mt][0].amin, rc[mt][1].amin, bm.x,
+            mma16816_zc(d2, hmul2(rc[mt][0].amin, 0x50005000u), hmul2(rc[mt][1].amin, 0x50005000u),
+                        rc[mt][0].amin, rc[mt][1].amin, bm.x,
                         bm.y);
 #pragma unroll
             for (int c = 0; c < 4; ++c) {
@@ -476,13 +490,8 @@ __device__ __forceinline__ void q6k_body(uint32_t wsl, int RB, uint32_t xsl, int
                     float scf[2];
 #pragma unroll
                     for (int rr = 0; rr < 2; ++rr) {
-                        const uint32_t ql = (s & 1) ? ql1[mt][rr] : ql0[mt][rr];
-                        const uint32_t nw = ((s >> 1) ? (ql >> 4) : ql) & 0x0f0f0f0fu;
-                        const uint32_t hw = (s <= 2) ? (qh[mt][rr] << (4 - 2 * s))
-                                                     : (qh[mt][rr] >> 2);
-                        const uint32_t v = nw | (hw & 0x30303030u);
-                        a[rr][0] = hsub2(__byte_perm(v, 0x6464u, 0x5240u), 0x64206420u);
-                        a[rr][1] = hsub2(__byte_perm(v, 0x6464u, 0x5341u), 0x64206420u);
+                        q6_decode((s & 1) ? ql1[mt][rr] : ql0[mt][rr], qh[mt][rr], s, a[rr][0],
+                                  a[rr][1]);
                         scf[rr] = (float)(int8_t)((sw[mt][rr][grp >> 2] >> (8 * (grp & 3))) & 0xffu);
                     }
 #pragma unroll
@@ -546,11 +555,8 @@ __device__ __forceinline__ void compute_fp4(uint32_t cbase, int cp, uint32_t sba
             for (int rr = 0; rr < 2; ++rr) {
                 const int r = mt * 16 + g + 8 * rr;
                 cw[mt][rr] = lds128(cbase + r * cp + 64 * hf + 16 * t);
-                // scale bytes 8hf + 2t, 8hf + 2t + 1 of the chunk's 16
-                const uint32_t sw = lds32(sbase + r * sp + 8 * hf + 4 * (t >> 1));
-                const uint32_t s2 = e4m3x2_to_h2((sw >> (16 * (t & 1))) & 0xffffu);
-                sA[mt][rr] = __byte_perm(s2, 0u, 0x1010u);
-                sB[mt][rr] = __byte_perm(s2, 0u, 0x3232u);
+                fp4_scales(lds32(sbase + r * sp + 8 * hf + 4 * (t >> 1)), t, sA[mt][rr],
+                           sB[mt][rr]);
             }
         }
 #pragma unroll
@@ -569,9 +575,7 @@ __device__ __forceinline__ void compute_fp4(uint32_t cbase, int cp, uint32_t sba
 #pragma unroll
                     for (int rr = 0; rr < 2; ++rr) {
                         const uint32_t w = word_of(cw[mt][rr], s >> 1) >> (16 * (s & 1));
-                        const uint32_t sc = (s < 4) ? sA[mt][rr] : sB[mt][rr];
-                        a[rr][0] = hmul2(e2m1x2_to_h2(w & 0xffu), sc);
-                        a[rr][1] = hmul2(e2m1x2_to_h2((w >> 8) & 0xffu), sc);
+                        fp4_decode(w, (s < 4) ? sA[mt][rr] : sB[mt][rr], a[rr][0], a[rr][1]);
                     }
 #pragma unroll
                     for (int gi = 0; gi < G; ++gi)
@@ -784,124 +788,7 @@ __device__ __forceinline__ int select_mat(const Params &p, int tile)
 }
 
 // ===========================================================================
-// skinny_kernel (N > 8): 4 warps, cp.async ring, x staged by qg_stage.cu.
-// ===========================================================================
-template <int T, int G>
-__device__ __forceinline__ void run_tile(const Params &p, const Mat &m, int rtile, uint8_t *smem)
-{
-    using F = Fmt<T>;
-    using S = Smem<T, G>;
-    constexpr int MT = Cfg<G>::MT;
-    constexpr int STAGES = Cfg<G>::STAGES;
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int g = lane >> 2, t = lane & 3;
-    const int rank = blockIdx.x;
-    const int ks = p.ks;                       // == m.kw
-    // K slice `rank`: super-blocks rank, rank + ks, rank + 2 ks, ...
-    const int nsb = (p.nb - rank + ks - 1) / ks;
-    const int tok0 = p.tok_base + blockIdx.z * kTokChunk;
-    const int ntok = min(8 * G, p.N - tok0);
-    const int row_w = rtile * Cfg<G>::ROWS + warp * MT * 16;
-    const uint32_t sbase = smem_u32(smem);
-    const uint8_t *xs = p.xs[F::XL] + (int64_t)tok0 * p.xs_tok_stride;
-
-    auto issue_w = [&](int i) {
-        const int sb = rank + i * ks;
-        const uint32_t dst = sbase + (i % STAGES) * S::STAGE + warp * S::WSLOT;
-#pragma unroll 1
-        for (int v = lane; v < MT * 16 * F::VPR; v += 32) {
-            const int r = v / F::VPR, c = v - r * F::VPR;
-            const int row = row_w + r;
-            const uint8_t *src = m.w;
-            int nbytes = 0;
-            if (row < m.M) {
-                nbytes = 16;
-                if (T == T_FP4) {
-                    src = (c < 8) ? m.w + (int64_t)row * m.row_bytes + sb * 128 + c * 16
-                                  : m.sc + (int64_t)row * m.sc_row_bytes + sb * 16;
-                } else if (T == T_Q6K) {
-                    const uint8_t *blk = m.w + (int64_t)row * m.row_bytes + (int64_t)sb * 210;
-                    const uint8_t *al = (const uint8_t *)((uintptr_t)blk & ~(uintptr_t)15);
-                    src = al + c * 16;
-                    const int64_t left = (m.w + m.w_bytes) - src;
-                    nbytes = left >= 16 ? 16 : (left > 0 ? (int)left : 0);
-                } else {
-                    src = m.w + (int64_t)row * m.row_bytes + (int64_t)sb * F::BB + c * 16;
-                }
-            }
-            cp_async16(dst + r * F::RB + c * 16, src, nbytes);
-        }
-    };
-    auto issue_x = [&](int i) {
-        const int sb = rank + i * ks;
-        const uint32_t dst = sbase + (i % STAGES) * S::STAGE + S::WPART;
-#pragma unroll 1
-        for (int v = threadIdx.x; v < ntok * F::XV; v += kThreads) {
-            const int n = v / F::XV, c = v - n * F::XV;
-            const uint8_t *src = xs + (int64_t)n * p.xs_tok_stride + (int64_t)sb * kXTok + c * 16;
-            cp_async16(dst + n * kXTok + c * 16, src, 16);
-        }
-    };
-
-    // Weights do not depend on earlier kernels: start them before waiting.
-#pragma unroll
-    for (int i = 0; i < STAGES - 1; ++i) {
-        if (i < nsb) issue_w(i);
-        cp_async_commit();
-    }
-    pdl_wait();
-#pragma unroll
-    for (int i = 0; i < STAGES - 1; ++i)
-        if (i < nsb) issue_x(i);
-    cp_async_commit();
-
-    Acc<T, MT, G> A;
-    A.zero();
-    const KSel ksel = k_sel(t);
-#pragma unroll 1
-    for (int i = 0; i < nsb; ++i) {
-        if (i == 0)
-            cp_async_wait<0>();
-        else
-            cp_async_wait<STAGES - 2>();
-        __syncthreads();
-        if (i + STAGES - 1 < nsb) {
-            issue_w(i + STAGES - 1);
-            issue_x(i + STAGES - 1);
-        }
-        cp_async_commit();
-        const uint32_t stage = sbase + (i % STAGES) * S::STAGE;
-        compute_sb<T, MT, G>(A, stage + warp * S::WSLOT, stage + S::WPART, kXTok, g, t, ntok, m,
-                             row_w, rank + i * ks, ksel);
-    }
-    cp_async_wait<0>();
-    __syncthreads();
-    reduce_and_store<T, MT, G>(A, reinterpret_cast<float *>(smem), rank, ks, threadIdx.x, kThreads,
-                               true, p, m, rtile * Cfg<G>::ROWS, tok0, g, t);
-}
-
-template <int TSET, int G>
-__global__ void __launch_bounds__(kThreads) skinny_kernel(const __grid_constant__ Params p)
-{
-    extern __shared__ __align__(128) uint8_t smem[];
-    // Let the next kernel in the stream start launching; it waits for this
-    // grid to finish before touching anything this grid writes.
-    pdl_trigger();
-    const int tile = blockIdx.y;
-    const Mat &m = p.mat[select_mat(p, tile)];
-    const int rtile = tile - m.tile_begin;
-    if constexpr ((TSET & TS_Q4K) != 0)
-        if (m.type == T_Q4K) return run_tile<T_Q4K, G>(p, m, rtile, smem);
-    if constexpr ((TSET & TS_Q5K) != 0)
-        if (m.type == T_Q5K) return run_tile<T_Q5K, G>(p, m, rtile, smem);
-    if constexpr ((TSET & TS_Q6K) != 0)
-        if (m.type == T_Q6K) return run_tile<T_Q6K, G>(p, m, rtile, smem);
-    if constexpr ((TSET & TS_FP4) != 0)
-        if (m.type == T_FP4) return run_tile<T_FP4, G>(p, m, rtile, smem);
-}
-
-// ===========================================================================
-// gemv_kernel (N <= 8): warp 0 produces, warps 1..CW consume (16 rows each).
+// qg_n8_kernel (N <= 8): warp 0 produces, warps 1..CW consume (16 rows each).
 // Shared memory: [full[STAGES], empty[STAGES] mbarriers | STAGES weight slots
 // of rows_cta * RB bytes | x region: N tokens x (this rank's super-blocks) x
 // 576 bytes, token stride p.xtok].
@@ -1164,7 +1051,7 @@ __device__ __forceinline__ void gemv_tile(const Params &p, const Mat &m, int rti
 // folded (the odd columns are never stored; the even ones get the same
 // arithmetic as for any other N).
 template <int TSET, bool ONE>
-__global__ void __launch_bounds__(32 * (kGemvCW + 1)) gemv_kernel(const __grid_constant__ Params p)
+__global__ void __launch_bounds__(32 * (kGemvCW + 1)) qg_n8_kernel(const __grid_constant__ Params p)
 {
     extern __shared__ __align__(128) uint8_t smem[];
     pdl_trigger();
@@ -1181,7 +1068,7 @@ __global__ void __launch_bounds__(32 * (kGemvCW + 1)) gemv_kernel(const __grid_c
         if (m.type == T_FP4) return gemv_tile<T_FP4, !ONE>(p, m, rtile, smem);
 }
 
-// Dynamic shared memory of gemv_kernel: barriers, `stages` ring slots of
+// Dynamic shared memory of qg_n8_kernel: barriers, `stages` ring slots of
 // `stage_bytes`, and the x region of N tokens x nb super-blocks.
 __host__ __device__ inline int gemv_xtok(int nb) { return nb * kXTok + ((nb & 1) ? 0 : 64); }
 __host__ __device__ inline int gemv_smem_bytes(int stage_bytes, int stages, int N, int nb)
@@ -1196,14 +1083,15 @@ __host__ __device__ inline int gemv_smem_bytes(int stage_bytes, int stages, int 
 namespace qg {
 
 // ===========================================================================
-// sk_kernel (N > 8, and N <= 8 when x does not fit gemv_kernel's shared
-// memory or the matrix is a Q4_K/Q5_K one of at most 4096 rows): warp 0 streams, per super-block of this cluster rank's K slice,
+// qg_sk_kernel (N > 8, and N <= 8 when x does not fit qg_n8_kernel's shared
+// memory or the matrix is a Q4_K/Q5_K one of at most 4096 rows): warp 0
+// streams, per super-block of this cluster rank's K slice,
 // the weights of 128 rows (one 3-D tensor copy; Q6_K rows are loaded by
 // their consumer warp with 16-byte cp.async) and the staged x of up to 32
 // tokens (one 2-D tensor copy) into an mbarrier ring; warps 1..8 each decode
 // and multiply 16 rows against G column groups.  The slices and their
-// rank-order sum through distributed shared memory are those of
-// skinny_kernel, so every row gets the same bits as on any other path.
+// rank-order sum through distributed shared memory follow the same plan as
+// qg_n8_kernel's in-CTA slices, so every row gets the same bits on either.
 // Shared memory: [full[4], empty[4] | ring | (after the loop) rank partials].
 // ===========================================================================
 constexpr int kSkCons = 8;
@@ -1416,7 +1304,7 @@ __device__ __forceinline__ void sk_tile(const Params &p, const Mat &m, int rtile
 }
 
 template <int TSET, int G, bool XIN = false>
-__global__ void __launch_bounds__(kSkThreads) sk_kernel(const __grid_constant__ Params p)
+__global__ void __launch_bounds__(kSkThreads) qg_sk_kernel(const __grid_constant__ Params p)
 {
     extern __shared__ __align__(128) uint8_t smem[];
     pdl_trigger();

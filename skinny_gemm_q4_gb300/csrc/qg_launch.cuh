@@ -7,15 +7,15 @@
 namespace qg {
 
 constexpr int kGemvMaxSmem = 200 * 1024;
-// Dynamic shared memory of skinny_kernel<TSET, G>.
-int skinny_smem_bytes(int tset, int G);
 
 cudaError_t launch_stage(const __half *x, int N, int K, int nb, int64_t tok_stride, uint8_t *xq4,
                          uint8_t *xq6, uint8_t *xfp4, cudaStream_t stream);
 cudaError_t launch_stage_tc4(const __half *x, int N, int K, int nb, int64_t chunk_stride,
                              uint8_t *out, cudaStream_t stream);
 cudaError_t launch_dequant(const Mat &m, int K, float *out, cudaStream_t stream);
-// tc_kernel (Q4_K, N >= 33, on the tensor core; defined in qg_inst_tc.cu);
+// Dequantize through the product kernels' decoders (qg_dequant.cu).
+cudaError_t launch_dequant_fast(const Mat &m, int K, float *out, cudaStream_t stream);
+// qg_tc_kernel (Q4_K, N >= 33, on the tensor core; defined in qg_inst_tc.cu);
 // G = token groups of 8 per CTA (1..8).
 cudaError_t launch_tc(int G, const Params &p, dim3 grid, int smem, cudaStream_t s);
 cudaError_t launch_ref_gemv(const Mat &m, int K, const __half *x, int N, int out_f32,
@@ -23,8 +23,6 @@ cudaError_t launch_ref_gemv(const Mat &m, int K, const __half *x, int N, int out
 
 // Per type-set launchers (defined in qg_inst_*.cu).
 #define QG_DECLARE_TSET(NAME)                                                           \
-    cudaError_t launch_skinny_##NAME(int G, const Params &p, dim3 grid, cudaStream_t s); \
-    int smem_skinny_##NAME(int G);                                                      \
     cudaError_t launch_gemv_##NAME(const Params &p, dim3 grid, int smem, cudaStream_t s); \
     cudaError_t launch_sk_##NAME(int G, const Params &p, dim3 grid, int smem, cudaStream_t s);
 QG_DECLARE_TSET(q4k)

@@ -70,7 +70,7 @@ __device__ float ref_weight(const RefMat &m, int row, int k)
     return __fmaf_rn(__fmul_rn(d, (float)sc), (float)q, -__fmul_rn(dmin, (float)mn));
 }
 
-__global__ void dequant_kernel(RefMat m, float *out)
+__global__ void qg_ref_dequant_kernel(RefMat m, float *out)
 {
     const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
     if (i >= (int64_t)m.M * m.K) return;
@@ -78,7 +78,7 @@ __global__ void dequant_kernel(RefMat m, float *out)
     out[i] = ref_weight(m, row, k);
 }
 
-__global__ void ref_gemv_kernel(RefMat m, const __half *x, int N, const __half *res, void *y,
+__global__ void qg_ref_kernel(RefMat m, const __half *x, int N, const __half *res, void *y,
                                 int out_f32)
 {
     pdl_trigger();
@@ -122,7 +122,7 @@ cudaError_t launch_dequant(const Mat &mm, int K, float *out, cudaStream_t stream
     const RefMat r = make_ref(mm, K);
     const int64_t total = (int64_t)r.M * K;
     const unsigned blocks = (unsigned)((total + 255) / 256);
-    dequant_kernel<<<blocks, 256, 0, stream>>>(r, out);
+    qg_ref_dequant_kernel<<<blocks, 256, 0, stream>>>(r, out);
     return cudaGetLastError();
 }
 
@@ -139,7 +139,7 @@ cudaError_t launch_ref_gemv(const Mat &mm, int K, const __half *x, int N, int ou
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, ref_gemv_kernel, r, x, N, mm.res, mm.y, out_f32);
+    return cudaLaunchKernelEx(&cfg, qg_ref_kernel, r, x, N, mm.res, mm.y, out_f32);
 }
 
 }  // namespace qg

@@ -13,7 +13,7 @@
 namespace qg {
 
 __global__ void __launch_bounds__(128)
-    stage_x_kernel(const __half *__restrict__ x, int N, int K, int nb, int64_t tok_stride,
+    qg_stage_kernel(const __half *__restrict__ x, int N, int K, int nb, int64_t tok_stride,
                    uint8_t *xq4, uint8_t *xq6, uint8_t *xfp4)
 {
     pdl_trigger();
@@ -43,13 +43,13 @@ cudaError_t launch_stage(const __half *x, int N, int K, int nb, int64_t tok_stri
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, stage_x_kernel, x, N, K, nb, tok_stride, xq4, xq6, xfp4);
+    return cudaLaunchKernelEx(&cfg, qg_stage_kernel, x, N, K, nb, tok_stride, xq4, xq6, xfp4);
 }
 
-// The same for tc_kernel's layout: token n of a 64-token chunk goes to row
+// The same for qg_tc_kernel's layout: token n of a 64-token chunk goes to row
 // n % 8 of 8-token group (n % 64) / 8; per chunk [super-block][8 groups][kTcXBlk].
 __global__ void __launch_bounds__(128)
-    stage_tc4_kernel(const __half *__restrict__ x, int N, int K, int nb, int64_t chunk_stride,
+    qg_stage_tc_kernel(const __half *__restrict__ x, int N, int K, int nb, int64_t chunk_stride,
                      uint8_t *out)
 {
     pdl_trigger();
@@ -78,7 +78,7 @@ cudaError_t launch_stage_tc4(const __half *x, int N, int K, int nb, int64_t chun
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, stage_tc4_kernel, x, N, K, nb, chunk_stride, out);
+    return cudaLaunchKernelEx(&cfg, qg_stage_tc_kernel, x, N, K, nb, chunk_stride, out);
 }
 
 }  // namespace qg

@@ -1,4 +1,4 @@
-// tc_kernel: the Q4_K product for prefill chunks (N >= 33) on the
+// qg_tc_kernel: the Q4_K product for prefill chunks (N >= 33) on the
 // 5th-generation tensor core.
 //
 // For N <= 32 every row must keep its bits whatever N is (TandemLLM
@@ -17,7 +17,7 @@
 //     "docs/kernels.md": dequantize in registers), WG0 qs chunks 0-1, WG1
 //     chunks 2-3 and the 6-bit mins (m*2^-24), into tensor memory;
 //   * warp 9 issues 16 MMAs for D1 = A.x and one for D2 = mins.(sub-block sums
-//     of x, hi + lo), N = all the CTA's tokens;
+//     of x, S = 32 hi + lo), N = all the CTA's tokens;
 //   * the row threads read D1, D2 back (double-buffered) and fold
 //       acc = fma(d * 2^22, D1, acc); acc = fma(-dmin * 2^24, D2, acc),
 //     WG0 the first half of the token groups, WG1 the rest.
@@ -32,7 +32,7 @@ constexpr int kTcRows = 128;
 constexpr int kTcTok = 64;            // tokens per CTA (8 groups of 8)
 constexpr int kTcXBlk = 4096 + 256;   // staged x per (super-block, 8-token group)
 constexpr int kTcStagesMax = 4;
-constexpr int kTcMinN = 33;           // smallest N served by tc_kernel
+constexpr int kTcMinN = 33;           // smallest N served by qg_tc_kernel
 
 // ---------------------------------------------------------------------------
 // x of one (token, super-block) into the tensor-core layout of its 8-token
@@ -43,7 +43,8 @@ constexpr int kTcMinN = 33;           // smallest N served by tc_kernel
 //               values (a0, a2, a1, a3, b0, b2, b1, b3) -- the order in
 //               which a weight row's qs word w of chunk c is decoded;
 //   [4096, 4352) core 0: fp16 hi of the 8 sub-block sums, core 1: the lo parts.
-// Lane l holds x[256 sb + 8 l .. + 8].  Sub-block sums as in stage_sb.
+// Lane l holds x[256 sb + 8 l .. + 8].  Sub-block sums as in stage_sb
+// (hi = fp16(S * 2^-5), lo = fp16(S - 32 hi)).
 // ---------------------------------------------------------------------------
 __device__ __forceinline__ void stage_tc4(uint4 v, int lane, uint8_t *blk, int nrow)
 {
@@ -77,8 +78,8 @@ __device__ __forceinline__ void stage_tc4(uint4 v, int lane, uint8_t *blk, int n
     sm = __fadd_rn(sm, __shfl_xor_sync(0xffffffffu, sm, 2));
     if ((lane & 3) == 0) {
         const int sbk = lane >> 2;
-        const __half hi = __float2half_rn(sm);
-        const __half lo = __float2half_rn(__fsub_rn(sm, __half2float(hi)));
+        const __half hi = __float2half_rn(__fmul_rn(sm, 0.03125f));
+        const __half lo = __float2half_rn(__fsub_rn(sm, __fmul_rn(__half2float(hi), 32.0f)));
         *reinterpret_cast<__half *>(blk + 4096 + 16 * nrow + 2 * sbk) = hi;
         *reinterpret_cast<__half *>(blk + 4096 + 128 + 16 * nrow + 2 * sbk) = lo;
     }
@@ -90,8 +91,9 @@ __device__ __forceinline__ void stage_tc4(uint4 v, int lane, uint8_t *blk, int n
 // 64 H .. 64 H + 63 (column (8 c + w) * 4 + q for chunk c, qs word w: q = 0
 // the low nibbles of bytes 0, 2; 1 of bytes 1, 3; 2, 3 the high nibbles --
 // the k order stage_tc4 gives x).  Half 0 returns d * 2^22 and -dmin * 2^24;
-// half 1 also writes the mins (m_2i, m_2i+1) as subnormals, twice, to
-// columns 128..135 (read by the last MMA of the super-block).
+// half 1 also writes the mins (m_2i, m_2i+1) to columns 128..135 (read by
+// the last MMA of the super-block): times 2^-19 against the hi sums (columns
+// 128..131), times 2^-24 (subnormals) against the lo sums (132..135).
 // ---------------------------------------------------------------------------
 template <int H>
 __device__ __forceinline__ void tc_decode_q4k(uint32_t ra, uint32_t ta, float &dd, float &dm)
@@ -112,11 +114,8 @@ __device__ __forceinline__ void tc_decode_q4k(uint32_t ra, uint32_t ta, float &d
         uint32_t a[32];
 #pragma unroll
         for (int w = 0; w < 8; ++w) {
-            const uint32_t v = q[w], v8 = q[w] >> 8;
-            a[4 * w + 0] = hmul2(v & 0x000f000fu, slo);
-            a[4 * w + 1] = hmul2(v8 & 0x000f000fu, slo);
-            a[4 * w + 2] = hmul2(v & 0x00f000f0u, shi);
-            a[4 * w + 3] = hmul2(v8 & 0x00f000f0u, shi);
+            kq_decode<T_Q4K>(q[w], 0u, 0, 0, slo, shi, a[4 * w + 0], a[4 * w + 1]);
+            kq_decode<T_Q4K>(q[w], 0u, 0, 1, slo, shi, a[4 * w + 2], a[4 * w + 3]);
         }
         tmem_st32(ta + 32 * c, a);
     }
@@ -135,6 +134,8 @@ __device__ __forceinline__ void tc_decode_q4k(uint32_t ra, uint32_t ta, float &d
         mn[5] = mn[1];
         mn[6] = mn[2];
         mn[7] = mn[3];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) mn[i] = hmul2(mn[i], 0x50005000u);  // * 32.0
         tmem_st8(ta + 128, mn);
     }
 }
@@ -154,7 +155,7 @@ __host__ __device__ inline int tc_smem_bytes(int G, int stages)
     const int red = kTcRows * 8 * G * 4;
     return 256 + (body > red ? body : red);
 }
-// Staged x of tc_kernel: [64-token chunk][super-block][8 groups][kTcXBlk].
+// Staged x of qg_tc_kernel: [64-token chunk][super-block][8 groups][kTcXBlk].
 __host__ __device__ inline int64_t tc_chunk_bytes(int nb) { return (int64_t)nb * 8 * kTcXBlk; }
 
 // Epilogue of one output element: residual (fp32 add before the single
@@ -171,7 +172,7 @@ __device__ __forceinline__ void tc_store(const Params &p, const Mat &m, int row,
 }
 
 template <int G>
-__global__ void __launch_bounds__(kTcThreads) tc_kernel(const __grid_constant__ Params p)
+__global__ void __launch_bounds__(kTcThreads) qg_tc_kernel(const __grid_constant__ Params p)
 {
     extern __shared__ __align__(1024) uint8_t smem[];
     pdl_trigger();

@@ -82,9 +82,11 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.qgemv_device_status.argtypes = [vp, ctypes.POINTER(ctypes.c_uint32), c_int]
     lib.qgemv_describe.argtypes = []
     lib.qgemv_describe.restype = ctypes.c_char_p
+    lib.qgemv_run_noalloc.argtypes = [c_int, i64, i64, vp, vp, ctypes.c_float, vp, i64, vp, c_int,
+                                      vp]
     for name in ("qgemv_create", "qgemv_run", "qgemv_run_add", "qgemv_pair_run",
                  "qgemv_triple_run", "qgemv_run_host", "qgemv_dequantize", "qgemv_plan_info",
-                 "qgemv_device_status"):
+                 "qgemv_device_status", "qgemv_run_noalloc"):
         getattr(lib, name).restype = c_int
     _lib = lib
     return lib
@@ -156,6 +158,8 @@ def qgemv_plan_info(h, N):
 
 
 def qgemv_device_status(h, clear: bool = False) -> int:
+    """The handle's device error word (h = None: qgemv_run_noalloc's, on the
+    current device)."""
     w = ctypes.c_uint32()
     _check(load().qgemv_device_status(h, ctypes.byref(w), 1 if clear else 0),
            "qgemv_device_status")
@@ -165,14 +169,9 @@ def qgemv_device_status(h, clear: bool = False) -> int:
 def qgemv_run_noalloc(qtype, M, K, w_ptr, scales_ptr, global_scale, x_ptr, N, y_ptr, ydt,
                       stream):
     """Allocation-free product (no handle; scratch in a fixed device array)."""
-    lib = load()
-    f = lib.qgemv_run_noalloc
-    f.argtypes = [ctypes.c_int, ctypes.c_int64, ctypes.c_int64, ctypes.c_void_p, ctypes.c_void_p,
-                  ctypes.c_float, ctypes.c_void_p, ctypes.c_int64, ctypes.c_void_p, ctypes.c_int,
-                  ctypes.c_void_p]
-    f.restype = ctypes.c_int
-    _check(f(qtype, M, K, w_ptr or None, scales_ptr or None, global_scale, x_ptr, N, y_ptr, ydt,
-             stream), "qgemv_run_noalloc")
+    _check(load().qgemv_run_noalloc(qtype, M, K, w_ptr or None, scales_ptr or None, global_scale,
+                                    x_ptr or None, N, y_ptr or None, ydt, stream),
+           "qgemv_run_noalloc")
 
 
 # ----------------------------------------------------- torch convenience

@@ -34,6 +34,23 @@ def test_exports_every_declared_symbol(lib):
         assert hasattr(lib, n), n
 
 
+CITES = re.compile(r'"docs/kernels\.md"|"docs/performance\.md"|"Kernels"|no counterpart')
+
+
+def test_every_declaration_cites_its_passage():
+    """Each exported call's comment in include/qgemv.h names the page passage
+    that defines it (or says that the pages have no counterpart)."""
+    with open(os.path.join(ROOT, "include", "qgemv.h")) as f:
+        src = f.read()
+    found = 0
+    for m in re.finditer(r"/\*((?:(?!\*/).)*)\*/\s*\n(?:[^;/]*?)\b(qgemv_[a-z_]+)\s*\(", src,
+                         re.S):
+        comment, name = m.group(1), m.group(2)
+        assert CITES.search(comment), f"{name}: no citation in its comment"
+        found += 1
+    assert found == len(_declared())
+
+
 def test_row_bytes_and_describe(lib):
     from skinny_gemm_q4_gb300 import qgemv as q
     assert q.qgemv_row_bytes(q.Q4_K, 2560) == 1440
@@ -104,3 +121,46 @@ def test_generators_are_seeded_and_shaped():
     assert scales.min() >= 0x08 and scales.max() <= 0x58
     x = synth.activations(9, 64, seed=0, duplicate_rows=True)
     assert np.array_equal(x[2], x[0]) and np.array_equal(x[5], x[3]) and np.array_equal(x[8], x[6])
+
+
+_NOALLOC_PROBE = r"""
+import ctypes, sys
+sys.path.insert(0, sys.argv[1])
+from skinny_gemm_q4_gb300 import qgemv as q
+lib = q.load()
+f = lib.qgemv_run_noalloc
+def call(t, M, K, w, sc, g, x, N, y, ydt=0):
+    st = f(t, M, K, w, sc, g, x, N, y, ydt, None)
+    return st, q.qgemv_last_error()
+out = []
+out.append(call(q.Q4_K, 16, 1 << 20, 4096, None, 1.0, 4096, 1, 4096))          # K > 931,840
+out.append(call(q.NVFP4_W4A16, 16, 2560, 4096, 8192, float("nan"), 4096, 1, 4096))
+out.append(call(q.Q4_K, 64 * 65536, 2560, 4096, None, 1.0, 4096, 1, 4096))     # grid rows
+out.append(call(q.Q4_K, 16, 2560, 4100, None, 1.0, 4096, 1, 4096))            # w alignment
+out.append(call(q.Q4_K, 16, 2560, 4096, None, 1.0, 4100, 1, 4096))            # x alignment
+out.append(call(q.Q4_K, 16, 2560, 4096, None, 1.0, 4096, 0, 4096))            # N
+out.append(call(q.Q4_K, 16, 2560, None, None, 1.0, 4096, 1, 4096))            # null w
+out.append(call(77, 16, 2560, 4096, None, 1.0, 4096, 1, 4096))                 # type
+out.append(call(q.Q4_K, 16, 2500, 4096, None, 1.0, 4096, 1, 4096))            # K % 256
+for st, msg in out:
+    print(st, "|", msg)
+"""
+
+
+def test_noalloc_validates_before_touching_the_device(lib, tmp_path):
+    """Every argument check of qgemv_run_noalloc runs before any CUDA call:
+    with no visible device (and fake addresses) each bad call returns its
+    validation status, never a CUDA error and never a launch."""
+    import subprocess
+    import sys
+    env = dict(os.environ, CUDA_VISIBLE_DEVICES="")
+    r = subprocess.run([sys.executable, "-c", _NOALLOC_PROBE, ROOT], env=env,
+                       capture_output=True, text=True, timeout=120)
+    assert r.returncode == 0, r.stderr
+    rows = [line.split(" | ", 1) for line in r.stdout.strip().splitlines()]
+    st = [int(a) for a, _ in rows]
+    msg = [b for _, b in rows]
+    assert st == [-2, -1, -2, -3, -3, -1, -1, -2, -2], rows
+    assert "2097152-byte" in msg[0] or "scratch" in msg[0]
+    assert "finite" in msg[1]
+    assert "rows" in msg[2]

@@ -25,14 +25,77 @@ def _built():
 
 
 @pytest.mark.parametrize("qtype", TYPES)
-@pytest.mark.parametrize("M,K", [(37, 768), (130, 2560)])
-def test_dequantize_bit_exact(qtype, M, K):
-    h, w, sc, g = make_matrix(qtype, M, K, seed=3)
+@pytest.mark.parametrize("M,K", [(37, 768), (130, 2560), (1030, 9728)])
+@pytest.mark.parametrize("flags", [0, qg.FLAG_FORCE_REFERENCE], ids=["product_decoders", "reference"])
+def test_dequantize_bit_exact(qtype, M, K, flags):
+    """qgemv_dequantize runs the product kernels' own decoders (and, with
+    FORCE_REFERENCE, the simple per-element reference decoder): every weight
+    equals the oracle's bit for bit (after -0 -> +0)."""
+    h, w, sc, g = make_matrix(qtype, M, K, seed=3, flags=flags)
     wd = h.dequantize()
     torch().cuda.synchronize()
     ref = oracle.dequantize(ORTYPE[qtype], w, M, K, scales=sc, global_scale=g)
     got = canon(wd.cpu().numpy())
     assert np.array_equal(got.view(np.uint32), canon(ref).view(np.uint32))
+
+
+# Shapes and one-hot chunk sizes that reach every mma.sync product kernel:
+# chunk 1 -> the N = 1 variant of the N <= 8 kernel; chunk 8 -> the N <= 8
+# kernel (Q6_K, NVFP4, and Q4_K/Q5_K above 4096 rows) or qg_sk_kernel with x
+# staged inside (Q4_K/Q5_K up to 4096 rows); chunks 16 and 32 -> qg_sk_kernel
+# after the staging launch (2 and 4 column groups).
+ONE_HOT = [(qg.Q4_K, 150, 1024), (qg.Q4_K, 4100, 512), (qg.Q5_K, 96, 768),
+           (qg.Q5_K, 4100, 512), (qg.Q6_K, 150, 1024), (qg.NVFP4_W4A16, 150, 1024)]
+
+
+@pytest.mark.parametrize("qtype,M,K", ONE_HOT)
+@pytest.mark.parametrize("chunk", [1, 8, 16, 32])
+def test_mma_sync_one_hot_is_the_exact_weight(qtype, M, K, chunk):
+    """x = e_k for every k, in calls of `chunk` rows: each mma.sync kernel
+    returns w[m][k] bit for bit (one exact product, the fold's single
+    rounding), so its decoders equal the oracle's dequantization."""
+    t = torch()
+    h, w, sc, g = make_matrix(qtype, M, K, seed=4, flags=qg.FLAG_MMA_SYNC_PREFILL)
+    x = to_dev(np.eye(K, dtype=np.float16))
+    y = t.cat([h.run(x[i:i + chunk], out_f32=True) for i in range(0, K, chunk)])
+    t.cuda.synchronize()
+    ref = oracle.dequantize(ORTYPE[qtype], w, M, K, scales=sc, global_scale=g)
+    assert np.array_equal(canon(y.cpu().numpy()).view(np.uint32), canon(ref.T).view(np.uint32))
+    assert h.device_status() == 0
+
+
+@pytest.mark.parametrize("qtype", TYPES)
+@pytest.mark.parametrize("N", [1, 5, 16, 40])
+def test_large_magnitude_x(qtype, N):
+    """x far outside N(0, 1): rows scaled by 2^8, 2^10, 2^12 and sub-blocks of
+    32 equal values near the fp16 limit (|sum| up to 32 * 65504, past the fp16
+    range, which the Q4_K/Q5_K min term's sub-block sums must still carry).
+    fp32 output within the tolerance; power-of-two scaling stays exact."""
+    M = 300
+    K = 5120 if qtype == qg.NVFP4_W4A16 else 2560
+    h, w, sc, g = make_matrix(qtype, M, K, seed=11)
+    base = synth.activations(N, K, seed=11).astype(np.float32)
+    x = base * (2.0 ** (8 + 2 * (np.arange(N) % 3)))[:, None]
+    x[0, 96:128] = 60000.0
+    x[-1, 0:32] = -65504.0
+    x[-1, 2048:2080] = 65504.0
+    x = x.astype(np.float16)
+    assert np.isfinite(x).all()
+    yref, mag = oracle.qgemv(ORTYPE[qtype], w, M, K, x, scales=sc, global_scale=g)
+    y = h.run(to_dev(x), out_f32=True).cpu().numpy()
+    check_close(y, yref, mag, what=f"large x {qtype} N={N}")
+    xs = base.astype(np.float16)
+    y1 = h.run(to_dev(xs), out_f32=True).cpu().numpy()
+    y256 = h.run(to_dev((xs.astype(np.float32) * 256).astype(np.float16)), out_f32=True).cpu().numpy()
+    # Exact scaling needs every nonzero sub-block sum of x at |S| >= 2^-9 (the
+    # Q4_K/Q5_K min term splits S = 32 hi + lo with hi an fp16 normal there).
+    S = np.abs(xs.astype(np.float64).reshape(N, K // 32, 32).sum(-1))
+    ok = ((S == 0) | (S >= 2.0 ** -9)).all(axis=1)
+    if qtype in (qg.Q6_K, qg.NVFP4_W4A16):
+        ok[:] = True
+    assert ok.any()
+    assert np.array_equal(y256[ok], 256 * y1[ok])
+    assert h.device_status() == 0
 
 
 @pytest.mark.parametrize("qtype", TYPES)
@@ -78,7 +141,10 @@ def test_product_matches_oracle(qtype, M, K, N):
 @pytest.mark.parametrize("qtype,M,K", [(qg.Q4_K, 9728, 2560), (qg.Q4_K, 4096, 2560),
                                        (qg.Q4_K, 2560, 4096), (qg.Q4_K, 1024, 2560),
                                        (qg.Q5_K, 2560, 9728),
-                                       (qg.Q6_K, 1024, 2560), (qg.NVFP4_W4A16, 7168, 5120)])
+                                       (qg.Q6_K, 1024, 2560), (qg.Q6_K, 2560, 9728),
+                                       (qg.NVFP4_W4A16, 7168, 5120),
+                                       (qg.NVFP4_W4A16, 27648, 5120),
+                                       (qg.NVFP4_W4A16, 5120, 27648)])
 def test_row_invariance_twins(qtype, M, K):
     """TandemLLM verify-twin rule: an N-row call equals N one-row calls bit
     for bit, N = 2..32, with rows that share inputs."""
@@ -263,7 +329,7 @@ def test_argument_errors_are_statuses():
     kw, rows, launches = h.plan_info(16)
     assert kw == 8 and rows == 128 and launches == 2     # staging + product
     kw, rows, launches = h.plan_info(4)
-    assert kw == 8 and rows == 128 and launches == 1     # sk_kernel stages x itself
+    assert kw == 8 and rows == 128 and launches == 1     # qg_sk_kernel stages x itself
     assert h.device_status() == 0
 
 

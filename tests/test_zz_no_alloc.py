@@ -1,13 +1,15 @@
-"""The allocation-free entry point (qgemv_run_noalloc) against qgemv_run.
+"""The allocation-free entry point (qgemv_run_noalloc) against the oracle and
+against qgemv_run.
 
-For callers that cannot allocate device memory while they run, the library
-offers a handle-free product whose scratch is a fixed array inside the
-library.  This file is collected last so that a run stopping at the first
-failure has run every other test before it.  Two calls in a row share the
-array; each must still match the handle-based qgemv_run within the parity
-tolerance (and in fact bit for bit: same arithmetic and plan)."""
-import ctypes
-
+Some callers cannot allocate device memory while they run (a serving runtime
+that owns all device memory in its own pool, a library that must keep its
+footprint fixed), so the library offers a handle-free product whose scratch
+is a fixed array inside the library.  This file is collected last so that a
+run stopping at the first failure has run every other test before it.  Two
+calls in a row share the array; each must match the CPU oracle within the
+parity tolerance and qgemv_run bit for bit (same plan and kernels), and its
+error word must stay clear.  (The argument checks, which run before the
+device is touched, are tested on the host in test_abi_host.py.)"""
 import numpy as np
 import pytest
 
@@ -39,8 +41,9 @@ def _noalloc(h, x, N, y, out_f32):
 
 @pytest.mark.parametrize("qtype,M,K,N", [(qg.Q4_K, 4096, 2560, 20), (qg.Q6_K, 1024, 9728, 40),
                                          (qg.NVFP4_W4A16, 2048, 5120, 9),
-                                         (qg.Q5_K, 640, 2560, 3)])
-def test_noalloc_matches_run_on_two_calls_in_a_row(qtype, M, K, N):
+                                         (qg.Q5_K, 640, 2560, 3), (qg.Q4_K, 9728, 2560, 1),
+                                         (qg.Q6_K, 2560, 9728, 1)])
+def test_noalloc_matches_oracle_and_run_on_two_calls_in_a_row(qtype, M, K, N):
     t = torch()
     h, w, sc, g = make_matrix(qtype, M, K, seed=21)
     h._gscale = g
@@ -52,21 +55,36 @@ def test_noalloc_matches_run_on_two_calls_in_a_row(qtype, M, K, N):
         _noalloc(h, to_dev(x), N, y, True)
         outs.append(y)
     t.cuda.synchronize()
+    assert qg.qgemv_device_status(None) == 0
     for x, y in zip(xs, outs):
+        yref, mag = oracle.qgemv(ORTYPE[qtype], w, M, K, x, scales=sc, global_scale=g, rows=rows)
+        check_close(y.cpu().numpy()[:, rows], yref, mag, what="noalloc vs oracle")
         ref = h.run(to_dev(x), out_f32=True)
         t.cuda.synchronize()
-        _, mag = oracle.qgemv(ORTYPE[qtype], w, M, K, x, scales=sc, global_scale=g, rows=rows)
         check_close(y.cpu().numpy()[:, rows], ref.cpu().numpy()[:, rows].astype(np.float64), mag,
                     what="noalloc vs qgemv_run")
         assert t.equal(y, ref)
 
 
-def test_noalloc_rejects_oversized_k_without_touching_the_gpu():
-    lib = qg.load()
-    f = lib.qgemv_run_noalloc
-    f.argtypes = [ctypes.c_int, ctypes.c_int64, ctypes.c_int64, ctypes.c_void_p, ctypes.c_void_p,
-                  ctypes.c_float, ctypes.c_void_p, ctypes.c_int64, ctypes.c_void_p, ctypes.c_int,
-                  ctypes.c_void_p]
-    f.restype = ctypes.c_int
-    st = f(qg.Q4_K, 16, 1 << 20, 4096, None, 1.0, 4096, 1, 4096, qg.OUT_F16, None)
-    assert st == -2 and "2 MiB" in qg.qgemv_last_error()
+def test_noalloc_q4k_prefill_chunk_keeps_the_mma_sync_bits():
+    """Q4_K at N = 40: qgemv_run_noalloc stays on the mma.sync kernels, so it
+    equals a handle created with QG_FLAG_MMA_SYNC_PREFILL bit for bit and the
+    default handle (tcgen05 engine) within the tolerance."""
+    t = torch()
+    M, K, N = 3000, 2560, 40
+    h, w, sc, g = make_matrix(qg.Q4_K, M, K, seed=23)
+    h._gscale = g
+    hm = qg.QGemv(qg.Q4_K, M, K, h._w, flags=qg.FLAG_MMA_SYNC_PREFILL)
+    x = synth.activations(N, K, seed=24, duplicate_rows=True)
+    xd = to_dev(x)
+    y = t.empty((N, M), dtype=t.float32, device="cuda")
+    _noalloc(h, xd, N, y, True)
+    ym = hm.run(xd, out_f32=True)
+    yd = h.run(xd, out_f32=True)
+    t.cuda.synchronize()
+    assert t.equal(y, ym)
+    rows = np.arange(0, M, 7)
+    yref, mag = oracle.qgemv(oracle.Q4_K, w, M, K, x, rows=rows)
+    check_close(y.cpu().numpy()[:, rows], yref, mag, what="noalloc N=40 vs oracle")
+    check_close(yd.cpu().numpy()[:, rows], yref, mag, what="default handle N=40 vs oracle")
+    assert qg.qgemv_device_status(None) == 0
