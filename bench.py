@@ -19,6 +19,7 @@ from __future__ import annotations
 import argparse
 import hashlib
 import json
+import math
 import os
 import subprocess
 import sys
@@ -109,6 +110,15 @@ class ClockSampler:
                 "power_w_max": max(float(r[3]) for r in rows if r[3].replace('.', '', 1).isdigit())}
 
 
+def _tensor_peak():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return float(d["bf16_tflops"]), "measured (bf16 dense burst; fp16 runs at the same rate)"
+    return 1900.0, "fallback"
+
+
 def _kernel_source_sha():
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "skinny_gemm_q4_gb300", "csrc")
@@ -119,9 +129,10 @@ def _kernel_source_sha():
     return h.hexdigest()[:16]
 
 
-def _traffic_record():
-    """DRAM bytes per launch of the dominant kernel from the committed ncu
-    summary, or None if the kernel sources changed since it was taken."""
+def _traffic_record(call):
+    """DRAM bytes per launch of one layer call's kernel from the committed ncu
+    summary (profiles/traffic.json), or None if the kernel sources changed
+    since it was taken or the call was not captured."""
     p = os.path.join(ROOT, "profiles", "traffic.json")
     if not os.path.exists(p):
         return None
@@ -129,7 +140,8 @@ def _traffic_record():
         rec = json.load(f)
     if rec.get("source_sha") != _kernel_source_sha():
         return None
-    return rec.get("dram_bytes_per_launch")
+    c = rec.get("calls", {}).get(call)
+    return None if c is None else c.get("dram_bytes_per_launch")
 
 
 def aggregate_ranks(ms_local, world, wbytes, steps, dist=None, device=None):
@@ -149,11 +161,50 @@ def layer_weight_bytes():
     return sum(M * synth.row_bytes(qt, K) for _, qt, M, K in synth.LAYER)
 
 
+# ---------------------------------------------------------------- CPU oracle
+
+def host_cores() -> int:
+    """Cores this process may run on (the cgroup / affinity set, else all)."""
+    try:
+        return len(os.sched_getaffinity(0))
+    except Exception:
+        return os.cpu_count() or 1
+
+
+def oracle_rows_timed(mats, cores):
+    """Run the oracle over every (matrix, rows) item, rows split into `cores`
+    contiguous parts run on that many threads (the C oracle releases the GIL;
+    rows are independent, so the results are those of one thread).  Returns
+    the wall time in seconds."""
+    import numpy as np
+
+    import oracle
+    from concurrent.futures import ThreadPoolExecutor
+    jobs = []
+    for qt, w, M, K, rows, x, sc in mats:
+        for part in np.array_split(rows, cores):
+            if part.size:
+                jobs.append((qt, w, M, K, part, x, sc))
+
+    def one(j):
+        qt, w, M, K, part, x, sc = j
+        oracle.qgemv(qt, w, M, K, x, scales=sc, rows=part)
+
+    t0 = time.perf_counter()
+    if cores == 1:
+        for j in jobs:
+            one(j)
+    else:
+        with ThreadPoolExecutor(max_workers=cores) as ex:
+            list(ex.map(one, jobs))
+    return time.perf_counter() - t0
+
+
 # ---------------------------------------------------------------- reference
 
 def run_reference(args):
     """The CPU oracle on a bounded sample of the same workload, timed on this
-    host's cores (single-threaded: the oracle as it stands)."""
+    host's cores (rows split over every core; the oracle itself as it stands)."""
     import numpy as np
 
     import oracle
@@ -162,49 +213,45 @@ def run_reference(args):
     if rank != 0:
         return
     oracle.build()
+    cores = host_cores()
     # Bounded sample: every frac-th row of each matrix of one layer, frac chosen
     # so that warmup + steps take about a minute on this host in total.
     full = []
     for i, (role, qt, M, K) in enumerate(synth.LAYER):
         w, sc, g = synth.weights(qt, M, K, seed=0, stream=100 + i)
         x = synth.activations(1, K, seed=0, stream=200 + i)
-        full.append((qt, w, M, K, x))
+        full.append((qt, w, M, K, x, sc))
 
     def make(frac):
-        mats = [(qt, w, M, K, np.arange(0, M, frac), x) for qt, w, M, K, x in full]
-        nbytes = sum(len(r) * synth.row_bytes(qt, K) for qt, w, M, K, r, x in mats)
+        mats = [(qt, w, M, K, np.arange(0, M, frac), x, sc) for qt, w, M, K, x, sc in full]
+        nbytes = sum(len(m[4]) * synth.row_bytes(m[0], m[3]) for m in mats)
         return mats, nbytes
 
-    def step(mats):
-        for qt, w, M, K, rows, x in mats:
-            oracle.qgemv(qt, w, M, K, x, rows=rows)
-
-    probe, probe_bytes = make(256)
-    t0 = time.perf_counter()
-    step(probe)
-    sec_per_byte = (time.perf_counter() - t0) / probe_bytes
+    probe, probe_bytes = make(64)
+    sec_per_byte = oracle_rows_timed(probe, cores) / probe_bytes
     budget = 60.0 / (args.steps + args.warmup)
-    frac = 16
+    frac = 1
     while frac < 4096 and make(frac)[1] * sec_per_byte > budget:
         frac *= 2
     mats, sample_bytes = make(frac)
     for _ in range(args.warmup):
-        step(mats)
-    t0 = time.perf_counter()
+        oracle_rows_timed(mats, cores)
+    dt = 0.0
     for _ in range(args.steps):
-        step(mats)
-    dt = (time.perf_counter() - t0) / args.steps
+        dt += oracle_rows_timed(mats, cores)
+    dt /= args.steps
     gbs = sample_bytes / dt / 1e9
+    what = "one whole decode layer" if frac == 1 else f"every {frac}th row of one decode layer"
     line = {
         "impl": "reference", "metric": METRIC, "value": round(gbs, 4), "unit": "GB/s",
         "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": round(dt * 1e3, 3), "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f64", "data": "synthetic",
         "config": {"workload": WORKLOAD, "N": 1, "layers": 1,
-                   "sample": f"every {frac}th row of each of the 7 matrices"},
-        "cpu_baseline": {"value": round(gbs, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
-                         "sample": f"1/{frac} of the rows of one decode layer "
-                                   f"({sample_bytes} weight bytes) per step"},
+                   "sample": f"{what} (7 matrices), N=1"},
+        "cpu_baseline": {"value": round(gbs, 4), "unit": "GB/s", "cores": cores, "kind": "oracle",
+                         "sample": f"{what}: {sample_bytes} weight bytes per step, rows split "
+                                   f"over {cores} threads"},
         "e2e": {"value": round(gbs, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
     }
@@ -212,6 +259,31 @@ def run_reference(args):
 
 
 # ---------------------------------------------------------------- our path
+
+def _graph_us(torch, side, ncalls, call, e0, e1):
+    """Capture ncalls calls call(i, stream) as one CUDA graph on `side`, replay
+    it once untimed, then time one replay with CUDA events: us per call."""
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(side):
+        with torch.cuda.graph(g, stream=side):
+            for i in range(ncalls):
+                call(i, torch.cuda.current_stream().cuda_stream)
+    g.replay()
+    torch.cuda.synchronize()
+    e0.record()
+    g.replay()
+    e1.record()
+    torch.cuda.synchronize()
+    us = e0.elapsed_time(e1) * 1e3 / ncalls
+    del g
+    return us
+
+
+def _bw(nbytes, us, peak):
+    gbs = nbytes / (us * 1e-6) / 1e9
+    return {"us_per_call": round(us, 3), "GBps": round(gbs, 1),
+            "frac_of_measured": round(gbs / peak, 4), "frac_of_8TBps": round(gbs / 8000.0, 4)}
+
 
 def run_ours(args):
     import numpy as np
@@ -232,15 +304,19 @@ def run_ours(args):
     b.build()
     qg.load()
     dev = torch.device("cuda", local)
+    peak, peak_kind = _peaks()
+    tpeak, tpeak_kind = _tensor_peak()
 
-    # 36 synthetic layers generated on the device.
+    # 36 synthetic layers generated on the device (128-token staging so the
+    # same handles serve the prefill chunks).
     layers = []
     for L in range(N_LAYERS):
         hs = {}
         for i, (role, qt, M, K) in enumerate(synth.LAYER):
             w, sc, g = synth.device_weights(qt, M, K, seed=rank, stream=1000 * L + i, device=dev)
-            hs[role] = qg.QGemv(qt, M, K, w, sc, g, max_tokens=32)
+            hs[role] = qg.QGemv(qt, M, K, w, sc, g, max_tokens=128)
         layers.append(hs)
+    all_handles = [h for hs in layers for h in hs.values()]
     x_qkv = synth.device_activations(1, 2560, 0, 1, dev)
     x_o = synth.device_activations(1, 4096, 0, 2, dev)
     res = synth.device_activations(1, 2560, 0, 3, dev)
@@ -260,19 +336,29 @@ def run_ours(args):
     x_g = synth.device_activations(rows, 2560, 0, 7, dev)
     y_g = torch.empty((rows, 9728), dtype=f16, device=dev)
 
+    def call_qkv(h, s):
+        qg.qgemv_triple_run(h["wq"].h, h["wk"].h, h["wv"].h, x_qkv.data_ptr(), 1,
+                            yq.data_ptr(), yk.data_ptr(), yv.data_ptr(), qg.OUT_F16, s)
+
+    def call_wo(h, s):
+        qg.qgemv_run_add(h["wo"].h, x_o.data_ptr(), 1, res.data_ptr(), yo.data_ptr(), s)
+
+    def call_pair(h, s):
+        qg.qgemv_pair_run(h["gate"].h, h["up"].h, x_ffn.data_ptr(), 1, yg.data_ptr(),
+                          yu.data_ptr(), qg.OUT_F16, s)
+
+    def call_down(h, s):
+        qg.qgemv_run(h["down"].h, x_dn.data_ptr(), 1, yd.data_ptr(), qg.OUT_F16, s)
+
+    CALLS = [("qkv", call_qkv, ["wq", "wk", "wv"]), ("wo", call_wo, ["wo"]),
+             ("pair", call_pair, ["gate", "up"]), ("down", call_down, ["down"])]
+
     def step(L):
         h = layers[L]
         s = torch.cuda.current_stream().cuda_stream
-        if part in ("layer", "qkv"):
-            qg.qgemv_triple_run(h["wq"].h, h["wk"].h, h["wv"].h, x_qkv.data_ptr(), 1,
-                                yq.data_ptr(), yk.data_ptr(), yv.data_ptr(), qg.OUT_F16, s)
-        if part in ("layer", "wo"):
-            qg.qgemv_run_add(h["wo"].h, x_o.data_ptr(), 1, res.data_ptr(), yo.data_ptr(), s)
-        if part in ("layer", "pair"):
-            qg.qgemv_pair_run(h["gate"].h, h["up"].h, x_ffn.data_ptr(), 1, yg.data_ptr(),
-                              yu.data_ptr(), qg.OUT_F16, s)
-        if part in ("layer", "down"):
-            qg.qgemv_run(h["down"].h, x_dn.data_ptr(), 1, yd.data_ptr(), qg.OUT_F16, s)
+        for name, fn, _ in CALLS:
+            if part in ("layer", name):
+                fn(h, s)
         if part == "gate":
             qg.qgemv_run(h["gate"].h, x_g.data_ptr(), rows, y_g.data_ptr(), qg.OUT_F16, s)
 
@@ -317,56 +403,64 @@ def run_ours(args):
     ms, value = aggregate_ranks(start.elapsed_time(end), world, wbytes, args.steps, dist, dev)
     ms_step = ms / args.steps
 
-    # Dominant kernel: the gate/up pair product (44% of the layer's bytes),
-    # timed alone back to back over the 36 layers (graph), CUDA events on the
-    # launching stream.
-    pair_bytes = 2 * 9728 * synth.row_bytes(synth.Q4_K, 2560)
-    reps = N_LAYERS * 4
-    pg = torch.cuda.CUDAGraph()
-    with torch.cuda.stream(side):
-        with torch.cuda.graph(pg, stream=side):
-            for i in range(reps):
-                h = layers[i % N_LAYERS]
-                qg.qgemv_pair_run(h["gate"].h, h["up"].h, x_ffn.data_ptr(), 1, yg.data_ptr(),
-                                  yu.data_ptr(), qg.OUT_F16, torch.cuda.current_stream().cuda_stream)
-    pg.replay()
-    torch.cuda.synchronize()
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record()
-    pg.replay()
-    e1.record()
-    torch.cuda.synchronize()
-    pair_us = e0.elapsed_time(e1) * 1e3 / reps
-    peak, peak_kind = _peaks()
-    achieved = pair_bytes / (pair_us * 1e-6) / 1e9
+    # Sustained: the same K-step graph replayed back to back for at least
+    # ~0.3 s (so the clock record has many samples); reported beside `value`.
+    reps = max(1, int(math.ceil(300.0 / max(ms_step * args.steps, 1e-3))))
+    reps = min(reps, 20000)
+    with ClockSampler(local) as clk2:
+        torch.cuda.synchronize()
+        clk2.mark_start()
+        start.record()
+        for _ in range(reps):
+            graph.replay()
+        end.record()
+        torch.cuda.synchronize()
+        clk2.mark_end()
+    sus_ms = start.elapsed_time(end) / (reps * args.steps)
+    sustained = {"ms_per_step": round(sus_ms, 5), "steps": reps * args.steps,
+                 "GBps": round(wbytes / (sus_ms * 1e-3) / 1e9, 1), "clocks": clk2.summary()}
+    del graph
 
-    # Skinny sweep on the gate matrices (Q4_K 9728 x 2560): one call per
-    # layer, N rows, graph replay over the 36 layers (cold), CUDA events.
-    sweep = None
-    if part == "layer" and not args.no_sweep:
-        sweep = {"matrix": "Q4_K 9728x2560 (gate of each layer)", "unit": "GB/s", "points": []}
-        xs = synth.device_activations(32, 2560, 0, 6, dev)
-        ys = torch.empty((32, 9728), dtype=f16, device=dev)
-        gbytes = 9728 * synth.row_bytes(synth.Q4_K, 2560)
-        for n in (1, 2, 4, 8, 16, 32):
-            sg = torch.cuda.CUDAGraph()
-            with torch.cuda.stream(side):
-                with torch.cuda.graph(sg, stream=side):
-                    for i in range(reps):
-                        qg.qgemv_run(layers[i % N_LAYERS]["gate"].h, xs.data_ptr(), n,
-                                     ys.data_ptr(), qg.OUT_F16,
-                                     torch.cuda.current_stream().cuda_stream)
-            sg.replay()
-            torch.cuda.synchronize()
-            e0.record()
-            sg.replay()
-            e1.record()
-            torch.cuda.synchronize()
-            us = e0.elapsed_time(e1) * 1e3 / reps
-            sweep["points"].append({"N": n, "us_per_call": round(us, 3),
-                                    "GBps": round(gbytes / (us * 1e-6) / 1e9, 1),
-                                    "frac_of_measured": round(gbytes / (us * 1e-6) / 1e9 / peak, 4)})
-            del sg
+    # Every kernel's bounded waits finished in time (a timed-out pipeline
+    # would return early with wrong results).
+    bad = [h for h in all_handles if h.device_status() != 0]
+    if bad:
+        print(json.dumps({"error": f"{len(bad)} handles report a device timeout"}))
+        sys.exit(3)
+
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    ncalls = N_LAYERS * 4
+
+    # Each call of the layer alone, back to back over the 36 layers.
+    calls = {}
+    if part == "layer":
+        for name, fn, rl in CALLS:
+            nb_ = sum(M * synth.row_bytes(qt, K) for r, qt, M, K in synth.LAYER if r in rl)
+            us = _graph_us(torch, side, ncalls, lambda i, s, fn=fn: fn(layers[i % N_LAYERS], s),
+                           e0, e1)
+            calls[name] = dict(_bw(nb_, us, peak), bytes_per_call=nb_)
+        dom = max(calls, key=lambda k: calls[k]["us_per_call"])
+    else:
+        dom = part if part in ("qkv", "wo", "pair", "down") else "pair"
+        rl = dict((n, r) for n, _, r in CALLS)[dom]
+        fn = dict((n, f) for n, f, _ in CALLS)[dom]
+        nb_ = sum(M * synth.row_bytes(qt, K) for r, qt, M, K in synth.LAYER if r in rl)
+        us = _graph_us(torch, side, ncalls, lambda i, s: fn(layers[i % N_LAYERS], s), e0, e1)
+        calls[dom] = dict(_bw(nb_, us, peak), bytes_per_call=nb_)
+    KERNEL_OF = {"qkv": "qg_n8_kernel<Q4_K|Q6_K> (QKV triple, N=1)",
+                 "wo": "qg_n8_kernel<Q4_K> (Wo + residual, N=1)",
+                 "pair": "qg_n8_kernel<Q4_K> (gate/up pair, N=1)",
+                 "down": "qg_n8_kernel<Q6_K> (down, N=1)"}
+    d = calls[dom]
+    roofline = {"bound": "hbm", "achieved": d["GBps"], "peak": peak, "unit": "GB/s",
+                "frac": round(d["GBps"] / peak, 4), "traffic": _traffic_record(dom),
+                "kernel": KERNEL_OF[dom] + ": the layer's costliest call, timed alone",
+                "per_launch_us": d["us_per_call"], "bytes_per_launch": d["bytes_per_call"],
+                "peak_kind": peak_kind}
+
+    configs = None
+    if part == "layer" and not args.no_configs:
+        configs = run_configs(args, torch, qg, synth, layers, side, e0, e1, peak, tpeak, dev)
 
     # End to end through the host-buffer entry point: per matrix, x from
     # pinned host memory, y back to pinned host memory, synchronized.
@@ -393,23 +487,27 @@ def run_ours(args):
 
     if rank != 0:
         return
-    # CPU baseline: the oracle on one whole layer (N = 1), single thread.
+    # CPU baseline: the oracle on one whole layer (N = 1), rows split over
+    # every host core, and single-threaded beside it.
     cpu = None
     if not args.no_cpu_baseline and world == 1 and part == "layer":
         import oracle
         oracle.build()
-        t_cpu = 0.0
+        mats = []
         for i, (role, qt, M, K) in enumerate(synth.LAYER):
             h = layers[0][role]
             w = h._w.cpu().numpy()
             sc = None if h._scales is None else h._scales.cpu().numpy()
             x = synth.activations(1, K, seed=0, stream=300 + i)
-            t0 = time.perf_counter()
-            oracle.qgemv(qt, w, M, K, x, scales=sc)
-            t_cpu += time.perf_counter() - t0
-        cpu = {"value": round(wbytes / t_cpu / 1e9, 4), "unit": "GB/s", "cores": 1,
+            mats.append((qt, w, M, K, np.arange(M), x, sc))
+        cores = host_cores()
+        t_all = oracle_rows_timed(mats, cores)
+        t_one = oracle_rows_timed(mats, 1)
+        cpu = {"value": round(wbytes / t_all / 1e9, 4), "unit": "GB/s", "cores": cores,
                "kind": "oracle",
-               "sample": "one whole decode layer (7 matrices, 63.9 MB of weights), N=1"}
+               "sample": "one whole decode layer (7 matrices, 63.9 MB of weights), N=1, rows "
+                         f"split over {cores} threads",
+               "single_thread_value": round(wbytes / t_one / 1e9, 4)}
 
     clocks = clk.summary()
     line = {
@@ -431,21 +529,133 @@ def run_ours(args):
                    "cold": "36 distinct layers (2.3 GB) > L2; no flush needed",
                    "pct_of_nominal_8TBps": round(100 * value / world / 8000.0, 2),
                    "pct_of_measured_hbm": round(100 * value / world / peak, 2)},
-        "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak,
-                     "unit": "GB/s", "frac": round(achieved / peak, 4),
-                     "traffic": _traffic_record(),
-                     "kernel": "gate/up pair call: gemv_kernel<Q4_K> (one launch, N=1)",
-                     "per_launch_us": round(pair_us, 3), "bytes_per_launch": pair_bytes,
-                     "peak_kind": peak_kind},
+        "roofline": roofline,
+        "calls": calls,
+        "sustained": sustained,
         "cpu_baseline": cpu,
         "e2e": None if e2e_val is None else {"value": round(e2e_val, 3), "unit": "GB/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h,
                 "how": "qgemv_run_host per matrix (pinned host x and y, synchronized)"},
-        "sweep": sweep,
+        "configs": configs,
+        "device_status": 0,
         "gpu_launches": launches_per_step * args.steps,
         "clocks": clocks,
     }
     print(json.dumps(line))
+
+
+def run_configs(args, torch, qg, synth, layers, side, e0, e1, peak, tpeak, dev):
+    """The other workloads, each timed cold (rotating copies > 4x L2) with
+    CUDA events over one graph replay: the single small GEMV, the skinny row
+    sweeps, prefill chunks over the 36-layer set and the NVFP4 ~10 GB set."""
+    f16 = torch.float16
+    out = {}
+    ncalls = N_LAYERS * 4
+
+    # Single Q4_K GEMV 256 x 2560, N = 1: copies covering > 4x L2.
+    c0 = synth.CONFIG0
+    nb0 = c0["M"] * synth.row_bytes(c0["qtype"], c0["K"])
+    copies = int(math.ceil(4 * 129e6 / nb0))
+    hs0 = []
+    for i in range(copies):
+        w, sc, g = synth.device_weights(c0["qtype"], c0["M"], c0["K"], seed=0, stream=50000 + i,
+                                        device=dev)
+        hs0.append(qg.QGemv(c0["qtype"], c0["M"], c0["K"], w, sc, g, max_tokens=8))
+    x0 = synth.device_activations(1, c0["K"], 0, 11, dev)
+    y0 = torch.empty((1, c0["M"]), dtype=f16, device=dev)
+    us = _graph_us(torch, side, copies, lambda i, s: qg.qgemv_run(
+        hs0[i].h, x0.data_ptr(), 1, y0.data_ptr(), qg.OUT_F16, s), e0, e1)
+    out["c0_q4k_256x2560_n1"] = dict(_bw(nb0, us, peak), copies=copies)
+    del hs0
+
+    # Skinny row sweeps: Q4_K 9728 x 2560 (the gate of each layer) and Q5_K
+    # 2560 x 9728 (36 copies), N rows.
+    hs5 = []
+    for L in range(N_LAYERS):
+        w, sc, g = synth.device_weights(synth.Q5_K, 2560, 9728, seed=0, stream=60000 + L,
+                                        device=dev)
+        hs5.append(qg.QGemv(synth.Q5_K, 2560, 9728, w, sc, g, max_tokens=32))
+    sweeps = {}
+    for name, hsel, M, K, qt in (
+            ("q4k_9728x2560", lambda i: layers[i % N_LAYERS]["gate"], 9728, 2560, synth.Q4_K),
+            ("q5k_2560x9728", lambda i: hs5[i % N_LAYERS], 2560, 9728, synth.Q5_K)):
+        xs = synth.device_activations(32, K, 0, 12, dev)
+        ys = torch.empty((32, M), dtype=f16, device=dev)
+        nbytes = M * synth.row_bytes(qt, K)
+        pts = []
+        for n in synth.SWEEP_N:
+            us = _graph_us(torch, side, ncalls, lambda i, s, n=n: qg.qgemv_run(
+                hsel(i).h, xs.data_ptr(), n, ys.data_ptr(), qg.OUT_F16, s), e0, e1)
+            pts.append(dict(_bw(nbytes, us, peak), N=n))
+        sweeps[name] = pts
+    out["c2_sweep"] = sweeps
+    del hs5
+
+    # Prefill chunks over the 36-layer Q4_K_M-mixed set: per layer the QKV
+    # triple, Wo + residual, the gate/up pair and down at N tokens.
+    layer_bytes = sum(M * synth.row_bytes(qt, K) for _, qt, M, K in synth.LAYER)
+    layer_mk = sum(M * K for _, qt, M, K in synth.LAYER)
+    pre = {}
+    for n in synth.PREFILL_N:
+        xq = synth.device_activations(n, 2560, 0, 13, dev)
+        xo = synth.device_activations(n, 4096, 0, 14, dev)
+        xd = synth.device_activations(n, 9728, 0, 15, dev)
+        rr = synth.device_activations(n, 2560, 0, 16, dev)
+        yb = {M: torch.empty((n, M), dtype=f16, device=dev) for M in (4096, 1024, 2560, 9728)}
+        yb2 = {M: torch.empty((n, M), dtype=f16, device=dev) for M in (1024, 9728)}
+
+        def layer_call(i, s, n=n, xq=xq, xo=xo, xd=xd, rr=rr, yb=yb, yb2=yb2):
+            h = layers[i % N_LAYERS]
+            qg.qgemv_triple_run(h["wq"].h, h["wk"].h, h["wv"].h, xq.data_ptr(), n,
+                                yb[4096].data_ptr(), yb[1024].data_ptr(), yb2[1024].data_ptr(),
+                                qg.OUT_F16, s)
+            qg.qgemv_run_add(h["wo"].h, xo.data_ptr(), n, rr.data_ptr(), yb[2560].data_ptr(), s)
+            qg.qgemv_pair_run(h["gate"].h, h["up"].h, xq.data_ptr(), n, yb[9728].data_ptr(),
+                              yb2[9728].data_ptr(), qg.OUT_F16, s)
+            qg.qgemv_run(h["down"].h, xd.data_ptr(), n, yb[2560].data_ptr(), qg.OUT_F16, s)
+
+        us = _graph_us(torch, side, N_LAYERS, layer_call, e0, e1)
+        tf = 2.0 * n * layer_mk / (us * 1e-6) / 1e12
+        d = _bw(layer_bytes, us, peak)
+        d = {"us_per_layer": d["us_per_call"], "GBps": d["GBps"],
+             "frac_of_measured_hbm": d["frac_of_measured"], "TFLOPs": round(tf, 1),
+             "frac_of_tensor_peak": round(tf / tpeak, 4),
+             "us_36_layers": round(us * N_LAYERS, 1)}
+        pre[f"N{n}"] = d
+    out["c3_prefill_36_layers"] = pre
+
+    # NVFP4 W4A16: 56 copies of {27648x5120, 5120x27648, 7168x5120} (~10 GB).
+    sets = args.nvfp4_sets
+    hs4 = []
+    set_bytes = 0
+    for M, K in synth.NVFP4_SHAPES:
+        set_bytes += M * K // 2 + M * K // 16 + 4
+    for c in range(sets):
+        for j, (M, K) in enumerate(synth.NVFP4_SHAPES):
+            w, sc, g = synth.device_weights(synth.NVFP4, M, K, seed=0, stream=70000 + 3 * c + j,
+                                            device=dev)
+            hs4.append(qg.QGemv(synth.NVFP4, M, K, w, sc, g, max_tokens=32))
+    xs4 = {K: synth.device_activations(32, K, 0, 17, dev) for K in (5120, 27648)}
+    ys4 = {M: torch.empty((32, M), dtype=f16, device=dev) for M in (27648, 5120, 7168)}
+    nv = {"copies": sets, "bytes_per_pass": sets * set_bytes}
+    for n in synth.NVFP4_N:
+        us = _graph_us(torch, side, len(hs4), lambda i, s, n=n: qg.qgemv_run(
+            hs4[i].h, xs4[hs4[i].K].data_ptr(), n, ys4[hs4[i].M].data_ptr(), qg.OUT_F16, s),
+            e0, e1)
+        total_us = us * len(hs4)
+        d = _bw(sets * set_bytes, total_us, peak)
+        nv[f"N{n}"] = {"us_per_pass": round(total_us, 1), "GBps": d["GBps"],
+                       "frac_of_measured": d["frac_of_measured"],
+                       "frac_of_8TBps": d["frac_of_8TBps"]}
+    out["c4_nvfp4_set"] = nv
+    bad = sum(1 for h in hs4 if h.device_status() != 0)
+    bad += sum(1 for hs in layers for h in hs.values() if h.device_status() != 0)
+    if bad:
+        print(json.dumps({"error": f"{bad} handles report a device timeout (configs)"}))
+        sys.exit(3)
+    del hs4
+    torch.cuda.empty_cache()
+    return out
 
 
 def main():
@@ -455,7 +665,12 @@ def main():
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--no-sweep", action="store_true", help="skip the N = 1..32 sweep line")
+    ap.add_argument("--no-configs", action="store_true",
+                    help="skip the other workloads (single GEMV, sweeps, prefill, NVFP4 set)")
+    ap.add_argument("--no-sweep", dest="no_configs", action="store_true",
+                    help="same as --no-configs")
+    ap.add_argument("--nvfp4-sets", type=int, default=56,
+                    help="copies of the three NVFP4 shapes (56: ~10 GB)")
     ap.add_argument("--part", default="layer", choices=["layer", "qkv", "wo", "pair", "down", "gate"],
                     help="time one call of the layer only (profiling); default: the whole layer")
     ap.add_argument("--rows", type=int, default=1,
