@@ -350,6 +350,10 @@ def run_ours(args):
     def call_down(h, s):
         qg.qgemv_run(h["down"].h, x_dn.data_ptr(), 1, yd.data_ptr(), qg.OUT_F16, s)
 
+    def call_pair_swiglu(h, s):
+        qg.qgemv_pair_swiglu_run(h["gate"].h, h["up"].h, x_ffn.data_ptr(), 1, yg.data_ptr(),
+                                 qg.OUT_F16, s)
+
     CALLS = [("qkv", call_qkv, ["wq", "wk", "wv"]), ("wo", call_wo, ["wo"]),
              ("pair", call_pair, ["gate", "up"]), ("down", call_down, ["down"])]
 
@@ -440,6 +444,12 @@ def run_ours(args):
                            e0, e1)
             calls[name] = dict(_bw(nb_, us, peak), bytes_per_call=nb_)
         dom = max(calls, key=lambda k: calls[k]["us_per_call"])
+        # the gate/up pair with the fused SwiGLU epilogue (h = silu(g) * u), not
+        # part of the step: the layer's pair returns g and u
+        nb_ = 2 * 9728 * synth.row_bytes(synth.Q4_K, 2560)
+        us = _graph_us(torch, side, ncalls,
+                       lambda i, s: call_pair_swiglu(layers[i % N_LAYERS], s), e0, e1)
+        calls["pair_swiglu"] = dict(_bw(nb_, us, peak), bytes_per_call=nb_)
     else:
         dom = part if part in ("qkv", "wo", "pair", "down") else "pair"
         rl = dict((n, r) for n, _, r in CALLS)[dom]

@@ -155,6 +155,24 @@ qg_status qgemv_triple_run(qg_handle *a, qg_handle *b, qg_handle *c, const void 
                            int64_t N, void *ya, void *yb, void *yc, qg_out ydt,
                            void *stream);
 
+/* Fused gate/up pair with the SwiGLU epilogue: h = silu(x . Wg^T) * (x . Wu^T),
+ * silu(v) = v / (1 + exp(-v)), written once to h without the two products
+ * ever reaching memory (reflex-llm "docs/kernels.md", SwiGLU section:
+ * output = silu(gate) x up, fusing avoids writing the intermediate;
+ * "docs/performance.md", Path B PR #15: batched gate/up + SwiGLU).
+ *   gate, up  handles of the same shape (M, K) and weight format
+ *   x         fp16 [N][K] device, 16-byte aligned
+ *   h         [N][M] device of type hdt (fp16 rounded to nearest-even, or
+ *             fp32), 4-byte aligned
+ * g and u are the fp32 values a plain qgemv_pair_run returns for the same x
+ * (bit for bit); silu and the product are evaluated in fp32 (expf) and
+ * rounded once to hdt.  Rows are row-invariant for every N (an elementwise
+ * epilogue on row-invariant products).  Q4_K calls with N >= 33 stay on the
+ * mma.sync kernels.  Errors: QG_EINVAL (null, shape mismatch, gate == up),
+ * QG_EUNSUPPORTED (different formats), QG_EALIGN, QG_ECUDA. */
+qg_status qgemv_pair_swiglu_run(qg_handle *gate, qg_handle *up, const void *x, int64_t N,
+                                void *h, qg_out hdt, void *stream);
+
 /* Host-buffer form of qgemv_run (the same operation as qgemv_run; the pages
  * time kernels with their inputs resident, TandemLLM "Kernels", How a kernel
  * gets in -- this entry times the whole round trip).

@@ -74,6 +74,10 @@ def _load():
         lib.or_qgemv_rows.argtypes = [i32, vp, vp, f32, i64, i64, vp, i64, vp, i64,
                                       vp, vp, vp, vp]
         lib.or_qgemv_rows.restype = i32
+        lib.or_silu.argtypes = [ctypes.c_double]
+        lib.or_silu.restype = ctypes.c_double
+        lib.or_swiglu.argtypes = [vp, vp, i64, vp]
+        lib.or_swiglu.restype = None
         _lib = lib
         return lib
 
@@ -157,3 +161,31 @@ def qgemv(qtype: int, w, M: int, K: int, x, scales=None, global_scale: float = 1
     if rc != 0:
         raise ValueError(f"oracle qgemv failed (rc={rc})")
     return y, mag
+
+
+def silu(v: float) -> float:
+    """silu(v) = v / (1 + exp(-v)) in float64 (reflex-llm "docs/kernels.md",
+    SwiGLU section)."""
+    return float(_load().or_silu(float(v)))
+
+
+def swiglu(g, u) -> np.ndarray:
+    """h = silu(g) * u elementwise in float64 (g, u: the oracle's float64
+    gate and up products for the same x)."""
+    g = np.ascontiguousarray(g, dtype=np.float64)
+    u = np.ascontiguousarray(u, dtype=np.float64)
+    if g.shape != u.shape:
+        raise ValueError("gate and up shapes differ")
+    h = np.empty_like(g)
+    _load().or_swiglu(_ptr(g), _ptr(u), g.size, _ptr(h))
+    return h
+
+
+def qgemv_swiglu(qtype_g: int, wg, qtype_u: int, wu, M: int, K: int, x, rows=None,
+                 scales_g=None, gscale_g: float = 1.0, scales_u=None, gscale_u: float = 1.0):
+    """The fused pair: h = silu(x.Wg^T) * (x.Wu^T) on selected rows, plus
+    both products and their magnitudes: (h, g, mag_g, u, mag_u), float64
+    [N][len(rows)]."""
+    g, mg = qgemv(qtype_g, wg, M, K, x, scales=scales_g, global_scale=gscale_g, rows=rows)
+    u, mu = qgemv(qtype_u, wu, M, K, x, scales=scales_u, global_scale=gscale_u, rows=rows)
+    return swiglu(g, u), g, mg, u, mu

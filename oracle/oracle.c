@@ -326,3 +326,21 @@ int or_qgemv_rows(int type, const uint8_t *w, const uint8_t *scales, float g,
     }
     return 0;
 }
+
+/* ------------------------------------------------------------------------ */
+/* SwiGLU of the gate/up pair (reflex-llm "docs/kernels.md", SwiGLU         */
+/* section: output = silu(gate) x up, silu(v) = v / (1 + exp(-v))).         */
+/* ------------------------------------------------------------------------ */
+
+double or_silu(double v)
+{
+    return v / (1.0 + exp(-v));
+}
+
+/* h[i] = silu(g[i]) * u[i] in float64, i < n (g and u are the oracle's
+ * float64 products of the gate and up matrices for the same x). */
+void or_swiglu(const double *g, const double *u, int64_t n, double *h)
+{
+    for (int64_t i = 0; i < n; ++i)
+        h[i] = or_silu(g[i]) * u[i];
+}

@@ -33,6 +33,9 @@ int or_qgemv_rows(int type, const uint8_t *w, const uint8_t *scales, float g,
                   const uint16_t *x, int64_t N, const uint16_t *residual,
                   double *y, double *mag, float *scratch);
 
+double or_silu(double v);
+void or_swiglu(const double *g, const double *u, int64_t n, double *h);
+
 #ifdef __cplusplus
 }
 #endif

@@ -304,7 +304,8 @@ cudaError_t launch_sk_tset(int tset, int G, const Params &p, dim3 grid, int smem
 // launch per chunk of at most max_tokens rows (several launches only when the
 // formats have no common kernel).
 qg_status run_product_mma(qg_handle *const *hs, int nh, const __half *x, int64_t N,
-                          void *const *ys, const __half *res, int out_f32, cudaStream_t s)
+                          void *const *ys, const __half *res, int out_f32, cudaStream_t s,
+                          bool swiglu = false)
 {
     const qg_handle *h0 = hs[0];
     uint32_t flags = 0;
@@ -322,6 +323,31 @@ qg_status run_product_mma(qg_handle *const *hs, int nh, const __half *x, int64_t
     for (int64_t c0 = 0; c0 < N; c0 += max_tokens) {
         const int n = (int)((N - c0) < max_tokens ? (N - c0) : max_tokens);
         const __half *xc = x + c0 * h0->K;
+        auto ref_fallback = [&](const Params &pp) -> qg_status {
+            if (swiglu) {
+                cudaError_t re = launch_ref_swiglu(pp.mat[0], pp.mat[1], (int)h0->K, xc, n,
+                                                   out_f32, s);
+                if (re != cudaSuccess) return cuda_fail(re, "reference kernel launch");
+                return QG_OK;
+            }
+            for (int j = 0; j < pp.nmat; ++j) {
+                cudaError_t re = launch_ref_gemv(pp.mat[j], (int)h0->K, xc, n, out_f32, s);
+                if (re != cudaSuccess) return cuda_fail(re, "reference kernel launch");
+            }
+            return QG_OK;
+        };
+        if (force_ref && swiglu) {
+            Params pp;
+            memset(&pp, 0, sizeof pp);
+            pp.nmat = 2;
+            for (int i = 0; i < 2; ++i)
+                pp.mat[i] = mat_of(hs[i], ys[i] ? (uint8_t *)ys[i] + c0 * hs[i]->M * (out_f32 ? 4 : 2)
+                                                : nullptr,
+                                   nullptr);
+            const qg_status rs = ref_fallback(pp);
+            if (rs != QG_OK) return rs;
+            continue;
+        }
         if (force_ref) {
             for (int i = 0; i < nh; ++i) {
                 Mat m = mat_of(hs[i], (uint8_t *)ys[i] + c0 * hs[i]->M * (out_f32 ? 4 : 2),
@@ -380,7 +406,8 @@ qg_status run_product_mma(qg_handle *const *hs, int nh, const __half *x, int64_t
                     const int idx = groups[gidx][j];
                     const qg_handle *h = hs[idx];
                     gts |= tset_bit(h->type);
-                    p.mat[j] = mat_of(h, (uint8_t *)ys[idx] + c0 * h->M * (out_f32 ? 4 : 2),
+                    p.mat[j] = mat_of(h, ys[idx] ? (uint8_t *)ys[idx] + c0 * h->M * (out_f32 ? 4 : 2)
+                                                 : nullptr,
                                       res ? res + c0 * h->M : nullptr);
                     p.mat[j].tile_begin = tiles;
                     const int R = kGemvRows / h->kw;
@@ -396,6 +423,7 @@ qg_status run_product_mma(qg_handle *const *hs, int nh, const __half *x, int64_t
                 p.xtok = gemv_xtok(h0->nb);
                 p.out_f32 = out_f32;
                 p.err = h0->err;
+                p.swiglu = swiglu ? 1 : 0;  // tiles interleaved: 2 tile + matrix
                 const dim3 grid(1u, (unsigned)tiles, 1u);
                 cudaError_t le = fault_at("launch") ? cudaErrorLaunchOutOfResources
                                                     : launch_gemv_tset(gts, p, grid, gemv_smem, s);
@@ -406,10 +434,8 @@ qg_status run_product_mma(qg_handle *const *hs, int nh, const __half *x, int64_t
                             return fail(QG_EFAULT_INJECTED, "injected fault: product launch");
                         return cuda_fail(le, "product kernel launch");
                     }
-                    for (int j = 0; j < p.nmat; ++j) {
-                        cudaError_t re = launch_ref_gemv(p.mat[j], (int)h0->K, xc, n, out_f32, s);
-                        if (re != cudaSuccess) return cuda_fail(re, "reference kernel launch");
-                    }
+                    const qg_status rs = ref_fallback(p);
+                    if (rs != QG_OK) return rs;
                     fail(QG_OK, "fast path launch failed (%s); used the reference kernel",
                          cudaGetErrorName(le));
                 }
@@ -470,7 +496,8 @@ qg_status run_product_mma(qg_handle *const *hs, int nh, const __half *x, int64_t
             for (int j = 0; j < gsize[gidx]; ++j) {
                 const qg_handle *h = hs[groups[gidx][j]];
                 const int idx = groups[gidx][j];
-                p.mat[j] = mat_of(h, (uint8_t *)ys[idx] + c0 * h->M * (out_f32 ? 4 : 2),
+                p.mat[j] = mat_of(h, ys[idx] ? (uint8_t *)ys[idx] + c0 * h->M * (out_f32 ? 4 : 2)
+                                             : nullptr,
                                   res ? res + c0 * h->M : nullptr);
                 p.mat[j].tile_begin = tiles;
                 tiles += (int)((h->M + rows - 1) / rows);
@@ -498,6 +525,7 @@ qg_status run_product_mma(qg_handle *const *hs, int nh, const __half *x, int64_t
             p.K = (int)h0->K;
             p.out_f32 = out_f32;
             p.err = h0->err;
+            p.swiglu = swiglu ? 1 : 0;  // tiles interleaved: 2 tile + matrix
             const dim3 grid((unsigned)p.ks, (unsigned)tiles, (unsigned)((n + kTokChunk - 1) / kTokChunk));
             // With no more CTAs than SMs, ask for more than half an SM's shared
             // memory: otherwise both CTAs of a cluster may be placed on one SM
@@ -519,10 +547,8 @@ qg_status run_product_mma(qg_handle *const *hs, int nh, const __half *x, int64_t
                         return fail(QG_EFAULT_INJECTED, "injected fault: product launch");
                     return cuda_fail(le, "product kernel launch");
                 }
-                for (int j = 0; j < p.nmat; ++j) {
-                    cudaError_t re = launch_ref_gemv(p.mat[j], (int)h0->K, xc, n, out_f32, s);
-                    if (re != cudaSuccess) return cuda_fail(re, "reference kernel launch");
-                }
+                const qg_status rs = ref_fallback(p);
+                if (rs != QG_OK) return rs;
                 fail(QG_OK, "fast path launch failed (%s); used the reference kernel",
                      cudaGetErrorName(le));
             }
@@ -611,7 +637,7 @@ qg_status run_product_tc(qg_handle *const *hs, int nh, const __half *x, int64_t 
 // unless QG_FLAG_MMA_SYNC_PREFILL is set; everything else runs on the
 // mma.sync kernels.
 qg_status run_product(qg_handle *const *hs, int nh, const __half *x, int64_t N, void *const *ys,
-                      const __half *res, int out_f32, cudaStream_t s)
+                      const __half *res, int out_f32, cudaStream_t s, bool swiglu = false)
 {
     g_err.clear();
     uint32_t flags = 0;
@@ -621,7 +647,7 @@ qg_status run_product(qg_handle *const *hs, int nh, const __half *x, int64_t N, 
     int ntc = 0, nmm = 0;
     for (int i = 0; i < nh; ++i) {
         if (hs[i]->type == QG_Q4_K && N >= kTcMinN && !(flags & QG_FLAG_MMA_SYNC_PREFILL) &&
-            !(flags & QG_FLAG_FORCE_REFERENCE)) {
+            !(flags & QG_FLAG_FORCE_REFERENCE) && !swiglu) {
             tc[ntc] = hs[i];
             ytc[ntc++] = ys[i];
         } else {
@@ -637,7 +663,7 @@ qg_status run_product(qg_handle *const *hs, int nh, const __half *x, int64_t N, 
         note = g_err;
     }
     if (nmm) {
-        st = run_product_mma(mm, nmm, x, N, ymm, res, out_f32, s);
+        st = run_product_mma(mm, nmm, x, N, ymm, res, out_f32, s, swiglu);
         if (st != QG_OK) return st;
         if (note.empty()) note = g_err;
     }
@@ -932,6 +958,23 @@ qg_status qgemv_triple_run(qg_handle *a, qg_handle *b, qg_handle *c, const void 
     void *ys[3] = {ya, yb, yc};
     return run_product(hs, 3, (const __half *)x, N, ys, nullptr, ydt == QG_OUT_F32,
                        (cudaStream_t)stream);
+}
+
+qg_status qgemv_pair_swiglu_run(qg_handle *gate, qg_handle *up, const void *x, int64_t N,
+                                void *h, qg_out hdt, void *stream)
+{
+    qg_status st = check_run_args(gate, x, N, h, hdt);
+    if (st != QG_OK) return st;
+    if (!up) return fail(QG_EINVAL, "null up handle");
+    if (gate == up) return fail(QG_EINVAL, "gate and up must be different handles");
+    if (gate->M != up->M || gate->K != up->K)
+        return fail(QG_EINVAL, "gate and up must have the same shape");
+    if (gate->type != up->type)
+        return fail(QG_EUNSUPPORTED, "gate and up must have the same weight format");
+    qg_handle *hs[2] = {gate, up};
+    void *ys[2] = {h, nullptr};
+    return run_product(hs, 2, (const __half *)x, N, ys, nullptr, hdt == QG_OUT_F32,
+                       (cudaStream_t)stream, true);
 }
 
 qg_status qgemv_run_host(qg_handle *h, const void *x_host, int64_t N, void *y_host, qg_out ydt,

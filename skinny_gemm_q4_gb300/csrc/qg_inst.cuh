@@ -37,11 +37,21 @@ static cudaError_t launch_gemv_one(const Params &p, dim3 grid, int smem, cudaStr
     cfg.blockDim = dim3(32 * (kGemvCW + 1));
     cfg.dynamicSmemBytes = smem;
     cfg.stream = stream;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchAttribute attr[2];
+    int na = 0;
+    attr[na].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[na].val.programmaticStreamSerializationAllowed = 1;
+    ++na;
+    if (p.swiglu) {
+        // the gate and up CTAs of one row tile form a cluster (SwiGLU epilogue)
+        attr[na].id = cudaLaunchAttributeClusterDimension;
+        attr[na].val.clusterDim.x = 1;
+        attr[na].val.clusterDim.y = 2;
+        attr[na].val.clusterDim.z = 1;
+        ++na;
+    }
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    cfg.numAttrs = na;
     if (p.N == 1) return cudaLaunchKernelEx(&cfg, qg_n8_kernel<TSET, true>, p);
     return cudaLaunchKernelEx(&cfg, qg_n8_kernel<TSET, false>, p);
 }
@@ -62,6 +72,10 @@ static cudaError_t launch_sk_one(const Params &p, dim3 grid, int smem, cudaStrea
             e = cudaFuncSetAttribute(qg_sk_kernel<TSET, G, XIN>,
                                      cudaFuncAttributePreferredSharedMemoryCarveout,
                                      cudaSharedmemCarveoutMaxShared);
+        // SwiGLU pairs of 8-slice matrices use clusters of 16 CTAs
+        if (e == cudaSuccess)
+            e = cudaFuncSetAttribute(qg_sk_kernel<TSET, G, XIN>,
+                                     cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
         if (e != cudaSuccess) return e;
         configured[dev] = 1;
     }
@@ -75,10 +89,11 @@ static cudaError_t launch_sk_one(const Params &p, dim3 grid, int smem, cudaStrea
     attr[na].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[na].val.programmaticStreamSerializationAllowed = 1;
     ++na;
-    if (p.ks > 1) {
+    if (p.ks > 1 || p.swiglu) {
+        // K-split ranks along x; for a SwiGLU pair the gate and up tiles along y
         attr[na].id = cudaLaunchAttributeClusterDimension;
         attr[na].val.clusterDim.x = (unsigned)p.ks;
-        attr[na].val.clusterDim.y = 1;
+        attr[na].val.clusterDim.y = p.swiglu ? 2u : 1u;
         attr[na].val.clusterDim.z = 1;
         ++na;
     }

@@ -100,6 +100,10 @@ struct Params {
     int out_f32;
     unsigned int *err;            // error word (timeouts)
     int xin;                      // qg_sk_kernel: x staged inside the kernel from p.x
+    int swiglu;                   // gate/up pair with the SwiGLU epilogue: mat[0] gate (its y
+                                  // receives h = silu(g) * u), mat[1] up, same M and K;
+                                  // blockIdx.y = 2 tile + matrix, and the two CTAs of a
+                                  // tile (times the K-split ranks) form one cluster
 };
 
 template <int T>
@@ -706,6 +710,23 @@ __device__ __forceinline__ void store_out4(const Params &p, const Mat &m, int ro
     store_out<T>(p, m, row + 3, tok, v.w);
 }
 
+// SwiGLU epilogue of the gate/up pair (reflex-llm "docs/kernels.md", SwiGLU
+// section): h = silu(g) * u, silu(v) = v / (1 + exp(-v)), in fp32 from the two
+// products' finished fp32 values, then one rounding to the output type.
+__device__ __forceinline__ float qg_silu(float v) { return __fdiv_rn(v, __fadd_rn(1.0f, expf(-v))); }
+
+__device__ __forceinline__ void store_h(const Params &p, const Mat &m, int row, int tok, float g,
+                                        float u)
+{
+    if (row >= m.M || tok >= p.N) return;
+    const float h = __fmul_rn(qg_silu(g), u);
+    const int64_t o = (int64_t)tok * m.M + row;
+    if (p.out_f32)
+        reinterpret_cast<float *>(m.y)[o] = h;
+    else
+        reinterpret_cast<__half *>(m.y)[o] = __float2half_rn(h);
+}
+
 // Rank-ordered K-split reduction through distributed shared memory, then the
 // epilogue.  Every rank publishes its partial tile in `red` (free shared
 // memory of at least ncons * MT * G * 4 floats); after a cluster barrier rank
@@ -717,13 +738,21 @@ __device__ __forceinline__ void store_out4(const Params &p, const Mat &m, int ro
 // every CTA in the cluster must call this.  cid/ncons: this thread's index
 // among the consumer threads; row_cta: the tile's first row (consumer warp w
 // holds rows row_cta + 16 MT w ..).
+//
+// SwiGLU pair (role 0: the gate CTA, 1: the up CTA of the same row tile; -1:
+// no SwiGLU): the cluster is [ks gate ranks | ks up ranks]; each up rank
+// keeps its finished share (global scale applied) in shared memory and the
+// gate rank of the same index reads it through distributed shared memory and
+// stores h = silu(g) * u.  g and u get exactly the sums they get in a plain
+// pair call.
 template <int T, int MT, int G>
 __device__ __forceinline__ void reduce_and_store(const Acc<T, MT, G> &A, float *red, int rank,
                                                  int ks, int cid, int ncons, bool consumer,
                                                  const Params &p, const Mat &m, int row_cta,
-                                                 int tok0, int g, int t)
+                                                 int tok0, int g, int t, int role = -1)
 {
     constexpr int E = MT * G * 4;  // partial floats per consumer thread
+    const uint32_t rank_base = (role == 1) ? (uint32_t)ks : 0u;
     if (ks > 1) {
         // partials published token-major, [token][row] of the tile, so that
         // a float4 of the share is four consecutive rows of one token
@@ -747,7 +776,8 @@ __device__ __forceinline__ void reduce_and_store(const Acc<T, MT, G> &A, float *
             float4 part[8];
 #pragma unroll
             for (int r = 0; r < 8; ++r)
-                if (r < ks) part[r] = ld_dsmem_v4(map_shared_rank(rbase + 4 * idx0, (uint32_t)r));
+                if (r < ks)
+                    part[r] = ld_dsmem_v4(map_shared_rank(rbase + 4 * idx0, rank_base + (uint32_t)r));
             float4 sum = part[0];
 #pragma unroll
             for (int r = 1; r < 8; ++r) {
@@ -759,12 +789,76 @@ __device__ __forceinline__ void reduce_and_store(const Acc<T, MT, G> &A, float *
                 }
             }
             const int tl = idx0 / nrows, rl = idx0 - tl * nrows;
-            store_out4<T>(p, m, row_cta + rl, tok0 + tl, sum);
+            if (role < 0) {
+                store_out4<T>(p, m, row_cta + rl, tok0 + tl, sum);
+            } else {
+                // this rank's finished share, after the partials it read
+                if (T == T_FP4) {
+                    sum.x *= m.gscale;
+                    sum.y *= m.gscale;
+                    sum.z *= m.gscale;
+                    sum.w *= m.gscale;
+                }
+                *reinterpret_cast<float4 *>(red + E * ncons + 4 * q4) = sum;
+            }
+        }
+        if (role >= 0) {
+            cluster_sync();  // every rank's share is in place
+            if (role == 0) {
+                const uint32_t xb = smem_u32(red + E * ncons);
+                for (int q4 = threadIdx.x; 4 * q4 < per; q4 += blockDim.x) {
+                    const int idx0 = rank * per + 4 * q4;
+                    const float4 gv = *reinterpret_cast<const float4 *>(red + E * ncons + 4 * q4);
+                    const float4 uv =
+                        ld_dsmem_v4(map_shared_rank(xb + 16 * q4, (uint32_t)(rank + ks)));
+                    const int tl = idx0 / nrows, rl = idx0 - tl * nrows;
+                    store_h(p, m, row_cta + rl, tok0 + tl, gv.x, uv.x);
+                    store_h(p, m, row_cta + rl + 1, tok0 + tl, gv.y, uv.y);
+                    store_h(p, m, row_cta + rl + 2, tok0 + tl, gv.z, uv.z);
+                    store_h(p, m, row_cta + rl + 3, tok0 + tl, gv.w, uv.w);
+                }
+            }
         }
         // every remote read has returned (its value was summed): the other
         // CTAs may exit once all have arrived; the y stores need no wait
         cluster_arrive_relaxed();
         cluster_wait();
+        return;
+    }
+    if (role >= 0) {
+        // no K split: the up CTA (cluster rank 1) publishes its values, indexed
+        // [element][consumer thread], for the gate CTA (rank 0)
+        if (consumer && role == 1) {
+#pragma unroll
+            for (int mt = 0; mt < MT; ++mt)
+#pragma unroll
+                for (int gi = 0; gi < G; ++gi)
+#pragma unroll
+                    for (int c = 0; c < 4; ++c) {
+                        float v = A.partial(mt, gi, c);
+                        if (T == T_FP4) v = v * m.gscale;
+                        red[((mt * G + gi) * 4 + c) * ncons + cid] = v;
+                    }
+        }
+        cluster_sync();
+        if (consumer && role == 0) {
+            const int row_w = row_cta + (cid >> 5) * MT * 16;
+            const uint32_t xb = smem_u32(red);
+#pragma unroll
+            for (int mt = 0; mt < MT; ++mt)
+#pragma unroll
+                for (int gi = 0; gi < G; ++gi)
+#pragma unroll
+                    for (int c = 0; c < 4; ++c) {
+                        float gv = A.partial(mt, gi, c);
+                        if (T == T_FP4) gv = gv * m.gscale;
+                        const float uv = ld_dsmem_f32(map_shared_rank(
+                            xb + 4 * (((mt * G + gi) * 4 + c) * ncons + cid), 1u));
+                        store_h(p, m, row_w + mt * 16 + g + 8 * (c >> 1),
+                                tok0 + 8 * gi + 2 * t + (c & 1), gv, uv);
+                    }
+        }
+        cluster_sync();  // the up CTA's values stay readable until read
         return;
     }
     if (!consumer) return;
@@ -816,7 +910,8 @@ __device__ __forceinline__ int gemv_stage_bytes(int kw)
 }
 
 template <int T, bool ODD>
-__device__ __forceinline__ void gemv_tile(const Params &p, const Mat &m, int rtile, uint8_t *smem)
+__device__ __forceinline__ void gemv_tile(const Params &p, const Mat &m, int rtile, uint8_t *smem,
+                                          int role)
 {
     using F = Fmt<T>;
     constexpr bool TMA = (T != T_Q6K);
@@ -1026,11 +1121,37 @@ __device__ __forceinline__ void gemv_tile(const Params &p, const Mat &m, int rti
         for (int cc = 0; cc < 4; ++cc) red[(c * 4 + cc) * 32 + lane] = v[cc];
     }
     __syncthreads();
-    if (warp == 0 || ks != 0) return;
-    for (int q = 1; q < kw; ++q) {
+    const bool fin = warp > 0 && ks == 0;  // slice-0 warps finish their rows
+    if (fin) {
+        for (int q = 1; q < kw; ++q) {
 #pragma unroll
-        for (int cc = 0; cc < 4; ++cc) v[cc] += red[((c + q) * 4 + cc) * 32 + lane];
+            for (int cc = 0; cc < 4; ++cc) v[cc] += red[((c + q) * 4 + cc) * 32 + lane];
+        }
     }
+    if (role >= 0) {
+        // SwiGLU pair: the up CTA (cluster rank 1) hands its finished values
+        // to the gate CTA (rank 0) of the same rows, which stores
+        // h = silu(g) * u; both get exactly the sums of a plain pair call.
+        float *xb = red + kGemvCW * 4 * 32;
+        if (fin && role == 1) {
+#pragma unroll
+            for (int cc = 0; cc < 4; ++cc)
+                xb[(c * 4 + cc) * 32 + lane] = (T == T_FP4) ? v[cc] * m.gscale : v[cc];
+        }
+        cluster_sync();
+        if (fin && role == 0) {
+#pragma unroll
+            for (int cc = 0; cc < 4; ++cc) {
+                const float u = ld_dsmem_f32(
+                    map_shared_rank(smem_u32(xb + (c * 4 + cc) * 32 + lane), 1u));
+                store_h(p, m, row_w + g + 8 * (cc >> 1), 2 * t + (cc & 1),
+                        (T == T_FP4) ? v[cc] * m.gscale : v[cc], u);
+            }
+        }
+        cluster_sync();  // the up CTA's values stay readable until read
+        return;
+    }
+    if (!fin) return;
 #pragma unroll
     for (int cc = 0; cc < 4; ++cc) {
         const int row = row_w + g + 8 * (cc >> 1);
@@ -1056,16 +1177,18 @@ __global__ void __launch_bounds__(32 * (kGemvCW + 1)) qg_n8_kernel(const __grid_
     extern __shared__ __align__(128) uint8_t smem[];
     pdl_trigger();
     const int tile = blockIdx.y;
-    const Mat &m = p.mat[select_mat(p, tile)];
-    const int rtile = tile - m.tile_begin;
+    const int mi = p.swiglu ? (tile & 1) : select_mat(p, tile);
+    const Mat &m = p.mat[mi];
+    const int rtile = p.swiglu ? (tile >> 1) : tile - m.tile_begin;
+    const int role = p.swiglu ? mi : -1;
     if constexpr ((TSET & TS_Q4K) != 0)
-        if (m.type == T_Q4K) return gemv_tile<T_Q4K, !ONE>(p, m, rtile, smem);
+        if (m.type == T_Q4K) return gemv_tile<T_Q4K, !ONE>(p, m, rtile, smem, role);
     if constexpr ((TSET & TS_Q5K) != 0)
-        if (m.type == T_Q5K) return gemv_tile<T_Q5K, !ONE>(p, m, rtile, smem);
+        if (m.type == T_Q5K) return gemv_tile<T_Q5K, !ONE>(p, m, rtile, smem, role);
     if constexpr ((TSET & TS_Q6K) != 0)
-        if (m.type == T_Q6K) return gemv_tile<T_Q6K, !ONE>(p, m, rtile, smem);
+        if (m.type == T_Q6K) return gemv_tile<T_Q6K, !ONE>(p, m, rtile, smem, role);
     if constexpr ((TSET & TS_FP4) != 0)
-        if (m.type == T_FP4) return gemv_tile<T_FP4, !ONE>(p, m, rtile, smem);
+        if (m.type == T_FP4) return gemv_tile<T_FP4, !ONE>(p, m, rtile, smem, role);
 }
 
 // Dynamic shared memory of qg_n8_kernel: barriers, `stages` ring slots of
@@ -1113,7 +1236,7 @@ __host__ __device__ inline int sk_smem_bytes(int wbytes, int G, int stages)
 
 template <int T, int G, bool XIN>
 __device__ __forceinline__ void sk_tile(const Params &p, const Mat &m, int rtile, uint8_t *smem,
-                                        int wbytes)
+                                        int wbytes, int role)
 {
     using F = Fmt<T>;
     constexpr int WP = (T == T_Q6K) ? 224 : (T == T_FP4) ? 128 : F::BB;  // weight row pitch
@@ -1300,7 +1423,8 @@ __device__ __forceinline__ void sk_tile(const Params &p, const Mat &m, int rtile
     if (err && p.err) atomicOr(p.err, err);
     __syncthreads();
     reduce_and_store<T, 1, G>(A, reinterpret_cast<float *>(smem + 128), rank, ks,
-                              threadIdx.x - 32, kSkCons * 32, warp > 0, p, m, row0, tok0, g, t);
+                              threadIdx.x - 32, kSkCons * 32, warp > 0, p, m, row0, tok0, g, t,
+                              role);
 }
 
 template <int TSET, int G, bool XIN = false>
@@ -1311,16 +1435,18 @@ __global__ void __launch_bounds__(kSkThreads) qg_sk_kernel(const __grid_constant
     int wbytes = 0;
     for (int i = 0; i < p.nmat; ++i) wbytes = max(wbytes, sk_wbytes(p.mat[i].type));
     const int tile = blockIdx.y;
-    const Mat &m = p.mat[select_mat(p, tile)];
-    const int rtile = tile - m.tile_begin;
+    const int mi = p.swiglu ? (tile & 1) : select_mat(p, tile);
+    const Mat &m = p.mat[mi];
+    const int rtile = p.swiglu ? (tile >> 1) : tile - m.tile_begin;
+    const int role = p.swiglu ? mi : -1;
     if constexpr ((TSET & TS_Q4K) != 0)
-        if (m.type == T_Q4K) return sk_tile<T_Q4K, G, XIN>(p, m, rtile, smem, wbytes);
+        if (m.type == T_Q4K) return sk_tile<T_Q4K, G, XIN>(p, m, rtile, smem, wbytes, role);
     if constexpr ((TSET & TS_Q5K) != 0)
-        if (m.type == T_Q5K) return sk_tile<T_Q5K, G, XIN>(p, m, rtile, smem, wbytes);
+        if (m.type == T_Q5K) return sk_tile<T_Q5K, G, XIN>(p, m, rtile, smem, wbytes, role);
     if constexpr ((TSET & TS_Q6K) != 0)
-        if (m.type == T_Q6K) return sk_tile<T_Q6K, G, XIN>(p, m, rtile, smem, wbytes);
+        if (m.type == T_Q6K) return sk_tile<T_Q6K, G, XIN>(p, m, rtile, smem, wbytes, role);
     if constexpr ((TSET & TS_FP4) != 0)
-        if (m.type == T_FP4) return sk_tile<T_FP4, G, XIN>(p, m, rtile, smem, wbytes);
+        if (m.type == T_FP4) return sk_tile<T_FP4, G, XIN>(p, m, rtile, smem, wbytes, role);
 }
 
 }  // namespace qg

@@ -20,6 +20,9 @@ cudaError_t launch_dequant_fast(const Mat &m, int K, float *out, cudaStream_t st
 cudaError_t launch_tc(int G, const Params &p, dim3 grid, int smem, cudaStream_t s);
 cudaError_t launch_ref_gemv(const Mat &m, int K, const __half *x, int N, int out_f32,
                             cudaStream_t stream);
+// Reference SwiGLU pair: h = silu(x.gate^T) * (x.up^T) into gate.y.
+cudaError_t launch_ref_swiglu(const Mat &gate, const Mat &up, int K, const __half *x, int N,
+                              int out_f32, cudaStream_t stream);
 
 // Per type-set launchers (defined in qg_inst_*.cu).
 #define QG_DECLARE_TSET(NAME)                                                           \

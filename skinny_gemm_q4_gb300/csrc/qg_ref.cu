@@ -103,6 +103,38 @@ __global__ void qg_ref_kernel(RefMat m, const __half *x, int N, const __half *re
     }
 }
 
+// Reference SwiGLU pair: one warp per (row, token) computes both products
+// as qg_ref_kernel does and stores h = silu(g) * u.
+__global__ void qg_ref_swiglu_kernel(RefMat mg, RefMat mu, const __half *x, int N, void *y,
+                                     int out_f32)
+{
+    pdl_trigger();
+    pdl_wait();
+    const int row = blockIdx.x * 4 + (threadIdx.x >> 5);
+    const int tok = blockIdx.y;
+    const int lane = threadIdx.x & 31;
+    if (row >= mg.M || tok >= N) return;
+    float ag = 0.0f, au = 0.0f;
+    for (int k = lane; k < mg.K; k += 32) {
+        const float xv = __half2float(x[(int64_t)tok * mg.K + k]);
+        ag = __fmaf_rn(ref_weight(mg, row, k), xv, ag);
+        au = __fmaf_rn(ref_weight(mu, row, k), xv, au);
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+        ag = __fadd_rn(ag, __shfl_xor_sync(0xffffffffu, ag, o));
+        au = __fadd_rn(au, __shfl_xor_sync(0xffffffffu, au, o));
+    }
+    if (lane == 0) {
+        const int64_t o = (int64_t)tok * mg.M + row;
+        const float h = __fmul_rn(qg_silu(ag), au);
+        if (out_f32)
+            reinterpret_cast<float *>(y)[o] = h;
+        else
+            reinterpret_cast<__half *>(y)[o] = __float2half_rn(h);
+    }
+}
+
 static RefMat make_ref(const Mat &mm, int K)
 {
     RefMat r;
@@ -142,4 +174,22 @@ cudaError_t launch_ref_gemv(const Mat &mm, int K, const __half *x, int N, int ou
     return cudaLaunchKernelEx(&cfg, qg_ref_kernel, r, x, N, mm.res, mm.y, out_f32);
 }
 
+}  // namespace qg
+
+namespace qg {
+cudaError_t launch_ref_swiglu(const Mat &gate, const Mat &up, int K, const __half *x, int N,
+                              int out_f32, cudaStream_t stream)
+{
+    const RefMat rg = make_ref(gate, K), ru = make_ref(up, K);
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)((rg.M + 3) / 4), (unsigned)N);
+    cfg.blockDim = dim3(128);
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, qg_ref_swiglu_kernel, rg, ru, x, N, gate.y, out_f32);
+}
 }  // namespace qg

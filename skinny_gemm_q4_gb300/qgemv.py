@@ -37,7 +37,7 @@ STATUS_NAMES = {0: "QG_OK", -1: "QG_EINVAL", -2: "QG_EUNSUPPORTED", -3: "QG_EALI
 EXPORTS = ["qgemv_create", "qgemv_run", "qgemv_run_add", "qgemv_pair_run", "qgemv_triple_run",
            "qgemv_run_host", "qgemv_dequantize", "qgemv_destroy", "qgemv_last_error",
            "qgemv_row_bytes", "qgemv_plan_info", "qgemv_describe", "qgemv_device_status",
-           "qgemv_run_noalloc"]
+           "qgemv_run_noalloc", "qgemv_pair_swiglu_run"]
 
 
 class QgOpts(ctypes.Structure):
@@ -84,9 +84,10 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.qgemv_describe.restype = ctypes.c_char_p
     lib.qgemv_run_noalloc.argtypes = [c_int, i64, i64, vp, vp, ctypes.c_float, vp, i64, vp, c_int,
                                       vp]
+    lib.qgemv_pair_swiglu_run.argtypes = [vp, vp, vp, i64, vp, c_int, vp]
     for name in ("qgemv_create", "qgemv_run", "qgemv_run_add", "qgemv_pair_run",
                  "qgemv_triple_run", "qgemv_run_host", "qgemv_dequantize", "qgemv_plan_info",
-                 "qgemv_device_status", "qgemv_run_noalloc"):
+                 "qgemv_device_status", "qgemv_run_noalloc", "qgemv_pair_swiglu_run"):
         getattr(lib, name).restype = c_int
     _lib = lib
     return lib
@@ -140,6 +141,11 @@ def qgemv_pair_run(a, b, x_ptr, N, ya, yb, ydt, stream):
 def qgemv_triple_run(a, b, c, x_ptr, N, ya, yb, yc, ydt, stream):
     _check(load().qgemv_triple_run(a, b, c, x_ptr, N, ya, yb, yc, ydt, stream),
            "qgemv_triple_run")
+
+
+def qgemv_pair_swiglu_run(gate, up, x_ptr, N, h_ptr, hdt, stream):
+    _check(load().qgemv_pair_swiglu_run(gate, up, x_ptr, N, h_ptr, hdt, stream),
+           "qgemv_pair_swiglu_run")
 
 
 def qgemv_run_host(h, x_host_ptr, N, y_host_ptr, ydt, stream):
@@ -257,3 +263,12 @@ def triple_run(a: QGemv, b: QGemv, c: QGemv, x, out_f32: bool = False, stream=No
     qgemv_triple_run(a.h, b.h, c.h, x.data_ptr(), N, ya.data_ptr(), yb.data_ptr(),
                      yc.data_ptr(), OUT_F32 if out_f32 else OUT_F16, _stream_ptr(stream))
     return ya, yb, yc
+
+
+def pair_swiglu_run(gate: QGemv, up: QGemv, x, out_f32: bool = False, stream=None):
+    """h = silu(x . gate^T) * (x . up^T), one launch."""
+    N = x.shape[0]
+    h = gate._y(N, out_f32, None)
+    qgemv_pair_swiglu_run(gate.h, up.h, x.data_ptr(), N, h.data_ptr(),
+                          OUT_F32 if out_f32 else OUT_F16, _stream_ptr(stream))
+    return h

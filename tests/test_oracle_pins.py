@@ -364,3 +364,56 @@ def test_row_bytes_match_block_sizes():
     assert oracle.row_bytes(oracle.Q5_K, 256) == facts["Q5_K"]
     assert oracle.row_bytes(oracle.Q6_K, 9728) == 7980
     assert oracle.row_bytes(oracle.NVFP4, 5120) == 2560
+
+
+# --------------------------------------------------------------- SwiGLU
+# reflex-llm "docs/kernels.md", SwiGLU section: output = silu(gate) x up,
+# silu(x) = x / (1 + exp(-x)).
+
+def test_silu_special_values_and_odd_part_identity():
+    """silu(0) = 0; silu(x) - silu(-x) = x (x*s(x) + x*s(-x) = x, s the
+    logistic); silu -> x for large x and -> 0 for large -x."""
+    assert oracle.silu(0.0) == 0.0
+    for v in np.linspace(-30, 30, 241):
+        d = oracle.silu(v) - oracle.silu(-v)
+        assert abs(d - v) <= 4 * np.finfo(np.float64).eps * max(1.0, abs(v)), v
+    assert oracle.silu(50.0) == 50.0
+    assert abs(oracle.silu(-50.0)) < 1e-19
+    # silu(1) = 1 / (1 + 1/e)
+    assert abs(oracle.silu(1.0) - 1.0 / (1.0 + np.exp(-1.0))) <= 2 ** -52
+
+
+def test_silu_matches_torch_float64():
+    torch = pytest.importorskip("torch")
+    v = np.random.default_rng(5).normal(0.0, 6.0, size=4096)
+    want = torch.nn.functional.silu(torch.from_numpy(v)).numpy()
+    got = np.array([oracle.silu(a) for a in v])
+    assert np.allclose(got, want, rtol=4 * np.finfo(np.float64).eps, atol=1e-300)
+
+
+def test_swiglu_is_silu_of_gate_times_up():
+    """oracle.swiglu against the definition with numpy's exp, elementwise;
+    a planted sign mistake (exp(+v)) keeps the odd-part identity but is
+    caught by the closed form silu(1) = 1 / (1 + 1/e)."""
+    rng = np.random.default_rng(6)
+    g = rng.normal(0, 4, size=(3, 257))
+    u = rng.normal(0, 4, size=(3, 257))
+    h = oracle.swiglu(g, u)
+    want = g / (1.0 + np.exp(-g)) * u
+    assert np.allclose(h, want, rtol=4 * np.finfo(np.float64).eps, atol=0)
+    bad = lambda v: v / (1.0 + np.exp(v))
+    assert abs(bad(1.0) - 1.0 / (1.0 + np.exp(-1.0))) > 0.1
+
+
+def test_qgemv_swiglu_combines_the_two_products():
+    from packers import pack_q4k_block
+    M, K = 3, 256
+    blk = pack_q4k_block(0.25, 0.0, [1] * 8, [0] * 8, np.full(256, 2, dtype=np.int64))
+    wg = np.tile(blk, (M, 1))
+    blk_u = pack_q4k_block(0.5, 0.0, [1] * 8, [0] * 8, np.full(256, 1, dtype=np.int64))
+    wu = np.tile(blk_u, (M, 1))
+    x = np.zeros((1, K), dtype=np.float16)
+    x[0, 0] = 1.0  # g = 0.25 * 2 = 0.5, u = 0.5
+    h, g, mg, u, mu = oracle.qgemv_swiglu(oracle.Q4_K, wg, oracle.Q4_K, wu, M, K, x)
+    assert np.all(g == 0.5) and np.all(u == 0.5)
+    assert np.allclose(h, 0.5 / (1 + np.exp(-0.5)) * 0.5, rtol=1e-15)
