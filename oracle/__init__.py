@@ -22,6 +22,7 @@ Q4_K = 12
 Q5_K = 13
 Q6_K = 14
 NVFP4 = 256
+FP8 = 257
 
 BLOCK_BYTES = {Q4_K: 144, Q5_K: 176, Q6_K: 210}
 
@@ -65,6 +66,8 @@ def _load():
         lib.or_e4m3_to_f64.restype = ctypes.c_double
         lib.or_e2m1_to_f64.argtypes = [ctypes.c_uint8]
         lib.or_e2m1_to_f64.restype = ctypes.c_double
+        lib.or_bf16_to_f64.argtypes = [ctypes.c_uint16]
+        lib.or_bf16_to_f64.restype = ctypes.c_double
         lib.or_row_bytes.argtypes = [i32, i64]
         lib.or_row_bytes.restype = i64
         lib.or_unpack_scale_min.argtypes = [vp, i32, vp, vp]
@@ -90,6 +93,12 @@ def _u8(a):
     return np.ascontiguousarray(a, dtype=np.uint8)
 
 
+def _bytes(a):
+    """The raw bytes of an array (FP8 bf16 scales may come as uint16 bits)."""
+    a = np.ascontiguousarray(a)
+    return a.view(np.uint8) if a.dtype.itemsize > 1 else a.astype(np.uint8, copy=False)
+
+
 def _f16bits(a):
     a = np.ascontiguousarray(a)
     if a.dtype == np.float16:
@@ -113,6 +122,10 @@ def e2m1_to_f64(code: int) -> float:
     return _load().or_e2m1_to_f64(code)
 
 
+def bf16_to_f64(bits: int) -> float:
+    return _load().or_bf16_to_f64(bits)
+
+
 def unpack_scale_min(scales12, s: int):
     """(sc, m) of sub-block s from the 12 packed bytes of a Q4_K/Q5_K block."""
     b = _u8(scales12)
@@ -126,7 +139,7 @@ def dequantize(qtype: int, w, M: int, K: int, scales=None, global_scale: float =
                rows=None) -> np.ndarray:
     """Decode W (packed bytes, row-major) to float32 [len(rows) or M][K]."""
     w = _u8(w)
-    sc = None if scales is None else _u8(scales)
+    sc = None if scales is None else _bytes(scales)
     if rows is None:
         nrows, rptr, ra = M, None, None
     else:
@@ -144,7 +157,7 @@ def qgemv(qtype: int, w, M: int, K: int, x, scales=None, global_scale: float = 1
           residual=None, rows=None):
     """The whole path on selected rows: y, mag (float64 [N][len(rows)])."""
     w = _u8(w)
-    sc = None if scales is None else _u8(scales)
+    sc = None if scales is None else _bytes(scales)
     xb = _f16bits(x).reshape(-1, K)
     N = xb.shape[0]
     if rows is None:

@@ -111,6 +111,23 @@ static uint16_t rd16(const uint8_t *p)
 /* Row sizes.                                                               */
 /* ------------------------------------------------------------------------ */
 
+/* bfloat16: 1 sign, 8 exponent (bias 127), 7 mantissa bits -- the upper half
+ * of an IEEE-754 binary32. */
+double or_bf16_to_f64(uint16_t b)
+{
+    int sign = (b >> 15) & 1;
+    int e = (b >> 7) & 0xff;
+    int f = b & 0x7f;
+    double v;
+    if (e == 0)
+        v = ldexp((double)f, -133);             /* subnormal: f * 2^-7 * 2^-126 */
+    else if (e == 255)
+        v = f ? NAN : INFINITY;
+    else
+        v = ldexp((double)(128 + f), e - 134);  /* (1 + f/128) * 2^(e-127) */
+    return sign ? -v : v;
+}
+
 int64_t or_block_bytes(int type)
 {
     switch (type) {
@@ -125,6 +142,8 @@ int64_t or_row_bytes(int type, int64_t K)
 {
     if (type == OR_NVFP4)
         return K / 2;           /* packed e2m1 codes; scales are separate */
+    if (type == OR_FP8)
+        return K;               /* one e4m3 code per weight; scales are separate */
     int64_t bb = or_block_bytes(type);
     if (bb < 0 || K % 256 != 0)
         return -1;
@@ -246,6 +265,20 @@ static void dequant_row_nvfp4(const uint8_t *codes, const uint8_t *scales,
     }
 }
 
+/* FP8 block-scaled (TandemLLM "Kernels", FP8 matrix products: e4m3 codes
+ * with one BF16 scale per 128 x 128 block).  Reading: codes uint8[M][K]
+ * row-major; scales bf16[ceil(M/128)][K/128] row-major; the weight of
+ * (m, k) is e4m3(code) * bf16(scale[m / 128][k / 128]).  The product needs
+ * 4 + 8 significant bits, so it is exact in float64 and in float32. */
+static void dequant_row_fp8(const uint8_t *codes, const uint16_t *scale_row, int64_t K,
+                            float *out)
+{
+    for (int64_t k = 0; k < K; ++k) {
+        double v = or_e4m3_to_f64(codes[k]) * or_bf16_to_f64(scale_row[k / 128]);
+        out[k] = to_f32_canonical(v);
+    }
+}
+
 /* ------------------------------------------------------------------------ */
 /* Public dequantization entry points.                                      */
 /* ------------------------------------------------------------------------ */
@@ -259,6 +292,8 @@ int or_dequant_rows(int type, const uint8_t *w, const uint8_t *scales, float g,
         return -1;
     if (type == OR_NVFP4 && (K % 16 != 0 || scales == NULL))
         return -1;
+    if (type == OR_FP8 && (K % 128 != 0 || scales == NULL))
+        return -1;
     for (int64_t i = 0; i < nrows; ++i) {
         int64_t r = rows ? rows[i] : i;
         if (r < 0 || r >= M)
@@ -267,6 +302,10 @@ int or_dequant_rows(int type, const uint8_t *w, const uint8_t *scales, float g,
         float *dst = out + i * K;
         if (type == OR_NVFP4) {
             dequant_row_nvfp4(row, scales + r * (K / 16), g, K, dst);
+            continue;
+        }
+        if (type == OR_FP8) {
+            dequant_row_fp8(row, (const uint16_t *)scales + (r / 128) * (K / 128), K, dst);
             continue;
         }
         for (int64_t b = 0; b < K / 256; ++b) {

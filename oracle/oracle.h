@@ -13,11 +13,12 @@ extern "C" {
 #endif
 
 /* Format ids (the K-quant numbers follow GGML's type enumeration). */
-enum { OR_Q4_K = 12, OR_Q5_K = 13, OR_Q6_K = 14, OR_NVFP4 = 256 };
+enum { OR_Q4_K = 12, OR_Q5_K = 13, OR_Q6_K = 14, OR_NVFP4 = 256, OR_FP8 = 257 };
 
 double or_f16_to_f64(uint16_t h);
 double or_e4m3_to_f64(uint8_t c);
 double or_e2m1_to_f64(uint8_t c);
+double or_bf16_to_f64(uint16_t b);
 
 int64_t or_block_bytes(int type);
 int64_t or_row_bytes(int type, int64_t K);

@@ -11,6 +11,10 @@ Field distributions (the workloads of the skinny GEMV study):
   * NVFP4: e2m1 code bytes uniform (all 16 codes), e4m3 group scales uniform
     over the 81 codes whose values lie in [2^-6, 16], one fp32 per-tensor
     scale uniform in [0.5, 1).
+  * FP8 (block-scaled e4m3, one bf16 scale per 128 x 128 block): codes
+    uniform over the 254 finite e4m3 codes (0x7F and 0xFF, the NaNs,
+    excluded); scales bf16(2^u) with u uniform in [-10, -6] (the size of a
+    block maximum over 448 for weights of a few hundredths).
   * x and residual: fp16 N(0, 1), rounded to nearest.
 
 Every tensor has its own stream: numpy's SeedSequence keyed by
@@ -25,9 +29,10 @@ Q4_K = 12
 Q5_K = 13
 Q6_K = 14
 NVFP4 = 256
+FP8 = 257
 
 BLOCK_BYTES = {Q4_K: 144, Q5_K: 176, Q6_K: 210}
-TYPE_NAMES = {Q4_K: "Q4_K", Q5_K: "Q5_K", Q6_K: "Q6_K", NVFP4: "NVFP4"}
+TYPE_NAMES = {Q4_K: "Q4_K", Q5_K: "Q5_K", Q6_K: "Q6_K", NVFP4: "NVFP4", FP8: "FP8"}
 
 # e4m3 codes 0x08 (2^-6, the smallest normal) .. 0x58 (16): 81 codes.
 E4M3_CODE_LO = 0x08
@@ -41,6 +46,8 @@ def _rng(seed: int, stream: int) -> np.random.Generator:
 def row_bytes(qtype: int, K: int) -> int:
     if qtype == NVFP4:
         return K // 2
+    if qtype == FP8:
+        return K
     return (K // 256) * BLOCK_BYTES[qtype]
 
 
@@ -91,6 +98,23 @@ def nvfp4_weights(M: int, K: int, seed: int = 0, stream: int = 0):
     return codes, scales, g
 
 
+def _bf16_bits(v: np.ndarray) -> np.ndarray:
+    """float32 values -> bf16 bits, round to nearest even (finite inputs)."""
+    u = np.ascontiguousarray(v, dtype=np.float32).view(np.uint32).astype(np.uint64)
+    u = (u + 0x7FFF + ((u >> 16) & 1)) >> 16
+    return u.astype(np.uint16)
+
+
+def fp8_weights(M: int, K: int, seed: int = 0, stream: int = 0):
+    """(codes uint8 [M][K], bf16 scales as uint16 bits [ceil(M/128)][K/128], 1.0)."""
+    rng = _rng(seed, stream)
+    finite = np.array([c for c in range(256) if (c & 0x7F) != 0x7F], dtype=np.uint8)
+    codes = finite[rng.integers(0, finite.size, size=(M, K))]
+    u = rng.uniform(-10.0, -6.0, size=((M + 127) // 128, K // 128))
+    scales = _bf16_bits(np.exp2(u).astype(np.float32))
+    return codes, scales, 1.0
+
+
 def weights(qtype: int, M: int, K: int, seed: int = 0, stream: int = 0):
     """(packed bytes, scales or None, global scale) for any supported type."""
     if qtype == Q4_K:
@@ -101,6 +125,8 @@ def weights(qtype: int, M: int, K: int, seed: int = 0, stream: int = 0):
         return q6k_weights(M, K, seed, stream), None, 1.0
     if qtype == NVFP4:
         return nvfp4_weights(M, K, seed, stream)
+    if qtype == FP8:
+        return fp8_weights(M, K, seed, stream)
     raise ValueError(f"unknown type {qtype}")
 
 
@@ -138,6 +164,13 @@ def device_weights(qtype: int, M: int, K: int, seed: int, stream: int, device="c
     scales uint8 [M][K/16] or None, global scale)."""
     import torch
     gen = _torch_gen(seed, stream, device)
+    if qtype == FP8:
+        codes = torch.randint(0, 254, (M, K), generator=gen, device=device, dtype=torch.int16)
+        # 0..253 -> the 254 finite codes (skip 0x7F)
+        codes = torch.where(codes >= 0x7F, codes + 1, codes).to(torch.uint8)
+        u = torch.rand(((M + 127) // 128, K // 128), generator=gen, device=device) * 4.0 - 10.0
+        scales = torch.exp2(u).to(torch.bfloat16).view(torch.int16).view(torch.uint8)
+        return codes, scales.reshape((M + 127) // 128, 2 * (K // 128)), 1.0
     if qtype == NVFP4:
         codes = torch.randint(0, 256, (M, K // 2), generator=gen, device=device,
                               dtype=torch.uint8)

@@ -12,6 +12,8 @@ every field's bit position.  Layout readings (GGML K-quant super-blocks of
                 64c+32+l bit 2c+1 of qh[l].
   Q6_K (210 B): ql[128] @0, qh[64] @128, int8 scales[16] @192, d @208.
   NVFP4:        element 2i in the low nibble of byte i, 2i+1 in the high one.
+  FP8:          e4m3 codes [M][K], bf16 scales [ceil(M/128)][K/128] (one per
+                128 x 128 block), weight = e4m3 * scale.
 """
 from __future__ import annotations
 
@@ -92,3 +94,23 @@ def pack_nvfp4_row(codes) -> np.ndarray:
     codes = np.asarray(codes, dtype=np.int64)
     assert codes.size % 2 == 0 and codes.min() >= 0 and codes.max() < 16
     return (codes[0::2] | (codes[1::2] << 4)).astype(np.uint8)
+
+
+def e4m3_code(v: float) -> int:
+    """The e4m3 ("fn": bias 7, no infinities) code of a value it represents
+    exactly, by search over the finite codes written from the definition."""
+    for c in range(256):
+        if (c & 0x7F) == 0x7F:
+            continue
+        s, e, m = c >> 7, (c >> 3) & 15, c & 7
+        val = (m / 8.0) * 2.0 ** -6 if e == 0 else (1 + m / 8.0) * 2.0 ** (e - 7)
+        if (-val if s else val) == v and not (v == 0 and s):
+            return c
+    raise ValueError(f"{v} is not an e4m3 value")
+
+
+def bf16_bits(v: float) -> int:
+    """bf16 bits of a value whose float32 form has a zero low half."""
+    b = int(np.array([v], dtype=np.float32).view(np.uint32)[0])
+    assert b & 0xFFFF == 0, v
+    return b >> 16

@@ -417,3 +417,66 @@ def test_qgemv_swiglu_combines_the_two_products():
     h, g, mg, u, mu = oracle.qgemv_swiglu(oracle.Q4_K, wg, oracle.Q4_K, wu, M, K, x)
     assert np.all(g == 0.5) and np.all(u == 0.5)
     assert np.allclose(h, 0.5 / (1 + np.exp(-0.5)) * 0.5, rtol=1e-15)
+
+
+# --------------------------------------------------------- FP8 block-scaled
+# TandemLLM "Kernels", FP8 matrix products: e4m3 codes with one BF16 scale
+# per 128 by 128 block.
+
+def test_bf16_decode_matches_numpy_and_torch_all_codes():
+    torch = pytest.importorskip("torch")
+    codes = np.arange(65536, dtype=np.uint32)
+    want = (codes << 16).astype(np.uint32).view(np.float32).astype(np.float64)
+    got = np.array([oracle.bf16_to_f64(int(c)) for c in codes])
+    fin = np.isfinite(want)
+    assert np.array_equal(got[fin], want[fin])
+    assert np.all(np.isnan(got[np.isnan(want)]))
+    t = torch.from_numpy(codes.astype(np.int32).astype(np.int16)).view(torch.bfloat16)
+    assert np.array_equal(got[fin], t.double().numpy()[fin])
+
+
+def test_fp8_closed_form_blocks_and_scale_indexing():
+    """Rows 0..129 (two row blocks) x K = 512 (four k blocks), every weight a
+    known e4m3 value times its block's scale; the scale of (m, k) is
+    scales[m // 128][k // 128] (a planted transpose of the block index fails)."""
+    from packers import bf16_bits, e4m3_code
+    M, K = 130, 512
+    vals = [0.0, 1.0, -2.0, 448.0, -448.0, 2.0 ** -9, 0.875, 13.0, -0.015625, 240.0]
+    rng = np.random.default_rng(7)
+    V = np.array(vals)[rng.integers(0, len(vals), size=(M, K))]
+    codes = np.vectorize(e4m3_code)(V).astype(np.uint8)
+    svals = np.array([[0.25, 3.0, -1.5, 2.0 ** -12], [8.0, 0.125, 1.0, -4.0]])
+    scales = np.vectorize(bf16_bits)(svals.astype(np.float32)).astype(np.uint16)
+    W = oracle.dequantize(oracle.FP8, codes, M, K, scales=scales)
+    expect = V * svals[np.arange(M)[:, None] // 128, np.arange(K)[None, :] // 128]
+    assert np.array_equal(W.astype(np.float64), expect)
+    wrong = V * svals.T[np.arange(K)[None, :] // 128 % 2, np.arange(M)[:, None] // 128 * 0]
+    assert not np.array_equal(W.astype(np.float64), wrong)
+
+
+def test_fp8_generator_has_no_nan_codes():
+    from skinny_gemm_q4_gb300 import synth
+    codes, scales, g = synth.fp8_weights(256, 1024, seed=3)
+    assert codes.shape == (256, 1024) and scales.shape == (2, 8) and g == 1.0
+    assert not np.any((codes & 0x7F) == 0x7F)
+    assert len(np.unique(codes)) == 254
+    W = oracle.dequantize(oracle.FP8, codes, 256, 1024, scales=scales)
+    assert np.isfinite(W).all()
+
+
+@pytest.mark.parametrize("qtype", [oracle.FP8])
+def test_fp8_one_hot_and_torch_matmul(qtype):
+    import torch
+    M, K = 130, 256
+    w, sc, g = _rand_matrix(qtype, M, K, seed=1)
+    W = oracle.dequantize(qtype, w, M, K, scales=sc, global_scale=g)
+    x = np.eye(K, dtype=np.float16) * np.float16(0.5)
+    y, _ = oracle.qgemv(qtype, w, M, K, x, scales=sc, global_scale=g)
+    assert np.array_equal(y, 0.5 * W.T.astype(np.float64))
+    from skinny_gemm_q4_gb300 import synth
+    x = synth.activations(5, K, seed=2)
+    y, mag = oracle.qgemv(qtype, w, M, K, x, scales=sc, global_scale=g)
+    ref = torch.from_numpy(x.astype(np.float64)) @ torch.from_numpy(W.astype(np.float64)).T
+    aref = torch.from_numpy(np.abs(x.astype(np.float64))) @ \
+        torch.from_numpy(np.abs(W.astype(np.float64))).T
+    assert np.allclose(y, ref.numpy(), rtol=0, atol=1e-12 * aref.numpy().max())
