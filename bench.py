@@ -659,11 +659,39 @@ def run_configs(args, torch, qg, synth, layers, side, e0, e1, peak, tpeak, dev):
                        "frac_of_8TBps": d["frac_of_8TBps"]}
     out["c4_nvfp4_set"] = nv
     bad = sum(1 for h in hs4 if h.device_status() != 0)
+    del hs4
+    torch.cuda.empty_cache()
+
+    # FP8 block-scaled W8A16 (e4m3 + one bf16 scale per 128 x 128 block) on
+    # the same three shapes: 8 copies (2.6 GB, > 4x L2).
+    fsets = 8
+    hs8 = []
+    f_bytes = 0
+    for M, K in synth.NVFP4_SHAPES:
+        f_bytes += M * K + ((M + 127) // 128) * (K // 128) * 2
+    for c in range(fsets):
+        for j, (M, K) in enumerate(synth.NVFP4_SHAPES):
+            w, sc, g = synth.device_weights(synth.FP8, M, K, seed=0, stream=80000 + 3 * c + j,
+                                            device=dev)
+            hs8.append(qg.QGemv(synth.FP8, M, K, w, sc, g, max_tokens=32))
+    f8 = {"copies": fsets, "bytes_per_pass": fsets * f_bytes,
+          "shapes": "27648x5120, 5120x27648, 7168x5120"}
+    for n in synth.NVFP4_N:
+        us = _graph_us(torch, side, len(hs8), lambda i, s, n=n: qg.qgemv_run(
+            hs8[i].h, xs4[hs8[i].K].data_ptr(), n, ys4[hs8[i].M].data_ptr(), qg.OUT_F16, s),
+            e0, e1)
+        total_us = us * len(hs8)
+        d = _bw(fsets * f_bytes, total_us, peak)
+        f8[f"N{n}"] = {"us_per_pass": round(total_us, 1), "GBps": d["GBps"],
+                       "frac_of_measured": d["frac_of_measured"],
+                       "frac_of_8TBps": d["frac_of_8TBps"]}
+    out["fp8_w8a16_set"] = f8
+    bad += sum(1 for h in hs8 if h.device_status() != 0)
     bad += sum(1 for hs in layers for h in hs.values() if h.device_status() != 0)
     if bad:
         print(json.dumps({"error": f"{bad} handles report a device timeout (configs)"}))
         sys.exit(3)
-    del hs4
+    del hs8
     torch.cuda.empty_cache()
     return out
 

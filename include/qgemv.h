@@ -28,6 +28,8 @@
  *   Q6_K, 210 B: ql[128], qh[64], int8 scales[16], fp16 d.
  *   NVFP4: codes uint8[M][K/2] (element 2i low nibble of byte i), e4m3
  *         scales uint8[M][K/16], fp32 global scale.
+ *   FP8:  e4m3 codes uint8[M][K] (one per weight), bf16 scales
+ *         [ceil(M/128)][K/128] row-major; w = e4m3 * scale[m/128][k/128].
  * A row of a K-quant matrix is K/256 consecutive blocks; rows are contiguous.
  */
 #ifndef QGEMV_H
@@ -47,7 +49,9 @@ typedef enum {
     QG_Q4_K = 12,
     QG_Q5_K = 13,
     QG_Q6_K = 14,
-    QG_NVFP4_W4A16 = 256
+    QG_NVFP4_W4A16 = 256,
+    QG_FP8_E4M3 = 257  /* block-scaled e4m3, one bf16 scale per 128 x 128 block
+                          (TandemLLM "Kernels", FP8 matrix products); id ours */
 } qg_type;
 
 typedef enum {
@@ -105,7 +109,9 @@ typedef struct qg_handle qg_handle;
  *                Q6_K matrix the 210-byte blocks are not aligned; they are
  *                staged through 16-byte aligned supersets and no byte outside
  *                the matrix is read.)
- *   scales_dev   NVFP4 only: e4m3 scales [M][K/16], 16-byte aligned; else NULL
+ *   scales_dev   NVFP4: e4m3 scales [M][K/16]; FP8: bf16 block scales
+ *                [ceil(M/128)][K/128] (K up to 57,344); 16-byte aligned; else
+ *                NULL
  *   global_scale NVFP4 only: per-tensor fp32 scale; ignored otherwise
  *   opts         nullable
  * Ownership: w_dev and scales_dev are borrowed and must outlive the handle and

@@ -87,18 +87,22 @@ int block_bytes(qg_type t)
     case QG_Q4_K: return 144;
     case QG_Q5_K: return 176;
     case QG_Q6_K: return 210;
+    case QG_FP8_E4M3: return 256;  // codes of one 256-wide super-block of a row
     default: return 0;
     }
 }
 
 bool type_known(int t)
 {
-    return t == QG_Q4_K || t == QG_Q5_K || t == QG_Q6_K || t == QG_NVFP4_W4A16;
+    return t == QG_Q4_K || t == QG_Q5_K || t == QG_Q6_K || t == QG_NVFP4_W4A16 ||
+           t == QG_FP8_E4M3;
 }
 
 int layout_of(qg_type t)
 {
-    return t == QG_Q6_K ? XL_Q6 : (t == QG_NVFP4_W4A16 ? XL_FP4 : XL_Q4);
+    if (t == QG_Q6_K) return XL_Q6;
+    if (t == QG_NVFP4_W4A16 || t == QG_FP8_E4M3) return XL_FP4;  // x in natural 16-byte units
+    return XL_Q4;
 }
 
 int tset_bit(qg_type t)
@@ -107,6 +111,7 @@ int tset_bit(qg_type t)
     case QG_Q4_K: return TS_Q4K;
     case QG_Q5_K: return TS_Q5K;
     case QG_Q6_K: return TS_Q6K;
+    case QG_FP8_E4M3: return TS_FP8;
     default: return TS_FP4;
     }
 }
@@ -165,6 +170,7 @@ cudaError_t launch_gemv_tset(int tset, const Params &p, dim3 grid, int smem, cud
     case TS_Q5K: return launch_gemv_q5k(p, grid, smem, s);
     case TS_Q6K: return launch_gemv_q6k(p, grid, smem, s);
     case TS_FP4: return launch_gemv_fp4(p, grid, smem, s);
+    case TS_FP8: return launch_gemv_fp8(p, grid, smem, s);
     case TS_Q4K | TS_Q6K: return launch_gemv_q4k_q6k(p, grid, smem, s);
     default: return cudaErrorInvalidValue;
     }
@@ -196,7 +202,7 @@ Mat mat_of(const qg_handle *h, void *y, const __half *res)
 bool tset_supported(int tset)
 {
     return tset == TS_Q4K || tset == TS_Q5K || tset == TS_Q6K || tset == TS_FP4 ||
-           tset == (TS_Q4K | TS_Q6K);
+           tset == TS_FP8 || tset == (TS_Q4K | TS_Q6K);
 }
 
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn()
@@ -221,7 +227,7 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn()
 // `bb` bytes (viewed as 8-byte elements): dims (bytes of a block, row, block),
 // box (bb, box_rows, box_blocks), so a copy lands as [block][row][bytes].
 bool encode_blocks(CUtensorMap *m, const void *base, int64_t row_bytes, int64_t rows, int bb,
-                   int box_rows, int box_blocks)
+                   int box_rows, int box_blocks, bool swizzle128 = false)
 {
     PFN_cuTensorMapEncodeTiled_v12000 fn = encode_fn();
     if (!fn) return false;
@@ -230,7 +236,8 @@ bool encode_blocks(CUtensorMap *m, const void *base, int64_t row_bytes, int64_t 
     cuuint32_t box[3] = {(cuuint32_t)(bb / 8), (cuuint32_t)box_rows, (cuuint32_t)box_blocks};
     cuuint32_t estr[3] = {1, 1, 1};
     return fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT64, 3, const_cast<void *>(base), dims, strides, box,
-              estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+              estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+              swizzle128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
@@ -251,15 +258,15 @@ bool encode_staged(CUtensorMap *m, const void *base, int nb, int64_t rows, int b
               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-int sk_tset_smem(int wbytes, int G, bool q6, int *stages)
+int sk_tset_smem(int wbytes, int G, bool q6, int *stages, bool fp8 = false)
 {
     int st = kSkStagesMax;
     // Two CTAs per SM where the ring allows it; Q6_K (weights two stages
     // ahead, by cp.async from the consumers) needs at least three slots.
-    while (st > 2 && sk_smem_bytes(wbytes, G, st) > 110 * 1024) --st;
+    while (st > 2 && sk_smem_bytes(wbytes, G, st, fp8) > 110 * 1024) --st;
     if (q6 && st < 3) st = 3;
     *stages = st;
-    return sk_smem_bytes(wbytes, G, st);
+    return sk_smem_bytes(wbytes, G, st, fp8);
 }
 
 // qg_sk_kernel with x staged inside (p.xin): ring of weights only, then this
@@ -272,14 +279,14 @@ bool sk_xin_ok(int64_t n, int nb, int kw)
     const int64_t nsb = (nb + kw - 1) / kw;  // super-blocks of the largest rank
     return n <= 8 && n * nsb <= 32 && nsb * 8 * groups_for(n) * kXTok <= kSkXinMax;
 }
-int sk_xin_smem(int wbytes, int G, bool q6, int nb, int ks, int *stages)
+int sk_xin_smem(int wbytes, int G, bool q6, int nb, int ks, int *stages, bool fp8 = false)
 {
     const int xreg = ((nb + ks - 1) / ks) * 8 * G * kXTok;
     if (xreg > kSkXinMax) return 0;
     const int red = kSkCons * 32 * G * 4 * 4;
     auto total = [&](int st) {
-        const int body = st * wbytes + xreg;
-        return 128 + (body > red ? body : red);
+        const int body = st * sk_slot_bytes(fp8, 0, wbytes) + xreg;
+        return (fp8 ? kFp8RingOffset : 128) + (body > red ? body : red);
     };
     int st = kSkStagesMax;
     while (st > 2 && total(st) > 110 * 1024) --st;
@@ -295,6 +302,7 @@ cudaError_t launch_sk_tset(int tset, int G, const Params &p, dim3 grid, int smem
     case TS_Q5K: return launch_sk_q5k(G, p, grid, smem, s);
     case TS_Q6K: return launch_sk_q6k(G, p, grid, smem, s);
     case TS_FP4: return launch_sk_fp4(G, p, grid, smem, s);
+    case TS_FP8: return launch_sk_fp8(G, p, grid, smem, s);
     case TS_Q4K | TS_Q6K: return launch_sk_q4k_q6k(G, p, grid, smem, s);
     default: return cudaErrorInvalidValue;
     }
@@ -319,6 +327,7 @@ qg_status run_product_mma(qg_handle *const *hs, int nh, const __half *x, int64_t
 
     int tset = 0;
     for (int i = 0; i < nh; ++i) tset |= tset_bit(hs[i]->type);
+    const bool fp8 = (tset & TS_FP8) != 0;  // FP8 launches hold FP8 matrices only
 
     for (int64_t c0 = 0; c0 < N; c0 += max_tokens) {
         const int n = (int)((N - c0) < max_tokens ? (N - c0) : max_tokens);
@@ -392,9 +401,9 @@ qg_status run_product_mma(qg_handle *const *hs, int nh, const __half *x, int64_t
             }
             const int min_stages = (h0->sms > 0 && tiles > h0->sms) ? 2 : 3;
             while (gemv_stages > min_stages &&
-                   gemv_smem_bytes(sbytes, gemv_stages, n, h0->nb) > 110 * 1024)
+                   gemv_smem_bytes(sbytes, gemv_stages, n, h0->nb, fp8) > 110 * 1024)
                 --gemv_stages;
-            gemv_smem = gemv_smem_bytes(sbytes, gemv_stages, n, h0->nb);
+            gemv_smem = gemv_smem_bytes(sbytes, gemv_stages, n, h0->nb, fp8);
         }
         if (n <= 8 && gemv_smem <= kGemvMaxSmem && gemv_x_fits(n, h0->nb) &&
             !sk_preferred(hs, nh, n)) {
@@ -510,8 +519,8 @@ qg_status run_product_mma(qg_handle *const *hs, int nh, const __half *x, int64_t
                 if (xh[l]) p.xm[l] = xh[l]->xmap[G - 1];
             int stages = 0;
             const int smem = xin ? sk_xin_smem(wbytes, G, q6, h0->nb,
-                                               hs[groups[gidx][0]]->kw, &stages)
-                                 : sk_tset_smem(wbytes, G, q6, &stages);
+                                               hs[groups[gidx][0]]->kw, &stages, fp8)
+                                 : sk_tset_smem(wbytes, G, q6, &stages, fp8);
             p.stages = stages;
             p.xin = xin ? 1 : 0;
             p.x = xc;
@@ -710,6 +719,11 @@ qg_status check_matrix(qg_type t, int64_t M, int64_t K, const void *w_dev, const
         if (!aligned(scales_dev, 16)) return fail(QG_EALIGN, "scales must be 16-byte aligned");
         if (!std::isfinite(global_scale)) return fail(QG_EINVAL, "global scale must be finite");
     }
+    if (t == QG_FP8_E4M3) {
+        if (!scales_dev) return fail(QG_EINVAL, "FP8 needs the bf16 block-scale array");
+        if (!aligned(scales_dev, 16)) return fail(QG_EALIGN, "scales must be 16-byte aligned");
+        if (K > kFp8MaxK) return fail(QG_EUNSUPPORTED, "FP8 supports K up to %d", kFp8MaxK);
+    }
     const int64_t rows_needed = (M + 63) / 64;
     if (rows_needed > 65535) return fail(QG_EUNSUPPORTED, "too many rows for one grid");
     return QG_OK;
@@ -735,7 +749,8 @@ qg_status init_handle(qg_handle *h, qg_type t, int64_t M, int64_t K, const void 
     h->sc = (const uint8_t *)scales_dev;
     h->gscale = (t == QG_NVFP4_W4A16) ? global_scale : 1.0f;
     h->row_bytes = qgemv_row_bytes(t, K);
-    h->sc_row_bytes = (t == QG_NVFP4_W4A16) ? K / 16 : 0;
+    // NVFP4: e4m3 bytes per row; FP8: bf16 bytes per 128-row block
+    h->sc_row_bytes = (t == QG_NVFP4_W4A16) ? K / 16 : (t == QG_FP8_E4M3) ? (K / 128) * 2 : 0;
     h->w_bytes = h->row_bytes * M;
     h->flags = flags;
     h->max_tokens = max_tokens;
@@ -748,7 +763,13 @@ qg_status init_handle(qg_handle *h, qg_type t, int64_t M, int64_t K, const void 
         cudaGetLastError();
         h->sms = 0;
     }
-    if (t != QG_Q6_K) {
+    if (t == QG_FP8_E4M3) {
+        // planes of 128 codes (one bf16 scale block wide), 128-byte swizzle
+        const int R = kGemvRows / h->kw;
+        bool ok = encode_blocks(&h->tmw, w_dev, h->row_bytes, M, 128, R, 2 * h->kw, true);
+        if (ok) ok = encode_blocks(&h->tmw1, w_dev, h->row_bytes, M, 128, kSkRows, 2, true);
+        if (!ok) return fail(QG_ECUDA, "tensor map encoding failed");
+    } else if (t != QG_Q6_K) {
         const int bb = (t == QG_NVFP4_W4A16) ? 128 : block_bytes(t);
         const int R = kGemvRows / h->kw;
         bool ok = encode_blocks(&h->tmw, w_dev, h->row_bytes, M, bb, R, h->kw);
@@ -824,6 +845,7 @@ int64_t qgemv_row_bytes(qg_type t, int64_t K)
 {
     if (!type_known(t) || K < 256 || K % 256 != 0) return -1;
     if (t == QG_NVFP4_W4A16) return K / 2;
+    if (t == QG_FP8_E4M3) return K;
     return (K / 256) * block_bytes(t);
 }
 
@@ -834,7 +856,7 @@ const char *qgemv_describe(void)
     static thread_local std::string d;
     const char *fi = getenv("QGEMV_FAULT_INJECT");
     d = std::string("qgemv: GB300 (sm_103a) fused 4-bit GEMV; formats Q4_K=12 Q5_K=13 Q6_K=14 "
-                    "NVFP4_W4A16=256; flags FORCE_REFERENCE=1 DEBUG_SYNC=2 NO_FALLBACK=4 "
+                    "NVFP4_W4A16=256 FP8_E4M3=257; flags FORCE_REFERENCE=1 DEBUG_SYNC=2 NO_FALLBACK=4 "
                     "MMA_SYNC_PREFILL=8; ") +
         "env QGEMV_FORCE_REFERENCE=" + (env_on("QGEMV_FORCE_REFERENCE") ? "1" : "0") +
         " QGEMV_DEBUG_SYNC=" + (env_on("QGEMV_DEBUG_SYNC") ? "1" : "0") +

@@ -7,6 +7,7 @@
 // thread mapping and turns every decoded A element into the weight the
 // product would return for a one-hot x = e_k, with the product's own
 // rounding steps:
+//   FP8          w = scale * A             (A = e4m3, exact in fp16)
 //   Q4_K / Q5_K  w = fma(-dmin * 2^24, m * 2^-24, (d * 2^22) * A)
 //                (A = sc * q * 2^-22; one rounding, as the product's fold)
 //   Q6_K         w = d * (sc * A)          (A = q - 32; both products exact)
@@ -25,7 +26,7 @@ namespace qg {
 namespace {
 
 constexpr int kDqWarps = 4;
-constexpr int kDqPitch = 224;  // bytes per row in shared memory (>= 210, 16-byte multiple)
+constexpr int kDqPitch = 272;  // bytes per row in shared memory (>= 256, 16-byte multiple)
 
 __device__ __forceinline__ float h_lo(uint32_t v)
 {
@@ -110,6 +111,32 @@ __device__ void dq_tile(const Mat &m, int K, int row0, int sb, uint32_t base, fl
                 }
             }
         }
+    } else if (T == T_FP8) {
+        // compute_fp8's mapping, without the swizzle (rows copied plainly):
+        // thread t, scale block c, word j -> elements 128c + 32t + 4j .. + 3
+#pragma unroll
+        for (int rr = 0; rr < 2; ++rr) {
+            const int row = row0 + g + 8 * rr;
+            const uint32_t ca = base + (g + 8 * rr) * kDqPitch;
+#pragma unroll
+            for (int c = 0; c < 2; ++c) {
+                float sc = 0.0f;
+                if (row < m.M) {
+                    const uint8_t *sp = m.sc + (int64_t)(row >> 7) * m.sc_row_bytes + 2 * (2 * sb + c);
+                    sc = bf16_to_f32((uint32_t)sp[0] | ((uint32_t)sp[1] << 8));
+                }
+                const uint4 w0 = lds128(ca + 128 * c + 32 * t), w1 = lds128(ca + 128 * c + 32 * t + 16);
+#pragma unroll
+                for (int j = 0; j < 8; ++j) {
+                    uint32_t x01, x23;
+                    fp8_decode(word_of(j < 4 ? w0 : w1, j & 3), x01, x23);
+                    const int el = 128 * c + 32 * t + 4 * j;
+                    const float a[4] = {h_lo(x01), h_hi(x01), h_lo(x23), h_hi(x23)};
+#pragma unroll
+                    for (int b = 0; b < 4; ++b) put(rr, el + b, __fmul_rn(sc, a[b]));
+                }
+            }
+        }
     } else {
 #pragma unroll
         for (int rr = 0; rr < 2; ++rr) {
@@ -148,7 +175,7 @@ __global__ void __launch_bounds__(32 * kDqWarps) qg_dequant_kernel(const Mat m, 
     // Copy the 16 rows' blocks (rows past M: zeros), 2 bytes at a time (Q6_K
     // blocks are 2-byte aligned; the others are read the same way).
     const int bytes = (m.type == T_FP4) ? 144 : (m.type == T_Q6K) ? 210
-                    : (m.type == T_Q5K) ? 176 : 144;
+                    : (m.type == T_Q5K) ? 176 : (m.type == T_FP8) ? 256 : 144;
     for (int v = lane; v < 16 * (bytes / 2); v += 32) {
         const int r = v / (bytes / 2), c = 2 * (v - r * (bytes / 2));
         const int row = row0 + r;
@@ -170,6 +197,7 @@ __global__ void __launch_bounds__(32 * kDqWarps) qg_dequant_kernel(const Mat m, 
     case T_Q4K: dq_tile<T_Q4K>(m, K, row0, sb, base, out); break;
     case T_Q5K: dq_tile<T_Q5K>(m, K, row0, sb, base, out); break;
     case T_Q6K: dq_tile<T_Q6K>(m, K, row0, sb, base, out); break;
+    case T_FP8: dq_tile<T_FP8>(m, K, row0, sb, base, out); break;
     default: dq_tile<T_FP4>(m, K, row0, sb, base, out); break;
     }
 }

@@ -49,8 +49,8 @@
 
 namespace qg {
 
-enum { T_Q4K = 12, T_Q5K = 13, T_Q6K = 14, T_FP4 = 256 };
-enum { TS_Q4K = 1, TS_Q5K = 2, TS_Q6K = 4, TS_FP4 = 8 };
+enum { T_Q4K = 12, T_Q5K = 13, T_Q6K = 14, T_FP4 = 256, T_FP8 = 257 };
+enum { TS_Q4K = 1, TS_Q5K = 2, TS_Q6K = 4, TS_FP4 = 8, TS_FP8 = 16 };
 // Staged-x layouts: B-fragment orders of the mma.sync kernels, and the
 // tensor-core core-matrix layout of qg_tc_kernel (qg_tc.cuh).
 enum { XL_Q4 = 0, XL_Q6 = 1, XL_FP4 = 2, XL_TC4 = 3, XL_COUNT = 4 };
@@ -68,11 +68,11 @@ struct Mat {
     CUtensorMap tmw1;      // the same maps with a box of 128 rows x 1 block (qg_sk_kernel)
     CUtensorMap tms1;
     const uint8_t *w;      // packed weights (codes for NVFP4)
-    const uint8_t *sc;     // NVFP4 e4m3 scales [M][K/16]
+    const uint8_t *sc;     // NVFP4 e4m3 scales [M][K/16]; FP8 bf16 scales [ceil(M/128)][K/128]
     void *y;               // output [N][M]
     const __half *res;     // residual [N][M] or null
     int64_t row_bytes;     // bytes per packed row
-    int64_t sc_row_bytes;  // NVFP4 scale bytes per row
+    int64_t sc_row_bytes;  // NVFP4 scale bytes per row; FP8 per 128-row block
     int64_t w_bytes;       // total packed bytes (Q6_K tail guard)
     int M;
     int type;
@@ -125,6 +125,11 @@ struct Fmt<T_FP4> {
     // row in shared memory: 128 code bytes, 16 scale bytes, 48 bytes of pad
     // (a 192-byte pitch keeps the two rows of an 8-lane phase on disjoint banks)
     static constexpr int BB = 128, RB = 192, VPR = 9, XL = XL_FP4, XV = 32, RBG = 144;
+};
+template <>
+struct Fmt<T_FP8> {
+    // 256 e4m3 codes per super-block and row; staged x in the NVFP4 order
+    static constexpr int BB = 256, RB = 256, VPR = 16, XL = XL_FP4, XV = 32, RBG = 256;
 };
 
 __device__ __forceinline__ uint32_t word_of(const uint4 &v, int i)
@@ -342,6 +347,17 @@ __device__ __forceinline__ void fp4_decode(uint32_t w, uint32_t sc, uint32_t &x0
     x02 = hmul2(e2m1x2_to_h2(w & 0xffu), sc);
     x13 = hmul2(e2m1x2_to_h2((w >> 8) & 0xffu), sc);
 }
+
+// FP8: one 32-bit word of e4m3 codes (elements e0..e3 in bytes 0..3) ->
+// (e0, e1) and (e2, e3) as fp16x2, exact (every e4m3 value is an fp16 value).
+__device__ __forceinline__ void fp8_decode(uint32_t w, uint32_t &x01, uint32_t &x23)
+{
+    x01 = e4m3x2_to_h2(w & 0xffffu);
+    x23 = e4m3x2_to_h2(w >> 16);
+}
+
+// bf16 bits -> fp32 (exact).
+__device__ __forceinline__ float bf16_to_f32(uint32_t b) { return __uint_as_float(b << 16); }
 
 // ---------------------------------------------------------------------------
 // Per-super-block compute, one function per format.  wsl: this warp's first
@@ -591,6 +607,75 @@ __device__ __forceinline__ void compute_fp4(uint32_t cbase, int cp, uint32_t sba
     }
 }
 
+// FP8 block-scaled (TandemLLM "Kernels", FP8 matrix products: e4m3 codes, one
+// bf16 scale per 128 x 128 block).  A super-block is two 128-wide scale
+// blocks c; block c of the warp's rows sits in shared memory as a plane of
+// 128-byte rows written by a tensor copy with 128-byte swizzle (16-byte chunk
+// q of row r at chunk q ^ (r & 7)), plane c at cbase + c * plane.  Thread t
+// owns bytes 32t .. 32t + 31 of each row of a block: MMA step j (0..7) takes
+// its word j, elements 32t + 4j .. + 3, as fragment columns (2t, 2t + 1) and
+// (2t + 8, 2t + 9) -- the staged x (NVFP4 order) gives x in the same order.
+// Per block: eight MMAs in one chain from C = 0, then acc = fma(scale, D, acc),
+// block 0 then block 1.  sc: the two scales as fp32.
+template <int MT, int G, bool ODD>
+__device__ __forceinline__ void compute_fp8(uint32_t cbase, int plane, uint32_t xsl, int xtok,
+                                            int g, int t, int ntok, const float (&sc)[2],
+                                            float (&acc)[MT][G][4])
+{
+    uint32_t xb[G];
+#pragma unroll
+    for (int gi = 0; gi < G; ++gi) xb[gi] = xsl + min(8 * gi + g, ntok - 1) * xtok;
+    float d[2][MT][G][4];
+#pragma unroll
+    for (int c = 0; c < 2; ++c) {
+        uint4 w[MT][2][2];  // [mt][row g / g + 8][chunk 2t / 2t + 1]
+#pragma unroll
+        for (int mt = 0; mt < MT; ++mt)
+#pragma unroll
+            for (int rr = 0; rr < 2; ++rr) {
+                const int r = mt * 16 + g + 8 * rr;
+                const uint32_t ra = cbase + c * plane + r * 128;
+                w[mt][rr][0] = lds128(ra + ((uint32_t)((2 * t) ^ (r & 7)) << 4));
+                w[mt][rr][1] = lds128(ra + ((uint32_t)((2 * t + 1) ^ (r & 7)) << 4));
+            }
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            uint4 B[G];
+#pragma unroll
+            for (int gi = 0; gi < G; ++gi) B[gi] = lds128(xb[gi] + ((c * 4 + q) * 4 + t) * 16);
+#pragma unroll
+            for (int jj = 0; jj < 2; ++jj) {
+                const int j = 2 * q + jj;
+#pragma unroll
+                for (int mt = 0; mt < MT; ++mt) {
+                    uint32_t a0, a1, a2, a3;
+                    fp8_decode(word_of(w[mt][0][j >> 2], j & 3), a0, a2);
+                    fp8_decode(word_of(w[mt][1][j >> 2], j & 3), a1, a3);
+#pragma unroll
+                    for (int gi = 0; gi < G; ++gi) {
+                        const uint32_t b0 = jj ? B[gi].z : B[gi].x, b1 = jj ? B[gi].w : B[gi].y;
+                        if (j == 0)
+                            mma16816_zc(d[c][mt][gi], a0, a1, a2, a3, b0, b1);
+                        else
+                            mma16816(d[c][mt][gi], a0, a1, a2, a3, b0, b1);
+                    }
+                }
+            }
+        }
+    }
+#pragma unroll
+    for (int c = 0; c < 2; ++c)
+#pragma unroll
+        for (int mt = 0; mt < MT; ++mt)
+#pragma unroll
+            for (int gi = 0; gi < G; ++gi)
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    if (!ODD && (e & 1)) continue;
+                    acc[mt][gi][e] = __fmaf_rn(sc[c], d[c][mt][gi][e], acc[mt][gi][e]);
+                }
+}
+
 // Per-CTA accumulator set: K-quants fold into one [MT][G][4]; NVFP4 keeps two
 // chains.  `finish` returns the rank partial sum of element (mt, gi, c).
 template <int T, int MT, int G>
@@ -643,6 +728,13 @@ __device__ __forceinline__ void compute_sb(Acc<T, MT, G> &A, uint32_t wsl, uint3
                     (sb - sb0q) * 210;
             }
         compute_q6k<MT, G, ODD>(wsl, cp, xsl, xtok, g, t, ntok, boff, A.a[0]);
+    } else if (T == T_FP8) {
+        // wsl: the warp's rows in the super-block's first scale-block plane;
+        // cp: the plane stride; fsc: the CTA's row of bf16 scales in shared
+        // memory (two per super-block)
+        const uint32_t sw = lds32(fsc + 4 * sb);
+        const float sc[2] = {bf16_to_f32(sw & 0xffffu), bf16_to_f32(sw >> 16)};
+        compute_fp8<MT, G, ODD>(wsl, cp, xsl, xtok, g, t, ntok, sc, A.a[0]);
     } else {
         compute_fp4<MT, G>(wsl, cp, fsc ? fsc : wsl + 128, fsc ? 16 : cp, xsl, xtok, g, t, ntok,
                            *reinterpret_cast<float(*)[2][MT][G][4]>(&A.a));
@@ -873,6 +965,24 @@ __device__ __forceinline__ void reduce_and_store(const Acc<T, MT, G> &A, float *
                              tok0 + 8 * gi + 2 * t + (c & 1), A.partial(mt, gi, c));
 }
 
+// FP8: the bf16 scales of the CTA's 128-row block (K/128 of them, K/256
+// 32-bit words) into shared memory at dst, by threads tid0.. of `nthr`.
+__device__ __forceinline__ void load_fp8_scales(const Mat &m, int K, int row0, uint32_t *dst,
+                                                int tid, int nthr)
+{
+    const uint32_t *src = reinterpret_cast<const uint32_t *>(m.sc + (int64_t)(row0 >> 7) *
+                                                                         m.sc_row_bytes);
+    for (int i = tid; i < K / 256; i += nthr) dst[i] = __ldg(src + i);
+}
+
+// Shared memory of an FP8 launch: barriers in [0, 64), the scale row in
+// [128, 1024) (K <= 57,344), the weight ring from the first 1024-byte
+// boundary at or after offset 1024 (the 128-byte swizzle of the tensor copies
+// needs 1024-byte aligned slots); the host adds 1024 bytes of slack.
+constexpr int kFp8RingOffset = 2048;  // bytes the ring may start after the base
+constexpr int kFp8MaxK = (1024 - 128) * 64;
+__device__ __forceinline__ uint32_t fp8_ring(uint32_t sbase) { return (sbase + 1024 + 1023) & ~1023u; }
+
 __device__ __forceinline__ int select_mat(const Params &p, int tile)
 {
     int mi = 0;
@@ -926,7 +1036,7 @@ __device__ __forceinline__ void gemv_tile(const Params &p, const Mat &m, int rti
     const uint32_t sbase = smem_u32(smem);
     const uint32_t bar_full = sbase, bar_empty = sbase + 8 * kGemvStagesMax;
     const int slot_bytes = gemv_stage_bytes<T>(kw);
-    const uint32_t slots = sbase + 128;
+    const uint32_t slots = (T == T_FP8) ? fp8_ring(sbase) : sbase + 128;
     const uint32_t xreg = slots + STAGES * slot_bytes;
 
     if (threadIdx.x == 0) {
@@ -955,6 +1065,9 @@ __device__ __forceinline__ void gemv_tile(const Params &p, const Mat &m, int rti
                 if (T == T_FP4) {
                     tma_load_3d_ef(dst, &m.tmw, 0, row0, sbq, fb, wpol);
                     tma_load_3d_ef(dst + kw * R * 128, &m.tms, 0, row0, sbq, fb, wpol);
+                } else if (T == T_FP8) {
+                    // planes of 128 codes: two per super-block
+                    tma_load_3d_ef(dst, &m.tmw, 0, row0, 2 * sbq, fb, wpol);
                 } else {
                     tma_load_3d_ef(dst, &m.tmw, 0, row0, sbq, fb, wpol);
                 }
@@ -1001,6 +1114,10 @@ __device__ __forceinline__ void gemv_tile(const Params &p, const Mat &m, int rti
     unsigned int err = 0;
     if (warp == 0) {
         for (int i = 0; i < STAGES && i < nst; ++i) produce(i, i);
+    } else if (T == T_FP8) {
+        // the block scales, like the weights, need nothing from earlier kernels
+        load_fp8_scales(m, p.K, row0, reinterpret_cast<uint32_t *>(smem + 128), threadIdx.x - 32,
+                        32 * kGemvCW);
     }
 
     // x for the whole K range, staged after the programmatic dependency (x
@@ -1078,6 +1195,7 @@ __device__ __forceinline__ void gemv_tile(const Params &p, const Mat &m, int rti
         uint32_t par = 0;
         const uint32_t wrow = (T == T_Q6K) ? (uint32_t)(16 * mg * q6_pitch(kw))
                             : (T == T_FP4) ? (uint32_t)((ks * R + 16 * mg) * 128)
+                            : (T == T_FP8) ? (uint32_t)((2 * ks * R + 16 * mg) * 128)
                                            : (uint32_t)((ks * R + 16 * mg) * F::BB);
         const uint32_t srow = (uint32_t)(kw * R * 128 + (ks * R + 16 * mg) * 16);
         for (int i = 0; i < nst; ++i) {
@@ -1092,6 +1210,9 @@ __device__ __forceinline__ void gemv_tile(const Params &p, const Mat &m, int rti
                 if (T == T_FP4) {
                     compute_sb<T, 1, 1, ODD>(A, sl + wrow, xsl, p.xtok, g, t, ntok, m, row_w, sb,
                                              ksel, 128, sl + srow);
+                } else if (T == T_FP8) {
+                    compute_sb<T, 1, 1, ODD>(A, sl + wrow, xsl, p.xtok, g, t, ntok, m, row_w, sb,
+                                             ksel, R * 128, sbase + 128);
                 } else if (T == T_Q6K) {
                     compute_sb<T, 1, 1, ODD>(A, sl + wrow, xsl, p.xtok, g, t, ntok, m, row_w, sb,
                                              ksel, q6_pitch(kw), 0u, i * kw);
@@ -1189,16 +1310,19 @@ __global__ void __launch_bounds__(32 * (kGemvCW + 1)) qg_n8_kernel(const __grid_
         if (m.type == T_Q6K) return gemv_tile<T_Q6K, !ONE>(p, m, rtile, smem, role);
     if constexpr ((TSET & TS_FP4) != 0)
         if (m.type == T_FP4) return gemv_tile<T_FP4, !ONE>(p, m, rtile, smem, role);
+    if constexpr ((TSET & TS_FP8) != 0)
+        if (m.type == T_FP8) return gemv_tile<T_FP8, !ONE>(p, m, rtile, smem, role);
 }
 
 // Dynamic shared memory of qg_n8_kernel: barriers, `stages` ring slots of
 // `stage_bytes`, and the x region of N tokens x nb super-blocks.
 __host__ __device__ inline int gemv_xtok(int nb) { return nb * kXTok + ((nb & 1) ? 0 : 64); }
-__host__ __device__ inline int gemv_smem_bytes(int stage_bytes, int stages, int N, int nb)
+__host__ __device__ inline int gemv_smem_bytes(int stage_bytes, int stages, int N, int nb,
+                                               bool fp8 = false)
 {
     const int body = stages * stage_bytes + N * gemv_xtok(nb);
-    const int red = kGemvCW * 4 * 32 * 4;  // slice partials overlay the ring
-    return 128 + (body > red ? body : red);
+    const int red = 2 * kGemvCW * 4 * 32 * 4;  // slice partials (+ SwiGLU exchange) overlay the ring
+    return (fp8 ? kFp8RingOffset : 128) + (body > red ? body : red);
 }
 
 }  // namespace qg
@@ -1224,12 +1348,23 @@ constexpr int kSkStagesMax = 4;
 
 __host__ __device__ inline int sk_wbytes(int type)
 {
-    return kSkRows * (type == T_Q6K ? 224 : type == T_Q5K ? 176 : 144);
+    return kSkRows * (type == T_FP8 ? 256 : type == T_Q6K ? 224 : type == T_Q5K ? 176 : 144);
+}
+// Bytes of one ring slot: the stage's bytes (weights only when x is staged in
+// the kernel), rounded up to 1024 for FP8 (swizzled tensor copies).
+__host__ __device__ inline int sk_slot_bytes(bool fp8, int stage_with_x, int wbytes)
+{
+    const int b = stage_with_x ? stage_with_x : wbytes;
+    return fp8 ? ((b + 1023) & ~1023) : b;
 }
 __host__ __device__ inline int sk_stage_bytes(int wbytes, int G) { return wbytes + 8 * G * kXTok; }
-__host__ __device__ inline int sk_smem_bytes(int wbytes, int G, int stages)
+__host__ __device__ inline int sk_smem_bytes(int wbytes, int G, int stages, bool fp8 = false)
 {
-    const int ring = stages * sk_stage_bytes(wbytes, G);
+    const int ring = stages * sk_slot_bytes(fp8, sk_stage_bytes(wbytes, G), wbytes);
+    if (fp8) {
+        const int red = kSkCons * 32 * G * 4 * 4;
+        return kFp8RingOffset + (ring > red ? ring : red);
+    }
     const int red = kSkCons * 32 * G * 4 * 4;
     return 128 + (ring > red ? ring : red);
 }
@@ -1252,10 +1387,10 @@ __device__ __forceinline__ void sk_tile(const Params &p, const Mat &m, int rtile
     // warps into a region after the ring (no staging launch); otherwise each
     // slot carries the stage's staged x, brought by TMA.
     constexpr bool xin = XIN;
-    const int sbytes = xin ? wbytes : sk_stage_bytes(wbytes, G);
+    const int sbytes = sk_slot_bytes(T == T_FP8, xin ? 0 : wbytes + 8 * G * kXTok, wbytes);
     const uint32_t sbase = smem_u32(smem);
     const uint32_t bar_full = sbase, bar_empty = sbase + 8 * kSkStagesMax;
-    const uint32_t ring = sbase + 128;
+    const uint32_t ring = (T == T_FP8) ? fp8_ring(sbase) : sbase + 128;
     const uint32_t xreg = ring + STAGES * sbytes;
     const uint32_t xbytes = xin ? 0u : (uint32_t)(8 * G * kXTok);
     (void)xreg;
@@ -1286,7 +1421,7 @@ __device__ __forceinline__ void sk_tile(const Params &p, const Mat &m, int rtile
                 const int sb = rank + i * ks;
                 const uint32_t dst = ring + i * sbytes, fb = bar_full + 8 * i;
                 mbar_arrive_expect_tx(fb, (T == T_Q6K ? 0u : (uint32_t)sk_wbytes(T)) + xbytes);
-                if (T != T_Q6K) tma_load_3d(dst, &m.tmw1, 0, row0, sb, fb);
+                if (T != T_Q6K) tma_load_3d(dst, &m.tmw1, 0, row0, T == T_FP8 ? 2 * sb : sb, fb);
                 if (T == T_FP4) tma_load_3d(dst + kSkRows * 128, &m.tms1, 0, row0, sb, fb);
             }
             pdl_wait();
@@ -1304,7 +1439,7 @@ __device__ __forceinline__ void sk_tile(const Params &p, const Mat &m, int rtile
                 const int sb = rank + i * ks;
                 const uint32_t dst = ring + slot * sbytes, fb = bar_full + 8 * slot;
                 mbar_arrive_expect_tx(fb, (T == T_Q6K ? 0u : (uint32_t)sk_wbytes(T)) + xbytes);
-                if (T != T_Q6K) tma_load_3d(dst, &m.tmw1, 0, row0, sb, fb);
+                if (T != T_Q6K) tma_load_3d(dst, &m.tmw1, 0, row0, T == T_FP8 ? 2 * sb : sb, fb);
                 if (T == T_FP4) tma_load_3d(dst + kSkRows * 128, &m.tms1, 0, row0, sb, fb);
                 if (!xin) tma_load_2d(dst + wbytes, &p.xm[F::XL], 72 * sb, tok0, fb);
                 if (++slot == STAGES) {
@@ -1349,6 +1484,9 @@ __device__ __forceinline__ void sk_tile(const Params &p, const Mat &m, int rtile
                 cp_async_commit();
             }
         }
+        if (T == T_FP8)  // the block scales need nothing from earlier kernels either
+            load_fp8_scales(m, p.K, row0, reinterpret_cast<uint32_t *>(smem + 128), threadIdx.x - 32,
+                            kSkCons * 32);
         // The weights need nothing from earlier kernels (their first stages
         // are on their way already); x, the residual and y may.
         pdl_wait();
@@ -1381,6 +1519,7 @@ __device__ __forceinline__ void sk_tile(const Params &p, const Mat &m, int rtile
             }
             bar_sync_named(3, kSkCons * 32);  // the consumer warps only
         }
+        if (T == T_FP8) bar_sync_named(4, kSkCons * 32);  // the consumer warps' scale row
         int slot = 0;
         uint32_t par = 0;
 #pragma unroll 1
@@ -1405,6 +1544,9 @@ __device__ __forceinline__ void sk_tile(const Params &p, const Mat &m, int rtile
             if (T == T_FP4) {
                 compute_sb<T, 1, G>(A, sl + 16 * cw * 128, xsl, kXTok, g, t, ntok, m, row_w, sb, ksel,
                                     128, sl + kSkRows * 128 + 16 * cw * 16);
+            } else if (T == T_FP8) {
+                compute_sb<T, 1, G>(A, sl + 16 * cw * 128, xsl, kXTok, g, t, ntok, m, row_w, sb, ksel,
+                                    kSkRows * 128, sbase + 128);
             } else if (T == T_Q6K) {
                 compute_sb<T, 1, G>(A, sl + 16 * cw * 224, xsl, kXTok, g, t, ntok, m, row_w, sb, ksel,
                                     224, 0u, sb);
@@ -1447,6 +1589,8 @@ __global__ void __launch_bounds__(kSkThreads) qg_sk_kernel(const __grid_constant
         if (m.type == T_Q6K) return sk_tile<T_Q6K, G, XIN>(p, m, rtile, smem, wbytes, role);
     if constexpr ((TSET & TS_FP4) != 0)
         if (m.type == T_FP4) return sk_tile<T_FP4, G, XIN>(p, m, rtile, smem, wbytes, role);
+    if constexpr ((TSET & TS_FP8) != 0)
+        if (m.type == T_FP8) return sk_tile<T_FP8, G, XIN>(p, m, rtile, smem, wbytes, role);
 }
 
 }  // namespace qg

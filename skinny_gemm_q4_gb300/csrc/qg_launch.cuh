@@ -32,6 +32,7 @@ QG_DECLARE_TSET(q4k)
 QG_DECLARE_TSET(q5k)
 QG_DECLARE_TSET(q6k)
 QG_DECLARE_TSET(fp4)
+QG_DECLARE_TSET(fp8)
 QG_DECLARE_TSET(q4k_q6k)
 #undef QG_DECLARE_TSET
 

@@ -37,6 +37,13 @@ __device__ __forceinline__ void scale_min_k4(const uint8_t *s12, int s, int &sc,
 __device__ float ref_weight(const RefMat &m, int row, int k)
 {
     const uint8_t *r = m.w + (int64_t)row * m.row_bytes;
+    if (m.type == T_FP8) {
+        const uint32_t e = e4m3x2_to_h2(r[k]);  // low byte -> low half
+        const float fe = __half2float(__ushort_as_half((unsigned short)(e & 0xffffu)));
+        const uint8_t *sp = m.sc + (int64_t)(row >> 7) * m.sc_row_bytes + 2 * (k >> 7);
+        const uint32_t sb = (uint32_t)sp[0] | ((uint32_t)sp[1] << 8);
+        return __fmul_rn(fe, __uint_as_float(sb << 16));
+    }
     if (m.type == T_FP4) {
         const uint32_t byte = r[k >> 1];
         const uint32_t code = (k & 1) ? (byte >> 4) : (byte & 15u);

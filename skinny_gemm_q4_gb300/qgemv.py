@@ -20,6 +20,7 @@ Q4_K = 12
 Q5_K = 13
 Q6_K = 14
 NVFP4_W4A16 = 256
+FP8_E4M3 = 257
 
 OUT_F16 = 0
 OUT_F32 = 1

@@ -23,7 +23,7 @@ def make_matrix(qtype, M, K, seed=0, stream=None, device="cuda", flags=0):
     t = torch()
     w, sc, g = synth.weights(qtype, M, K, seed=seed, stream=qtype if stream is None else stream)
     wd = t.from_numpy(np.ascontiguousarray(w)).to(device)
-    sd = None if sc is None else t.from_numpy(np.ascontiguousarray(sc)).to(device)
+    sd = None if sc is None else t.from_numpy(np.ascontiguousarray(sc).view(np.uint8)).to(device)
     h = qg.QGemv(qtype, M, K, wd, sd, g, flags=flags)
     return h, w, sc, g
 

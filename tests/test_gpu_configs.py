@@ -11,7 +11,7 @@ from skinny_gemm_q4_gb300 import synth
 pytestmark = pytest.mark.gpu
 
 ORTYPE = {qg.Q4_K: oracle.Q4_K, qg.Q5_K: oracle.Q5_K, qg.Q6_K: oracle.Q6_K,
-          qg.NVFP4_W4A16: oracle.NVFP4}
+          qg.NVFP4_W4A16: oracle.NVFP4, qg.FP8_E4M3: oracle.FP8}
 
 
 @pytest.fixture(scope="module", autouse=True)

@@ -11,9 +11,9 @@ from skinny_gemm_q4_gb300 import synth
 
 pytestmark = pytest.mark.gpu
 
-TYPES = [qg.Q4_K, qg.Q5_K, qg.Q6_K, qg.NVFP4_W4A16]
+TYPES = [qg.Q4_K, qg.Q5_K, qg.Q6_K, qg.NVFP4_W4A16, qg.FP8_E4M3]
 ORTYPE = {qg.Q4_K: oracle.Q4_K, qg.Q5_K: oracle.Q5_K, qg.Q6_K: oracle.Q6_K,
-          qg.NVFP4_W4A16: oracle.NVFP4}
+          qg.NVFP4_W4A16: oracle.NVFP4, qg.FP8_E4M3: oracle.FP8}
 
 
 @pytest.fixture(scope="module", autouse=True)
@@ -45,7 +45,8 @@ def test_dequantize_bit_exact(qtype, M, K, flags):
 # staged inside (Q4_K/Q5_K up to 4096 rows); chunks 16 and 32 -> qg_sk_kernel
 # after the staging launch (2 and 4 column groups).
 ONE_HOT = [(qg.Q4_K, 150, 1024), (qg.Q4_K, 4100, 512), (qg.Q5_K, 96, 768),
-           (qg.Q5_K, 4100, 512), (qg.Q6_K, 150, 1024), (qg.NVFP4_W4A16, 150, 1024)]
+           (qg.Q5_K, 4100, 512), (qg.Q6_K, 150, 1024), (qg.NVFP4_W4A16, 150, 1024),
+           (qg.FP8_E4M3, 150, 1024), (qg.FP8_E4M3, 4100, 512)]
 
 
 @pytest.mark.parametrize("qtype,M,K", ONE_HOT)
@@ -72,7 +73,7 @@ def test_large_magnitude_x(qtype, N):
     range, which the Q4_K/Q5_K min term's sub-block sums must still carry).
     fp32 output within the tolerance; power-of-two scaling stays exact."""
     M = 300
-    K = 5120 if qtype == qg.NVFP4_W4A16 else 2560
+    K = 5120 if qtype in (qg.NVFP4_W4A16, qg.FP8_E4M3) else 2560
     h, w, sc, g = make_matrix(qtype, M, K, seed=11)
     base = synth.activations(N, K, seed=11).astype(np.float32)
     x = base * (2.0 ** (8 + 2 * (np.arange(N) % 3)))[:, None]
@@ -91,7 +92,7 @@ def test_large_magnitude_x(qtype, N):
     # Q4_K/Q5_K min term splits S = 32 hi + lo with hi an fp16 normal there).
     S = np.abs(xs.astype(np.float64).reshape(N, K // 32, 32).sum(-1))
     ok = ((S == 0) | (S >= 2.0 ** -9)).all(axis=1)
-    if qtype in (qg.Q6_K, qg.NVFP4_W4A16):
+    if qtype in (qg.Q6_K, qg.NVFP4_W4A16, qg.FP8_E4M3):
         ok[:] = True
     assert ok.any()
     assert np.array_equal(y256[ok], 256 * y1[ok])
@@ -118,6 +119,7 @@ CASES = [
     (qg.Q5_K, 130, 4096), (qg.Q5_K, 64, 1536),
     (qg.Q6_K, 200, 2560), (qg.Q6_K, 45, 9728),
     (qg.NVFP4_W4A16, 150, 5120), (qg.NVFP4_W4A16, 33, 768),
+    (qg.FP8_E4M3, 150, 5120), (qg.FP8_E4M3, 300, 768), (qg.FP8_E4M3, 33, 2560),
 ]
 
 
@@ -144,7 +146,8 @@ def test_product_matches_oracle(qtype, M, K, N):
                                        (qg.Q6_K, 1024, 2560), (qg.Q6_K, 2560, 9728),
                                        (qg.NVFP4_W4A16, 7168, 5120),
                                        (qg.NVFP4_W4A16, 27648, 5120),
-                                       (qg.NVFP4_W4A16, 5120, 27648)])
+                                       (qg.NVFP4_W4A16, 5120, 27648),
+                                       (qg.FP8_E4M3, 7168, 5120), (qg.FP8_E4M3, 2560, 9728)])
 def test_row_invariance_twins(qtype, M, K):
     """TandemLLM verify-twin rule: an N-row call equals N one-row calls bit
     for bit, N = 2..32, with rows that share inputs."""
@@ -203,9 +206,9 @@ def test_tcgen05_prefill_engine(M, K, N):
     assert h.device_status() == 0 and h2.device_status() == 0
 
 
-@pytest.mark.parametrize("qtype", [qg.Q4_K, qg.Q6_K, qg.NVFP4_W4A16])
+@pytest.mark.parametrize("qtype", [qg.Q4_K, qg.Q6_K, qg.NVFP4_W4A16, qg.FP8_E4M3])
 def test_sign_and_power_of_two_scaling_exact(qtype):
-    M, K = 96, 2560 if qtype != qg.NVFP4_W4A16 else 5120
+    M, K = 96, 2560 if qtype not in (qg.NVFP4_W4A16, qg.FP8_E4M3) else 5120
     h, w, sc, g = make_matrix(qtype, M, K, seed=7)
     x = synth.activations(5, K, seed=7)
     y = h.run(to_dev(x), out_f32=True).cpu().numpy()

@@ -15,7 +15,7 @@ from skinny_gemm_q4_gb300 import synth
 pytestmark = pytest.mark.gpu
 
 ORTYPE = {qg.Q4_K: oracle.Q4_K, qg.Q5_K: oracle.Q5_K, qg.Q6_K: oracle.Q6_K,
-          qg.NVFP4_W4A16: oracle.NVFP4}
+          qg.NVFP4_W4A16: oracle.NVFP4, qg.FP8_E4M3: oracle.FP8}
 
 
 @pytest.fixture(scope="module", autouse=True)
@@ -42,7 +42,7 @@ def _ref(qtype, gate, up, M, K, x, rows):
 # ranks) and every format.
 SHAPES = [(qg.Q4_K, 9728, 2560), (qg.Q4_K, 300, 2560), (qg.Q5_K, 130, 4096),
           (qg.Q6_K, 200, 2560), (qg.NVFP4_W4A16, 150, 5120), (qg.Q4_K, 2000, 256),
-          (qg.Q5_K, 700, 512)]
+          (qg.Q5_K, 700, 512), (qg.FP8_E4M3, 260, 2560)]
 
 
 @pytest.mark.parametrize("qtype,M,K", SHAPES)

@@ -21,7 +21,7 @@ from skinny_gemm_q4_gb300 import synth
 pytestmark = pytest.mark.gpu
 
 ORTYPE = {qg.Q4_K: oracle.Q4_K, qg.Q5_K: oracle.Q5_K, qg.Q6_K: oracle.Q6_K,
-          qg.NVFP4_W4A16: oracle.NVFP4}
+          qg.NVFP4_W4A16: oracle.NVFP4, qg.FP8_E4M3: oracle.FP8}
 
 
 @pytest.fixture(scope="module", autouse=True)
@@ -41,6 +41,7 @@ def _noalloc(h, x, N, y, out_f32):
 
 @pytest.mark.parametrize("qtype,M,K,N", [(qg.Q4_K, 4096, 2560, 20), (qg.Q6_K, 1024, 9728, 40),
                                          (qg.NVFP4_W4A16, 2048, 5120, 9),
+                                         (qg.FP8_E4M3, 1000, 5120, 12),
                                          (qg.Q5_K, 640, 2560, 3), (qg.Q4_K, 9728, 2560, 1),
                                          (qg.Q6_K, 2560, 9728, 1)])
 def test_noalloc_matches_oracle_and_run_on_two_calls_in_a_row(qtype, M, K, N):
