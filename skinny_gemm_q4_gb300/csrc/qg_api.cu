@@ -566,9 +566,39 @@ qg_status run_product_mma(qg_handle *const *hs, int nh, const __half *x, int64_t
     return QG_OK;
 }
 
-// Q4_K handles sharing x, N >= 33, on the tensor core (qg_tc_kernel): x staged
-// once per chunk by qg_stage_tc_kernel, one product launch per group of equal
-// chunk count (cluster size).
+// K slices of a qg_tc_kernel launch: as many CTAs (row tiles x token chunks
+// x slices; one per SM) as fit in one wave on the GB300's 152 SMs, at most 8
+// (a portable cluster) and at most nb.
+constexpr int kNumSMs = 152;
+static int tc_ksplit(int tiles, int zchunks, int nb)
+{
+    const int ctas = tiles * zchunks;
+    int ks = kNumSMs / ctas;
+    if (ks < 1) ks = 1;
+    if (ks > 8) ks = 8;
+    if (ks > nb) ks = nb;
+    return ks;
+}
+
+// Ring depths of qg_tc_kernel: x ring 2..3 slots, weight ring 2..4 slots,
+// within the shared-memory budget (x first: it is the larger copy).
+static bool tc_stages(int T, int G, int *ws, int *xs)
+{
+    for (int x = 3; x >= 2; --x)
+        for (int w = 4; w >= 2; --w)
+            if (tc_smem_bytes(T, G, w, x) <= kTcMaxSmem && (x == 2 || w >= 3)) {
+                *ws = w;
+                *xs = x;
+                return true;
+            }
+    return false;
+}
+
+static bool tc_type(qg_type t) { return t == QG_Q4_K || t == QG_Q5_K || t == QG_Q6_K; }
+
+// K-quant handles sharing x, N >= 33, on the tensor core (qg_tc_kernel): x
+// staged once per chunk by qg_stage_tc_kernel, one product launch per weight
+// format (the matrices of a launch share its K split).
 qg_status run_product_tc(qg_handle *const *hs, int nh, const __half *x, int64_t N,
                          void *const *ys, const __half *res, int out_f32, cudaStream_t s)
 {
@@ -587,16 +617,18 @@ qg_status run_product_tc(qg_handle *const *hs, int nh, const __half *x, int64_t 
         if (fault_at("stage")) return fail(QG_EFAULT_INJECTED, "injected fault: staging launch");
         cudaError_t e = launch_stage_tc4(xc, n, (int)h0->K, nb, chunk_stride, h0->xs, s);
         if (e != cudaSuccess) return cuda_fail(e, "staging kernel launch");
-        const int G = n >= kTcTok ? 8 : (n + 7) / 8;
+        const int nt = n < kTcTok ? n : kTcTok;
+        const int G = 2 * ((nt + 15) / 16);  // MMA N = 8 G, a multiple of 16
+        const int zc = (n + kTcTok - 1) / kTcTok;
         bool done[3] = {false, false, false};
         for (int a = 0; a < nh; ++a) {
             if (done[a]) continue;
-            const int kw = hs[a]->kw;
+            const qg_type t = hs[a]->type;
             Params p;
             memset(&p, 0, sizeof p);
             int tiles = 0;
             for (int j = a; j < nh; ++j) {
-                if (done[j] || hs[j]->kw != kw) continue;
+                if (done[j] || hs[j]->type != t) continue;
                 done[j] = true;
                 const qg_handle *h = hs[j];
                 Mat &m = p.mat[p.nmat++];
@@ -605,6 +637,7 @@ qg_status run_product_tc(qg_handle *const *hs, int nh, const __half *x, int64_t 
                 m.tile_begin = tiles;
                 tiles += (int)((h->M + kTcRows - 1) / kTcRows);
             }
+            const int ks = tc_ksplit(tiles, zc, nb);
             p.xs[XL_TC4] = h0->xs;
             p.xs_tok_stride = chunk_stride;
             p.x = xc;
@@ -612,16 +645,26 @@ qg_status run_product_tc(qg_handle *const *hs, int nh, const __half *x, int64_t 
             p.tok_base = 0;
             p.K = (int)h0->K;
             p.nb = nb;
-            p.ks = kw;
+            p.ks = ks;
             p.out_f32 = out_f32;
             p.err = h0->err;
-            int stages = kTcStagesMax;
-            while (stages > 2 && tc_smem_bytes(G, stages) > 200 * 1024) --stages;
-            p.stages = stages;
-            const int smem = tc_smem_bytes(G, stages);
-            const dim3 grid((unsigned)kw, (unsigned)tiles, (unsigned)((n + kTcTok - 1) / kTcTok));
-            cudaError_t le = fault_at("launch") ? cudaErrorLaunchOutOfResources
-                                                : launch_tc(G, p, grid, smem, s);
+            int ws = 0, xs = 0;
+            const int T = (t == QG_Q4_K) ? T_Q4K : (t == QG_Q5_K) ? T_Q5K : T_Q6K;
+            cudaError_t le = cudaErrorInvalidValue;
+            if (tc_stages(T, G, &ws, &xs)) {
+                p.stages = ws;
+                p.xstages = xs;
+                const int smem = tc_smem_bytes(T, G, ws, xs);
+                const dim3 grid((unsigned)ks, (unsigned)tiles, (unsigned)zc);
+                if (fault_at("launch"))
+                    le = cudaErrorLaunchOutOfResources;
+                else if (T == T_Q4K)
+                    le = launch_tc_q4k(G, p, grid, smem, s);
+                else if (T == T_Q5K)
+                    le = launch_tc_q5k(G, p, grid, smem, s);
+                else
+                    le = launch_tc_q6k(G, p, grid, smem, s);
+            }
             if (le != cudaSuccess) {
                 cudaGetLastError();
                 if (flags & QG_FLAG_NO_FALLBACK) {
@@ -641,8 +684,9 @@ qg_status run_product_tc(qg_handle *const *hs, int nh, const __half *x, int64_t 
     return QG_OK;
 }
 
-// Every product call: Q4_K handles of calls with N >= 33 (prefill chunks;
-// rows need not keep their bits across N there) go to the tcgen05 engine
+// Every product call: Q4_K, Q5_K and Q6_K handles of calls with N >= 33
+// (prefill chunks; rows need not keep their bits across N there) go to the
+// tcgen05 engine
 // unless QG_FLAG_MMA_SYNC_PREFILL is set; everything else runs on the
 // mma.sync kernels.
 qg_status run_product(qg_handle *const *hs, int nh, const __half *x, int64_t N, void *const *ys,
@@ -655,7 +699,7 @@ qg_status run_product(qg_handle *const *hs, int nh, const __half *x, int64_t N, 
     void *ytc[3], *ymm[3];
     int ntc = 0, nmm = 0;
     for (int i = 0; i < nh; ++i) {
-        if (hs[i]->type == QG_Q4_K && N >= kTcMinN && !(flags & QG_FLAG_MMA_SYNC_PREFILL) &&
+        if (tc_type(hs[i]->type) && N >= kTcMinN && !(flags & QG_FLAG_MMA_SYNC_PREFILL) &&
             !(flags & QG_FLAG_FORCE_REFERENCE) && !swiglu) {
             tc[ntc] = hs[i];
             ytc[ntc++] = ys[i];
@@ -862,7 +906,7 @@ const char *qgemv_describe(void)
         " QGEMV_DEBUG_SYNC=" + (env_on("QGEMV_DEBUG_SYNC") ? "1" : "0") +
         " QGEMV_FAULT_INJECT=" + (fi ? fi : "") +
         "; staging " + std::to_string(kXTok) + " B per token per 256 columns; " +
-        "K slices kw in {1,2,4,8} fixed by (M, K); Q4_K N >= 33 on the tcgen05 engine "
+        "K slices kw in {1,2,4,8} fixed by (M, K); Q4_K/Q5_K/Q6_K N >= 33 on the tcgen05 engine "
         "unless MMA_SYNC_PREFILL";
     return d.c_str();
 }
@@ -883,12 +927,12 @@ qg_status qgemv_create(qg_handle **out, qg_type t, int64_t M, int64_t K, const v
 
     qg_handle *h = new (std::nothrow) qg_handle();
     if (!h) return fail(QG_ENOMEM, "host allocation failed");
-    // staged x: [token][super-block][576] for the mma.sync kernels; Q4_K
-    // prefill chunks use the same buffer as [64-token chunk][super-block][8
+    // staged x: [token][super-block][576] for the mma.sync kernels; K-quant
+    // prefill chunks use the same buffer as [128-token chunk][super-block][16
     // groups][kTcXBlk] (qg_tc_kernel)
     const int nb = (int)(K / 256);
     size_t xs_bytes = (size_t)max_tokens * nb * kXTok;
-    if (t == QG_Q4_K) {
+    if (tc_type(t)) {
         const size_t tc = (size_t)((max_tokens + kTcTok - 1) / kTcTok) * tc_chunk_bytes(nb);
         if (tc > xs_bytes) xs_bytes = tc;
     }
@@ -1087,9 +1131,12 @@ qg_status qgemv_plan_info(const qg_handle *h, int64_t N, int32_t *ksplit, int32_
     const int64_t chunks = (N + h->max_tokens - 1) / h->max_tokens;
     const int64_t nfirst = N < h->max_tokens ? N : h->max_tokens;
     if (ksplit) *ksplit = h->kw;
-    if (h->type == QG_Q4_K && N >= kTcMinN && !(h->flags & QG_FLAG_MMA_SYNC_PREFILL) &&
+    if (tc_type(h->type) && N >= kTcMinN && !(h->flags & QG_FLAG_MMA_SYNC_PREFILL) &&
         !(h->flags & QG_FLAG_FORCE_REFERENCE)) {
         // qg_tc_kernel: 128 rows per CTA, one staging launch per chunk
+        const int tiles = (int)((h->M + kTcRows - 1) / kTcRows);
+        const int zc = (int)((nfirst + kTcTok - 1) / kTcTok);
+        if (ksplit) *ksplit = tc_ksplit(tiles, zc, h->nb);
         if (rows_cta) *rows_cta = kTcRows;
         if (launches) *launches = (int32_t)(2 * chunks);
         return QG_OK;

@@ -1,10 +1,14 @@
-// Launchers of qg_tc_kernel (Q4_K prefill chunks on the 5th-generation tensor core).
+// Launchers of qg_tc_kernel (K-quant prefill chunks on the 5th-generation
+// tensor core).  Each qg_inst_tc_*.cu defines QG_TC_TYPE and QG_TC_NAME and
+// includes this file: one translation unit per weight format, so that they
+// compile in parallel.
+#pragma once
 #include "qg_launch.cuh"
 #include "qg_tc.cuh"
 
 namespace qg {
 
-template <int G>
+template <int T, int G>
 static cudaError_t launch_tc_one(const Params &p, dim3 grid, int smem, cudaStream_t stream)
 {
     static int configured[64] = {0};
@@ -12,12 +16,12 @@ static cudaError_t launch_tc_one(const Params &p, dim3 grid, int smem, cudaStrea
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
-    if (smem > kGemvMaxSmem) return cudaErrorInvalidValue;
+    if (smem > kTcMaxSmem) return cudaErrorInvalidValue;
     if (!configured[dev]) {
-        e = cudaFuncSetAttribute(qg_tc_kernel<G>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 kGemvMaxSmem);
+        e = cudaFuncSetAttribute(qg_tc_kernel<T, G>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 kTcMaxSmem);
         if (e == cudaSuccess)
-            e = cudaFuncSetAttribute(qg_tc_kernel<G>,
+            e = cudaFuncSetAttribute(qg_tc_kernel<T, G>,
                                      cudaFuncAttributePreferredSharedMemoryCarveout,
                                      cudaSharedmemCarveoutMaxShared);
         if (e != cudaSuccess) return e;
@@ -42,20 +46,21 @@ static cudaError_t launch_tc_one(const Params &p, dim3 grid, int smem, cudaStrea
     }
     cfg.attrs = attr;
     cfg.numAttrs = na;
-    return cudaLaunchKernelEx(&cfg, qg_tc_kernel<G>, p);
+    return cudaLaunchKernelEx(&cfg, qg_tc_kernel<T, G>, p);
 }
 
-cudaError_t launch_tc(int G, const Params &p, dim3 grid, int smem, cudaStream_t s)
+cudaError_t QG_TC_NAME(int G, const Params &p, dim3 grid, int smem, cudaStream_t s)
 {
+    constexpr int T = QG_TC_TYPE;
     switch (G) {
-    case 1: return launch_tc_one<1>(p, grid, smem, s);
-    case 2: return launch_tc_one<2>(p, grid, smem, s);
-    case 3: return launch_tc_one<3>(p, grid, smem, s);
-    case 4: return launch_tc_one<4>(p, grid, smem, s);
-    case 5: return launch_tc_one<5>(p, grid, smem, s);
-    case 6: return launch_tc_one<6>(p, grid, smem, s);
-    case 7: return launch_tc_one<7>(p, grid, smem, s);
-    case 8: return launch_tc_one<8>(p, grid, smem, s);
+    case 2: return launch_tc_one<T, 2>(p, grid, smem, s);
+    case 4: return launch_tc_one<T, 4>(p, grid, smem, s);
+    case 6: return launch_tc_one<T, 6>(p, grid, smem, s);
+    case 8: return launch_tc_one<T, 8>(p, grid, smem, s);
+    case 10: return launch_tc_one<T, 10>(p, grid, smem, s);
+    case 12: return launch_tc_one<T, 12>(p, grid, smem, s);
+    case 14: return launch_tc_one<T, 14>(p, grid, smem, s);
+    case 16: return launch_tc_one<T, 16>(p, grid, smem, s);
     default: return cudaErrorInvalidValue;
     }
 }

@@ -96,6 +96,7 @@ struct Params {
     int nb;                       // 256-wide super-blocks along K
     int ks;                       // cluster size along x (the matrices' kw)
     int stages;                   // ring depth (qg_n8_kernel)
+    int xstages;                  // x ring depth (qg_tc_kernel; p.stages: its weight ring)
     int xtok;                     // token stride of the in-kernel x region (qg_n8_kernel)
     int out_f32;
     unsigned int *err;            // error word (timeouts)

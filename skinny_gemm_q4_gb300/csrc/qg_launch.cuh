@@ -15,9 +15,11 @@ cudaError_t launch_stage_tc4(const __half *x, int N, int K, int nb, int64_t chun
 cudaError_t launch_dequant(const Mat &m, int K, float *out, cudaStream_t stream);
 // Dequantize through the product kernels' decoders (qg_dequant.cu).
 cudaError_t launch_dequant_fast(const Mat &m, int K, float *out, cudaStream_t stream);
-// qg_tc_kernel (Q4_K, N >= 33, on the tensor core; defined in qg_inst_tc.cu);
-// G = token groups of 8 per CTA (1..8).
-cudaError_t launch_tc(int G, const Params &p, dim3 grid, int smem, cudaStream_t s);
+// qg_tc_kernel (Q4_K / Q5_K / Q6_K, N >= 33, on the tensor core; defined in
+// qg_inst_tc*.cu); G = token groups of 8 per CTA (even, 2..16).
+cudaError_t launch_tc_q4k(int G, const Params &p, dim3 grid, int smem, cudaStream_t s);
+cudaError_t launch_tc_q5k(int G, const Params &p, dim3 grid, int smem, cudaStream_t s);
+cudaError_t launch_tc_q6k(int G, const Params &p, dim3 grid, int smem, cudaStream_t s);
 cudaError_t launch_ref_gemv(const Mat &m, int K, const __half *x, int N, int out_f32,
                             cudaStream_t stream);
 // Reference SwiGLU pair: h = silu(x.gate^T) * (x.up^T) into gate.y.

@@ -47,6 +47,13 @@ __device__ __forceinline__ uint2 lds64(uint32_t addr)
     return v;
 }
 
+__device__ __forceinline__ uint32_t lds16(uint32_t addr)
+{
+    unsigned short v;
+    asm volatile("ld.shared.u16 %0, [%1];\n" : "=h"(v) : "r"(addr));
+    return v;
+}
+
 __device__ __forceinline__ uint32_t lds32(uint32_t addr)
 {
     uint32_t v;
@@ -169,6 +176,13 @@ __device__ __forceinline__ uint32_t map_shared_rank(uint32_t addr, uint32_t rank
     return r;
 }
 
+__device__ __forceinline__ void st_dsmem_v4(uint32_t addr, float a, float b, float c, float d)
+{
+    asm volatile("st.shared::cluster.v4.f32 [%0], {%1, %2, %3, %4};\n" ::"r"(addr), "f"(a), "f"(b),
+                 "f"(c), "f"(d)
+                 : "memory");
+}
+
 __device__ __forceinline__ float4 ld_dsmem_v4(uint32_t addr)
 {
     float4 v;
@@ -234,6 +248,29 @@ __device__ __forceinline__ bool mbar_wait(uint32_t addr, uint32_t parity,
 {
     for (uint32_t i = 0; i < limit; ++i)
         if (mbar_try_wait(addr, parity)) return true;
+    return false;
+}
+
+// Non-blocking probe of a phase (no suspend): cheaper than try_wait for a
+// single thread that must get back to issuing work as soon as the phase is
+// complete.
+__device__ __forceinline__ bool mbar_test(uint32_t addr, uint32_t parity)
+{
+    uint32_t ok;
+    asm volatile(
+        "{\n .reg .pred p;\n mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+        " selp.u32 %0, 1, 0, p;\n}\n"
+        : "=r"(ok)
+        : "r"(addr), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+// Bounded spin on mbar_test (the same contract as mbar_wait).
+__device__ __forceinline__ bool mbar_wait_spin(uint32_t addr, uint32_t parity,
+                                               uint32_t limit = (1u << 26))
+{
+    for (uint32_t i = 0; i < limit; ++i)
+        if (mbar_test(addr, parity)) return true;
     return false;
 }
 
@@ -389,6 +426,22 @@ __device__ __forceinline__ void tmem_ld8(uint32_t taddr, uint32_t (&v)[8])
                  : "memory");
 }
 
+// Load 32 consecutive columns of this thread's lane (call tc_wait_ld before use).
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&v)[32])
+{
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, "
+        "%11, %12, %13, %14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, "
+        "%28, %29, %30, %31}, [%32];\n"
+        : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]),
+          "=r"(v[7]), "=r"(v[8]), "=r"(v[9]), "=r"(v[10]), "=r"(v[11]), "=r"(v[12]), "=r"(v[13]),
+          "=r"(v[14]), "=r"(v[15]), "=r"(v[16]), "=r"(v[17]), "=r"(v[18]), "=r"(v[19]),
+          "=r"(v[20]), "=r"(v[21]), "=r"(v[22]), "=r"(v[23]), "=r"(v[24]), "=r"(v[25]),
+          "=r"(v[26]), "=r"(v[27]), "=r"(v[28]), "=r"(v[29]), "=r"(v[30]), "=r"(v[31])
+        : "r"(taddr)
+        : "memory");
+}
+
 // Shared-memory matrix descriptor, no swizzle, K-major: core matrices of 8
 // rows x 16 bytes; the two byte strides (between core matrices adjacent in K
 // and in the other dimension) are both `stride`.
@@ -419,6 +472,59 @@ __device__ __forceinline__ void tc_mma(uint32_t d_t, uint32_t a_t, uint64_t b_de
         " tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n}\n" ::"r"(d_t),
         "r"(a_t), "l"(b_desc), "r"(idesc), "r"(accumulate)
         : "memory");
+}
+// D[tmem] (+)= A[smem] . B[smem]^T (both operands by shared-memory descriptor).
+__device__ __forceinline__ void tc_mma_ss(uint32_t d_t, uint64_t a_desc, uint64_t b_desc,
+                                          uint32_t idesc, uint32_t accumulate)
+{
+    asm volatile(
+        "{\n .reg .pred p;\n setp.ne.u32 p, %4, 0;\n"
+        " tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::"r"(d_t),
+        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+// Eight MMAs of consecutive k-steps, D[d] (+)= A[a0 + 8 s] . B[b0 + s * 256 B]
+// (s = 0..7; the first accumulates iff acc0), issued back to back while two
+// mbarrier phases are probed (test_wait, no suspend): returns 1 iff both
+// (bar1, par1) and (bar2, par2) were complete.  The probes' latency hides
+// behind the MMAs, whose issue is close to synchronous with the tensor core.
+__device__ __forceinline__ uint32_t tc_mma8_probe(uint32_t d, uint32_t a0, uint64_t b0,
+                                                  uint32_t idesc, uint32_t acc0, uint32_t bar1,
+                                                  uint32_t par1, uint32_t bar2, uint32_t par2)
+{
+    uint32_t ok;
+    asm volatile(
+        "{\n"
+        " .reg .pred q1, q2, pa, pt;\n"
+        " .reg .b64 bd;\n"
+        " .reg .b32 aa;\n"
+        " mbarrier.test_wait.parity.shared::cta.b64 q1, [%6], %7;\n"
+        " mbarrier.test_wait.parity.shared::cta.b64 q2, [%8], %9;\n"
+        " setp.ne.u32 pa, %5, 0;\n"
+        " setp.eq.u32 pt, %5, %5;\n"
+        " tcgen05.mma.cta_group::1.kind::f16 [%1], [%2], %3, %4, pa;\n"
+        " add.u32 aa, %2, 8;\n add.u64 bd, %3, 16;\n"
+        " tcgen05.mma.cta_group::1.kind::f16 [%1], [aa], bd, %4, pt;\n"
+        " add.u32 aa, %2, 16;\n add.u64 bd, %3, 32;\n"
+        " tcgen05.mma.cta_group::1.kind::f16 [%1], [aa], bd, %4, pt;\n"
+        " add.u32 aa, %2, 24;\n add.u64 bd, %3, 48;\n"
+        " tcgen05.mma.cta_group::1.kind::f16 [%1], [aa], bd, %4, pt;\n"
+        " add.u32 aa, %2, 32;\n add.u64 bd, %3, 64;\n"
+        " tcgen05.mma.cta_group::1.kind::f16 [%1], [aa], bd, %4, pt;\n"
+        " add.u32 aa, %2, 40;\n add.u64 bd, %3, 80;\n"
+        " tcgen05.mma.cta_group::1.kind::f16 [%1], [aa], bd, %4, pt;\n"
+        " add.u32 aa, %2, 48;\n add.u64 bd, %3, 96;\n"
+        " tcgen05.mma.cta_group::1.kind::f16 [%1], [aa], bd, %4, pt;\n"
+        " add.u32 aa, %2, 56;\n add.u64 bd, %3, 112;\n"
+        " tcgen05.mma.cta_group::1.kind::f16 [%1], [aa], bd, %4, pt;\n"
+        " and.pred q1, q1, q2;\n"
+        " selp.u32 %0, 1, 0, q1;\n"
+        "}\n"
+        : "=r"(ok)
+        : "r"(d), "r"(a0), "l"(b0), "r"(idesc), "r"(acc0), "r"(bar1), "r"(par1), "r"(bar2),
+          "r"(par2)
+        : "memory");
+    return ok;
 }
 // Arrive on a CTA mbarrier once all tcgen05.mma issued so far by this thread complete.
 __device__ __forceinline__ void tc_commit(uint32_t mbar)

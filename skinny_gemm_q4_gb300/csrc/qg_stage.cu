@@ -46,8 +46,9 @@ cudaError_t launch_stage(const __half *x, int N, int K, int nb, int64_t tok_stri
     return cudaLaunchKernelEx(&cfg, qg_stage_kernel, x, N, K, nb, tok_stride, xq4, xq6, xfp4);
 }
 
-// The same for qg_tc_kernel's layout: token n of a 64-token chunk goes to row
-// n % 8 of 8-token group (n % 64) / 8; per chunk [super-block][8 groups][kTcXBlk].
+// The same for qg_tc_kernel's layout: token n of a 128-token chunk goes to
+// row n % 8 of 8-token group (n % 128) / 8 of its super-block block (two
+// halves, see stage_tc4).
 __global__ void __launch_bounds__(128)
     qg_stage_tc_kernel(const __half *__restrict__ x, int N, int K, int nb, int64_t chunk_stride,
                      uint8_t *out)
@@ -59,9 +60,8 @@ __global__ void __launch_bounds__(128)
     if (warp >= N * nb) return;
     const int n = warp / nb, sb = warp - n * nb;
     const uint4 v = *reinterpret_cast<const uint4 *>(x + (int64_t)n * K + 256 * sb + 8 * lane);
-    uint8_t *blk = out + (int64_t)(n / kTcTok) * chunk_stride + (int64_t)sb * (8 * kTcXBlk) +
-                   ((n % kTcTok) / 8) * kTcXBlk;
-    stage_tc4(v, lane, blk, n % 8);
+    uint8_t *sbb = out + (int64_t)(n / kTcTok) * chunk_stride + (int64_t)sb * (kTcGroups * kTcXBlk);
+    stage_tc4(v, lane, sbb, (n % kTcTok) / 8, n % 8);
 }
 
 cudaError_t launch_stage_tc4(const __half *x, int N, int K, int nb, int64_t chunk_stride,
