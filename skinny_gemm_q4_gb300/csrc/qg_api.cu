@@ -566,18 +566,40 @@ qg_status run_product_mma(qg_handle *const *hs, int nh, const __half *x, int64_t
     return QG_OK;
 }
 
-// K slices of a qg_tc_kernel launch: as many CTAs (row tiles x token chunks
-// x slices; one per SM) as fit in one wave on the GB300's 152 SMs, at most 8
-// (a portable cluster) and at most nb.
+// Plan of a qg_tc_kernel launch over `tiles` row tiles, n tokens and nb
+// super-blocks: token tiles of 8 G tokens (G even, <= 16) and K slices ks
+// (<= 8, a portable cluster; <= nb), with at most one CTA per SM of the
+// GB300's 152 in one wave.  A K split costs a cluster reduction at the end
+// (rank partials through distributed shared memory); a token split costs a
+// second decode of the weights.  Estimated time per CTA: super-blocks x the
+// time of one (about 1.2 us on GB300, nearly independent of the tile width:
+// it is bound by the MMA warp's issue loop) + the epilogue (about 4 us with
+// a cluster reduction, 2 us without); ties go to the wider tile.
 constexpr int kNumSMs = 152;
-static int tc_ksplit(int tiles, int zchunks, int nb)
+struct TcPlan {
+    int G, zc, ks;
+};
+static TcPlan tc_plan(int tiles, int n, int nb)
 {
-    const int ctas = tiles * zchunks;
-    int ks = kNumSMs / ctas;
-    if (ks < 1) ks = 1;
-    if (ks > 8) ks = 8;
-    if (ks > nb) ks = nb;
-    return ks;
+    TcPlan best = {0, 0, 0};
+    double best_t = 1e30;
+    for (int w = 64; w <= kTcTok; w *= 2) {  // token tile width
+        if (w == 64 && n <= 32) continue;
+        const int nt = n < w ? n : w;
+        const int G = 2 * ((nt + 15) / 16);
+        const int zc = (n + 8 * G - 1) / (8 * G);
+        const int ctas = tiles * zc;
+        int ks = ctas >= kNumSMs ? 1 : kNumSMs / ctas;
+        if (ks > 8) ks = 8;
+        if (ks > nb) ks = nb;
+        const int waves = (ctas * ks + kNumSMs - 1) / kNumSMs;
+        const double t = waves * ((double)((nb + ks - 1) / ks) * 1.2 + (ks > 1 ? 4.0 : 2.0));
+        if (t <= best_t) {
+            best_t = t;
+            best = {G, zc, ks};
+        }
+    }
+    return best;
 }
 
 // Ring depths of qg_tc_kernel: x ring 2..3 slots, weight ring 2..4 slots,
@@ -617,9 +639,7 @@ qg_status run_product_tc(qg_handle *const *hs, int nh, const __half *x, int64_t 
         if (fault_at("stage")) return fail(QG_EFAULT_INJECTED, "injected fault: staging launch");
         cudaError_t e = launch_stage_tc4(xc, n, (int)h0->K, nb, chunk_stride, h0->xs, s);
         if (e != cudaSuccess) return cuda_fail(e, "staging kernel launch");
-        const int nt = n < kTcTok ? n : kTcTok;
-        const int G = 2 * ((nt + 15) / 16);  // MMA N = 8 G, a multiple of 16
-        const int zc = (n + kTcTok - 1) / kTcTok;
+
         bool done[3] = {false, false, false};
         for (int a = 0; a < nh; ++a) {
             if (done[a]) continue;
@@ -637,7 +657,8 @@ qg_status run_product_tc(qg_handle *const *hs, int nh, const __half *x, int64_t 
                 m.tile_begin = tiles;
                 tiles += (int)((h->M + kTcRows - 1) / kTcRows);
             }
-            const int ks = tc_ksplit(tiles, zc, nb);
+            const TcPlan pl = tc_plan(tiles, n, nb);
+            const int G = pl.G, zc = pl.zc, ks = pl.ks;  // MMA N = 8 G, a multiple of 16
             p.xs[XL_TC4] = h0->xs;
             p.xs_tok_stride = chunk_stride;
             p.x = xc;
@@ -1135,8 +1156,7 @@ qg_status qgemv_plan_info(const qg_handle *h, int64_t N, int32_t *ksplit, int32_
         !(h->flags & QG_FLAG_FORCE_REFERENCE)) {
         // qg_tc_kernel: 128 rows per CTA, one staging launch per chunk
         const int tiles = (int)((h->M + kTcRows - 1) / kTcRows);
-        const int zc = (int)((nfirst + kTcTok - 1) / kTcTok);
-        if (ksplit) *ksplit = tc_ksplit(tiles, zc, h->nb);
+        if (ksplit) *ksplit = tc_plan(tiles, (int)nfirst, h->nb).ks;
         if (rows_cta) *rows_cta = kTcRows;
         if (launches) *launches = (int32_t)(2 * chunks);
         return QG_OK;

@@ -526,6 +526,37 @@ __device__ __forceinline__ uint32_t tc_mma8_probe(uint32_t d, uint32_t a0, uint6
         : "memory");
     return ok;
 }
+// The same with four MMAs (s = 0..3).
+__device__ __forceinline__ uint32_t tc_mma4_probe(uint32_t d, uint32_t a0, uint64_t b0,
+                                                  uint32_t idesc, uint32_t acc0, uint32_t bar1,
+                                                  uint32_t par1, uint32_t bar2, uint32_t par2)
+{
+    uint32_t ok;
+    asm volatile(
+        "{\n"
+        " .reg .pred q1, q2, pa, pt;\n"
+        " .reg .b64 bd;\n"
+        " .reg .b32 aa;\n"
+        " mbarrier.test_wait.parity.shared::cta.b64 q1, [%6], %7;\n"
+        " mbarrier.test_wait.parity.shared::cta.b64 q2, [%8], %9;\n"
+        " setp.ne.u32 pa, %5, 0;\n"
+        " setp.eq.u32 pt, %5, %5;\n"
+        " tcgen05.mma.cta_group::1.kind::f16 [%1], [%2], %3, %4, pa;\n"
+        " add.u32 aa, %2, 8;\n add.u64 bd, %3, 16;\n"
+        " tcgen05.mma.cta_group::1.kind::f16 [%1], [aa], bd, %4, pt;\n"
+        " add.u32 aa, %2, 16;\n add.u64 bd, %3, 32;\n"
+        " tcgen05.mma.cta_group::1.kind::f16 [%1], [aa], bd, %4, pt;\n"
+        " add.u32 aa, %2, 24;\n add.u64 bd, %3, 48;\n"
+        " tcgen05.mma.cta_group::1.kind::f16 [%1], [aa], bd, %4, pt;\n"
+        " and.pred q1, q1, q2;\n"
+        " selp.u32 %0, 1, 0, q1;\n"
+        "}\n"
+        : "=r"(ok)
+        : "r"(d), "r"(a0), "l"(b0), "r"(idesc), "r"(acc0), "r"(bar1), "r"(par1), "r"(bar2),
+          "r"(par2)
+        : "memory");
+    return ok;
+}
 // Arrive on a CTA mbarrier once all tcgen05.mma issued so far by this thread complete.
 __device__ __forceinline__ void tc_commit(uint32_t mbar)
 {

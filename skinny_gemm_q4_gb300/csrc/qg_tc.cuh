@@ -18,15 +18,15 @@
 //     the staged x of the CTA's tokens by one bulk copy, into separate rings;
 //   * warps 0..7 (two warpgroups, one thread per row): dequantize the row's
 //     256 weights exactly into four 64-wide chunks of the A operand in tensor
-//     memory (WG0 chunks 0, 1; WG1 chunks 2, 3 and, for Q4_K / Q5_K, the
-//     sub-block mins into a small A tile in shared memory); then fold the
-//     previous super-block, each warpgroup half of the tokens:
+//     memory (Q4_K / Q5_K: WG0 chunks 0, 2, WG1 chunks 1, 3 and the
+//     sub-block mins into a small A tile in shared memory; Q6_K: WG0 chunks
+//     0, 1, WG1 chunks 2, 3); then fold the previous super-block, each
+//     warpgroup half of the tokens:
 //       acc = fma(d', D1, acc) [; acc = fma(-dmin', D2, acc)]
 //     with that super-block's d (and dmin) kept from its decode;
-//   * warp 9 (MMA): per warpgroup's two chunks, as soon as they are decoded,
-//     8 MMAs into the super-block's accumulator D1 (double-buffered in
-//     tensor memory); then one MMA of the mins against the sub-block sums of
-//     x into D2.
+//   * warp 9 (MMA): per chunk, as soon as it is decoded, 4 MMAs into the
+//     super-block's accumulator D1 (double-buffered in tensor memory); then
+//     one MMA of the mins against the sub-block sums of x into D2.
 // The decode of super-block i + 1 runs during the MMAs of i, and the fold
 // of i - 1 after it, so decode, MMA and fold of successive super-blocks
 // overlap.
@@ -384,7 +384,11 @@ __global__ void __launch_bounds__(kTcThreads, 1) qg_tc_kernel(const __grid_const
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int rank = blockIdx.x, ks = p.ks;
     const int nsb = (p.nb - rank + ks - 1) / ks;  // super-blocks rank, rank + ks, ...
-    const int tok0 = p.tok_base + blockIdx.z * kTcTok;
+    // token tile blockIdx.z: 8 G tokens, groups goff .. goff + G - 1 of the
+    // staged 128-token chunk zch
+    const int tz = blockIdx.z * 8 * G;
+    const int zch = tz / kTcTok, goff = (tz % kTcTok) / 8;
+    const int tok0 = p.tok_base + tz;
     const int ntok = min(8 * G, p.N - tok0);
     const int row0 = rtile * kTcRows;
     const int WS = p.stages, XS = p.xstages;
@@ -406,9 +410,9 @@ __global__ void __launch_bounds__(kTcThreads, 1) qg_tc_kernel(const __grid_const
             mbar_init(b_xfull2 + 8 * s, 1);  // x half 1 (k-steps 8..15, sub-block sums)
             mbar_init(b_xempty + 8 * s, 1);
         }
-        for (int h = 0; h < 2; ++h) {  // per row warpgroup: its two A chunks
-            mbar_init(b_afull + 8 * h, kTcRows);
-            mbar_init(b_aempty + 8 * h, 1);
+        for (int c = 0; c < 4; ++c) {  // per A chunk (decoded by one warpgroup)
+            mbar_init(b_afull + 8 * c, kTcRows);
+            mbar_init(b_aempty + 8 * c, 1);
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(b_dfull + 8 * b, 1);
@@ -434,96 +438,102 @@ __global__ void __launch_bounds__(kTcThreads, 1) qg_tc_kernel(const __grid_const
         // ---------------- producer ----------------
         if (lane == 0) {
             const uint8_t *xs =
-                p.xs[XL_TC4] + (int64_t)blockIdx.z * p.xs_tok_stride;
+                p.xs[XL_TC4] + (int64_t)zch * p.xs_tok_stride;
             auto load_w = [&](int i) {
                 const uint32_t fb = b_wfull + 8 * (i % WS);
                 mbar_arrive_expect_tx(fb, (uint32_t)WSLOT);
                 tma_load_3d(wring + (i % WS) * WSLOT, &m.tmw1, 0, row0, rank + i * ks, fb);
             };
-            int iw = 0, ix = 0;
-            if (KQ)
-                for (; iw < WS && iw < nsb; ++iw) load_w(iw);  // weights need nothing earlier
-            else
-                iw = nsb;
+            const int wpre = KQ ? min(WS, nsb) : 0, xpre = min(XS, nsb);
+            for (int i = 0; i < wpre; ++i) load_w(i);  // weights need nothing earlier
             pdl_wait();  // the staged x is written by the kernel just before
-            // Both rings refilled as soon as their slots free up, neither
-            // waiting behind the other (bounded polling).
-            uint32_t spins = 0;
-            while ((ix < nsb || iw < nsb) && !err) {
-                bool progress = false;
-                if (ix < nsb && (ix < XS || mbar_test(b_xempty + 8 * (ix % XS),
-                                                      (uint32_t)(((ix / XS) - 1) & 1)))) {
-                    const int xsl = ix % XS;
-                    const uint8_t *src = xs + (int64_t)(rank + ix * ks) * (kTcGroups * kTcXBlk);
-                    const uint32_t dst = xring + xsl * XSLOT;
-                    mbar_arrive_expect_tx(b_xfull + 8 * xsl, (uint32_t)(G * kTcXHalf0));
-                    bulk_g2s(dst, src, (uint32_t)(G * kTcXHalf0), b_xfull + 8 * xsl);
-                    mbar_arrive_expect_tx(b_xfull2 + 8 * xsl, (uint32_t)(G * kTcXHalf1));
-                    bulk_g2s(dst + G * kTcXHalf0, src + kTcXHalf1Off, (uint32_t)(G * kTcXHalf1),
-                             b_xfull2 + 8 * xsl);
-                    ++ix;
-                    progress = true;
+            auto load_x = [&](int i) {
+                const int xsl = i % XS;
+                const uint8_t *src = xs + (int64_t)(rank + i * ks) * (kTcGroups * kTcXBlk);
+                const uint32_t dst = xring + xsl * XSLOT;
+                mbar_arrive_expect_tx(b_xfull + 8 * xsl, (uint32_t)(G * kTcXHalf0));
+                bulk_g2s(dst, src + goff * kTcXHalf0, (uint32_t)(G * kTcXHalf0), b_xfull + 8 * xsl);
+                mbar_arrive_expect_tx(b_xfull2 + 8 * xsl, (uint32_t)(G * kTcXHalf1));
+                bulk_g2s(dst + G * kTcXHalf0, src + kTcXHalf1Off + goff * kTcXHalf1,
+                         (uint32_t)(G * kTcXHalf1), b_xfull2 + 8 * xsl);
+            };
+            for (int i = 0; i < xpre; ++i) load_x(i);
+            // Refills in the order the slots free up: the decoders finish
+            // super-block i before its MMAs complete.  Blocking waits
+            // (try_wait suspends), so this warp takes no issue slots from the
+            // decoders while it waits.
+            for (int i = 0; i < nsb; ++i) {
+                if (KQ && i + WS < nsb) {
+                    if (!mbar_wait(b_wempty + 8 * (i % WS), (uint32_t)((i / WS) & 1))) {
+                        err |= ERR_EMPTY_TIMEOUT;
+                        break;
+                    }
+                    load_w(i + WS);
                 }
-                if (iw < nsb &&
-                    mbar_test(b_wempty + 8 * (iw % WS), (uint32_t)(((iw / WS) - 1) & 1))) {
-                    load_w(iw);
-                    ++iw;
-                    progress = true;
+                if (i + XS < nsb) {
+                    if (!mbar_wait(b_xempty + 8 * (i % XS), (uint32_t)((i / XS) & 1))) {
+                        err |= ERR_EMPTY_TIMEOUT;
+                        break;
+                    }
+                    load_x(i + XS);
                 }
-                if (progress)
-                    spins = 0;
-                else if (++spins > (1u << 26))
-                    err |= ERR_EMPTY_TIMEOUT;
             }
         }
     } else if (warp == 9) {
         // ---------------- MMA issue ----------------
         // One thread.  The tensor core idles while this thread is not issuing,
-        // so the phases needed next are probed inside each batch of 8 MMAs
-        // (tc_mma8_probe) and only waited for when not yet complete.
+        // so the phase needed next is probed inside each batch of 4 MMAs
+        // (tc_mma4_probe) and only waited for (try_wait, suspending: no issue
+        // slots taken from the decoders) when not yet complete.
         int issued = 0;
         if (lane == 0) {
-            bool ready_x = false, ready_d = false;  // probed during the previous batch
+            bool ready = false;  // x half 0, D1[b] and chunk 0, probed in the previous batch
             for (int i = 0; i < nsb; ++i) {
                 const int b = i & 1, xsl = i % XS;
-                const uint32_t px = (uint32_t)((i / XS) & 1);
-                // x half 0 landed; D1[b] read back by the folds of super-block i - 2
-                if ((!ready_x && !mbar_wait_spin(b_xfull + 8 * xsl, px)) ||
-                    (i >= 2 && !ready_d &&
-                     !mbar_wait_spin(b_dfree + 8 * b, (uint32_t)(((i >> 1) - 1) & 1))) ||
-                    !mbar_wait_spin(b_afull, (uint32_t)(i & 1))) {
+                const uint32_t px = (uint32_t)((i / XS) & 1), pa = (uint32_t)(i & 1);
+                // x half 0 landed; D1[b] read back by the folds of super-block i - 2;
+                // chunk 0 decoded
+                if (!ready &&
+                    (!mbar_wait(b_xfull + 8 * xsl, px) ||
+                     (i >= 2 && !mbar_wait(b_dfree + 8 * b, (uint32_t)(((i >> 1) - 1) & 1))) ||
+                     !mbar_wait(b_afull, pa))) {
                     err |= ERR_FULL_TIMEOUT;
                     break;
                 }
-                tc_fence_after();
                 const uint32_t xb = xring + xsl * XSLOT, xb1 = xb + G * kTcXHalf0;
-                // chunks 0, 1 (warpgroup 0) against x half 0; probe warpgroup 1's
-                // chunks and x half 1
-                uint32_t ok = tc_mma8_probe(tbase + kD1 + 8 * G * b, tbase,
-                                            smem_desc2(xb, 128, kTcXHalf0), kIdesc, 0u,
-                                            b_afull + 8, (uint32_t)(i & 1), b_xfull2 + 8 * xsl, px);
-                tc_commit(b_aempty);
-                if (!ok && (!mbar_wait_spin(b_afull + 8, (uint32_t)(i & 1)) ||
-                            !mbar_wait_spin(b_xfull2 + 8 * xsl, px))) {
-                    err |= ERR_FULL_TIMEOUT;
-                    break;
+                const uint32_t d1 = tbase + kD1 + 8 * G * b;
+                bool ok = true;
+#pragma unroll
+                for (int c = 0; c < 4; ++c) {
+                    tc_fence_after();
+                    // next: chunk c + 1 (and x half 1 before chunk 2); after
+                    // chunk 3: the folds of i - 1 (D2, next D1) and the next
+                    // super-block's x half 0
+                    uint32_t q1 = b_afull + 8 * (c + 1), p1 = pa, q2 = q1, p2 = pa;
+                    if (c == 1) q2 = b_xfull2 + 8 * xsl, p2 = px;
+                    if (c == 3) {
+                        const int ni = (i + 1 < nsb) ? i + 1 : i;
+                        q1 = (i >= 1) ? b_dfree + 8 * ((i - 1) & 1) : b_xfull + 8 * xsl;
+                        p1 = (i >= 1) ? (uint32_t)(((i - 1) >> 1) & 1) : px;
+                        q2 = b_xfull + 8 * (ni % XS), p2 = (uint32_t)((ni / XS) & 1);
+                    }
+                    const uint64_t bd = (c < 2) ? smem_desc2(xb + 1024 * c, 128, kTcXHalf0)
+                                                : smem_desc2(xb1 + 1024 * (c - 2), 128, kTcXHalf1);
+                    const uint32_t r = tc_mma4_probe(d1, tbase + 32 * c, bd, kIdesc, c ? 1u : 0u,
+                                                     q1, p1, q2, p2);
+                    tc_commit(b_aempty + 8 * c);
+                    if (c < 3 && !r && (!mbar_wait(q1, p1) || (c == 1 && !mbar_wait(q2, p2)))) {
+                        ok = false;
+                        break;
+                    }
+                    if (c == 3) ready = r;
                 }
-                tc_fence_after();
-                // chunks 2, 3 against x half 1; probe the folds of i - 1 (D2 and
-                // the next D1 buffer) and the next super-block's x half 0
-                const int ni = (i + 1 < nsb) ? i + 1 : i;
-                const uint32_t pd = (i >= 1) ? b_dfree + 8 * ((i - 1) & 1) : b_xfull + 8 * xsl;
-                const uint32_t pdp = (i >= 1) ? (uint32_t)(((i - 1) >> 1) & 1) : px;
-                ok = tc_mma8_probe(tbase + kD1 + 8 * G * b, tbase + 64,
-                                   smem_desc2(xb1, 128, kTcXHalf1), kIdesc, 1u, pd, pdp,
-                                   b_xfull + 8 * (ni % XS), (uint32_t)((ni / XS) & 1));
-                tc_commit(b_aempty + 8);
-                ready_x = ok;
-                ready_d = ok;
                 // D2 is single-buffered: the folds of super-block i - 1 must
                 // have read it.
-                if (!ok && KQ && i >= 1 &&
-                    !mbar_wait_spin(b_dfree + 8 * ((i - 1) & 1), (uint32_t)(((i - 1) >> 1) & 1))) {
+                if (ok && !ready && KQ && i >= 1 &&
+                    !mbar_wait(b_dfree + 8 * ((i - 1) & 1), (uint32_t)(((i - 1) >> 1) & 1)))
+                    ok = false;
+                if (!ok) {
                     err |= ERR_FULL_TIMEOUT;
                     break;
                 }
@@ -533,6 +543,12 @@ __global__ void __launch_bounds__(kTcThreads, 1) qg_tc_kernel(const __grid_const
                 tc_commit(b_dfull + 8 * b);
                 tc_commit(b_xempty + 8 * xsl);
                 ++issued;
+                // the probe after chunk 3 covered x half 0 and the folds, not
+                // the next chunk 0: wait for that one at the top
+                if (ready && i + 1 < nsb && !mbar_wait(b_afull, (uint32_t)((i + 1) & 1))) {
+                    err |= ERR_FULL_TIMEOUT;
+                    break;
+                }
             }
             // Nothing of this CTA may still run on the tensor core when its
             // tensor memory is released (matters only after a timeout).
@@ -659,41 +675,43 @@ __global__ void __launch_bounds__(kTcThreads, 1) qg_tc_kernel(const __grid_const
                 // d: window bytes 208 + off, 209 + off (chunk 13)
                 dcur = lds16(ws + 13u * (kTcRows * 16) + 16 * r + off);
             }
-            // this warpgroup's chunks of super-block i - 1 must have left the
-            // tensor core
-            if (i > 0 && !mbar_wait(b_aempty + 8 * wg, (uint32_t)((i - 1) & 1))) {
-                ok = false;
-                break;
-            }
-            tc_fence_after();
 #pragma unroll 1
             for (int cc = 0; cc < 2; ++cc) {
-                const int c = 2 * wg + cc;
+                // K-quants: WG0 chunks 0, 2 and WG1 chunks 1, 3 (interleaved, so a
+                // chunk's decode has three chunks of MMAs to hide behind); Q6_K:
+                // WG h the two chunks of block half h (one realigned load)
+                const int c = KQ ? wg + 2 * cc : 2 * wg + cc;
+                // chunk c of super-block i - 1 must have left the tensor core
+                if (i > 0 && !mbar_wait(b_aempty + 8 * c, (uint32_t)((i - 1) & 1))) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
                 uint32_t a[32];
                 if (KQ)
                     tc_chunk_kq<T>(ws + (uint32_t)(r * BB), c, a);
                 else
                     tc_chunk_q6(q6, cc, a);
                 tmem_st32(tl + 32 * c, a);
+                if (KQ && c == 3) {
+                    // mins tile of this super-block: core (k-core kc, rows 8 g..)
+                    // at 256 g + 128 kc + 16 (r % 8); free since super-block
+                    // i - 2's MMAs completed before chunk 3 of i - 1 did
+                    uint4 hi, lo;
+                    tc_mins_kq(ws + (uint32_t)(r * BB), hi, lo);
+                    const uint32_t t0 = amin + kTcMinTile * (i & 1) + 256 * (r >> 3) + 16 * (r & 7);
+                    asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};\n" ::"r"(t0), "r"(hi.x),
+                                 "r"(hi.y), "r"(hi.z), "r"(hi.w)
+                                 : "memory");
+                    asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};\n" ::"r"(t0 + 128),
+                                 "r"(lo.x), "r"(lo.y), "r"(lo.z), "r"(lo.w)
+                                 : "memory");
+                    fence_proxy_async_smem();
+                }
+                tc_wait_st();
+                tc_fence_before();
+                mbar_arrive(b_afull + 8 * c);
             }
-            if (KQ && wg == 1) {
-                // mins tile of this super-block: core (k-core kc, rows 8 g..)
-                // at 256 g + 128 kc + 16 (r % 8); free since super-block
-                // i - 2's MMAs completed before WG1's chunks of i - 1 did
-                uint4 hi, lo;
-                tc_mins_kq(ws + (uint32_t)(r * BB), hi, lo);
-                const uint32_t t0 = amin + kTcMinTile * (i & 1) + 256 * (r >> 3) + 16 * (r & 7);
-                asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};\n" ::"r"(t0), "r"(hi.x),
-                             "r"(hi.y), "r"(hi.z), "r"(hi.w)
-                             : "memory");
-                asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};\n" ::"r"(t0 + 128),
-                             "r"(lo.x), "r"(lo.y), "r"(lo.z), "r"(lo.w)
-                             : "memory");
-                fence_proxy_async_smem();
-            }
-            tc_wait_st();
-            tc_fence_before();
-            mbar_arrive(b_afull + 8 * wg);
             if (!ok) break;
             __syncwarp();
             if (lane == 0) mbar_arrive(b_wempty + 8 * slot);

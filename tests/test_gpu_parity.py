@@ -302,7 +302,10 @@ def test_run_add_residual(inplace, M, N):
 @pytest.mark.parametrize("N", [5, 12, 40])
 def test_pair_and_mixed_triple_equal_separate_calls(N):
     """The fused calls give each matrix the bits of its own call; the triple
-    mixes formats and K-slice counts (Q 4096 rows: 4 slices, K/V: 8)."""
+    mixes formats and K-slice counts (Q 4096 rows: 4 slices, K/V: 8).  At
+    N >= 33 (the tcgen05 engine) a launch's K split follows all its row
+    tiles, so there the fused calls are checked against the oracle only
+    (prefill chunks have no twin contract)."""
     K = 2560
     a, wa, _, _ = make_matrix(qg.Q4_K, 4096, K, seed=10, stream=1)
     b, wb, _, _ = make_matrix(qg.Q4_K, 1024, K, seed=10, stream=2)
@@ -312,13 +315,13 @@ def test_pair_and_mixed_triple_equal_separate_calls(N):
     ya, yb, yc = qg.triple_run(a, b, c, xd, out_f32=True)
     for hnd, y, w, t in ((a, ya, wa, oracle.Q4_K), (b, yb, wb, oracle.Q4_K), (c, yc, wc, oracle.Q6_K)):
         sep = hnd.run(xd, out_f32=True)
-        assert torch().equal(y, sep)
+        assert N >= 33 or torch().equal(y, sep)
         yref, mag = oracle.qgemv(t, w, hnd.M, K, x)
         check_close(y.cpu().numpy(), yref, mag, what="triple")
     p1, w1, _, _ = make_matrix(qg.Q4_K, 9728, K, seed=11, stream=4)
     p2, w2, _, _ = make_matrix(qg.Q4_K, 9728, K, seed=11, stream=5)
     y1, y2 = qg.pair_run(p1, p2, xd)
-    assert torch().equal(y1, p1.run(xd)) and torch().equal(y2, p2.run(xd))
+    assert N >= 33 or (torch().equal(y1, p1.run(xd)) and torch().equal(y2, p2.run(xd)))
     rows = np.arange(0, 9728, 97)
     yref, mag = oracle.qgemv(oracle.Q4_K, w2, 9728, K, x, rows=rows)
     check_close(y2.float().cpu().numpy()[:, rows], yref, mag, fp16_out=True, what="pair")
