@@ -568,13 +568,14 @@ qg_status run_product_mma(qg_handle *const *hs, int nh, const __half *x, int64_t
 
 // Plan of a qg_tc_kernel launch over `tiles` row tiles, n tokens and nb
 // super-blocks: token tiles of 8 G tokens (G even, <= 16) and K slices ks
-// (<= 8, a portable cluster; <= nb), with at most one CTA per SM of the
-// GB300's 152 in one wave.  A K split costs a cluster reduction at the end
-// (rank partials through distributed shared memory); a token split costs a
-// second decode of the weights.  Estimated time per CTA: super-blocks x the
-// time of one (about 1.2 us on GB300, nearly independent of the tile width:
-// it is bound by the MMA warp's issue loop) + the epilogue (about 4 us with
-// a cluster reduction, 2 us without); ties go to the wider tile.
+// (<= 8; <= nb), one CTA per SM.  A K split costs a cluster reduction at the
+// end (rank partials through distributed shared memory) and is bounded by
+// how many clusters of ks CTAs the GPU holds at once (a cluster lives in one
+// GPC, so 7 or 8 CTA clusters leave SMs idle); a token split costs a second
+// decode of the weights.  Estimated time: waves x (super-blocks per CTA x
+// the time of one, about 1.2 us on GB300 and nearly independent of the tile
+// width, + the epilogue, about 4 us with a cluster reduction and 2 us
+// without); ties go to the wider tile, then to the smaller K split.
 constexpr int kNumSMs = 152;
 struct TcPlan {
     int G, zc, ks;
@@ -588,15 +589,18 @@ static TcPlan tc_plan(int tiles, int n, int nb)
         const int nt = n < w ? n : w;
         const int G = 2 * ((nt + 15) / 16);
         const int zc = (n + 8 * G - 1) / (8 * G);
-        const int ctas = tiles * zc;
-        int ks = ctas >= kNumSMs ? 1 : kNumSMs / ctas;
-        if (ks > 8) ks = 8;
-        if (ks > nb) ks = nb;
-        const int waves = (ctas * ks + kNumSMs - 1) / kNumSMs;
-        const double t = waves * ((double)((nb + ks - 1) / ks) * 1.2 + (ks > 1 ? 4.0 : 2.0));
-        if (t <= best_t) {
-            best_t = t;
-            best = {G, zc, ks};
+        const int clusters = tiles * zc;
+        for (int ks = 8; ks >= 1; --ks) {
+            if (ks > nb) continue;
+            int cap = tc_cluster_capacity(ks);
+            if (cap <= 0) cap = kNumSMs / ks;
+            const int waves = (clusters + cap - 1) / cap;
+            const double t =
+                waves * ((double)((nb + ks - 1) / ks) * 1.2 + (ks > 1 ? 4.0 : 2.0));
+            if (t < best_t - 1e-9 || (t <= best_t + 1e-9 && 8 * G >= 8 * best.G)) {
+                best_t = t;
+                best = {G, zc, ks};
+            }
         }
     }
     return best;

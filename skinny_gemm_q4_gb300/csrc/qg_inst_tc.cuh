@@ -49,6 +49,48 @@ static cudaError_t launch_tc_one(const Params &p, dim3 grid, int smem, cudaStrea
     return cudaLaunchKernelEx(&cfg, qg_tc_kernel<T, G>, p);
 }
 
+#ifdef QG_TC_CAPACITY
+// How many clusters of ks CTAs of qg_tc_kernel (one CTA per SM) the GPU runs
+// at once: a cluster must fit in one GPC, so for ks > 2 this is less than
+// 152 / ks.  Queried once per device and cluster size; 0 on failure.
+int tc_cluster_capacity(int ks)
+{
+    static int cache[64][9];
+    static bool filled[64][9];
+    int dev = 0;
+    if (ks < 1 || ks > 8 || cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
+    if (filled[dev][ks]) return cache[dev][ks];
+    auto fn = qg_tc_kernel<QG_TC_TYPE, 16>;
+    if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, kTcMaxSmem) !=
+        cudaSuccess) {
+        cudaGetLastError();
+        return 0;
+    }
+    if (ks > 1 && cudaFuncSetAttribute(fn, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) !=
+                      cudaSuccess)
+        cudaGetLastError();
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)ks, 152, 1);
+    cfg.blockDim = dim3(kTcThreads);
+    cfg.dynamicSmemBytes = kTcMinSmem;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = (unsigned)ks;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    int n = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, fn, &cfg) != cudaSuccess) {
+        cudaGetLastError();
+        n = 0;
+    }
+    cache[dev][ks] = n;
+    filled[dev][ks] = true;
+    return n;
+}
+#endif
+
 cudaError_t QG_TC_NAME(int G, const Params &p, dim3 grid, int smem, cudaStream_t s)
 {
     constexpr int T = QG_TC_TYPE;
