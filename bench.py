@@ -317,41 +317,42 @@ def run_ours(args):
             hs[role] = qg.QGemv(qt, M, K, w, sc, g, max_tokens=128)
         layers.append(hs)
     all_handles = [h for hs in layers for h in hs.values()]
-    x_qkv = synth.device_activations(1, 2560, 0, 1, dev)
-    x_o = synth.device_activations(1, 4096, 0, 2, dev)
-    res = synth.device_activations(1, 2560, 0, 3, dev)
-    x_ffn = synth.device_activations(1, 2560, 0, 4, dev)
-    x_dn = synth.device_activations(1, 9728, 0, 5, dev)
-    f16 = torch.float16
-    yq = torch.empty((1, 4096), dtype=f16, device=dev)
-    yk = torch.empty((1, 1024), dtype=f16, device=dev)
-    yv = torch.empty((1, 1024), dtype=f16, device=dev)
-    yo = torch.empty((1, 2560), dtype=f16, device=dev)
-    yg = torch.empty((1, 9728), dtype=f16, device=dev)
-    yu = torch.empty((1, 9728), dtype=f16, device=dev)
-    yd = torch.empty((1, 2560), dtype=f16, device=dev)
-
     part = args.part
-    rows = max(1, args.rows) if part == "gate" else 1
+    rows = max(1, args.rows) if part in ("gate", "prefill") else 1
+    nl = rows if part == "prefill" else 1  # tokens of the layer calls
+    x_qkv = synth.device_activations(nl, 2560, 0, 1, dev)
+    x_o = synth.device_activations(nl, 4096, 0, 2, dev)
+    res = synth.device_activations(nl, 2560, 0, 3, dev)
+    x_ffn = synth.device_activations(nl, 2560, 0, 4, dev)
+    x_dn = synth.device_activations(nl, 9728, 0, 5, dev)
+    f16 = torch.float16
+    yq = torch.empty((nl, 4096), dtype=f16, device=dev)
+    yk = torch.empty((nl, 1024), dtype=f16, device=dev)
+    yv = torch.empty((nl, 1024), dtype=f16, device=dev)
+    yo = torch.empty((nl, 2560), dtype=f16, device=dev)
+    yg = torch.empty((nl, 9728), dtype=f16, device=dev)
+    yu = torch.empty((nl, 9728), dtype=f16, device=dev)
+    yd = torch.empty((nl, 2560), dtype=f16, device=dev)
+
     x_g = synth.device_activations(rows, 2560, 0, 7, dev)
     y_g = torch.empty((rows, 9728), dtype=f16, device=dev)
 
     def call_qkv(h, s):
-        qg.qgemv_triple_run(h["wq"].h, h["wk"].h, h["wv"].h, x_qkv.data_ptr(), 1,
+        qg.qgemv_triple_run(h["wq"].h, h["wk"].h, h["wv"].h, x_qkv.data_ptr(), nl,
                             yq.data_ptr(), yk.data_ptr(), yv.data_ptr(), qg.OUT_F16, s)
 
     def call_wo(h, s):
-        qg.qgemv_run_add(h["wo"].h, x_o.data_ptr(), 1, res.data_ptr(), yo.data_ptr(), s)
+        qg.qgemv_run_add(h["wo"].h, x_o.data_ptr(), nl, res.data_ptr(), yo.data_ptr(), s)
 
     def call_pair(h, s):
-        qg.qgemv_pair_run(h["gate"].h, h["up"].h, x_ffn.data_ptr(), 1, yg.data_ptr(),
+        qg.qgemv_pair_run(h["gate"].h, h["up"].h, x_ffn.data_ptr(), nl, yg.data_ptr(),
                           yu.data_ptr(), qg.OUT_F16, s)
 
     def call_down(h, s):
-        qg.qgemv_run(h["down"].h, x_dn.data_ptr(), 1, yd.data_ptr(), qg.OUT_F16, s)
+        qg.qgemv_run(h["down"].h, x_dn.data_ptr(), nl, yd.data_ptr(), qg.OUT_F16, s)
 
     def call_pair_swiglu(h, s):
-        qg.qgemv_pair_swiglu_run(h["gate"].h, h["up"].h, x_ffn.data_ptr(), 1, yg.data_ptr(),
+        qg.qgemv_pair_swiglu_run(h["gate"].h, h["up"].h, x_ffn.data_ptr(), nl, yg.data_ptr(),
                                  qg.OUT_F16, s)
 
     CALLS = [("qkv", call_qkv, ["wq", "wk", "wv"]), ("wo", call_wo, ["wo"]),
@@ -361,18 +362,21 @@ def run_ours(args):
         h = layers[L]
         s = torch.cuda.current_stream().cuda_stream
         for name, fn, _ in CALLS:
-            if part in ("layer", name):
+            if part in ("layer", "prefill", name):
                 fn(h, s)
         if part == "gate":
             qg.qgemv_run(h["gate"].h, x_g.data_ptr(), rows, y_g.data_ptr(), qg.OUT_F16, s)
 
-    roles = {"layer": [r for r, _, _, _ in synth.LAYER], "qkv": ["wq", "wk", "wv"],
+    roles = {"layer": [r for r, _, _, _ in synth.LAYER], "prefill": [r for r, _, _, _ in synth.LAYER],
+             "qkv": ["wq", "wk", "wv"],
              "wo": ["wo"], "pair": ["gate", "up"], "down": ["down"], "gate": ["gate"]}[part]
     wbytes = sum(M * synth.row_bytes(qt, K) for r, qt, M, K in synth.LAYER if r in roles)
     # N = 1: one product kernel per call (x staged in-kernel)
     launches_per_step = 4 if part == "layer" else 1
     if part == "gate":
         launches_per_step = layers[0]["gate"].plan_info(rows)[2]
+    if part == "prefill":  # staging + product per call (Q4_K and Q6_K launches of the triple)
+        launches_per_step = sum(layers[0][r].plan_info(rows)[2] for r in ("wq", "wo", "gate", "down")) + 1
 
     for i in range(args.warmup):
         step(i % N_LAYERS)
@@ -709,11 +713,13 @@ def main():
                     help="same as --no-configs")
     ap.add_argument("--nvfp4-sets", type=int, default=56,
                     help="copies of the three NVFP4 shapes (56: ~10 GB)")
-    ap.add_argument("--part", default="layer", choices=["layer", "qkv", "wo", "pair", "down", "gate"],
-                    help="time one call of the layer only (profiling); default: the whole layer")
+    ap.add_argument("--part", default="layer",
+                    choices=["layer", "qkv", "wo", "pair", "down", "gate", "prefill"],
+                    help="time one call of the layer only (profiling); prefill: the whole layer "
+                         "at --rows tokens; default: the whole layer at N = 1")
     ap.add_argument("--rows", type=int, default=1,
                     help="N for --part gate (the gate matrix alone at N rows: the skinny and "
-                         "prefill kernels, for profiling)")
+                         "prefill kernels) and --part prefill (for profiling)")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
