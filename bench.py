@@ -279,6 +279,18 @@ def _graph_us(torch, side, ncalls, call, e0, e1):
     return us
 
 
+def _kernel_name(call, n):
+    """The product kernel that serves one layer call at n tokens."""
+    types = {"qkv": "Q4_K|Q6_K", "wo": "Q4_K", "pair": "Q4_K", "gate": "Q4_K", "down": "Q6_K"}[call]
+    what = {"qkv": "QKV triple", "wo": "Wo + residual", "pair": "gate/up pair", "gate": "gate",
+            "down": "down"}[call]
+    # N = 2..8 on Q4_K/Q5_K matrices of at most 4096 rows (Wo) runs the
+    # K-sliced kernel too
+    n8 = n == 1 or (n <= 8 and call != "wo")
+    kern = "qg_n8_kernel" if n8 else ("qg_sk_kernel" if n <= 32 else "qg_tc_kernel")
+    return f"{kern}<{types}> ({what}, N={n})"
+
+
 def _bw(nbytes, us, peak):
     gbs = nbytes / (us * 1e-6) / 1e9
     return {"us_per_call": round(us, 3), "GBps": round(gbs, 1),
@@ -441,36 +453,55 @@ def run_ours(args):
 
     # Each call of the layer alone, back to back over the 36 layers.
     calls = {}
-    if part == "layer":
+    if part in ("layer", "prefill"):
         for name, fn, rl in CALLS:
             nb_ = sum(M * synth.row_bytes(qt, K) for r, qt, M, K in synth.LAYER if r in rl)
             us = _graph_us(torch, side, ncalls, lambda i, s, fn=fn: fn(layers[i % N_LAYERS], s),
                            e0, e1)
-            calls[name] = dict(_bw(nb_, us, peak), bytes_per_call=nb_)
+            calls[name] = dict(_bw(nb_, us, peak), bytes_per_call=nb_,
+                               flops_per_call=2 * nl * sum(M * K for r, _, M, K in synth.LAYER
+                                                           if r in rl))
         dom = max(calls, key=lambda k: calls[k]["us_per_call"])
-        # the gate/up pair with the fused SwiGLU epilogue (h = silu(g) * u), not
-        # part of the step: the layer's pair returns g and u
-        nb_ = 2 * 9728 * synth.row_bytes(synth.Q4_K, 2560)
+        if part == "layer":
+            # the gate/up pair with the fused SwiGLU epilogue (h = silu(g) * u),
+            # not part of the step: the layer's pair returns g and u
+            nb_ = 2 * 9728 * synth.row_bytes(synth.Q4_K, 2560)
+            us = _graph_us(torch, side, ncalls,
+                           lambda i, s: call_pair_swiglu(layers[i % N_LAYERS], s), e0, e1)
+            calls["pair_swiglu"] = dict(_bw(nb_, us, peak), bytes_per_call=nb_)
+    elif part == "gate":
+        dom = "gate"
+        nb_ = 9728 * synth.row_bytes(synth.Q4_K, 2560)
         us = _graph_us(torch, side, ncalls,
-                       lambda i, s: call_pair_swiglu(layers[i % N_LAYERS], s), e0, e1)
-        calls["pair_swiglu"] = dict(_bw(nb_, us, peak), bytes_per_call=nb_)
+                       lambda i, s: qg.qgemv_run(layers[i % N_LAYERS]["gate"].h, x_g.data_ptr(),
+                                                 rows, y_g.data_ptr(), qg.OUT_F16, s), e0, e1)
+        calls[dom] = dict(_bw(nb_, us, peak), bytes_per_call=nb_, flops_per_call=2 * rows * 9728 * 2560)
     else:
-        dom = part if part in ("qkv", "wo", "pair", "down") else "pair"
+        dom = part
         rl = dict((n, r) for n, _, r in CALLS)[dom]
         fn = dict((n, f) for n, f, _ in CALLS)[dom]
         nb_ = sum(M * synth.row_bytes(qt, K) for r, qt, M, K in synth.LAYER if r in rl)
         us = _graph_us(torch, side, ncalls, lambda i, s: fn(layers[i % N_LAYERS], s), e0, e1)
         calls[dom] = dict(_bw(nb_, us, peak), bytes_per_call=nb_)
-    KERNEL_OF = {"qkv": "qg_n8_kernel<Q4_K|Q6_K> (QKV triple, N=1)",
-                 "wo": "qg_n8_kernel<Q4_K> (Wo + residual, N=1)",
-                 "pair": "qg_n8_kernel<Q4_K> (gate/up pair, N=1)",
-                 "down": "qg_n8_kernel<Q6_K> (down, N=1)"}
     d = calls[dom]
-    roofline = {"bound": "hbm", "achieved": d["GBps"], "peak": peak, "unit": "GB/s",
-                "frac": round(d["GBps"] / peak, 4), "traffic": _traffic_record(dom),
-                "kernel": KERNEL_OF[dom] + ": the layer's costliest call, timed alone",
-                "per_launch_us": d["us_per_call"], "bytes_per_launch": d["bytes_per_call"],
-                "peak_kind": peak_kind}
+    ntok = rows if part in ("gate", "prefill") else 1
+    kname = _kernel_name(dom, ntok)
+    flops = d.get("flops_per_call", 0)
+    if ntok >= 33 and flops / (tpeak * 1e12) > d["bytes_per_call"] / (peak * 1e9):
+        # more tensor time than weight-stream time at this token count
+        tf = flops / (d["us_per_call"] * 1e-6) / 1e12
+        roofline = {"bound": "tensor", "achieved": round(tf, 1), "peak": tpeak, "unit": "TFLOP/s",
+                    "frac": round(tf / tpeak, 4), "traffic": None,
+                    "kernel": kname + ": the costliest call, timed alone",
+                    "per_launch_us": d["us_per_call"], "flops_per_launch": flops,
+                    "weight_GBps": d["GBps"], "peak_kind": tpeak_kind}
+    else:
+        roofline = {"bound": "hbm", "achieved": d["GBps"], "peak": peak, "unit": "GB/s",
+                    "frac": round(d["GBps"] / peak, 4),
+                    "traffic": _traffic_record(dom) if ntok == 1 else None,
+                    "kernel": kname + ": the costliest call, timed alone",
+                    "per_launch_us": d["us_per_call"], "bytes_per_launch": d["bytes_per_call"],
+                    "peak_kind": peak_kind}
 
     configs = None
     if part == "layer" and not args.no_configs:
