@@ -370,9 +370,30 @@ def run_ours(args):
     CALLS = [("qkv", call_qkv, ["wq", "wk", "wv"]), ("wo", call_wo, ["wo"]),
              ("pair", call_pair, ["gate", "up"]), ("down", call_down, ["down"])]
 
+    # The layer's four calls as one decode chain (qgemv_chain_run): one
+    # persistent launch at N <= 8; at larger N the calls run one by one.
+    chain = None
+    if args.layer_api != "calls":
+        chain = qg.Chain(qg.CHAIN_PERSISTENT if args.layer_api == "persistent" else 0)
+    chain_calls = []
+    if chain is not None:
+        for hs in layers:
+            chain_calls.append(qg.make_calls([
+                (qg.CALL_TRIPLE, [hs["wq"].h, hs["wk"].h, hs["wv"].h], x_qkv.data_ptr(), nl,
+                 [yq.data_ptr(), yk.data_ptr(), yv.data_ptr()], qg.OUT_F16, None),
+                (qg.CALL_RUN_ADD, [hs["wo"].h], x_o.data_ptr(), nl, [yo.data_ptr()], qg.OUT_F16,
+                 res.data_ptr()),
+                (qg.CALL_PAIR, [hs["gate"].h, hs["up"].h], x_ffn.data_ptr(), nl,
+                 [yg.data_ptr(), yu.data_ptr()], qg.OUT_F16, None),
+                (qg.CALL_RUN, [hs["down"].h], x_dn.data_ptr(), nl, [yd.data_ptr()], qg.OUT_F16,
+                 None)]))
+
     def step(L):
         h = layers[L]
         s = torch.cuda.current_stream().cuda_stream
+        if chain is not None and part in ("layer", "prefill"):
+            qg.qgemv_chain_run(chain.c, chain_calls[L], s)
+            return
         for name, fn, _ in CALLS:
             if part in ("layer", "prefill", name):
                 fn(h, s)
@@ -384,7 +405,7 @@ def run_ours(args):
              "wo": ["wo"], "pair": ["gate", "up"], "down": ["down"], "gate": ["gate"]}[part]
     wbytes = sum(M * synth.row_bytes(qt, K) for r, qt, M, K in synth.LAYER if r in roles)
     # N = 1: one product kernel per call (x staged in-kernel)
-    launches_per_step = 4 if part == "layer" else 1
+    launches_per_step = (1 if args.layer_api == "persistent" else 4) if part == "layer" else 1
     if part == "gate":
         launches_per_step = layers[0]["gate"].plan_info(rows)[2]
     if part == "prefill":  # staging + product per call (Q4_K and Q6_K launches of the triple)
@@ -444,6 +465,8 @@ def run_ours(args):
     # Every kernel's bounded waits finished in time (a timed-out pipeline
     # would return early with wrong results).
     bad = [h for h in all_handles if h.device_status() != 0]
+    if chain is not None and chain.status() != 0:
+        bad.append(chain)
     if bad:
         print(json.dumps({"error": f"{len(bad)} handles report a device timeout"}))
         sys.exit(3)
@@ -469,6 +492,18 @@ def run_ours(args):
             us = _graph_us(torch, side, ncalls,
                            lambda i, s: call_pair_swiglu(layers[i % N_LAYERS], s), e0, e1)
             calls["pair_swiglu"] = dict(_bw(nb_, us, peak), bytes_per_call=nb_)
+            # the whole layer as one persistent launch (QG_CHAIN_PERSISTENT),
+            # for comparison with the step's launch per call
+            pchain = qg.Chain(qg.CHAIN_PERSISTENT)
+            lb = sum(M * synth.row_bytes(qt, K) for _, qt, M, K in synth.LAYER)
+            us = _graph_us(torch, side, ncalls,
+                           lambda i, s: qg.qgemv_chain_run(pchain.c, chain_calls[i % N_LAYERS], s),
+                           e0, e1) if chain_calls else 0.0
+            if chain_calls:
+                calls["layer_persistent_chain"] = dict(_bw(lb, us, peak), bytes_per_call=lb)
+                if pchain.status() != 0:
+                    print(json.dumps({"error": "persistent chain reports a device timeout"}))
+                    sys.exit(3)
     elif part == "gate":
         dom = "gate"
         nb_ = 9728 * synth.row_bytes(synth.Q4_K, 2560)
@@ -570,6 +605,10 @@ def run_ours(args):
         "data": "synthetic",
         "config": {"workload": WORKLOAD if part == "layer" else WORKLOAD + ":" + part, "N": rows,
                    "layers_rotated": N_LAYERS,
+                   "layer_api": {"chain": "qgemv_chain_run (a launch per call, PDL-chained)",
+                                 "persistent": "qgemv_chain_run (one persistent launch)",
+                                 "calls": "four entry-point calls"}[args.layer_api]
+                   if part in ("layer", "prefill") else "one call",
                    "weight_bytes_per_step": wbytes,
                    "cold": "36 distinct layers (2.3 GB) > L2; no flush needed",
                    "pct_of_nominal_8TBps": round(100 * value / world / 8000.0, 2),
@@ -748,6 +787,10 @@ def main():
                     choices=["layer", "qkv", "wo", "pair", "down", "gate", "prefill"],
                     help="time one call of the layer only (profiling); prefill: the whole layer "
                          "at --rows tokens; default: the whole layer at N = 1")
+    ap.add_argument("--layer-api", default="chain", choices=["chain", "persistent", "calls"],
+                    help="layer step through one decode chain call (qgemv_chain_run: one "
+                         "launch per matrix call, PDL-chained), the same in one persistent "
+                         "launch, or four separate entry-point calls")
     ap.add_argument("--rows", type=int, default=1,
                     help="N for --part gate (the gate matrix alone at N rows: the skinny and "
                          "prefill kernels) and --part prefill (for profiling)")

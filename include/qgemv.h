@@ -268,6 +268,82 @@ qg_status qgemv_run_noalloc(qg_type t, int64_t M, int64_t K, const void *w_dev,
                             const void *scales_dev, float global_scale, const void *x,
                             int64_t N, void *y, qg_out ydt, void *stream);
 
+/* ------------------------------------------------------------------------
+ * Decode chains: the calls of a transformer layer (QKV triple, Wo + residual,
+ * gate/up pair, down) in one persistent launch that stays resident on the
+ * SMs, so the weight stream does not drain and refill at every call boundary
+ * (reflex-llm "docs/performance.md", Level 4: persistent kernels that stay
+ * resident on the SM; Path C: the per-call launch and tail costs of small
+ * matrices).
+ * ------------------------------------------------------------------------ */
+
+/* Kinds of chain calls; each is the operation of the named entry point. */
+typedef enum {
+    QG_CALL_RUN = 0,     /* y[0] = x . W0^T                     (qgemv_run)        */
+    QG_CALL_RUN_ADD = 1, /* y[0] = residual + x . W0^T, fp16    (qgemv_run_add)    */
+    QG_CALL_PAIR = 2,    /* y[i] = x . Wi^T, i < 2              (qgemv_pair_run)   */
+    QG_CALL_TRIPLE = 3   /* y[i] = x . Wi^T, i < 3              (qgemv_triple_run) */
+} qg_call_kind;
+
+/* One call of a chain; the arguments have the meaning, layout and checks of
+ * the named entry point. */
+typedef struct qg_call {
+    int32_t kind;          /* qg_call_kind */
+    int32_t out_dtype;     /* qg_out of y (QG_CALL_RUN_ADD: must be QG_OUT_F16) */
+    int64_t N;             /* tokens */
+    qg_handle *h[3];       /* 1, 1, 2 or 3 handles by kind (equal K); the rest ignored */
+    const void *x;         /* fp16 [N][K] device, 16-byte aligned */
+    const void *residual;  /* QG_CALL_RUN_ADD: fp16 [N][M] device (may equal y[0]) */
+    void *y[3];            /* outputs, device, one per handle */
+} qg_call;
+
+typedef struct qg_chain qg_chain;
+
+/* qgemv_chain_create flags. */
+enum {
+    QG_CHAIN_PERSISTENT = 1u << 0  /* run eligible calls in one persistent launch
+                                      (default: one launch per call, each
+                                      chained to the previous one by
+                                      programmatic dependent launch) */
+};
+
+/* Create a chain on the current device: the state of the persistent launch
+ * (reflex-llm "docs/performance.md", Level 4): a pair of device counters and
+ * an error word (16 bytes of device memory, zeroed).  flags: QG_CHAIN_*.
+ * Errors: QG_EINVAL (null out, unknown flag), QG_ENOMEM, QG_ECUDA. */
+qg_status qgemv_chain_create(qg_chain **out, uint32_t flags);
+
+/* Run calls[0 .. ncalls-1] in order on `stream` (reflex-llm
+ * "docs/performance.md", Level 4 persistent kernels; the calls are those of
+ * "docs/kernels.md", uint32-loads section).  Results: those of issuing
+ * the same calls one by one through their entry points on the same stream,
+ * bit for bit; in particular call c reads its x and residual only after
+ * calls 0 .. c-1 have written all their outputs, so a call may consume an
+ * earlier call's output.  By default each call runs through its entry point
+ * (one launch per call, chained by programmatic dependent launch: measured
+ * the faster form on GB300).  With QG_CHAIN_PERSISTENT, up to four
+ * consecutive calls run in one persistent launch when each has N <= 8, x of
+ * at most 48 KB (N * K/256 * 576 bytes), Q4_K or Q6_K handles on the chain's
+ * device and no QG_FLAG_FORCE_REFERENCE / QG_FLAG_DEBUG_SYNC; the other calls
+ * run through their entry points, in order.  Every call is checked (as its entry point
+ * checks it) before anything is launched.  Launches of one chain must be
+ * ordered (one stream, or streams ordered by events): they share its
+ * counters.  The call does not synchronize.  Errors: QG_EINVAL (null c or
+ * calls, ncalls < 1, bad kind, a call's own argument errors), QG_EALIGN,
+ * QG_EUNSUPPORTED, QG_ECUDA. */
+qg_status qgemv_chain_run(qg_chain *c, const qg_call *calls, int32_t ncalls, void *stream);
+
+/* Read (and with clear != 0, reset) the chain's device error word: bits 1
+ * and 2 as for qgemv_device_status, bit 4: a wait for the earlier calls'
+ * outputs ran out (results undefined); the kernel never traps (reflex-llm
+ * "docs/kernels.md", uint32-loads section: a fault must never crash
+ * generation).  Synchronous.  Errors: QG_EINVAL (null c), QG_ECUDA. */
+qg_status qgemv_chain_status(qg_chain *c, uint32_t *flags_out, int clear);
+
+/* Free the chain's state (NULL is a no-op); the pages have no counterpart
+ * (library housekeeping).  No launch of it may be in flight. */
+void qgemv_chain_destroy(qg_chain *c);
+
 /* Human-readable description of the options in effect (flags, environment
  * overrides QGEMV_FORCE_REFERENCE, QGEMV_DEBUG_SYNC, QGEMV_FAULT_INJECT)
  * (TandemLLM "Kernels", Knobs: every switch and the values in effect can be

@@ -11,6 +11,7 @@
 #include <cstring>
 #include <string>
 
+#include "qg_chain.cuh"
 #include "qg_launch.cuh"
 #include "qg_tc.cuh"
 #include "qgemv.h"
@@ -45,6 +46,14 @@ struct qg_handle {
     void *hy;
     size_t hy_cap;
     bool owns_buffers;     // xs and err were allocated by qgemv_create
+};
+
+struct qg_chain {
+    int device;
+    int sms;
+    uint32_t flags;       // QG_CHAIN_*
+    unsigned int *words;  // [0] calls finished (summed over CTAs), [1] CTAs past their
+                          // waits, [2] error word
 };
 
 namespace {
@@ -908,6 +917,136 @@ qg_status run_with_scratch(qg_type t, int64_t M, int64_t K, const void *w_dev,
 void set_last_error(const char *msg) { g_err = msg; }
 }  // namespace qg
 
+namespace {
+
+int call_nh(int kind) { return kind == QG_CALL_PAIR ? 2 : kind == QG_CALL_TRIPLE ? 3 : 1; }
+
+qg_status check_call(const qg_call &c)
+{
+    if (c.kind < QG_CALL_RUN || c.kind > QG_CALL_TRIPLE)
+        return fail(QG_EINVAL, "bad chain call kind %d", (int)c.kind);
+    const int nh = call_nh(c.kind);
+    const qg_out ydt = c.kind == QG_CALL_RUN_ADD ? QG_OUT_F16 : (qg_out)c.out_dtype;
+    if (c.kind == QG_CALL_RUN_ADD && c.out_dtype != QG_OUT_F16)
+        return fail(QG_EINVAL, "a residual call writes fp16");
+    for (int i = 0; i < nh; ++i) {
+        const qg_status st = check_run_args(c.h[i], c.x, c.N, c.y[i], ydt);
+        if (st != QG_OK) return st;
+        if (c.h[i]->K != c.h[0]->K) return fail(QG_EINVAL, "the handles of a call must share K");
+        for (int j = 0; j < i; ++j)
+            if (c.y[i] == c.y[j]) return fail(QG_EINVAL, "the outputs of a call must differ");
+    }
+    if (c.kind == QG_CALL_RUN_ADD) {
+        if (!c.residual) return fail(QG_EINVAL, "null residual");
+        if (!aligned(c.residual, 2)) return fail(QG_EALIGN, "residual misaligned");
+    }
+    return QG_OK;
+}
+
+qg_status run_call(const qg_call &c, cudaStream_t s)
+{
+    void *sv = (void *)s;
+    switch (c.kind) {
+    case QG_CALL_RUN: return qgemv_run(c.h[0], c.x, c.N, c.y[0], (qg_out)c.out_dtype, sv);
+    case QG_CALL_RUN_ADD: return qgemv_run_add(c.h[0], c.x, c.N, c.residual, c.y[0], sv);
+    case QG_CALL_PAIR:
+        return qgemv_pair_run(c.h[0], c.h[1], c.x, c.N, c.y[0], c.y[1], (qg_out)c.out_dtype, sv);
+    default:
+        return qgemv_triple_run(c.h[0], c.h[1], c.h[2], c.x, c.N, c.y[0], c.y[1], c.y[2],
+                                (qg_out)c.out_dtype, sv);
+    }
+}
+
+// Calls the persistent chain kernel serves: N <= 8 with x in shared memory,
+// Q4_K / Q6_K handles on the chain's device, default arithmetic flags.
+bool chain_ok(const qg_chain *ch, const qg_call &c)
+{
+    if (c.N > 8 || !gemv_x_fits(c.N, c.h[0]->nb)) return false;
+    for (int i = 0; i < call_nh(c.kind); ++i) {
+        const qg_handle *h = c.h[i];
+        if (h->type != QG_Q4_K && h->type != QG_Q6_K) return false;
+        if (h->flags & (QG_FLAG_FORCE_REFERENCE | QG_FLAG_DEBUG_SYNC)) return false;
+        if (h->device != ch->device) return false;
+    }
+    return !env_on("QGEMV_FORCE_REFERENCE") && !env_on("QGEMV_DEBUG_SYNC");
+}
+
+// One persistent launch for calls[0 .. n-1] (all chain_ok).
+qg_status launch_chain_calls(qg_chain *ch, const qg_call *calls, int n, cudaStream_t s)
+{
+    ChainParams p;
+    memset(&p, 0, sizeof p);
+    int nm = 0, xbytes = 0, maxtiles = 0;
+    bool one = true;
+    for (int c = 0; c < n; ++c) {
+        const qg_call &q = calls[c];
+        ChainCall &cl = p.call[c];
+        const int nh = call_nh(q.kind);
+        cl.mat0 = nm;
+        cl.nmat = nh;
+        int tiles = 0, slot = 0;
+        for (int i = 0; i < nh; ++i) {
+            const qg_handle *h = q.h[i];
+            Mat m = mat_of(h, q.y[i], q.kind == QG_CALL_RUN_ADD ? (const __half *)q.residual
+                                                                : nullptr);
+            m.tile_begin = tiles;
+            const int R = kGemvRows / h->kw;
+            tiles += (int)((h->M + R - 1) / R);
+            p.mat[nm++] = m;
+            const int b = gemv_stage_bytes_host(h->type, h->kw);
+            slot = b > slot ? b : slot;
+        }
+        const qg_handle *h0 = q.h[0];
+        cl.tiles = tiles;
+        cl.slot_bytes = slot;
+        cl.N = (int)q.N;
+        cl.K = (int)h0->K;
+        cl.nb = h0->nb;
+        cl.xtok = gemv_xtok(h0->nb);
+        cl.out_f32 = (q.kind != QG_CALL_RUN_ADD && q.out_dtype == QG_OUT_F32) ? 1 : 0;
+        cl.x = (const __half *)q.x;
+        const int xb = (int)q.N * cl.xtok;
+        xbytes = xb > xbytes ? xb : xbytes;
+        maxtiles = tiles > maxtiles ? tiles : maxtiles;
+        one = one && q.N == 1;
+    }
+    // Each side gets half of the CTA's shared memory; its ring is what the
+    // barriers, the largest staged x and the partials leave, re-cut per call
+    // into as many slots of the call's largest stage as fit.
+    const int side = (chain_max_smem() / 2) & ~1023;
+    const int ring = side - chain_side_bytes(0, xbytes);
+    int ring_used = 0;
+    for (int c = 0; c < n; ++c) {
+        ChainCall &cl = p.call[c];
+        int st = ring / cl.slot_bytes;
+        st = st < kChainSlots ? st : kChainSlots;
+        if (st < 2) return fail(QG_EUNSUPPORTED, "chain does not fit shared memory");
+        cl.stages = st;
+        ring_used = st * cl.slot_bytes > ring_used ? st * cl.slot_bytes : ring_used;
+    }
+    const int smem = 2 * side;
+    const int per_sm = chain_ctas_per_sm(smem, one);
+    if (per_sm < 1 || ch->sms < 1) return fail(QG_EUNSUPPORTED, "chain kernel does not fit an SM");
+    // Every CTA must be resident at once (they wait for one another): one per
+    // SM, each side a virtual CTA (tiles t and t + grid share an SM).
+    int grid = per_sm * ch->sms;
+    grid = grid < maxtiles ? grid : maxtiles;
+    p.ncalls = n;
+    p.side_bytes = side;
+    p.xoff = kChainHdr + ring_used;
+    p.redoff = p.xoff + xbytes;
+    p.err = ch->words + 2;
+    p.ctr = ch->words;
+    const cudaError_t e = launch_chain(p, grid, smem, one, s);
+    if (e != cudaSuccess) {
+        cudaGetLastError();
+        return cuda_fail(e, "chain kernel launch");
+    }
+    return QG_OK;
+}
+
+}  // namespace
+
 extern "C" {
 
 int64_t qgemv_row_bytes(qg_type t, int64_t K)
@@ -1180,6 +1319,89 @@ qg_status qgemv_plan_info(const qg_handle *h, int64_t N, int32_t *ksplit, int32_
     if (rows_cta && nfirst <= 8 && gv_x_ok(h, nfirst) && !(h->flags & QG_FLAG_FORCE_REFERENCE))
         *rows_cta = kGemvRows / h->kw;
     return QG_OK;
+}
+
+
+qg_status qgemv_chain_create(qg_chain **out, uint32_t flags)
+{
+    if (!out) return fail(QG_EINVAL, "null out");
+    *out = nullptr;
+    if (flags & ~(uint32_t)QG_CHAIN_PERSISTENT) return fail(QG_EINVAL, "unknown chain flag");
+    qg_chain *c = new qg_chain();
+    c->flags = flags;
+    cudaError_t e = cudaGetDevice(&c->device);
+    if (e == cudaSuccess)
+        e = cudaDeviceGetAttribute(&c->sms, cudaDevAttrMultiProcessorCount, c->device);
+    if (e != cudaSuccess) {
+        delete c;
+        return cuda_fail(e, "device query");
+    }
+    e = cudaMalloc(&c->words, 4 * sizeof(unsigned int));
+    if (e != cudaSuccess) {
+        cudaGetLastError();
+        delete c;
+        return fail(QG_ENOMEM, "chain counters: %s", cudaGetErrorName(e));
+    }
+    e = cudaMemset(c->words, 0, 4 * sizeof(unsigned int));
+    if (e != cudaSuccess) {
+        cudaFree(c->words);
+        delete c;
+        return cuda_fail(e, "chain counters reset");
+    }
+    *out = c;
+    return QG_OK;
+}
+
+qg_status qgemv_chain_run(qg_chain *c, const qg_call *calls, int32_t ncalls, void *stream)
+{
+    g_err.clear();
+    if (!c || !calls) return fail(QG_EINVAL, "null chain or calls");
+    if (ncalls < 1) return fail(QG_EINVAL, "ncalls must be >= 1");
+    for (int i = 0; i < ncalls; ++i) {
+        const qg_status st = check_call(calls[i]);
+        if (st != QG_OK) return st;
+    }
+    const cudaStream_t s = (cudaStream_t)stream;
+    int i = 0;
+    while (i < ncalls) {
+        int j = i;
+        if (c->flags & QG_CHAIN_PERSISTENT)
+            while (j < ncalls && j - i < kChainMaxCalls && chain_ok(c, calls[j])) ++j;
+        if (j - i >= 2 && !fault_at("chain")) {
+            const qg_status st = launch_chain_calls(c, calls + i, j - i, s);
+            if (st == QG_OK) {
+                i = j;
+                continue;
+            }
+            if (st != QG_EUNSUPPORTED) return st;
+        }
+        // one call through its entry point
+        const qg_status st = run_call(calls[i], s);
+        if (st != QG_OK) return st;
+        ++i;
+    }
+    return QG_OK;
+}
+
+qg_status qgemv_chain_status(qg_chain *c, uint32_t *flags_out, int clear)
+{
+    if (!c) return fail(QG_EINVAL, "null chain");
+    unsigned int w = 0;
+    cudaError_t e = cudaMemcpy(&w, c->words + 2, sizeof w, cudaMemcpyDeviceToHost);
+    if (e != cudaSuccess) return cuda_fail(e, "chain error word read");
+    if (clear && w) {
+        e = cudaMemset(c->words + 2, 0, sizeof(unsigned int));
+        if (e != cudaSuccess) return cuda_fail(e, "chain error word reset");
+    }
+    if (flags_out) *flags_out = w;
+    return QG_OK;
+}
+
+void qgemv_chain_destroy(qg_chain *c)
+{
+    if (!c) return;
+    cudaFree(c->words);
+    delete c;
 }
 
 }  // extern "C"

@@ -1020,6 +1020,70 @@ __device__ __forceinline__ int gemv_stage_bytes(int kw)
     return kw * R * Fmt<T>::BB;
 }
 
+// One stage of the N <= 8 weight ring: super-blocks i*kw .. i*kw + kw - 1 of
+// rows row0 .. row0 + R - 1 into the slot at shared address dst (generic
+// pointer dstp), completing on the full barrier fb.  stage_bytes must be
+// exactly the bytes the tensor copies deliver (gemv_stage_bytes<T>(kw)): the
+// barrier's phase completes when that many have landed.  Called by the
+// whole producer warp.  The weights are read once per call: evict-first in L2.
+template <int T>
+__device__ __forceinline__ void gemv_produce(const Mat &m, int kw, int R, int row0, int nb, int i,
+                                             uint32_t dst, uint8_t *dstp, uint32_t fb,
+                                             int stage_bytes, uint64_t wpol, int lane)
+{
+    const int sbq = i * kw;
+    if (T != T_Q6K) {
+        if (lane == 0) {
+            mbar_arrive_expect_tx(fb, (uint32_t)stage_bytes);
+            if (T == T_FP4) {
+                tma_load_3d_ef(dst, &m.tmw, 0, row0, sbq, fb, wpol);
+                tma_load_3d_ef(dst + kw * R * 128, &m.tms, 0, row0, sbq, fb, wpol);
+            } else if (T == T_FP8) {
+                // planes of 128 codes: two per super-block
+                tma_load_3d_ef(dst, &m.tmw, 0, row0, 2 * sbq, fb, wpol);
+            } else {
+                tma_load_3d_ef(dst, &m.tmw, 0, row0, sbq, fb, wpol);
+            }
+        }
+        return;
+    }
+    // Q6_K: per row, the aligned superset of the stage's blocks; anything
+    // past the end of the matrix is not read.
+    const int nv = min(kw, nb - sbq);
+    const int pitch = q6_pitch(kw);
+    const uint8_t *end = m.w + m.w_bytes;
+    uint32_t bytes = 0;
+    for (int r = lane; r < R; r += 32) {
+        const int row = row0 + r;
+        if (row >= m.M) continue;
+        const uint8_t *blk = m.w + (int64_t)row * m.row_bytes + (int64_t)sbq * 210;
+        const uint8_t *al = (const uint8_t *)((uintptr_t)blk & ~(uintptr_t)15);
+        const uint8_t *stop = blk + 210 * nv;
+        uint32_t n = (uint32_t)(((stop - al) + 15) & ~(int64_t)15);
+        if (al + n > end) {
+            n = (uint32_t)((end - al) & ~(int64_t)15);
+            uint8_t *d = dstp + r * pitch;
+            for (uint32_t b = n; al + b < stop; ++b) d[b] = al[b];
+        }
+        bytes += n;
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) bytes += __shfl_xor_sync(0xffffffffu, bytes, o);
+    __syncwarp();
+    if (lane == 0) mbar_arrive_expect_tx(fb, bytes);
+    __syncwarp();
+    for (int r = lane; r < R; r += 32) {
+        const int row = row0 + r;
+        if (row >= m.M) continue;
+        const uint8_t *blk = m.w + (int64_t)row * m.row_bytes + (int64_t)sbq * 210;
+        const uint8_t *al = (const uint8_t *)((uintptr_t)blk & ~(uintptr_t)15);
+        const uint8_t *stop = blk + 210 * nv;
+        uint32_t n = (uint32_t)(((stop - al) + 15) & ~(int64_t)15);
+        if (al + n > end) n = (uint32_t)((end - al) & ~(int64_t)15);
+        if (n) bulk_g2s_ef(dst + r * pitch, al, n, fb, wpol);
+    }
+}
+
 template <int T, bool ODD>
 __device__ __forceinline__ void gemv_tile(const Params &p, const Mat &m, int rtile, uint8_t *smem,
                                           int role)
@@ -1054,62 +1118,11 @@ __device__ __forceinline__ void gemv_tile(const Params &p, const Mat &m, int rti
     __syncthreads();
 
     // Producer: fill slot `slot` with stage i (super-blocks i*kw .. i*kw + kw - 1).
-    // The weights are read once per call: evict-first in L2.
     const uint64_t wpol = l2_evict_first_policy();
     auto produce = [&](int i, int slot) {
-        const int sbq = i * kw;
         const uint32_t dst = slots + slot * slot_bytes;
-        const uint32_t fb = bar_full + 8 * slot;
-        if (TMA) {
-            if (lane == 0) {
-                mbar_arrive_expect_tx(fb, (uint32_t)slot_bytes);
-                if (T == T_FP4) {
-                    tma_load_3d_ef(dst, &m.tmw, 0, row0, sbq, fb, wpol);
-                    tma_load_3d_ef(dst + kw * R * 128, &m.tms, 0, row0, sbq, fb, wpol);
-                } else if (T == T_FP8) {
-                    // planes of 128 codes: two per super-block
-                    tma_load_3d_ef(dst, &m.tmw, 0, row0, 2 * sbq, fb, wpol);
-                } else {
-                    tma_load_3d_ef(dst, &m.tmw, 0, row0, sbq, fb, wpol);
-                }
-            }
-        } else {
-            // Q6_K: per row, the aligned superset of the stage's blocks;
-            // anything past the end of the matrix is not read.
-            const int nv = min(kw, p.nb - sbq);
-            const int pitch = q6_pitch(kw);
-            const uint8_t *end = m.w + m.w_bytes;
-            uint32_t bytes = 0;
-            for (int r = lane; r < R; r += 32) {
-                const int row = row0 + r;
-                if (row >= m.M) continue;
-                const uint8_t *blk = m.w + (int64_t)row * m.row_bytes + (int64_t)sbq * 210;
-                const uint8_t *al = (const uint8_t *)((uintptr_t)blk & ~(uintptr_t)15);
-                const uint8_t *stop = blk + 210 * nv;
-                uint32_t n = (uint32_t)(((stop - al) + 15) & ~(int64_t)15);
-                if (al + n > end) {
-                    n = (uint32_t)((end - al) & ~(int64_t)15);
-                    uint8_t *d = smem + (dst - sbase) + r * pitch;
-                    for (uint32_t b = n; al + b < stop; ++b) d[b] = al[b];
-                }
-                bytes += n;
-            }
-#pragma unroll
-            for (int o = 16; o > 0; o >>= 1) bytes += __shfl_xor_sync(0xffffffffu, bytes, o);
-            __syncwarp();
-            if (lane == 0) mbar_arrive_expect_tx(fb, bytes);
-            __syncwarp();
-            for (int r = lane; r < R; r += 32) {
-                const int row = row0 + r;
-                if (row >= m.M) continue;
-                const uint8_t *blk = m.w + (int64_t)row * m.row_bytes + (int64_t)sbq * 210;
-                const uint8_t *al = (const uint8_t *)((uintptr_t)blk & ~(uintptr_t)15);
-                const uint8_t *stop = blk + 210 * nv;
-                uint32_t n = (uint32_t)(((stop - al) + 15) & ~(int64_t)15);
-                if (al + n > end) n = (uint32_t)((end - al) & ~(int64_t)15);
-                if (n) bulk_g2s_ef(dst + r * pitch, al, n, fb, wpol);
-            }
-        }
+        gemv_produce<T>(m, kw, R, row0, p.nb, i, dst, smem + (dst - sbase), bar_full + 8 * slot,
+                        slot_bytes, wpol, lane);
     };
 
     unsigned int err = 0;

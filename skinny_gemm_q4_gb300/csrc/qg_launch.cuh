@@ -28,6 +28,13 @@ cudaError_t launch_ref_gemv(const Mat &m, int K, const __half *x, int N, int out
 cudaError_t launch_ref_swiglu(const Mat &gate, const Mat &up, int K, const __half *x, int N,
                               int out_f32, cudaStream_t stream);
 
+// The persistent decode chain (qg_chain.cuh, defined in qg_inst_chain.cu):
+// CTAs of `smem` bytes that one SM holds at once (0: unknown), and the launch.
+struct ChainParams;
+int chain_max_smem();
+int chain_ctas_per_sm(int smem, bool one);
+cudaError_t launch_chain(const ChainParams &p, int grid, int smem, bool one, cudaStream_t s);
+
 // Per type-set launchers (defined in qg_inst_*.cu).
 #define QG_DECLARE_TSET(NAME)                                                           \
     cudaError_t launch_gemv_##NAME(const Params &p, dim3 grid, int smem, cudaStream_t s); \

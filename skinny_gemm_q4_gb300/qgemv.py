@@ -38,11 +38,26 @@ STATUS_NAMES = {0: "QG_OK", -1: "QG_EINVAL", -2: "QG_EUNSUPPORTED", -3: "QG_EALI
 EXPORTS = ["qgemv_create", "qgemv_run", "qgemv_run_add", "qgemv_pair_run", "qgemv_triple_run",
            "qgemv_run_host", "qgemv_dequantize", "qgemv_destroy", "qgemv_last_error",
            "qgemv_row_bytes", "qgemv_plan_info", "qgemv_describe", "qgemv_device_status",
-           "qgemv_run_noalloc", "qgemv_pair_swiglu_run"]
+           "qgemv_run_noalloc", "qgemv_pair_swiglu_run", "qgemv_chain_create",
+           "qgemv_chain_run", "qgemv_chain_status", "qgemv_chain_destroy"]
+
+CHAIN_PERSISTENT = 1
+
+CALL_RUN = 0
+CALL_RUN_ADD = 1
+CALL_PAIR = 2
+CALL_TRIPLE = 3
 
 
 class QgOpts(ctypes.Structure):
     _fields_ = [("flags", ctypes.c_uint32), ("max_tokens", ctypes.c_int32)]
+
+
+class QgCall(ctypes.Structure):
+    """struct qg_call (one call of a decode chain)."""
+    _fields_ = [("kind", ctypes.c_int32), ("out_dtype", ctypes.c_int32), ("N", ctypes.c_int64),
+                ("h", ctypes.c_void_p * 3), ("x", ctypes.c_void_p),
+                ("residual", ctypes.c_void_p), ("y", ctypes.c_void_p * 3)]
 
 
 class QgemvError(RuntimeError):
@@ -86,9 +101,15 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.qgemv_run_noalloc.argtypes = [c_int, i64, i64, vp, vp, ctypes.c_float, vp, i64, vp, c_int,
                                       vp]
     lib.qgemv_pair_swiglu_run.argtypes = [vp, vp, vp, i64, vp, c_int, vp]
+    lib.qgemv_chain_create.argtypes = [ctypes.POINTER(vp), ctypes.c_uint32]
+    lib.qgemv_chain_run.argtypes = [vp, ctypes.POINTER(QgCall), i32, vp]
+    lib.qgemv_chain_status.argtypes = [vp, ctypes.POINTER(ctypes.c_uint32), c_int]
+    lib.qgemv_chain_destroy.argtypes = [vp]
+    lib.qgemv_chain_destroy.restype = None
     for name in ("qgemv_create", "qgemv_run", "qgemv_run_add", "qgemv_pair_run",
                  "qgemv_triple_run", "qgemv_run_host", "qgemv_dequantize", "qgemv_plan_info",
-                 "qgemv_device_status", "qgemv_run_noalloc", "qgemv_pair_swiglu_run"):
+                 "qgemv_device_status", "qgemv_run_noalloc", "qgemv_pair_swiglu_run",
+                 "qgemv_chain_create", "qgemv_chain_run", "qgemv_chain_status"):
         getattr(lib, name).restype = c_int
     _lib = lib
     return lib
@@ -179,6 +200,42 @@ def qgemv_run_noalloc(qtype, M, K, w_ptr, scales_ptr, global_scale, x_ptr, N, y_
     _check(load().qgemv_run_noalloc(qtype, M, K, w_ptr or None, scales_ptr or None, global_scale,
                                     x_ptr or None, N, y_ptr or None, ydt, stream),
            "qgemv_run_noalloc")
+
+
+def qgemv_chain_create(flags: int = 0) -> int:
+    c = ctypes.c_void_p()
+    _check(load().qgemv_chain_create(ctypes.byref(c), flags), "qgemv_chain_create")
+    return c.value
+
+
+def qgemv_chain_run(c, calls, stream):
+    """calls: a QgCall array (see make_calls)."""
+    _check(load().qgemv_chain_run(c, calls, len(calls), stream), "qgemv_chain_run")
+
+
+def qgemv_chain_status(c, clear: bool = False) -> int:
+    w = ctypes.c_uint32()
+    _check(load().qgemv_chain_status(c, ctypes.byref(w), 1 if clear else 0), "qgemv_chain_status")
+    return w.value
+
+
+def qgemv_chain_destroy(c):
+    if c:
+        load().qgemv_chain_destroy(c)
+
+
+def make_calls(specs):
+    """QgCall array from (kind, handles, x_ptr, N, ys, out_dtype, residual_ptr)
+    tuples (raw pointers and handle values)."""
+    arr = (QgCall * len(specs))()
+    for i, (kind, hs, x, N, ys, odt, res) in enumerate(specs):
+        c = arr[i]
+        c.kind, c.out_dtype, c.N, c.x, c.residual = kind, odt, N, x, res or None
+        for j, h in enumerate(hs):
+            c.h[j] = h
+        for j, y in enumerate(ys):
+            c.y[j] = y
+    return arr
 
 
 # ----------------------------------------------------- torch convenience
@@ -273,3 +330,29 @@ def pair_swiglu_run(gate: QGemv, up: QGemv, x, out_f32: bool = False, stream=Non
     qgemv_pair_swiglu_run(gate.h, up.h, x.data_ptr(), N, h.data_ptr(),
                           OUT_F32 if out_f32 else OUT_F16, _stream_ptr(stream))
     return h
+
+
+class Chain:
+    """A decode chain: consecutive calls in one persistent launch where the
+    library can, with the results of issuing them one by one."""
+
+    def __init__(self, flags: int = 0):
+        self.c = qgemv_chain_create(flags)
+
+    def run(self, calls, stream=None):
+        """calls: QgCall array from make_calls (reusable across runs)."""
+        qgemv_chain_run(self.c, calls, _stream_ptr(stream))
+
+    def status(self, clear: bool = False) -> int:
+        return qgemv_chain_status(self.c, clear)
+
+    def close(self):
+        if getattr(self, "c", None):
+            qgemv_chain_destroy(self.c)
+            self.c = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass

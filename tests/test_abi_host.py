@@ -92,6 +92,11 @@ def test_null_handle_calls_are_errors(lib):
     assert lib.qgemv_dequantize(None, 16, None) == -1
     assert lib.qgemv_run_host(None, 16, 1, 16, 0, None) == -1
     lib.qgemv_destroy(None)
+    from skinny_gemm_q4_gb300 import qgemv as q
+    calls = q.make_calls([(q.CALL_RUN, [None], 16, 1, [16], 0, None)])
+    assert lib.qgemv_chain_run(None, calls, 1, None) == -1
+    assert lib.qgemv_chain_status(None, None, 0) == -1
+    lib.qgemv_chain_destroy(None)
 
 
 def test_product_path_never_imports_the_oracle():
