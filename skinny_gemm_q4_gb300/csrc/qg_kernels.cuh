@@ -1181,7 +1181,12 @@ __device__ __forceinline__ void gemv_tile(const Params &p, const Mat &m, int rti
             }
         }
     }
-    __syncthreads();
+    // x is staged.  The Q6_K producer took no part in it and may still be
+    // issuing its first stages' per-row copies: only the consumers meet.
+    if (TMA)
+        __syncthreads();
+    else if (warp > 0)
+        bar_sync_named(1, 32 * kGemvCW);
 
     Acc<T, 1, 1> A;
     A.zero();
