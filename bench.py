@@ -542,28 +542,62 @@ def run_ours(args):
     if part == "layer" and not args.no_configs:
         configs = run_configs(args, torch, qg, synth, layers, side, e0, e1, peak, tpeak, dev)
 
-    # End to end through the host-buffer entry point: per matrix, x from
-    # pinned host memory, y back to pinned host memory, synchronized.
-    e2e_steps = min(args.steps, N_LAYERS) if part == "layer" else 0
-    hx = {K: torch.from_numpy(np.random.default_rng(K).standard_normal((1, K)).astype(np.float16))
-          .pin_memory() for K in (2560, 4096, 9728)}
-    hy = {M: torch.empty((1, M), dtype=f16).pin_memory() for M in (4096, 1024, 2560, 9728)}
-    h2d = sum(K * 2 for _, _, M, K in synth.LAYER)
-    d2h = sum(M * 2 for _, _, M, K in synth.LAYER)
-    s = torch.cuda.current_stream().cuda_stream
-    for L in range(2 if e2e_steps else 0):
-        for role, qt, M, K in synth.LAYER:
-            qg.qgemv_run_host(layers[L][role].h, hx[K].data_ptr(), 1, hy[M].data_ptr(),
-                              qg.OUT_F16, s)
-    barrier()
-    t0 = time.perf_counter()
-    for i in range(e2e_steps):
-        for role, qt, M, K in synth.LAYER:
-            qg.qgemv_run_host(layers[i % N_LAYERS][role].h, hx[K].data_ptr(), 1,
-                              hy[M].data_ptr(), qg.OUT_F16, s)
-    e2e_s = (time.perf_counter() - t0) / max(e2e_steps, 1)
-    barrier()
-    e2e_val = world * wbytes / e2e_s / 1e9 if e2e_steps else None
+    # End to end through the public API, as a user runs a decode step: the
+    # step's inputs (x of the four calls and the residual, one pinned host
+    # buffer, a new one each step out of four) copied to the device, the layer
+    # by one qgemv_chain_run call, every output copied back to pinned host
+    # memory, and the stream synchronized before the next step.
+    e2e_steps = min(args.steps, 4 * N_LAYERS) if part == "layer" else 0
+    e2e_val = None
+    h2d = d2h = 0
+    if e2e_steps:
+        kin = {"qkv": 2560, "o": 4096, "res": 2560, "ffn": 2560, "dn": 9728}
+        kout = {"q": 4096, "k": 1024, "v": 1024, "o": 2560, "g": 9728, "u": 9728, "d": 2560}
+        din = torch.empty(sum(kin.values()), dtype=f16, device=dev)
+        dout = torch.empty(sum(kout.values()), dtype=f16, device=dev)
+        hins = [torch.from_numpy(np.random.default_rng(100 + r).standard_normal(din.numel())
+                                 .astype(np.float16)).pin_memory() for r in range(4)]
+        hout = torch.empty(dout.numel(), dtype=f16).pin_memory()
+        h2d, d2h = din.numel() * 2, dout.numel() * 2
+
+        def views(buf, sizes):
+            out, o = {}, 0
+            for k, n in sizes.items():
+                out[k] = buf[o:o + n]
+                o += n
+            return out
+        vi, vo = views(din, kin), views(dout, kout)
+        ptr = lambda t: t.data_ptr()
+        e2e_calls = [qg.make_calls([
+            (qg.CALL_TRIPLE, [hs["wq"].h, hs["wk"].h, hs["wv"].h], ptr(vi["qkv"]), 1,
+             [ptr(vo["q"]), ptr(vo["k"]), ptr(vo["v"])], qg.OUT_F16, None),
+            (qg.CALL_RUN_ADD, [hs["wo"].h], ptr(vi["o"]), 1, [ptr(vo["o"])], qg.OUT_F16,
+             ptr(vi["res"])),
+            (qg.CALL_PAIR, [hs["gate"].h, hs["up"].h], ptr(vi["ffn"]), 1,
+             [ptr(vo["g"]), ptr(vo["u"])], qg.OUT_F16, None),
+            (qg.CALL_RUN, [hs["down"].h], ptr(vi["dn"]), 1, [ptr(vo["d"])], qg.OUT_F16, None)])
+            for hs in layers]
+        echain = qg.Chain()
+        cs = torch.cuda.current_stream()
+
+        def e2e_step(i):
+            din.copy_(hins[i % 4], non_blocking=True)
+            qg.qgemv_chain_run(echain.c, e2e_calls[i % N_LAYERS], cs.cuda_stream)
+            hout.copy_(dout, non_blocking=True)
+            cs.synchronize()
+
+        for i in range(max(args.warmup, 3)):
+            e2e_step(i)
+        barrier()
+        t0 = time.perf_counter()
+        for i in range(e2e_steps):
+            e2e_step(i)
+        e2e_s = (time.perf_counter() - t0) / e2e_steps
+        barrier()
+        e2e_val = world * wbytes / e2e_s / 1e9
+        if echain.status() != 0:
+            print(json.dumps({"error": "end-to-end chain reports a device timeout"}))
+            sys.exit(3)
 
     if rank != 0:
         return
@@ -619,7 +653,10 @@ def run_ours(args):
         "cpu_baseline": cpu,
         "e2e": None if e2e_val is None else {"value": round(e2e_val, 3), "unit": "GB/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h,
-                "how": "qgemv_run_host per matrix (pinned host x and y, synchronized)"},
+                "steps": e2e_steps,
+                "how": "per step: one pinned-host -> device copy of the step's inputs, "
+                       "qgemv_chain_run (the layer), one device -> pinned-host copy of all "
+                       "outputs, stream synchronized"},
         "configs": configs,
         "device_status": 0,
         "gpu_launches": launches_per_step * args.steps,
