@@ -1037,6 +1037,7 @@ qg_status launch_chain_calls(qg_chain *ch, const qg_call *calls, int n, cudaStre
     p.redoff = p.xoff + xbytes;
     p.err = ch->words + 2;
     p.ctr = ch->words;
+    p.hold_publish = fault_at("chain_publish") ? 1 : 0;
     const cudaError_t e = launch_chain(p, grid, smem, one, s);
     if (e != cudaSuccess) {
         cudaGetLastError();
@@ -1367,7 +1368,7 @@ qg_status qgemv_chain_run(qg_chain *c, const qg_call *calls, int32_t ncalls, voi
         int j = i;
         if (c->flags & QG_CHAIN_PERSISTENT)
             while (j < ncalls && j - i < kChainMaxCalls && chain_ok(c, calls[j])) ++j;
-        if (j - i >= 2 && !fault_at("chain")) {
+        if (j - i >= 2) {
             const qg_status st = launch_chain_calls(c, calls + i, j - i, s);
             if (st == QG_OK) {
                 i = j;

@@ -55,7 +55,19 @@ struct ChainParams {
     int xoff, redoff;    // offsets (within a side) of the staged x and the slice partials
     unsigned int *err;   // error word (timeouts)
     unsigned int *ctr;   // [0] calls finished, summed over CTAs; [1] CTAs done waiting
+    int hold_publish;    // test hook: virtual CTA 0 never publishes (the others' waits run out)
 };
+
+// Longest wait for the earlier calls' outputs before a side gives up (sets
+// ERR_CHAIN_TIMEOUT and goes on): far beyond any call's duration.
+constexpr unsigned long long kChainWaitNs = 500ull * 1000 * 1000;
+
+__device__ __forceinline__ unsigned long long globaltimer_ns()
+{
+    unsigned long long t;
+    asm volatile("mov.u64 %0, %%globaltimer;\n" : "=l"(t));
+    return t;
+}
 
 __device__ __forceinline__ uint4 ld_cg_v4(const void *p)
 {
@@ -338,9 +350,9 @@ __global__ void __launch_bounds__(kChainThreads, 1) qg_chain_kernel(const __grid
                 // every side of every CTA has stored its outputs of calls 0 .. c-1
                 if (tid == 32) {
                     const unsigned int target = (unsigned int)G * (unsigned int)c;
-                    uint32_t it = 0;
+                    const unsigned long long t0 = globaltimer_ns();
                     while (ld_acquire_u32(p.ctr) < target) {
-                        if (++it == (1u << 22)) {
+                        if (globaltimer_ns() - t0 > kChainWaitNs) {
                             err |= ERR_CHAIN_TIMEOUT;
                             break;
                         }
@@ -374,7 +386,7 @@ __global__ void __launch_bounds__(kChainThreads, 1) qg_chain_kernel(const __grid
                 // orders every consumer thread's stores before the release
                 bar_sync_named(bar, 32 * kGemvCW);
                 if (tid == 32) {
-                    red_release_add(p.ctr, 1u);
+                    if (!(p.hold_publish && b == 0)) red_release_add(p.ctr, 1u);
                     mbar_arrive(sbase + 128);
                 }
             }

@@ -219,3 +219,36 @@ def test_chain_in_a_graph(layer, chain_flags):
                        ("d", sd)):
             assert t.equal(ys[k], sep), (rep, k)
     assert ch.status() == 0
+
+
+def test_persistent_chain_reports_a_wait_that_runs_out(layer, monkeypatch):
+    """Failure detection without a GPU fault: with QGEMV_FAULT_INJECT=
+    chain_publish one side of the persistent launch never publishes its
+    outputs, so every other side's wait for the earlier calls runs out (about
+    half a second each) and sets bit 4 of the chain's error word instead of
+    hanging; the next launches are correct and report nothing."""
+    t = torch()
+    N = 1
+    xs = {k: to_dev(synth.activations(N, K, seed=47, stream=s))
+          for k, K, s in (("qkv", 2560, 1), ("o", 4096, 2), ("ffn", 2560, 3), ("dn", 9728, 4))}
+    res = to_dev(synth.residual(N, 2560, seed=47))
+    M = {"q": 4096, "k": 1024, "v": 1024, "o": 2560, "g": 9728, "u": 9728, "d": 2560}
+    ys = {k: _empty(N, m) for k, m in M.items()}
+    calls = _layer_calls(layer, xs, ys, N, res, False)
+    ch = qg.Chain(qg.CHAIN_PERSISTENT)
+    monkeypatch.setenv("QGEMV_FAULT_INJECT", "chain_publish")
+    ch.run(calls)
+    t.cuda.synchronize()
+    monkeypatch.delenv("QGEMV_FAULT_INJECT")
+    assert ch.status(clear=True) & 4
+    assert ch.status() == 0
+    ch.run(calls)
+    L = {k: v[0] for k, v in layer.items()}
+    sq, sk, sv = qg.triple_run(L["wq"], L["wk"], L["wv"], xs["qkv"])
+    so = L["wo"].run_add(xs["o"], res)
+    sg, su = qg.pair_run(L["gate"], L["up"], xs["ffn"])
+    sd = L["down"].run(xs["dn"])
+    t.cuda.synchronize()
+    for k, sep in (("q", sq), ("k", sk), ("v", sv), ("o", so), ("g", sg), ("u", su), ("d", sd)):
+        assert t.equal(ys[k], sep), k
+    assert ch.status() == 0
