@@ -587,6 +587,16 @@ __device__ __forceinline__ void compute_fp4(uint32_t cbase, int cp, uint32_t sba
             for (int gi = 0; gi < G; ++gi)
                 B[gi] = lds128(xsl + min(8 * gi + g, ntok - 1) * xtok +
                                ((hf * 4 + sp) * 4 + t) * 16);
+            // word sp of the thread's 16 code bytes feeds steps 2 sp (bytes 0,
+            // 1) and 2 sp + 1 (bytes 2, 3): the values fp4_decode gives, with
+            // the four conversions reading the word's bytes directly
+            uint32_t hw[MT][2][4];
+#pragma unroll
+            for (int mt = 0; mt < MT; ++mt)
+#pragma unroll
+                for (int rr = 0; rr < 2; ++rr)
+                    e2m1x8_to_h2x4(word_of(cw[mt][rr], sp), hw[mt][rr][0], hw[mt][rr][1],
+                                   hw[mt][rr][2], hw[mt][rr][3]);
 #pragma unroll
             for (int jj = 0; jj < 2; ++jj) {
                 const int s = 2 * sp + jj;  // step: bytes 2s, 2s+1 of the thread's 16
@@ -595,8 +605,9 @@ __device__ __forceinline__ void compute_fp4(uint32_t cbase, int cp, uint32_t sba
                     uint32_t a[2][2];
 #pragma unroll
                     for (int rr = 0; rr < 2; ++rr) {
-                        const uint32_t w = word_of(cw[mt][rr], s >> 1) >> (16 * (s & 1));
-                        fp4_decode(w, (s < 4) ? sA[mt][rr] : sB[mt][rr], a[rr][0], a[rr][1]);
+                        const uint32_t sc = (s < 4) ? sA[mt][rr] : sB[mt][rr];
+                        a[rr][0] = hmul2(hw[mt][rr][2 * jj], sc);
+                        a[rr][1] = hmul2(hw[mt][rr][2 * jj + 1], sc);
                     }
 #pragma unroll
                     for (int gi = 0; gi < G; ++gi)

@@ -117,6 +117,18 @@ __device__ __forceinline__ uint32_t e2m1x2_to_h2(uint32_t byte_in_low8)
     return d;
 }
 
+// Four code bytes of w (eight e2m1 values) -> four fp16x2, byte i in h[i],
+// each byte's low nibble in the low half, exact.
+__device__ __forceinline__ void e2m1x8_to_h2x4(uint32_t w, uint32_t &h0, uint32_t &h1, uint32_t &h2,
+                                               uint32_t &h3)
+{
+    asm("{\n .reg .b8 b0, b1, b2, b3;\n mov.b32 {b0, b1, b2, b3}, %4;\n"
+        " cvt.rn.f16x2.e2m1x2 %0, b0;\n cvt.rn.f16x2.e2m1x2 %1, b1;\n"
+        " cvt.rn.f16x2.e2m1x2 %2, b2;\n cvt.rn.f16x2.e2m1x2 %3, b3;\n}\n"
+        : "=r"(h0), "=r"(h1), "=r"(h2), "=r"(h3)
+        : "r"(w));
+}
+
 // Two packed e4m3 codes (low byte first) -> fp16x2, exact.
 __device__ __forceinline__ uint32_t e4m3x2_to_h2(uint32_t pair_in_low16)
 {
