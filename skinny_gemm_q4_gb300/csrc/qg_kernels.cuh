@@ -353,8 +353,7 @@ __device__ __forceinline__ void fp4_decode(uint32_t w, uint32_t sc, uint32_t &x0
 // (e0, e1) and (e2, e3) as fp16x2, exact (every e4m3 value is an fp16 value).
 __device__ __forceinline__ void fp8_decode(uint32_t w, uint32_t &x01, uint32_t &x23)
 {
-    x01 = e4m3x2_to_h2(w & 0xffffu);
-    x23 = e4m3x2_to_h2(w >> 16);
+    e4m3x4_to_h2x2(w, x01, x23);
 }
 
 // bf16 bits -> fp32 (exact).

@@ -140,6 +140,16 @@ __device__ __forceinline__ uint32_t e4m3x2_to_h2(uint32_t pair_in_low16)
     return d;
 }
 
+// Four packed e4m3 codes -> (e0, e1) and (e2, e3) as fp16x2, exact: both
+// conversions read their 16-bit halves of w directly.
+__device__ __forceinline__ void e4m3x4_to_h2x2(uint32_t w, uint32_t &lo2, uint32_t &hi2)
+{
+    asm("{\n .reg .b16 lo, hi;\n mov.b32 {lo, hi}, %2;\n"
+        " cvt.rn.f16x2.e4m3x2 %0, lo;\n cvt.rn.f16x2.e4m3x2 %1, hi;\n}\n"
+        : "=r"(lo2), "=r"(hi2)
+        : "r"(w));
+}
+
 // Programmatic dependent launch controls (no-ops without a PDL predecessor).
 __device__ __forceinline__ void pdl_wait()
 {
