@@ -325,7 +325,10 @@ qg_status qgemv_chain_create(qg_chain **out, uint32_t flags);
  * consecutive calls run in one persistent launch when each has N <= 8, x of
  * at most 48 KB (N * K/256 * 576 bytes), Q4_K or Q6_K handles on the chain's
  * device and no QG_FLAG_FORCE_REFERENCE / QG_FLAG_DEBUG_SYNC; the other calls
- * run through their entry points, in order.  Every call is checked (as its entry point
+ * run through their entry points, in order.  The persistent form puts one CTA
+ * on every SM and its CTAs wait for one another: kernels of other streams that
+ * hold SMs meanwhile can delay some CTAs past the waits' limit (reported by
+ * qgemv_chain_status, bit 4).  Every call is checked (as its entry point
  * checks it) before anything is launched.  Launches of one chain must be
  * ordered (one stream, or streams ordered by events): they share its
  * counters.  The call does not synchronize.  Errors: QG_EINVAL (null c or
