@@ -109,3 +109,59 @@ def test_nvfp4_full_size(M, K):
         yref, mag = oracle.qgemv(oracle.NVFP4, w, M, K, x[:N], scales=sc, global_scale=g,
                                  rows=rows)
         check_close(y[:, rows], yref, mag, what=f"nvfp4 {M}x{K} N={N}")
+
+
+@pytest.mark.parametrize("N", [1, 33, 128])
+def test_36_layer_set_as_the_bench_runs_it(N):
+    """The decode-layer set the bench times: 36 layers of device-generated
+    weights (2.3 GB), each layer's four calls in the bench's form (at N = 1
+    one qgemv_chain_run, at N = 33 and 128 the prefill chunks), with device-
+    generated x.  Sampled rows of every matrix of every layer against the
+    oracle (weights, x and residual copied back from the generators'
+    buffers)."""
+    t = torch()
+    dev = t.device("cuda", 0)
+    f16 = t.float16
+    ORT = {qg.Q4_K: oracle.Q4_K, qg.Q6_K: oracle.Q6_K}
+    xs = {k: synth.device_activations(N, K, 0, s, dev)
+          for k, K, s in (("qkv", 2560, 1), ("o", 4096, 2), ("res", 2560, 3), ("ffn", 2560, 4),
+                          ("dn", 9728, 5))}
+    xh = {k: v.cpu().numpy() for k, v in xs.items()}
+    M = {"q": 4096, "k": 1024, "v": 1024, "o": 2560, "g": 9728, "u": 9728, "d": 2560}
+    ys = {k: t.empty((N, m), dtype=f16, device=dev) for k, m in M.items()}
+    P = lambda v: v.data_ptr()
+    chain = qg.Chain()
+    out_of = {"wq": ("q", "qkv"), "wk": ("k", "qkv"), "wv": ("v", "qkv"), "wo": ("o", "o"),
+              "gate": ("g", "ffn"), "up": ("u", "ffn"), "down": ("d", "dn")}
+    rng = np.random.default_rng(36)
+    worst = 0.0
+    for L in range(36):
+        hs, host = {}, {}
+        for i, (role, qt, Mr, K) in enumerate(synth.LAYER):
+            w, sc, g = synth.device_weights(qt, Mr, K, seed=0, stream=1000 * L + i, device=dev)
+            hs[role] = qg.QGemv(qt, Mr, K, w, sc, g, max_tokens=128)
+            host[role] = w
+        h = {k: v.h for k, v in hs.items()}
+        calls = qg.make_calls([
+            (qg.CALL_TRIPLE, [h["wq"], h["wk"], h["wv"]], P(xs["qkv"]), N,
+             [P(ys["q"]), P(ys["k"]), P(ys["v"])], qg.OUT_F16, None),
+            (qg.CALL_RUN_ADD, [h["wo"]], P(xs["o"]), N, [P(ys["o"])], qg.OUT_F16, P(xs["res"])),
+            (qg.CALL_PAIR, [h["gate"], h["up"]], P(xs["ffn"]), N, [P(ys["g"]), P(ys["u"])],
+             qg.OUT_F16, None),
+            (qg.CALL_RUN, [h["down"]], P(xs["dn"]), N, [P(ys["d"])], qg.OUT_F16, None)])
+        chain.run(calls)
+        t.cuda.synchronize()
+        for role, qt, Mr, K in synth.LAYER:
+            yk, xk = out_of[role]
+            rows = np.unique(np.concatenate([[0, Mr - 1], rng.integers(0, Mr, 3)]))
+            wrows = host[role][t.from_numpy(rows).to(dev)].cpu().numpy()
+            yref, mag = oracle.qgemv(ORT[qt], wrows, len(rows), K, xh[xk],
+                                     residual=xh["res"][:, rows] if role == "wo" else None)
+            got = ys[yk].float().cpu().numpy()[:, rows]
+            worst = max(worst, check_close(got, yref, mag, fp16_out=True,
+                                           what=f"layer {L} {role} N={N}"))
+        for v in hs.values():
+            assert v.device_status() == 0
+        del hs, host
+    assert chain.status() == 0
+    assert worst <= 1.0
