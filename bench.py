@@ -408,8 +408,8 @@ def run_ours(args):
     launches_per_step = (1 if args.layer_api == "persistent" else 4) if part == "layer" else 1
     if part == "gate":
         launches_per_step = layers[0]["gate"].plan_info(rows)[2]
-    if part == "prefill":  # staging + product per call (Q4_K and Q6_K launches of the triple)
-        launches_per_step = sum(layers[0][r].plan_info(rows)[2] for r in ("wq", "wo", "gate", "down")) + 1
+    if part == "prefill":  # staging + product per call (one launch for the mixed-format triple)
+        launches_per_step = sum(layers[0][r].plan_info(rows)[2] for r in ("wq", "wo", "gate", "down"))
 
     for i in range(args.warmup):
         step(i % N_LAYERS)

@@ -653,15 +653,21 @@ qg_status run_product_tc(qg_handle *const *hs, int nh, const __half *x, int64_t 
         cudaError_t e = launch_stage_tc4(xc, n, (int)h0->K, nb, chunk_stride, h0->xs, s);
         if (e != cudaSuccess) return cuda_fail(e, "staging kernel launch");
 
+        // One launch per format, except that Q4_K and Q6_K matrices of one
+        // call (the QKV triple) share a launch of the mixed kernel.
+        auto cls = [](qg_type ty) { return ty == QG_Q5_K ? 1 : 0; };
         bool done[3] = {false, false, false};
         for (int a = 0; a < nh; ++a) {
             if (done[a]) continue;
             const qg_type t = hs[a]->type;
+            bool mixed = false;
+            for (int j = a; j < nh; ++j)
+                mixed = mixed || (!done[j] && cls(hs[j]->type) == cls(t) && hs[j]->type != t);
             Params p;
             memset(&p, 0, sizeof p);
             int tiles = 0;
             for (int j = a; j < nh; ++j) {
-                if (done[j] || hs[j]->type != t) continue;
+                if (done[j] || (mixed ? cls(hs[j]->type) != cls(t) : hs[j]->type != t)) continue;
                 done[j] = true;
                 const qg_handle *h = hs[j];
                 Mat &m = p.mat[p.nmat++];
@@ -682,16 +688,30 @@ qg_status run_product_tc(qg_handle *const *hs, int nh, const __half *x, int64_t 
             p.ks = ks;
             p.out_f32 = out_f32;
             p.err = h0->err;
-            int ws = 0, xs = 0;
+            int ws = 0, xs = 0, ws6 = 0, xs6 = 0;
             const int T = (t == QG_Q4_K) ? T_Q4K : (t == QG_Q5_K) ? T_Q5K : T_Q6K;
             cudaError_t le = cudaErrorInvalidValue;
-            if (tc_stages(T, G, &ws, &xs)) {
+            // mixed: ring depths both formats' layouts fit, the larger layout's bytes
+            const bool staged = mixed ? (tc_stages(T_Q4K, G, &ws, &xs) &&
+                                         tc_stages(T_Q6K, G, &ws6, &xs6))
+                                      : tc_stages(T, G, &ws, &xs);
+            if (staged) {
+                if (mixed) {
+                    ws = ws < ws6 ? ws : ws6;
+                    xs = xs < xs6 ? xs : xs6;
+                }
                 p.stages = ws;
                 p.xstages = xs;
-                const int smem = tc_smem_bytes(T, G, ws, xs);
+                int smem = tc_smem_bytes(T, G, ws, xs);
+                if (mixed) {
+                    const int a4 = tc_smem_bytes(T_Q4K, G, ws, xs), a6 = tc_smem_bytes(T_Q6K, G, ws, xs);
+                    smem = a4 > a6 ? a4 : a6;
+                }
                 const dim3 grid((unsigned)ks, (unsigned)tiles, (unsigned)zc);
                 if (fault_at("launch"))
                     le = cudaErrorLaunchOutOfResources;
+                else if (mixed)
+                    le = launch_tc_q4k_q6k(G, p, grid, smem, s);
                 else if (T == T_Q4K)
                     le = launch_tc_q4k(G, p, grid, smem, s);
                 else if (T == T_Q5K)

@@ -1,7 +1,8 @@
 // Launchers of qg_tc_kernel (K-quant prefill chunks on the 5th-generation
 // tensor core).  Each qg_inst_tc_*.cu defines QG_TC_TYPE and QG_TC_NAME and
 // includes this file: one translation unit per weight format, so that they
-// compile in parallel.
+// compile in parallel.  With QG_TC_MIXED the launcher runs
+// qg_tc_mixed_kernel (Q4_K and Q6_K tiles in one launch).
 #pragma once
 #include "qg_launch.cuh"
 #include "qg_tc.cuh"
@@ -17,12 +18,16 @@ static cudaError_t launch_tc_one(const Params &p, dim3 grid, int smem, cudaStrea
     if (e != cudaSuccess) return e;
     if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
     if (smem > kTcMaxSmem) return cudaErrorInvalidValue;
+#ifdef QG_TC_MIXED
+    (void)T;
+    auto fn = qg_tc_mixed_kernel<G>;
+#else
+    auto fn = qg_tc_kernel<T, G>;
+#endif
     if (!configured[dev]) {
-        e = cudaFuncSetAttribute(qg_tc_kernel<T, G>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 kTcMaxSmem);
+        e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, kTcMaxSmem);
         if (e == cudaSuccess)
-            e = cudaFuncSetAttribute(qg_tc_kernel<T, G>,
-                                     cudaFuncAttributePreferredSharedMemoryCarveout,
+            e = cudaFuncSetAttribute(fn, cudaFuncAttributePreferredSharedMemoryCarveout,
                                      cudaSharedmemCarveoutMaxShared);
         if (e != cudaSuccess) return e;
         configured[dev] = 1;
@@ -46,7 +51,7 @@ static cudaError_t launch_tc_one(const Params &p, dim3 grid, int smem, cudaStrea
     }
     cfg.attrs = attr;
     cfg.numAttrs = na;
-    return cudaLaunchKernelEx(&cfg, qg_tc_kernel<T, G>, p);
+    return cudaLaunchKernelEx(&cfg, fn, p);
 }
 
 #ifdef QG_TC_CAPACITY

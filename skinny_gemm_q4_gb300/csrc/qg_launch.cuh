@@ -20,6 +20,8 @@ cudaError_t launch_dequant_fast(const Mat &m, int K, float *out, cudaStream_t st
 cudaError_t launch_tc_q4k(int G, const Params &p, dim3 grid, int smem, cudaStream_t s);
 cudaError_t launch_tc_q5k(int G, const Params &p, dim3 grid, int smem, cudaStream_t s);
 cudaError_t launch_tc_q6k(int G, const Params &p, dim3 grid, int smem, cudaStream_t s);
+// Q4_K and Q6_K matrices of one call in one launch (qg_tc_mixed_kernel).
+cudaError_t launch_tc_q4k_q6k(int G, const Params &p, dim3 grid, int smem, cudaStream_t s);
 // Clusters of ks qg_tc_kernel CTAs the GPU holds at once (0: unknown).
 int tc_cluster_capacity(int ks);
 cudaError_t launch_ref_gemv(const Mat &m, int K, const __half *x, int N, int out_f32,

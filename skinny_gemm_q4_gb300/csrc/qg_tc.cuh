@@ -366,7 +366,7 @@ __device__ __forceinline__ void tc_tile_out(const TcOut &o, const float *tile, i
 // super-block i waits until the fold of i - 1 has read it).
 // ---------------------------------------------------------------------------
 template <int T, int G>
-__global__ void __launch_bounds__(kTcThreads, 1) qg_tc_kernel(const __grid_constant__ Params p)
+__device__ __forceinline__ void tc_body(const Params &p, const Mat &m, const int rtile)
 {
     static_assert(G % 2 == 0 && G >= 2 && G <= kTcGroups, "MMA N = 8 G must be a multiple of 16");
     constexpr bool KQ = (T != T_Q6K);  // Q4_K / Q5_K: the mins term
@@ -377,10 +377,8 @@ __global__ void __launch_bounds__(kTcThreads, 1) qg_tc_kernel(const __grid_const
     constexpr uint32_t kIdesc = tc_idesc_f16(8 * G);
     constexpr uint32_t kD1 = 128, kD2 = 128 + 16 * G;
 
-    extern __shared__ __align__(1024) uint8_t smem[];
-    pdl_trigger();
-    const Mat &m = p.mat[select_mat(p, blockIdx.y)];
-    const int rtile = blockIdx.y - m.tile_begin;
+    extern __shared__ __align__(1024) uint8_t smem_tc[];
+    uint8_t *const smem = smem_tc;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int rank = blockIdx.x, ks = p.ks;
     const int nsb = (p.nb - rank + ks - 1) / ks;  // super-blocks rank, rank + ks, ...
@@ -793,6 +791,28 @@ __global__ void __launch_bounds__(kTcThreads, 1) qg_tc_kernel(const __grid_const
     }
     bar_sync_named(1, 256);  // the row threads
     tc_tile_out(out, otile, 8 * G, row0, tok0, threadIdx.x, 256);
+}
+
+template <int T, int G>
+__global__ void __launch_bounds__(kTcThreads, 1) qg_tc_kernel(const __grid_constant__ Params p)
+{
+    pdl_trigger();
+    const Mat &m = p.mat[select_mat(p, blockIdx.y)];
+    tc_body<T, G>(p, m, blockIdx.y - m.tile_begin);
+}
+
+// Q4_K and Q6_K matrices of one call (the QKV triple) in one launch: each
+// CTA runs the pipeline of its tile's format; the launch's shared memory and
+// ring depths fit both formats (a cluster's CTAs share a tile, so a format).
+template <int G>
+__global__ void __launch_bounds__(kTcThreads, 1) qg_tc_mixed_kernel(const __grid_constant__ Params p)
+{
+    pdl_trigger();
+    const Mat &m = p.mat[select_mat(p, blockIdx.y)];
+    if (m.type == T_Q6K)
+        tc_body<T_Q6K, G>(p, m, blockIdx.y - m.tile_begin);
+    else
+        tc_body<T_Q4K, G>(p, m, blockIdx.y - m.tile_begin);
 }
 
 }  // namespace qg
