@@ -281,9 +281,10 @@ def _graph_us(torch, side, ncalls, call, e0, e1):
 
 def _kernel_name(call, n):
     """The product kernel that serves one layer call at n tokens."""
-    types = {"qkv": "Q4_K|Q6_K", "wo": "Q4_K", "pair": "Q4_K", "gate": "Q4_K", "down": "Q6_K"}[call]
+    types = {"qkv": "Q4_K|Q6_K", "wo": "Q4_K", "pair": "Q4_K", "gate": "Q4_K", "down": "Q6_K",
+             "nvfp4": "NVFP4"}[call]
     what = {"qkv": "QKV triple", "wo": "Wo + residual", "pair": "gate/up pair", "gate": "gate",
-            "down": "down"}[call]
+            "down": "down", "nvfp4": "27648 x 5120"}[call]
     # N = 2..8 on Q4_K/Q5_K matrices of at most 4096 rows (Wo) runs the
     # K-sliced kernel too
     n8 = n == 1 or (n <= 8 and call != "wo")
@@ -328,9 +329,17 @@ def run_ours(args):
             w, sc, g = synth.device_weights(qt, M, K, seed=rank, stream=1000 * L + i, device=dev)
             hs[role] = qg.QGemv(qt, M, K, w, sc, g, max_tokens=128)
         layers.append(hs)
+    # --part nvfp4: six copies of the NVFP4 27648 x 5120 matrix (478 MB > L2)
+    NV_M, NV_K = 27648, 5120
+    nv = []
+    if args.part == "nvfp4":
+        for c in range(6):
+            w, sc, g = synth.device_weights(synth.NVFP4, NV_M, NV_K, seed=rank, stream=9000 + c,
+                                            device=dev)
+            nv.append(qg.QGemv(synth.NVFP4, NV_M, NV_K, w, sc, g))
     all_handles = [h for hs in layers for h in hs.values()]
     part = args.part
-    rows = max(1, args.rows) if part in ("gate", "prefill") else 1
+    rows = max(1, args.rows) if part in ("gate", "prefill", "nvfp4") else 1
     nl = rows if part == "prefill" else 1  # tokens of the layer calls
     x_qkv = synth.device_activations(nl, 2560, 0, 1, dev)
     x_o = synth.device_activations(nl, 4096, 0, 2, dev)
@@ -347,6 +356,8 @@ def run_ours(args):
     yd = torch.empty((nl, 2560), dtype=f16, device=dev)
 
     x_g = synth.device_activations(rows, 2560, 0, 7, dev)
+    x_nv = synth.device_activations(rows, NV_K, 0, 8, dev)
+    y_nv = torch.empty((rows, NV_M), dtype=f16, device=dev)
     y_g = torch.empty((rows, 9728), dtype=f16, device=dev)
 
     def call_qkv(h, s):
@@ -394,6 +405,9 @@ def run_ours(args):
         if chain is not None and part in ("layer", "prefill"):
             qg.qgemv_chain_run(chain.c, chain_calls[L], s)
             return
+        if part == "nvfp4":
+            qg.qgemv_run(nv[L % len(nv)].h, x_nv.data_ptr(), rows, y_nv.data_ptr(), qg.OUT_F16, s)
+            return
         for name, fn, _ in CALLS:
             if part in ("layer", "prefill", name):
                 fn(h, s)
@@ -401,9 +415,11 @@ def run_ours(args):
             qg.qgemv_run(h["gate"].h, x_g.data_ptr(), rows, y_g.data_ptr(), qg.OUT_F16, s)
 
     roles = {"layer": [r for r, _, _, _ in synth.LAYER], "prefill": [r for r, _, _, _ in synth.LAYER],
-             "qkv": ["wq", "wk", "wv"],
+             "qkv": ["wq", "wk", "wv"], "nvfp4": [],
              "wo": ["wo"], "pair": ["gate", "up"], "down": ["down"], "gate": ["gate"]}[part]
     wbytes = sum(M * synth.row_bytes(qt, K) for r, qt, M, K in synth.LAYER if r in roles)
+    if part == "nvfp4":  # codes, e4m3 scales (one per 16 weights), the tensor scale
+        wbytes = NV_M * (synth.row_bytes(synth.NVFP4, NV_K) + NV_K // 16) + 4
     # N = 1: one product kernel per call (x staged in-kernel)
     launches_per_step = (1 if args.layer_api == "persistent" else 4) if part == "layer" else 1
     if part == "gate":
@@ -504,6 +520,13 @@ def run_ours(args):
                 if pchain.status() != 0:
                     print(json.dumps({"error": "persistent chain reports a device timeout"}))
                     sys.exit(3)
+    elif part == "nvfp4":
+        dom = "nvfp4"
+        us = _graph_us(torch, side, ncalls,
+                       lambda i, s: qg.qgemv_run(nv[i % len(nv)].h, x_nv.data_ptr(), rows,
+                                                 y_nv.data_ptr(), qg.OUT_F16, s), e0, e1)
+        calls[dom] = dict(_bw(wbytes, us, peak), bytes_per_call=wbytes,
+                          flops_per_call=2 * rows * NV_M * NV_K)
     elif part == "gate":
         dom = "gate"
         nb_ = 9728 * synth.row_bytes(synth.Q4_K, 2560)
@@ -519,7 +542,7 @@ def run_ours(args):
         us = _graph_us(torch, side, ncalls, lambda i, s: fn(layers[i % N_LAYERS], s), e0, e1)
         calls[dom] = dict(_bw(nb_, us, peak), bytes_per_call=nb_)
     d = calls[dom]
-    ntok = rows if part in ("gate", "prefill") else 1
+    ntok = rows if part in ("gate", "prefill", "nvfp4") else 1
     kname = _kernel_name(dom, ntok)
     flops = d.get("flops_per_call", 0)
     if ntok >= 33 and flops / (tpeak * 1e12) > d["bytes_per_call"] / (peak * 1e9):
@@ -644,7 +667,9 @@ def run_ours(args):
                                  "calls": "four entry-point calls"}[args.layer_api]
                    if part in ("layer", "prefill") else "one call",
                    "weight_bytes_per_step": wbytes,
-                   "cold": "36 distinct layers (2.3 GB) > L2; no flush needed",
+                   "cold": ("6 copies of the matrix (478 MB) > L2; no flush needed"
+                            if part == "nvfp4" else
+                            "36 distinct layers (2.3 GB) > L2; no flush needed"),
                    "pct_of_nominal_8TBps": round(100 * value / world / 8000.0, 2),
                    "pct_of_measured_hbm": round(100 * value / world / peak, 2)},
         "roofline": roofline,
@@ -821,7 +846,7 @@ def main():
     ap.add_argument("--nvfp4-sets", type=int, default=56,
                     help="copies of the three NVFP4 shapes (56: ~10 GB)")
     ap.add_argument("--part", default="layer",
-                    choices=["layer", "qkv", "wo", "pair", "down", "gate", "prefill"],
+                    choices=["layer", "qkv", "wo", "pair", "down", "gate", "prefill", "nvfp4"],
                     help="time one call of the layer only (profiling); prefill: the whole layer "
                          "at --rows tokens; default: the whole layer at N = 1")
     ap.add_argument("--layer-api", default="chain", choices=["chain", "persistent", "calls"],
