@@ -9,7 +9,12 @@
 // outputs of calls 0 .. c-1 (a device counter with release/acquire ordering),
 // so any call may read what an earlier call wrote, exactly as the same calls
 // issued one by one on a stream.  Weights never change during a chain, so the
-// producer warp prefetches the next tiles' weights across that wait.
+// producer warp issues the next call's weights as soon as its own side has
+// published (without waiting for the other CTAs).
+//
+// On GB300 the same calls as one launch each, chained by programmatic
+// dependent launch, measured faster (the decode layer 29.0 vs 35.0 us), so
+// this form is opt-in (QG_CHAIN_PERSISTENT).
 //
 // Placement: one CTA per SM holding two independent pipelines ("sides"),
 // each a producer warp and 8 consumer warps with its own ring, staged x and
