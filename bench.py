@@ -119,13 +119,17 @@ def _tensor_peak():
     return 1900.0, "fallback"
 
 
+# The sources the N <= 8 kernels (the calls `traffic` covers) are built from.
+_N8_SOURCES = ("qg_api.cu", "qg_inst.cuh", "qg_inst_q4k.cu", "qg_inst_q6k.cu", "qg_kernels.cuh",
+               "qg_launch.cuh", "qg_ptx.cuh")
+
+
 def _kernel_source_sha():
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "skinny_gemm_q4_gb300", "csrc")
-    for f in sorted(os.listdir(csrc)):
-        if f.endswith((".cu", ".cuh")):
-            with open(os.path.join(csrc, f), "rb") as fh:
-                h.update(fh.read())
+    for f in _N8_SOURCES:
+        with open(os.path.join(csrc, f), "rb") as fh:
+            h.update(fh.read())
     return h.hexdigest()[:16]
 
 
