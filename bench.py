@@ -569,11 +569,11 @@ def run_ours(args):
     if part == "layer" and not args.no_configs:
         configs = run_configs(args, torch, qg, synth, layers, side, e0, e1, peak, tpeak, dev)
 
-    # End to end through the public API, as a user runs a decode step: the
-    # step's inputs (x of the four calls and the residual, one pinned host
-    # buffer, a new one each step out of four) copied to the device, the layer
-    # by one qgemv_chain_run call, every output copied back to pinned host
-    # memory, and the stream synchronized before the next step.
+    # End to end through the public API, as a user runs a decode step: one
+    # qgemv_chain_run_host call copies the step's inputs (x of the four calls
+    # and the residual, one pinned host buffer, a new one each step out of
+    # four) to the device, runs the layer's calls, copies every output back to
+    # pinned host memory and synchronizes the stream.
     e2e_steps = min(args.steps, 4 * N_LAYERS) if part == "layer" else 0
     e2e_val = None
     h2d = d2h = 0
@@ -608,10 +608,10 @@ def run_ours(args):
         cs = torch.cuda.current_stream()
 
         def e2e_step(i):
-            din.copy_(hins[i % 4], non_blocking=True)
-            qg.qgemv_chain_run(echain.c, e2e_calls[i % N_LAYERS], cs.cuda_stream)
-            hout.copy_(dout, non_blocking=True)
-            cs.synchronize()
+            # inputs in, the layer, outputs out, synchronized: one library call
+            qg.qgemv_chain_run_host(echain.c, e2e_calls[i % N_LAYERS], hins[i % 4].data_ptr(),
+                                    din.data_ptr(), h2d, dout.data_ptr(), hout.data_ptr(), d2h,
+                                    cs.cuda_stream)
 
         for i in range(max(args.warmup, 3)):
             e2e_step(i)
@@ -683,9 +683,9 @@ def run_ours(args):
         "e2e": None if e2e_val is None else {"value": round(e2e_val, 3), "unit": "GB/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h,
                 "steps": e2e_steps,
-                "how": "per step: one pinned-host -> device copy of the step's inputs, "
-                       "qgemv_chain_run (the layer), one device -> pinned-host copy of all "
-                       "outputs, stream synchronized"},
+                "how": "per step: qgemv_chain_run_host -- the step's inputs copied from "
+                       "pinned host memory to the device, the layer's calls, all outputs "
+                       "copied back to pinned host memory, stream synchronized"},
         "configs": configs,
         "device_status": 0,
         "gpu_launches": launches_per_step * args.steps,

@@ -336,6 +336,22 @@ qg_status qgemv_chain_create(qg_chain **out, uint32_t flags);
  * QG_EUNSUPPORTED, QG_ECUDA. */
 qg_status qgemv_chain_run(qg_chain *c, const qg_call *calls, int32_t ncalls, void *stream);
 
+/* One decode step with its inputs and outputs in host memory (the pages
+ * time kernels with their inputs resident, TandemLLM "Kernels", How a kernel
+ * gets in -- this entry times the whole round trip): copies in_bytes from
+ * in_host to in_dev, runs calls[0 .. ncalls-1] as qgemv_chain_run does (their
+ * x, residuals and outputs are device buffers, typically inside in_dev and
+ * out_dev), copies out_bytes from out_dev to out_host and synchronizes the
+ * stream.  When a host buffer is page-locked and mapped (cudaHostAlloc, or
+ * registered as mapped), the copy is whole 16-byte units and every address is
+ * 16-byte aligned, the SMs copy it through the mapped buffer (a small kernel
+ * chained to the calls); otherwise the copy engine does.  Errors: those of
+ * qgemv_chain_run, QG_EINVAL (null buffer with a nonzero size), QG_ECUDA. */
+qg_status qgemv_chain_run_host(qg_chain *c, const qg_call *calls, int32_t ncalls,
+                               const void *in_host, void *in_dev, size_t in_bytes,
+                               const void *out_dev, void *out_host, size_t out_bytes,
+                               void *stream);
+
 /* Read (and with clear != 0, reset) the chain's device error word: bits 1
  * and 2 as for qgemv_device_status, bit 4: a wait for the earlier calls'
  * outputs ran out (results undefined); the kernel never traps (reflex-llm

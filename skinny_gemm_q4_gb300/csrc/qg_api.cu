@@ -1404,6 +1404,60 @@ qg_status qgemv_chain_run(qg_chain *c, const qg_call *calls, int32_t ncalls, voi
     return QG_OK;
 }
 
+// The address a kernel uses for a host buffer: its mapped device address if
+// the buffer is page-locked and mapped, else null (copy-engine path).
+static const void *mapped_device_ptr(const void *host)
+{
+    cudaPointerAttributes a;
+    if (cudaPointerGetAttributes(&a, host) != cudaSuccess) {
+        cudaGetLastError();
+        return nullptr;
+    }
+    return a.type == cudaMemoryTypeHost ? a.devicePointer : nullptr;
+}
+
+// One host <-> device transfer of a chain step: by the SMs through the mapped
+// host buffer when it is page-locked, mapped and the copy is whole 16-byte
+// units, else by the copy engine.
+static qg_status step_copy(const void *src, void *dst, size_t bytes, bool to_device,
+                           cudaStream_t s)
+{
+    if (bytes == 0) return QG_OK;
+    const void *hp = to_device ? src : dst;
+    const void *mapped = mapped_device_ptr(hp);
+    if (mapped && bytes % 16 == 0 && aligned(src, 16) && aligned(dst, 16) && aligned(mapped, 16)) {
+        const cudaError_t e = to_device ? launch_copy16(mapped, dst, bytes, s)
+                                        : launch_copy16(src, const_cast<void *>(mapped), bytes, s);
+        if (e == cudaSuccess) return QG_OK;
+        cudaGetLastError();
+    }
+    const cudaError_t e = cudaMemcpyAsync(dst, src, bytes,
+                                          to_device ? cudaMemcpyHostToDevice : cudaMemcpyDeviceToHost, s);
+    return e == cudaSuccess ? QG_OK : cuda_fail(e, "step copy");
+}
+
+qg_status qgemv_chain_run_host(qg_chain *c, const qg_call *calls, int32_t ncalls,
+                               const void *in_host, void *in_dev, size_t in_bytes,
+                               const void *out_dev, void *out_host, size_t out_bytes,
+                               void *stream)
+{
+    g_err.clear();
+    if (!c || !calls) return fail(QG_EINVAL, "null chain or calls");
+    if ((in_bytes && (!in_host || !in_dev)) || (out_bytes && (!out_dev || !out_host)))
+        return fail(QG_EINVAL, "null step buffer");
+    for (int i = 0; i < ncalls; ++i) {
+        const qg_status st = check_call(calls[i]);
+        if (st != QG_OK) return st;
+    }
+    const cudaStream_t s = (cudaStream_t)stream;
+    qg_status st = step_copy(in_host, in_dev, in_bytes, true, s);
+    if (st == QG_OK) st = qgemv_chain_run(c, calls, ncalls, stream);
+    if (st == QG_OK) st = step_copy(out_dev, out_host, out_bytes, false, s);
+    if (st != QG_OK) return st;
+    const cudaError_t e = cudaStreamSynchronize(s);
+    return e == cudaSuccess ? QG_OK : cuda_fail(e, "stream synchronize");
+}
+
 qg_status qgemv_chain_status(qg_chain *c, uint32_t *flags_out, int clear)
 {
     if (!c) return fail(QG_EINVAL, "null chain");

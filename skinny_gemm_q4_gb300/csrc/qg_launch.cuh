@@ -10,6 +10,9 @@ constexpr int kGemvMaxSmem = 200 * 1024;
 
 cudaError_t launch_stage(const __half *x, int N, int K, int nb, int64_t tok_stride, uint8_t *xq4,
                          uint8_t *xq6, uint8_t *xfp4, cudaStream_t stream);
+// Copy of `bytes` (a multiple of 16, both addresses 16-byte aligned) by the
+// SMs; either side may be mapped page-locked host memory (qg_stage.cu).
+cudaError_t launch_copy16(const void *src, void *dst, size_t bytes, cudaStream_t s);
 cudaError_t launch_stage_tc4(const __half *x, int N, int K, int nb, int64_t chunk_stride,
                              uint8_t *out, cudaStream_t stream);
 cudaError_t launch_dequant(const Mat &m, int K, float *out, cudaStream_t stream);

@@ -82,3 +82,39 @@ cudaError_t launch_stage_tc4(const __half *x, int N, int K, int nb, int64_t chun
 }
 
 }  // namespace qg
+
+namespace qg {
+
+// Copy of n16 16-byte units by the SMs (host <-> device through mapped,
+// page-locked host memory, for the small per-step buffers where a copy-engine
+// transfer costs several microseconds of setup).  Ordered like the kernels
+// around it: it waits for the previous kernel before touching either buffer.
+__global__ void __launch_bounds__(256) qg_copy16_kernel(const uint4 *__restrict__ src,
+                                                        uint4 *__restrict__ dst, int64_t n16)
+{
+    pdl_trigger();
+    pdl_wait();
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n16;
+         i += (int64_t)gridDim.x * blockDim.x)
+        dst[i] = src[i];
+}
+
+cudaError_t launch_copy16(const void *src, void *dst, size_t bytes, cudaStream_t s)
+{
+    const int64_t n16 = (int64_t)(bytes / 16);
+    if (n16 == 0) return cudaSuccess;
+    int64_t blocks = (n16 + 255) / 256;
+    if (blocks > 304) blocks = 304;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)blocks);
+    cfg.blockDim = dim3(256);
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, qg_copy16_kernel, (const uint4 *)src, (uint4 *)dst, n16);
+}
+
+}  // namespace qg

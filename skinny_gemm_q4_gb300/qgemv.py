@@ -39,7 +39,8 @@ EXPORTS = ["qgemv_create", "qgemv_run", "qgemv_run_add", "qgemv_pair_run", "qgem
            "qgemv_run_host", "qgemv_dequantize", "qgemv_destroy", "qgemv_last_error",
            "qgemv_row_bytes", "qgemv_plan_info", "qgemv_describe", "qgemv_device_status",
            "qgemv_run_noalloc", "qgemv_pair_swiglu_run", "qgemv_chain_create",
-           "qgemv_chain_run", "qgemv_chain_status", "qgemv_chain_destroy"]
+           "qgemv_chain_run", "qgemv_chain_status", "qgemv_chain_destroy",
+           "qgemv_chain_run_host"]
 
 CHAIN_PERSISTENT = 1
 
@@ -104,12 +105,16 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.qgemv_chain_create.argtypes = [ctypes.POINTER(vp), ctypes.c_uint32]
     lib.qgemv_chain_run.argtypes = [vp, ctypes.POINTER(QgCall), i32, vp]
     lib.qgemv_chain_status.argtypes = [vp, ctypes.POINTER(ctypes.c_uint32), c_int]
+    sz = ctypes.c_size_t
+    lib.qgemv_chain_run_host.argtypes = [vp, ctypes.POINTER(QgCall), i32, vp, vp, sz, vp, vp, sz,
+                                         vp]
     lib.qgemv_chain_destroy.argtypes = [vp]
     lib.qgemv_chain_destroy.restype = None
     for name in ("qgemv_create", "qgemv_run", "qgemv_run_add", "qgemv_pair_run",
                  "qgemv_triple_run", "qgemv_run_host", "qgemv_dequantize", "qgemv_plan_info",
                  "qgemv_device_status", "qgemv_run_noalloc", "qgemv_pair_swiglu_run",
-                 "qgemv_chain_create", "qgemv_chain_run", "qgemv_chain_status"):
+                 "qgemv_chain_create", "qgemv_chain_run", "qgemv_chain_status",
+                 "qgemv_chain_run_host"):
         getattr(lib, name).restype = c_int
     _lib = lib
     return lib
@@ -211,6 +216,14 @@ def qgemv_chain_create(flags: int = 0) -> int:
 def qgemv_chain_run(c, calls, stream):
     """calls: a QgCall array (see make_calls)."""
     _check(load().qgemv_chain_run(c, calls, len(calls), stream), "qgemv_chain_run")
+
+
+def qgemv_chain_run_host(c, calls, in_host, in_dev, in_bytes, out_dev, out_host, out_bytes,
+                         stream):
+    """One step with host inputs and outputs (raw pointers); synchronizes."""
+    _check(load().qgemv_chain_run_host(c, calls, len(calls), in_host or None, in_dev or None,
+                                       in_bytes, out_dev or None, out_host or None, out_bytes,
+                                       stream), "qgemv_chain_run_host")
 
 
 def qgemv_chain_status(c, clear: bool = False) -> int:

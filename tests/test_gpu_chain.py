@@ -252,3 +252,43 @@ def test_persistent_chain_reports_a_wait_that_runs_out(layer, monkeypatch):
     for k, sep in (("q", sq), ("k", sk), ("v", sv), ("o", so), ("g", sg), ("u", su), ("d", sd)):
         assert t.equal(ys[k], sep), k
     assert ch.status() == 0
+
+
+@pytest.mark.parametrize("pinned", [True, False], ids=["pinned", "pageable"])
+def test_chain_run_host_round_trip(layer, pinned):
+    """qgemv_chain_run_host: the step's inputs from host memory, the layer's
+    calls, every output back to host memory, synchronized.  Page-locked
+    buffers go through the SMs' copy kernel, pageable ones through the copy
+    engine; both give the device path's bytes."""
+    t = torch()
+    N = 2
+    kin = {"qkv": 2560, "o": 4096, "res": 2560, "ffn": 2560, "dn": 9728}
+    kout = {"q": 4096, "k": 1024, "v": 1024, "o": 2560, "g": 9728, "u": 9728, "d": 2560}
+    nin, nout = N * sum(kin.values()), N * sum(kout.values())
+    hin = t.from_numpy(synth.activations(1, nin, seed=48).reshape(-1))
+    hout = t.empty(nout, dtype=t.float16)
+    if pinned:
+        hin, hout = hin.pin_memory(), hout.pin_memory()
+    din = t.empty(nin, dtype=t.float16, device="cuda")
+    dout = t.empty(nout, dtype=t.float16, device="cuda")
+
+    def views(buf, sizes):
+        out, o = {}, 0
+        for k, n in sizes.items():
+            out[k] = buf[o:o + N * n].view(N, n)
+            o += N * n
+        return out
+    xs, ys = views(din, kin), views(dout, kout)
+    calls = _layer_calls(layer, xs, ys, N, xs["res"], False)
+    ch = qg.Chain()
+    s = t.cuda.current_stream().cuda_stream
+    qg.qgemv_chain_run_host(ch.c, calls, hin.data_ptr(), din.data_ptr(), nin * 2, dout.data_ptr(),
+                            hout.data_ptr(), nout * 2, s)
+    ref_in = hin.cuda()
+    assert t.equal(din, ref_in)
+    xr, yr = views(ref_in, kin), views(t.empty_like(dout), kout)
+    qg.qgemv_chain_run(ch.c, _layer_calls(layer, xr, yr, N, xr["res"], False), s)
+    t.cuda.synchronize()
+    ref_out = t.cat([yr[k].reshape(-1) for k in kout])
+    assert t.equal(hout, ref_out.cpu())
+    assert ch.status() == 0
