@@ -1443,6 +1443,7 @@ qg_status qgemv_chain_run_host(qg_chain *c, const qg_call *calls, int32_t ncalls
 {
     g_err.clear();
     if (!c || !calls) return fail(QG_EINVAL, "null chain or calls");
+    if (ncalls < 1) return fail(QG_EINVAL, "ncalls must be >= 1");
     if ((in_bytes && (!in_host || !in_dev)) || (out_bytes && (!out_dev || !out_host)))
         return fail(QG_EINVAL, "null step buffer");
     for (int i = 0; i < ncalls; ++i) {

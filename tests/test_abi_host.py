@@ -96,6 +96,7 @@ def test_null_handle_calls_are_errors(lib):
     calls = q.make_calls([(q.CALL_RUN, [None], 16, 1, [16], 0, None)])
     assert lib.qgemv_chain_run(None, calls, 1, None) == -1
     assert lib.qgemv_chain_status(None, None, 0) == -1
+    assert lib.qgemv_chain_run_host(None, calls, 1, None, None, 0, None, None, 0, None) == -1
     lib.qgemv_chain_destroy(None)
 
 
