@@ -662,7 +662,9 @@ def run_ours(args):
         "higher_is_better": True,
         "scaling": "weak",
         "vs_baseline": None,
-        "dtype": "f16 x, fp32 accumulate, 4-bit weights",
+        "dtype": "f16",  # MMA operands (x, decoded weights); see "accumulate"
+        "accumulate": "f32",
+        "weights": "4-bit block formats (Q4_K, Q6_K in the decode layer)",
         "data": "synthetic",
         "config": {"workload": WORKLOAD if part == "layer" else WORKLOAD + ":" + part, "N": rows,
                    "layers_rotated": N_LAYERS,
