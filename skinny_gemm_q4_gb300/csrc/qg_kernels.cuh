@@ -37,7 +37,9 @@
 //                 are not 16-byte aligned: one 1-D bulk copy per row of the
 //                 aligned superset); 8 consumer warps decode and multiply; x
 //                 is staged inside the kernel.
-//   qg_sk_kernel  (the rest up to N = 32, and N >= 33 except Q4_K): x staged
+//   qg_sk_kernel  (the rest up to N = 32; N >= 33 for NVFP4 and FP8, and for
+//                 K-quants created with QG_FLAG_MMA_SYNC_PREFILL; the other
+//                 K-quant calls at N >= 33 run on the tcgen05 engine): x staged
 //                 once per call by qg_stage.cu; a producer warp streams 128
 //                 weight rows and the staged x of one super-block per stage by
 //                 TMA; cluster ranks are slices.
